@@ -1,0 +1,210 @@
+// kernels_fp8.cu -- per-tensor amax-scaled FP8 fake quant.
+//
+// optirs-gpu quantization.rs, module docs "fp8 quantization (E4M3 / E5M2)",
+// fp8_quantize_magnitude and fake_quant_fp8: the value is rounded to the
+// nearest FP8 grid point (ties to even), magnitudes above the format maximum
+// and infinities saturate to +-max, NaN stays NaN, signed zero is kept.  The
+// per-tensor scale follows ferrum-kernels marlin_repack.rs
+// (prepare_f16_weight_for_fp8_marlin: scale = absmax / 448; a zero scale
+// encodes as byte 0).
+//
+// The cast itself is the hardware saturating conversion
+// cvt.rn.satfinite.{e4m3x2,e5m2x2}.f32 (round to nearest even, +-inf and
+// overflow -> +-max, NaN -> NaN), decoded back with cvt.rn.f16x2.{e4m3x2,
+// e5m2x2} (every FP8 value is exact in fp16).  The library's tests compare
+// this against the rule above over every fp16, every bf16 and sampled fp32
+// bit patterns, ties included.  NaN handling is made explicit (code 0x7F,
+// canonical quiet NaN output) instead of relying on the conversion's NaN
+// payload.
+#include <cuda_fp16.h>
+
+#include "qat_device.cuh"
+#include "qat_launch.h"
+
+namespace qat {
+
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2_encode(float lo, float hi) {
+  uint16_t r;
+  if (FMT == QAT_E4M3)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int FMT>
+__device__ __forceinline__ void fp8x2_decode(uint32_t c2, float& lo, float& hi) {
+  uint32_t h2;
+  uint16_t c = (uint16_t)c2;
+  if (FMT == QAT_E4M3)
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  else
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(c));
+  lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+  hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+}
+
+struct Fp8Params {
+  float s;    // scale
+  float lim;  // fmt_max * s: the STE window |x| <= lim
+  int mode;   // 0 normal, 1 zero scale, 2 invalid given scale
+};
+
+constexpr uint32_t kNaN32 = 0x7fc00000u;
+constexpr uint32_t kNaN16 = 0x7fc0u;
+
+template <typename T, int FMT, bool FULL>
+__device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, int64_t tile,
+                                         const Fp8Params& p, void* __restrict__ y,
+                                         uint8_t* __restrict__ codes, uint32_t* __restrict__ mask,
+                                         int lane) {
+  constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
+  const int64_t tb = tile * kTile;
+  V32 v[SLOTS];
+  int cnt[SLOTS];
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+    int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+    if (FULL) {
+      cnt[j] = VEC;
+      v[j] = ld_v32(static_cast<const char*>(x) + base * T::BYTES);
+    } else {
+      int64_t c = n - base;
+      cnt[j] = c >= VEC ? VEC : (c > 0 ? (int)c : 0);
+      v[j] = load_vec<T>(x, cnt[j] > 0 ? base : 0, cnt[j]);
+    }
+  }
+  uint32_t mw[SLOTS];
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+    const int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+    V32 out;
+    CodeVec<8, VEC> cv;
+    cv.clear();
+    uint32_t mb = 0u;
+#pragma unroll
+    for (int e = 0; e < VEC; e += 2) {
+      const float x0 = elem<T>(v[j], e), x1 = elem<T>(v[j], e + 1);
+      const bool n0 = isnan(x0), n1 = isnan(x1);
+      uint32_t c0, c1;
+      float y0, y1;
+      if (p.mode == 0) {
+        const float t0 = __fdiv_rn(x0, p.s), t1 = __fdiv_rn(x1, p.s);
+        const uint32_t c2 = fp8x2_encode<FMT>(t0, t1);
+        float d0, d1;
+        fp8x2_decode<FMT>(c2, d0, d1);
+        c0 = c2 & 0xffu;
+        c1 = (c2 >> 8) & 0xffu;
+        y0 = __fmul_rn(d0, p.s);
+        y1 = __fmul_rn(d1, p.s);
+      } else {
+        c0 = c1 = 0u;
+        y0 = y1 = 0.0f;
+      }
+      if (p.mode != 2) {
+        if (n0) c0 = 0x7fu;
+        if (n1) c1 = 0x7fu;
+        mb |= (uint32_t)(fabsf(x0) <= p.lim) << e;
+        mb |= (uint32_t)(fabsf(x1) <= p.lim) << (e + 1);
+      }
+      if (FULL || e < cnt[j]) cv.set(e, (int)c0);
+      if (FULL || e + 1 < cnt[j]) cv.set(e + 1, (int)c1);
+      if (T::BYTES == 4) {
+        out.w[e] = (p.mode != 2 && n0) ? kNaN32 : __float_as_uint(y0);
+        out.w[e + 1] = (p.mode != 2 && n1) ? kNaN32 : __float_as_uint(y1);
+      } else {
+        uint32_t w = pack_bf16x2(y0, y1);
+        if (p.mode != 2) {
+          if (n0) w = (w & 0xffff0000u) | kNaN16;
+          if (n1) w = (w & 0x0000ffffu) | (kNaN16 << 16);
+        }
+        out.w[e >> 1] = w;
+      }
+    }
+    if (!FULL) mb &= (cnt[j] >= 32) ? 0xffffffffu : ((1u << cnt[j]) - 1u);
+    if (cnt[j] > 0) {
+      store_vec<T>(y, base, out, cnt[j]);
+      if (codes) cv.store(codes, base, cnt[j]);
+    }
+    mw[j] = mask_word_of_slot<VEC>(mb, lane);
+  }
+  if (mask) {
+    uint32_t w = gather_tile_word<VEC, SLOTS>(mw, lane);
+    int64_t wi = tile * 32 + lane;
+    if (FULL || wi < (n + 31) / 32) mask[wi] = w;
+  }
+}
+
+template <typename T, int FMT, bool GIVEN>
+__global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, int64_t n,
+                                                    const uint4* __restrict__ part, int nparts,
+                                                    float* scale, void* y, uint8_t* codes,
+                                                    uint32_t* mask, int32_t* flags) {
+  constexpr float kMax = FMT == QAT_E4M3 ? 448.0f : 57344.0f;
+  __shared__ uint32_t red[4 * 8];
+  __shared__ Fp8Params sp;
+  if (GIVEN) {
+    if (threadIdx.x == 0) {
+      float s = scale[0];
+      sp.s = s;
+      sp.mode = (isnan(s) || isinf(s) || s < 0.0f) ? 2 : (s == 0.0f ? 1 : 0);
+      sp.lim = __fmul_rn(kMax, s);
+      if (blockIdx.x == 0) flag_or(flags, sp.mode == 2 ? QAT_FLAG_BAD_PARAMS : 0);
+    }
+  } else {
+    Stats st = reduce_partials<false>(part, nparts, red);
+    if (threadIdx.x == 0) {
+      float s = __fdiv_rn(st.absmax_f(), kMax);
+      sp.s = s;
+      sp.mode = s == 0.0f ? 1 : 0;
+      sp.lim = __fmul_rn(kMax, s);
+      if (blockIdx.x == 0) {
+        scale[0] = s;
+        flag_or(flags, st.nonfinite ? QAT_FLAG_NONFINITE_INPUT : 0);
+      }
+    }
+  }
+  __syncthreads();
+  const Fp8Params p = sp;
+  const int lane = threadIdx.x & 31;
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  const int64_t nfull = n / kTile;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
+       t += wstride) {
+    const int64_t tile = GIVEN ? t : ntiles - 1 - t;
+    if (tile < nfull) fp8_tile<T, FMT, true>(x, n, tile, p, y, codes, mask, lane);
+    else fp8_tile<T, FMT, false>(x, n, tile, p, y, codes, mask, lane);
+  }
+}
+
+template <typename T, int FMT>
+static void fp8_t(bool given, const void* x, int64_t n, const void* ws, int nparts, float* scale,
+                  void* y, uint8_t* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  int64_t g = (ntiles + 7) / 8;
+  int64_t cap = (int64_t)device_info().sms * 8;
+  int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
+  const uint4* part = static_cast<const uint4*>(ws);
+  if (given)
+    k_fp8_tensor<T, FMT, true><<<grid, 256, 0, s>>>(x, n, part, nparts, scale, y, codes, mask, flags);
+  else
+    k_fp8_tensor<T, FMT, false><<<grid, 256, 0, s>>>(x, n, part, nparts, scale, y, codes, mask, flags);
+}
+
+qat_status launch_fp8_tensor(qat_dtype dt, qat_fp8_format fmt, bool given, const void* x, int64_t n,
+                             const void* ws, int nparts, float* scale, void* y, uint8_t* codes,
+                             uint32_t* mask, int32_t* flags, cudaStream_t s) {
+  if (dt == QAT_F32) {
+    if (fmt == QAT_E4M3) fp8_t<F32, QAT_E4M3>(given, x, n, ws, nparts, scale, y, codes, mask, flags, s);
+    else fp8_t<F32, QAT_E5M2>(given, x, n, ws, nparts, scale, y, codes, mask, flags, s);
+  } else {
+    if (fmt == QAT_E4M3) fp8_t<BF16, QAT_E4M3>(given, x, n, ws, nparts, scale, y, codes, mask, flags, s);
+    else fp8_t<BF16, QAT_E5M2>(given, x, n, ws, nparts, scale, y, codes, mask, flags, s);
+  }
+  count_launch(1);
+  return launch_status();
+}
+
+}  // namespace qat

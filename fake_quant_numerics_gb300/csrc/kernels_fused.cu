@@ -1,0 +1,314 @@
+// kernels_fused.cu -- single-pass per-unit calibration + integer fake quant.
+//
+// A unit (one row, axis-0 channel of optirs-gpu quantization.rs
+// per_channel_params; or one group of consecutive elements along the last
+// dimension, cs349e 05_quantization_basics.py demo 3) is small enough to stay
+// on chip, so its statistics and its quantization share one read of x:
+//
+//   k_int_groups: units of L = VEC * LPG elements (LPG = 2..32 lanes, a
+//     power of two).  Each unit lives in LPG adjacent lanes of one warp tile;
+//     its absmax / min / max is a shuffle reduction over those lanes.
+//   k_int_rows:   units of L elements, L % 32 == 0, up to 256 * NV vectors.
+//     One thread block per unit, statistics by a block reduction.
+//
+// Calibration follows QuantParams::from_absmax / from_minmax; the element map
+// follows QuantParams::quantize / dequantize and the STE window of
+// fake_quant_backward.  STATS_ONLY instantiations write the unit statistics
+// (absmax, min, max) instead.
+#include "qat_device.cuh"
+#include "qat_launch.h"
+
+namespace qat {
+
+template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY, bool FULL>
+__device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n, int64_t tile,
+                                           float* scale, int32_t* zp, float* absmax, float* minv,
+                                           float* maxv, void* __restrict__ y,
+                                           void* __restrict__ codes, uint32_t* __restrict__ mask,
+                                           int lane, int& fl) {
+  constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
+  constexpr int L = VEC * LPG;
+  constexpr bool NEED_MINMAX = AFFINE || STATS_ONLY;
+  const int64_t tb = tile * kTile;
+  V32 v[SLOTS];
+  bool present[SLOTS];
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+    int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+    // n is a multiple of L, so a lane's vector is entirely present or absent
+    present[j] = FULL || base < n;
+    if (present[j]) {
+      v[j] = ld_v32(static_cast<const char*>(x) + base * T::BYTES);
+    } else {
+#pragma unroll
+      for (int w = 0; w < 8; ++w) v[j].w[w] = 0u;
+    }
+  }
+  uint32_t mw[SLOTS];
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+    const int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+    const int64_t u = base / L;
+    Stats st;
+    st.init();
+    if (present[j]) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) st.add<NEED_MINMAX>(elem_bits<T>(v[j], e));
+    }
+    st.reduce_lanes<NEED_MINMAX>(LPG);
+    const bool leader = present[j] && (lane % LPG) == 0;
+    if (STATS_ONLY) {
+      if (leader) {
+        if (absmax) absmax[u] = st.absmax_f();
+        if (minv) minv[u] = st.min_f();
+        if (maxv) maxv[u] = st.max_f();
+      }
+      if (present[j] && st.nonfinite) fl |= QAT_FLAG_NONFINITE_INPUT;
+      mw[j] = 0u;
+      continue;
+    }
+    IntParams p;
+    int f = calibrate<BITS, AFFINE>(st, p);
+    if (leader) {
+      scale[u] = p.s;
+      if (zp) zp[u] = p.zp;
+    }
+    if (present[j]) fl |= f;
+    OutVec<T> ov;
+    CodeVec<BITS, VEC> cv;
+    cv.clear();
+    uint32_t mb = 0u;
+    if (!p.dead) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        int q;
+        float yv;
+        uint32_t m;
+        int_elem<false>(elem<T>(v[j], e), p, q, yv, m);
+        ov.set(e, yv);
+        cv.set(e, q);
+        mb |= m << e;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) ov.set(e, 0.0f);
+    }
+    if (!present[j]) mb = 0u;
+    if (present[j]) {
+      if (y) st_v32(static_cast<char*>(y) + base * T::BYTES, ov.v);
+      if (codes) cv.store(codes, base, VEC);
+    }
+    mw[j] = mask_word_of_slot<VEC>(mb, lane);
+  }
+  if (!STATS_ONLY && mask) {
+    uint32_t w = gather_tile_word<VEC, SLOTS>(mw, lane);
+    int64_t wi = tile * 32 + lane;
+    if (FULL || wi < (n + 31) / 32) mask[wi] = w;
+  }
+}
+
+template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY>
+__global__ void __maxnreg__(80) k_int_groups(const void* __restrict__ x, int64_t n, float* scale,
+                                             int32_t* zp, float* absmax, float* minv, float* maxv,
+                                             void* y, void* codes, uint32_t* mask, int32_t* flags) {
+  const int lane = threadIdx.x & 31;
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  const int64_t nfull = n / kTile;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  int fl = 0;
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
+       t += wstride) {
+    if (t < nfull)
+      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, true>(x, n, t, scale, zp, absmax, minv, maxv, y,
+                                                         codes, mask, lane, fl);
+    else
+      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, false>(x, n, t, scale, zp, absmax, minv, maxv,
+                                                          y, codes, mask, lane, fl);
+  }
+  warp_flag_or(flags, fl);
+}
+
+// ---------------------------------------------------------------------------
+// one thread block (256 threads) per unit of L elements, NV vectors / thread
+// ---------------------------------------------------------------------------
+template <typename T, int BITS, bool AFFINE, int NV, bool STATS_ONLY>
+__global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, int64_t units,
+                                                  int64_t L, float* scale, int32_t* zp,
+                                                  float* absmax, float* minv, float* maxv, void* y,
+                                                  void* codes, uint32_t* mask, int32_t* flags) {
+  constexpr int VEC = T::VEC, NT = 256;
+  constexpr int LPW = 32 / VEC;
+  constexpr bool NEED_MINMAX = AFFINE || STATS_ONLY;
+  __shared__ uint32_t red[4 * 8];
+  const int lane = threadIdx.x & 31;
+  const int nvec = (int)(L / VEC);
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int64_t ub = u * L;
+    V32 v[NV];
+    Stats st;
+    st.init();
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      int vi = threadIdx.x + j * NT;
+      if (vi < nvec) {
+        v[j] = ld_v32(static_cast<const char*>(x) + (ub + (int64_t)vi * VEC) * T::BYTES);
+      } else {
+#pragma unroll
+        for (int w = 0; w < 8; ++w) v[j].w[w] = 0u;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      int vi = threadIdx.x + j * NT;
+      if (vi < nvec) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) st.add<NEED_MINMAX>(elem_bits<T>(v[j], e));
+      }
+    }
+    Stats b = block_reduce_stats<NEED_MINMAX>(st, red);
+    if (STATS_ONLY) {
+      if (threadIdx.x == 0) {
+        if (absmax) absmax[u] = b.absmax_f();
+        if (minv) minv[u] = b.min_f();
+        if (maxv) maxv[u] = b.max_f();
+        flag_or(flags, b.nonfinite ? QAT_FLAG_NONFINITE_INPUT : 0);
+      }
+      continue;
+    }
+    IntParams p;
+    int f = calibrate<BITS, AFFINE>(b, p);
+    if (threadIdx.x == 0) {
+      scale[u] = p.s;
+      if (zp) zp[u] = p.zp;
+      flag_or(flags, f);
+    }
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int vi = threadIdx.x + j * NT;
+      const bool present = vi < nvec;
+      const int64_t base = ub + (int64_t)vi * VEC;
+      OutVec<T> ov;
+      CodeVec<BITS, VEC> cv;
+      cv.clear();
+      uint32_t mb = 0u;
+      if (!p.dead) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          int q;
+          float yv;
+          uint32_t m;
+          int_elem<false>(elem<T>(v[j], e), p, q, yv, m);
+          ov.set(e, yv);
+          cv.set(e, q);
+          mb |= m << e;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) ov.set(e, 0.0f);
+      }
+      if (present) {
+        if (y) st_v32(static_cast<char*>(y) + base * T::BYTES, ov.v);
+        if (codes) cv.store(codes, base, VEC);
+      }
+      // L % 32 == 0: the LPW lanes of a mask word are all present or all absent
+      uint32_t w = mask_word_of_slot<VEC>(present ? mb : 0u, lane);
+      if (mask && present && (lane % LPW) == 0) mask[base >> 5] = w;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+static int lpg_of(qat_dtype dt, int64_t L) {
+  const int vec = dt == QAT_F32 ? F32::VEC : BF16::VEC;
+  for (int lpg = 2; lpg <= 32; lpg <<= 1)
+    if (L == (int64_t)vec * lpg) return lpg;
+  return 0;
+}
+
+static int nv_of(qat_dtype dt, int64_t L) {
+  const int vec = dt == QAT_F32 ? F32::VEC : BF16::VEC;
+  if (L % 32 != 0) return 0;
+  int64_t nvec = L / vec;
+  for (int nv = 1; nv <= 8; nv <<= 1)
+    if (nvec <= 256 * nv) return nv;
+  return 0;
+}
+
+bool fused_units_supported(qat_dtype dt, int64_t L) { return lpg_of(dt, L) || nv_of(dt, L); }
+
+template <typename T, int BITS, bool AFFINE, bool SO>
+static void groups_t(int lpg, const void* x, int64_t n, float* scale, int32_t* zp, float* absmax,
+                     float* minv, float* maxv, void* y, void* codes, uint32_t* mask, int32_t* flags,
+                     cudaStream_t s) {
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  int64_t g = (ntiles + 7) / 8;
+  int64_t cap = (int64_t)device_info().sms * 8;
+  int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
+#define QAT_G(LP) \
+  k_int_groups<T, BITS, AFFINE, LP, SO><<<grid, 256, 0, s>>>(x, n, scale, zp, absmax, minv, maxv, y, codes, mask, flags)
+  switch (lpg) {
+    case 2: QAT_G(2); break;
+    case 4: QAT_G(4); break;
+    case 8: QAT_G(8); break;
+    case 16: QAT_G(16); break;
+    default: QAT_G(32); break;
+  }
+#undef QAT_G
+}
+
+template <typename T, int BITS, bool AFFINE, bool SO>
+static void rows_t(int nv, const void* x, int64_t units, int64_t L, float* scale, int32_t* zp,
+                   float* absmax, float* minv, float* maxv, void* y, void* codes, uint32_t* mask,
+                   int32_t* flags, cudaStream_t s) {
+  int64_t cap = (int64_t)device_info().sms * 8;
+  int grid = (int)(units > cap ? cap : (units < 1 ? 1 : units));
+#define QAT_R(NV) \
+  k_int_rows<T, BITS, AFFINE, NV, SO><<<grid, 256, 0, s>>>(x, units, L, scale, zp, absmax, minv, maxv, y, codes, mask, flags)
+  switch (nv) {
+    case 1: QAT_R(1); break;
+    case 2: QAT_R(2); break;
+    case 4: QAT_R(4); break;
+    default: QAT_R(8); break;
+  }
+#undef QAT_R
+}
+
+template <typename T, int BITS, bool AFFINE, bool SO>
+static void fused_t(const void* x, int64_t units, int64_t L, float* scale, int32_t* zp,
+                    float* absmax, float* minv, float* maxv, void* y, void* codes, uint32_t* mask,
+                    int32_t* flags, cudaStream_t s) {
+  const qat_dtype dt = T::kDtype;
+  int lpg = lpg_of(dt, L);
+  if (lpg)
+    groups_t<T, BITS, AFFINE, SO>(lpg, x, units * L, scale, zp, absmax, minv, maxv, y, codes, mask,
+                                  flags, s);
+  else
+    rows_t<T, BITS, AFFINE, SO>(nv_of(dt, L), x, units, L, scale, zp, absmax, minv, maxv, y, codes,
+                                mask, flags, s);
+}
+
+qat_status launch_int_fused(qat_dtype dt, int bits, bool affine, bool stats_only, const void* x,
+                            int64_t units, int64_t L, float* scale, int32_t* zp, float* absmax,
+                            float* minv, float* maxv, void* y, void* codes, uint32_t* mask,
+                            int32_t* flags, cudaStream_t s) {
+  if (!fused_units_supported(dt, L)) return QAT_ERR_UNSUPPORTED;
+#define QAT_F(T, B, A, SO) \
+  fused_t<T, B, A, SO>(x, units, L, scale, zp, absmax, minv, maxv, y, codes, mask, flags, s)
+  if (stats_only) {
+    if (dt == QAT_F32) QAT_F(F32, 8, false, true);
+    else QAT_F(BF16, 8, false, true);
+  } else if (dt == QAT_F32) {
+    if (bits == 8) { if (affine) QAT_F(F32, 8, true, false); else QAT_F(F32, 8, false, false); }
+    else { if (affine) QAT_F(F32, 4, true, false); else QAT_F(F32, 4, false, false); }
+  } else {
+    if (bits == 8) { if (affine) QAT_F(BF16, 8, true, false); else QAT_F(BF16, 8, false, false); }
+    else { if (affine) QAT_F(BF16, 4, true, false); else QAT_F(BF16, 4, false, false); }
+  }
+#undef QAT_F
+  count_launch(1);
+  return launch_status();
+}
+
+}  // namespace qat

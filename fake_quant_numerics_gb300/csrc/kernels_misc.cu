@@ -1,0 +1,294 @@
+// kernels_misc.cu -- straight-through-estimator backward and the two-level
+// 4-bit block format.
+//
+// STE (optirs-gpu quantization.rs, fake_quant_backward): the incoming
+// gradient passes where the forward input lay inside the clamp window and is
+// zero elsewhere.  The forward kernels already evaluated the window into a
+// packed bit mask, so the backward pass is one read of grad + mask and one
+// write of grad_in.
+//
+// Two-level 4-bit (aprender-train double_quant.rs, quantize_4bit_double,
+// reconstruct_scales, dequantize_4bit_double): 64-element absmax blocks with
+// 4-bit codes (two per byte, even element in the high nibble) and scale
+// absmax / 7; every 256 block scales are re-quantized to uint8 against their
+// maximum (the fp32 super-scale, floored at 1e-8).  One thread block handles
+// one super-block of 256 * 64 = 16384 elements; the codes never depend on the
+// super-scale, so they are written as soon as their block scale is known, and
+// only the optional fused round trip waits for the super-scale.
+#include "qat_device.cuh"
+#include "qat_launch.h"
+
+namespace qat {
+
+// ---------------------------------------------------------------------------
+// STE backward
+// ---------------------------------------------------------------------------
+template <typename T, bool FULL>
+__device__ __forceinline__ void ste_tile(const void* __restrict__ g, int64_t n, int64_t tile,
+                                         const uint32_t* __restrict__ mask, void* __restrict__ dx,
+                                         int lane) {
+  constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC), LPW = 32 / VEC;
+  const int64_t tb = tile * kTile;
+  const int64_t nwords = (n + 31) / 32;
+  const int64_t wi = tile * 32 + lane;
+  uint32_t word = 0u;
+  if (FULL || wi < nwords) word = __ldg(mask + wi);
+  V32 v[SLOTS];
+  int cnt[SLOTS];
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+    int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+    if (FULL) {
+      cnt[j] = VEC;
+      v[j] = ld_v32(static_cast<const char*>(g) + base * T::BYTES);
+    } else {
+      int64_t c = n - base;
+      cnt[j] = c >= VEC ? VEC : (c > 0 ? (int)c : 0);
+      v[j] = load_vec<T>(g, cnt[j] > 0 ? base : 0, cnt[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+    const int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+    const uint32_t w = __shfl_sync(kFull, word, j * VEC + lane / LPW);
+    const uint32_t bits = (w >> ((lane % LPW) * VEC)) & ((1u << VEC) - 1u);
+    V32 o;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint32_t sel;
+      if (T::BYTES == 4) {
+        sel = ((bits >> k) & 1u) ? 0xffffffffu : 0u;
+      } else {
+        sel = (((bits >> (2 * k)) & 1u) ? 0x0000ffffu : 0u) |
+              (((bits >> (2 * k + 1)) & 1u) ? 0xffff0000u : 0u);
+      }
+      o.w[k] = v[j].w[k] & sel;
+    }
+    if (cnt[j] > 0) store_vec<T>(dx, base, o, cnt[j]);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_ste(const void* __restrict__ g, int64_t n,
+                                             const uint32_t* __restrict__ mask, void* dx) {
+  const int lane = threadIdx.x & 31;
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  const int64_t nfull = n / kTile;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
+       t += wstride) {
+    if (t < nfull) ste_tile<T, true>(g, n, t, mask, dx, lane);
+    else ste_tile<T, false>(g, n, t, mask, dx, lane);
+  }
+}
+
+qat_status launch_ste(qat_dtype dt, const void* g, int64_t n, const uint32_t* mask, void* dx,
+                      cudaStream_t s) {
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  int64_t gr = (ntiles + 7) / 8;
+  int64_t cap = (int64_t)device_info().sms * 8;
+  int grid = (int)(gr > cap ? cap : (gr < 1 ? 1 : gr));
+  if (dt == QAT_F32) k_ste<F32><<<grid, 256, 0, s>>>(g, n, mask, dx);
+  else k_ste<BF16><<<grid, 256, 0, s>>>(g, n, mask, dx);
+  count_launch(1);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// two-level 4-bit quantization
+// ---------------------------------------------------------------------------
+constexpr int kQ4Block = 64;
+constexpr int kQ4Super = 256;                       // block scales per super-block
+constexpr int kQ4SuperElems = kQ4Block * kQ4Super;  // 16384
+constexpr int kQ4Threads = 512;
+constexpr int kQ4Slots = kQ4SuperElems / (kQ4Threads * 8);  // 4 vectors of 8 fp32 per thread
+
+// code = clamp(round_half_away(x / s), -8, 7); s == 0 or NaN -> 0
+__device__ __forceinline__ int q4_code(float x, float s) {
+  if (s == 0.0f) return 0;
+  float r = roundf(__fdiv_rn(x, s));
+  int k = __float2int_rz(r);  // r is integral; NaN -> 0
+  return min(max(k, -8), 7);
+}
+
+__device__ __forceinline__ int nibble_value(uint32_t packed, int e) {
+  // element e of 8: byte e/2, even element in the high nibble
+  int shift = (e >> 1) * 8 + ((e & 1) ? 0 : 4);
+  int nib = (int)((packed >> shift) & 0xfu);
+  return nib >= 8 ? nib - 16 : nib;
+}
+
+template <bool ROUNDTRIP>
+__global__ void __launch_bounds__(kQ4Threads) k_q4_quant(const float* __restrict__ x, int64_t n,
+                                                         uint8_t* __restrict__ data,
+                                                         uint8_t* __restrict__ qscales,
+                                                         float* __restrict__ sup,
+                                                         float* __restrict__ y) {
+  __shared__ float s_scale[kQ4Super];
+  __shared__ float s_q[kQ4Super];
+  __shared__ float s_red[kQ4Threads / 32];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t nsuper = (n + kQ4SuperElems - 1) / kQ4SuperElems;
+  const int64_t nblocks = (n + kQ4Block - 1) / kQ4Block;
+  const int64_t nbytes = (n + 1) / 2;
+  for (int64_t sb = blockIdx.x; sb < nsuper; sb += gridDim.x) {
+    const int64_t e0 = sb * kQ4SuperElems;
+    const bool full = e0 + kQ4SuperElems <= n;
+    V32 v[kQ4Slots];
+    int cnt[kQ4Slots];
+#pragma unroll
+    for (int j = 0; j < kQ4Slots; ++j) {
+      int64_t base = e0 + (int64_t)(j * kQ4Threads + tid) * 8;
+      if (full) {
+        cnt[j] = 8;
+        v[j] = ld_v32(x + base);
+      } else {
+        int64_t c = n - base;
+        cnt[j] = c >= 8 ? 8 : (c > 0 ? (int)c : 0);
+        v[j] = load_vec<F32>(x, cnt[j] > 0 ? base : 0, cnt[j]);
+      }
+    }
+    uint32_t packed[kQ4Slots];
+#pragma unroll
+    for (int j = 0; j < kQ4Slots; ++j) {
+      // level 1: absmax over the 64-element block = 8 lanes x 8 elements
+      uint32_t a = 0u;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        uint32_t ab = v[j].w[e] & 0x7fffffffu;
+        a = max(a, ab <= 0x7f800000u ? ab : 0u);  // NaN does not take part
+      }
+      a = max(a, __shfl_xor_sync(kFull, a, 1));
+      a = max(a, __shfl_xor_sync(kFull, a, 2));
+      a = max(a, __shfl_xor_sync(kFull, a, 4));
+      const float s = __fdiv_rn(__uint_as_float(a), 7.0f);
+      uint32_t pk = 0u;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        int c = (full || e < cnt[j]) ? q4_code(__uint_as_float(v[j].w[e]), s) : 0;
+        pk |= ((uint32_t)c & 0xfu) << ((e >> 1) * 8 + ((e & 1) ? 0 : 4));
+      }
+      packed[j] = pk;
+      const int64_t base = e0 + (int64_t)(j * kQ4Threads + tid) * 8;
+      if (cnt[j] == 8) {
+        *reinterpret_cast<uint32_t*>(data + base / 2) = pk;
+      } else if (cnt[j] > 0) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          if (base / 2 + b < nbytes) data[base / 2 + b] = (uint8_t)(pk >> (8 * b));
+      }
+      if ((lane & 7) == 0) s_scale[j * (kQ4Threads / 8) + (tid >> 3)] = cnt[j] > 0 ? s : 0.0f;
+    }
+    __syncthreads();
+    // level 2: super = max(max scale, 1e-8); q = clamp(round(scale / super * 255), 0, 255)
+    const int64_t b0 = sb * kQ4Super;
+    float sc = 0.0f, m = 0.0f;
+    if (tid < kQ4Super) {
+      sc = s_scale[tid];
+      m = sc;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    if (lane == 0) s_red[tid >> 5] = m;
+    __syncthreads();
+    float mx = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kQ4Super / 32; ++w) mx = fmaxf(mx, s_red[w]);
+    const float super = fmaxf(mx, 1e-8f);
+    if (tid < kQ4Super) {
+      float r = roundf(__fmul_rn(__fdiv_rn(sc, super), 255.0f));
+      int q = __float2int_rz(r);  // NaN (inf / inf) -> 0
+      q = min(max(q, 0), 255);
+      if (b0 + tid < nblocks) qscales[b0 + tid] = (uint8_t)q;
+      s_q[tid] = (float)q;
+    }
+    if (tid == 0) sup[sb] = super;
+    if (ROUNDTRIP) {
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kQ4Slots; ++j) {
+        const float rs = __fmul_rn(__fdiv_rn(s_q[j * (kQ4Threads / 8) + (tid >> 3)], 255.0f), super);
+        V32 o;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          o.w[e] = __float_as_uint(__fmul_rn((float)nibble_value(packed[j], e), rs));
+        const int64_t base = e0 + (int64_t)(j * kQ4Threads + tid) * 8;
+        if (cnt[j] > 0) store_vec<F32>(y, base, o, cnt[j]);
+      }
+    }
+    __syncthreads();  // shared arrays are reused by the next super-block
+  }
+}
+
+qat_status launch_q4_quant(const float* x, int64_t n, uint8_t* data, uint8_t* qscales, float* sup,
+                           float* y, cudaStream_t s) {
+  const int64_t nsuper = (n + kQ4SuperElems - 1) / kQ4SuperElems;
+  int64_t cap = (int64_t)device_info().sms * 4;
+  int grid = (int)(nsuper > cap ? cap : (nsuper < 1 ? 1 : nsuper));
+  if (y) k_q4_quant<true><<<grid, kQ4Threads, 0, s>>>(x, n, data, qscales, sup, y);
+  else k_q4_quant<false><<<grid, kQ4Threads, 0, s>>>(x, n, data, qscales, sup, y);
+  count_launch(1);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// two-level 4-bit dequantization: each lane turns 8 codes (one 32-bit word)
+// into 8 floats (one 32-byte store); a warp covers 256 contiguous elements
+// per store instruction
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_q4_dequant(const uint8_t* __restrict__ data,
+                                                    const uint8_t* __restrict__ qscales,
+                                                    const float* __restrict__ sup, int64_t n,
+                                                    float* __restrict__ y) {
+  constexpr int K = 4;  // octets per lane per step
+  const int lane = threadIdx.x & 31;
+  const int64_t noct = (n + 7) / 8;
+  const int64_t nbytes = (n + 1) / 2;
+  const int64_t nsteps = (noct + 32 * K - 1) / (32 * K);
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t st = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); st < nsteps;
+       st += wstride) {
+    uint32_t pk[K];
+    int64_t oct[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      oct[k] = st * (32 * K) + k * 32 + lane;
+      if (oct[k] * 8 + 8 <= n) {
+        pk[k] = __ldg(reinterpret_cast<const uint32_t*>(data) + oct[k]);
+      } else {
+        pk[k] = 0u;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          if (oct[k] * 4 + b < nbytes) pk[k] |= (uint32_t)data[oct[k] * 4 + b] << (8 * b);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int64_t e0 = oct[k] * 8;
+      if (e0 >= n) continue;
+      const int64_t blk = e0 / kQ4Block;
+      const float rs =
+          __fmul_rn(__fdiv_rn((float)__ldg(qscales + blk), 255.0f), __ldg(sup + blk / kQ4Super));
+      V32 o;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        o.w[e] = __float_as_uint(__fmul_rn((float)nibble_value(pk[k], e), rs));
+      int64_t c = n - e0;
+      store_vec<F32>(y, e0, o, c >= 8 ? 8 : (int)c);
+    }
+  }
+}
+
+qat_status launch_q4_dequant(const uint8_t* data, const uint8_t* qscales, const float* sup,
+                             int64_t n, float* y, cudaStream_t s) {
+  const int64_t noct = (n + 7) / 8;
+  const int64_t nsteps = (noct + 127) / 128;
+  int64_t g = (nsteps + 7) / 8;
+  int64_t cap = (int64_t)device_info().sms * 8;
+  int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
+  k_q4_dequant<<<grid, 256, 0, s>>>(data, qscales, sup, n, y);
+  count_launch(1);
+  return launch_status();
+}
+
+}  // namespace qat

@@ -1,0 +1,425 @@
+// kernels_tensor.cu -- per-tensor statistics, integer fake quant with one
+// parameter set or per-unit parameter arrays, and the warp-per-unit fallback.
+//
+// Integer fake quant (optirs-gpu quantization.rs, module docs "Integer
+// quantization", QuantParams::quantize / dequantize / real_min / real_max,
+// fake_quant_int, fake_quant_int_per_channel, fake_quant_backward):
+//   q = clamp(rne(x / scale) + zp, qmin, qmax), y = (q - zp) * scale,
+//   mask = x in [(qmin - zp) * scale, (qmax - zp) * scale].
+// Per-tensor calibration needs the whole tensor's statistics before the first
+// element is quantized, so it is two passes: k_stats_tensor writes one
+// partial per block, k_int_tensor re-reduces the partials in every block (an
+// exact, order-free max/min) and streams the tensor a second time, in reverse
+// tile order so the tail of the first pass is still in L2.
+#include "qat_device.cuh"
+#include "qat_launch.h"
+
+namespace qat {
+
+// ---------------------------------------------------------------------------
+// per-tensor statistics: one uint4 partial {absmax bits, min key, max key,
+// nonfinite} per block
+// ---------------------------------------------------------------------------
+template <typename T, bool MINMAX, bool FULL>
+__device__ __forceinline__ void stats_tile(const void* __restrict__ x, int64_t n, int64_t tile,
+                                           Stats& st, int lane) {
+  constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
+  const int64_t tb = tile * kTile;
+  V32 v[SLOTS];
+  int cnt[SLOTS];
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+    int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+    if (FULL) {
+      cnt[j] = VEC;
+      v[j] = ld_v32(static_cast<const char*>(x) + base * T::BYTES);
+    } else {
+      int64_t c = n - base;
+      cnt[j] = c >= VEC ? VEC : (c > 0 ? (int)c : 0);
+      v[j] = load_vec<T>(x, cnt[j] > 0 ? base : 0, cnt[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e)
+      if (FULL || e < cnt[j]) st.add<MINMAX>(elem_bits<T>(v[j], e));
+  }
+}
+
+template <typename T, bool MINMAX>
+__global__ void __launch_bounds__(512) k_stats_tensor(const void* __restrict__ x, int64_t n,
+                                                      uint4* __restrict__ part) {
+  __shared__ uint32_t red[4 * 16];
+  const int lane = threadIdx.x & 31;
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  const int64_t nfull = n / kTile;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  Stats st;
+  st.init();
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
+       t += wstride) {
+    if (t < nfull) stats_tile<T, MINMAX, true>(x, n, t, st, lane);
+    else stats_tile<T, MINMAX, false>(x, n, t, st, lane);
+  }
+  Stats b = block_reduce_stats<MINMAX>(st, red);
+  if (threadIdx.x == 0) part[blockIdx.x] = make_uint4(b.amax, b.kmin, b.kmax, b.nonfinite);
+}
+
+__global__ void __launch_bounds__(256) k_stats_finalize(const uint4* __restrict__ part, int nparts,
+                                                        float* absmax, float* minv, float* maxv,
+                                                        int32_t* flags) {
+  __shared__ uint32_t red[4 * 8];
+  Stats s = reduce_partials<true>(part, nparts, red);
+  if (threadIdx.x == 0) {
+    if (absmax) absmax[0] = s.absmax_f();
+    if (minv) minv[0] = s.min_f();
+    if (maxv) maxv[0] = s.max_f();
+    flag_or(flags, s.nonfinite ? QAT_FLAG_NONFINITE_INPUT : 0);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// integer fake quant, one parameter set (calibrated from partials or given)
+// ---------------------------------------------------------------------------
+template <typename T, int BITS, bool AFFINE, bool GIVEN, bool FULL>
+__device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, int64_t tile,
+                                         const IntParams& p, void* __restrict__ y,
+                                         void* __restrict__ codes, uint32_t* __restrict__ mask,
+                                         int lane) {
+  constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
+  const int64_t tb = tile * kTile;
+  V32 v[SLOTS];
+  int cnt[SLOTS];
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+    int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+    if (FULL) {
+      cnt[j] = VEC;
+      v[j] = ld_v32(static_cast<const char*>(x) + base * T::BYTES);
+    } else {
+      int64_t c = n - base;
+      cnt[j] = c >= VEC ? VEC : (c > 0 ? (int)c : 0);
+      v[j] = load_vec<T>(x, cnt[j] > 0 ? base : 0, cnt[j]);
+    }
+  }
+  uint32_t mw[SLOTS];
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+    int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+    OutVec<T> ov;
+    CodeVec<BITS, VEC> cv;
+    cv.clear();
+    uint32_t mb = 0u;
+    if (!p.dead) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        int q;
+        float yv;
+        uint32_t m;
+        int_elem<GIVEN>(elem<T>(v[j], e), p, q, yv, m);
+        ov.set(e, yv);
+        if (FULL || e < cnt[j]) cv.set(e, q);
+        mb |= m << e;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) ov.set(e, 0.0f);
+    }
+    if (!FULL) mb &= (cnt[j] >= 32) ? 0xffffffffu : ((1u << cnt[j]) - 1u);
+    if (cnt[j] > 0) {
+      if (y) store_vec<T>(y, base, ov.v, cnt[j]);
+      if (codes) cv.store(codes, base, cnt[j]);
+    }
+    mw[j] = mask_word_of_slot<VEC>(mb, lane);
+  }
+  if (mask) {
+    uint32_t w = gather_tile_word<VEC, SLOTS>(mw, lane);
+    int64_t wi = tile * 32 + lane;
+    if (FULL || wi < (n + 31) / 32) mask[wi] = w;
+  }
+}
+
+template <typename T, int BITS, bool AFFINE, bool GIVEN>
+__global__ void __launch_bounds__(256) k_int_tensor(const void* __restrict__ x, int64_t n,
+                                                    const uint4* __restrict__ part, int nparts,
+                                                    float* scale, int32_t* zp, void* y, void* codes,
+                                                    uint32_t* mask, int32_t* flags) {
+  __shared__ uint32_t red[4 * 8];
+  __shared__ IntParams sp;
+  if (GIVEN) {
+    if (threadIdx.x == 0) {
+      int f = given_params<BITS, AFFINE>(scale[0], zp ? zp[0] : 0, sp);
+      if (blockIdx.x == 0) flag_or(flags, f);
+    }
+  } else {
+    Stats st = reduce_partials<AFFINE>(part, nparts, red);
+    if (threadIdx.x == 0) {
+      int f = calibrate<BITS, AFFINE>(st, sp);
+      if (blockIdx.x == 0) {
+        scale[0] = sp.s;
+        if (zp) zp[0] = sp.zp;
+        flag_or(flags, f);
+      }
+    }
+  }
+  __syncthreads();
+  const IntParams p = sp;
+  const int lane = threadIdx.x & 31;
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  const int64_t nfull = n / kTile;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
+       t += wstride) {
+    // calibrated: reverse order, so the first tiles read are the ones the
+    // statistics pass touched last (still in L2)
+    const int64_t tile = GIVEN ? t : ntiles - 1 - t;
+    if (tile < nfull) int_tile<T, BITS, AFFINE, GIVEN, true>(x, n, tile, p, y, codes, mask, lane);
+    else int_tile<T, BITS, AFFINE, GIVEN, false>(x, n, tile, p, y, codes, mask, lane);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// integer fake quant with per-unit parameter arrays, unit = element / L
+// (given per-row / per-group parameters, and the calibrated fallback for unit
+// lengths the fused kernels do not cover)
+// ---------------------------------------------------------------------------
+template <typename T, int BITS, bool AFFINE, bool GIVEN>
+__global__ void __launch_bounds__(256) k_int_units(const void* __restrict__ x, int64_t n, int64_t L,
+                                                   const float* __restrict__ scale,
+                                                   const int32_t* __restrict__ zp,
+                                                   const uint8_t* __restrict__ dead, void* y,
+                                                   void* codes, uint32_t* mask, int32_t* flags) {
+  constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
+  constexpr int qmin = QRange<BITS, AFFINE>::qmin, qmax = QRange<BITS, AFFINE>::qmax;
+  const int lane = threadIdx.x & 31;
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t tile = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tile < ntiles;
+       tile += wstride) {
+    const int64_t tb = tile * kTile;
+    uint32_t mw[SLOTS];
+    int fl = 0;
+#pragma unroll
+    for (int j = 0; j < SLOTS; ++j) {
+      int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+      int64_t c = n - base;
+      int cnt = c >= VEC ? VEC : (c > 0 ? (int)c : 0);
+      V32 v = load_vec<T>(x, cnt > 0 ? base : 0, cnt);
+      OutVec<T> ov;
+      CodeVec<BITS, VEC> cv;
+      cv.clear();
+      uint32_t mb = 0u;
+      int64_t cur = -1;
+      IntParams p;
+      p.s = 1.0f;
+      p.zp = 0;
+      p.dead = 1;
+      finish_params(p, qmin, qmax);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        int q = 0;
+        float yv = 0.0f;
+        uint32_t m = 0u;
+        if (e < cnt) {
+          int64_t u = (base + e) / L;
+          if (u != cur) {
+            cur = u;
+            if (GIVEN) {
+              fl |= given_params<BITS, AFFINE>(scale[u], zp ? zp[u] : 0, p);
+            } else {
+              p.s = scale[u];
+              p.zp = AFFINE ? zp[u] : 0;
+              p.dead = dead[u];
+              finish_params(p, qmin, qmax);
+            }
+          }
+          if (!p.dead) int_elem<GIVEN>(elem<T>(v, e), p, q, yv, m);
+        }
+        ov.set(e, yv);
+        cv.set(e, q);
+        mb |= m << e;
+      }
+      if (cnt > 0) {
+        if (y) store_vec<T>(y, base, ov.v, cnt);
+        if (codes) cv.store(codes, base, cnt);
+      }
+      mw[j] = mask_word_of_slot<VEC>(mb, lane);
+    }
+    if (mask) {
+      uint32_t w = gather_tile_word<VEC, SLOTS>(mw, lane);
+      int64_t wi = tile * 32 + lane;
+      if (wi < (n + 31) / 32) mask[wi] = w;
+    }
+    warp_flag_or(flags, fl);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// warp-per-unit statistics for any unit length (scalar loads)
+//   MODE 0: absmax / minv / maxv per unit, QAT_FLAG_NONFINITE_INPUT
+//   MODE 1: calibrated int params -> scale, zp, dead (per unit)
+// ---------------------------------------------------------------------------
+template <typename T, int MODE, int BITS, bool AFFINE>
+__global__ void __launch_bounds__(256) k_unit_generic(const void* __restrict__ x, int64_t units,
+                                                      int64_t L, float* absmax, float* minv,
+                                                      float* maxv, float* scale, int32_t* zp,
+                                                      uint8_t* dead, int32_t* flags) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units;
+       u += wstride) {
+    Stats st;
+    st.init();
+    const int64_t off = u * L;
+    for (int64_t i = lane; i < L; i += 32) st.add<true>(load_elem_bits<T>(x, off + i));
+    st.reduce_lanes<true>(32);
+    if (lane == 0) {
+      if (MODE == 0) {
+        if (absmax) absmax[u] = st.absmax_f();
+        if (minv) minv[u] = st.min_f();
+        if (maxv) maxv[u] = st.max_f();
+        flag_or(flags, st.nonfinite ? QAT_FLAG_NONFINITE_INPUT : 0);
+      } else {
+        IntParams p;
+        int f = calibrate<BITS, AFFINE>(st, p);
+        scale[u] = p.s;
+        if (zp) zp[u] = p.zp;
+        dead[u] = (uint8_t)p.dead;
+        flag_or(flags, f);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+int stats_grid(int64_t n) {
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  const int64_t warps_per_block = 16;  // 512 threads
+  int64_t g = (ntiles + warps_per_block - 1) / warps_per_block;
+  int64_t cap = (int64_t)device_info().sms * 2;
+  if (cap > kMaxPartials) cap = kMaxPartials;
+  if (g > cap) g = cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+static int map_grid(int64_t n, int per_sm) {
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  int64_t g = (ntiles + 7) / 8;  // 8 warps per 256-thread block
+  int64_t cap = (int64_t)device_info().sms * per_sm;
+  if (g > cap) g = cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+qat_status launch_stats_tensor(qat_dtype dt, const void* x, int64_t n, bool minmax, void* ws,
+                               int grid, cudaStream_t s) {
+  uint4* part = static_cast<uint4*>(ws);
+  if (dt == QAT_F32) {
+    if (minmax) k_stats_tensor<F32, true><<<grid, 512, 0, s>>>(x, n, part);
+    else k_stats_tensor<F32, false><<<grid, 512, 0, s>>>(x, n, part);
+  } else {
+    if (minmax) k_stats_tensor<BF16, true><<<grid, 512, 0, s>>>(x, n, part);
+    else k_stats_tensor<BF16, false><<<grid, 512, 0, s>>>(x, n, part);
+  }
+  count_launch(1);
+  return launch_status();
+}
+
+qat_status launch_stats_finalize(const void* ws, int nparts, float* absmax, float* minv, float* maxv,
+                                 int32_t* flags, cudaStream_t s) {
+  k_stats_finalize<<<1, 256, 0, s>>>(static_cast<const uint4*>(ws), nparts, absmax, minv, maxv,
+                                     flags);
+  count_launch(1);
+  return launch_status();
+}
+
+template <typename T, int BITS, bool AFFINE>
+static void int_tensor_t(bool given, const void* x, int64_t n, const void* ws, int nparts,
+                         float* scale, int32_t* zp, void* y, void* codes, uint32_t* mask,
+                         int32_t* flags, cudaStream_t s) {
+  const int grid = map_grid(n, 8);
+  const uint4* part = static_cast<const uint4*>(ws);
+  if (given)
+    k_int_tensor<T, BITS, AFFINE, true>
+        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, y, codes, mask, flags);
+  else
+    k_int_tensor<T, BITS, AFFINE, false>
+        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, y, codes, mask, flags);
+}
+
+qat_status launch_int_tensor(qat_dtype dt, int bits, bool affine, bool given, const void* x,
+                             int64_t n, const void* ws, int nparts, float* scale, int32_t* zp,
+                             void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
+#define QAT_IT(T, B, A) int_tensor_t<T, B, A>(given, x, n, ws, nparts, scale, zp, y, codes, mask, flags, s)
+  if (dt == QAT_F32) {
+    if (bits == 8) { if (affine) QAT_IT(F32, 8, true); else QAT_IT(F32, 8, false); }
+    else { if (affine) QAT_IT(F32, 4, true); else QAT_IT(F32, 4, false); }
+  } else {
+    if (bits == 8) { if (affine) QAT_IT(BF16, 8, true); else QAT_IT(BF16, 8, false); }
+    else { if (affine) QAT_IT(BF16, 4, true); else QAT_IT(BF16, 4, false); }
+  }
+#undef QAT_IT
+  count_launch(1);
+  return launch_status();
+}
+
+template <typename T, int BITS, bool AFFINE>
+static void int_units_t(bool given, const void* x, int64_t n, int64_t L, const float* scale,
+                        const int32_t* zp, const uint8_t* dead, void* y, void* codes, uint32_t* mask,
+                        int32_t* flags, cudaStream_t s) {
+  const int grid = map_grid(n, 8);
+  if (given)
+    k_int_units<T, BITS, AFFINE, true>
+        <<<grid, 256, 0, s>>>(x, n, L, scale, zp, dead, y, codes, mask, flags);
+  else
+    k_int_units<T, BITS, AFFINE, false>
+        <<<grid, 256, 0, s>>>(x, n, L, scale, zp, dead, y, codes, mask, flags);
+}
+
+qat_status launch_int_units(qat_dtype dt, int bits, bool affine, bool given, const void* x,
+                            int64_t n, int64_t L, const float* scale, const int32_t* zp,
+                            const uint8_t* dead, void* y, void* codes, uint32_t* mask,
+                            int32_t* flags, cudaStream_t s) {
+#define QAT_IU(T, B, A) int_units_t<T, B, A>(given, x, n, L, scale, zp, dead, y, codes, mask, flags, s)
+  if (dt == QAT_F32) {
+    if (bits == 8) { if (affine) QAT_IU(F32, 8, true); else QAT_IU(F32, 8, false); }
+    else { if (affine) QAT_IU(F32, 4, true); else QAT_IU(F32, 4, false); }
+  } else {
+    if (bits == 8) { if (affine) QAT_IU(BF16, 8, true); else QAT_IU(BF16, 8, false); }
+    else { if (affine) QAT_IU(BF16, 4, true); else QAT_IU(BF16, 4, false); }
+  }
+#undef QAT_IU
+  count_launch(1);
+  return launch_status();
+}
+
+template <typename T>
+static void unit_generic_t(int mode, int bits, bool affine, const void* x, int64_t units, int64_t L,
+                           float* absmax, float* minv, float* maxv, float* scale, int32_t* zp,
+                           uint8_t* dead, int32_t* flags, cudaStream_t s) {
+  int64_t g = (units + 7) / 8;
+  int64_t cap = (int64_t)device_info().sms * 8;
+  int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
+#define QAT_UG(M, B, A) \
+  k_unit_generic<T, M, B, A><<<grid, 256, 0, s>>>(x, units, L, absmax, minv, maxv, scale, zp, dead, flags)
+  if (mode == 0) QAT_UG(0, 8, false);
+  else if (bits == 8) { if (affine) QAT_UG(1, 8, true); else QAT_UG(1, 8, false); }
+  else { if (affine) QAT_UG(1, 4, true); else QAT_UG(1, 4, false); }
+#undef QAT_UG
+}
+
+qat_status launch_unit_generic(qat_dtype dt, int mode, int bits, bool affine, const void* x,
+                               int64_t units, int64_t L, float* absmax, float* minv, float* maxv,
+                               float* scale, int32_t* zp, uint8_t* dead, int32_t* flags,
+                               cudaStream_t s) {
+  if (dt == QAT_F32)
+    unit_generic_t<F32>(mode, bits, affine, x, units, L, absmax, minv, maxv, scale, zp, dead, flags, s);
+  else
+    unit_generic_t<BF16>(mode, bits, affine, x, units, L, absmax, minv, maxv, scale, zp, dead, flags, s);
+  count_launch(1);
+  return launch_status();
+}
+
+}  // namespace qat

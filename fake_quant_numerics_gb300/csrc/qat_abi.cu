@@ -1,0 +1,245 @@
+// qat_abi.cu -- the exported C entry points: argument validation, path
+// selection and kernel launches.  See include/qat.h for the contract.
+#include <atomic>
+#include <cstdint>
+
+#include "qat_device.cuh"
+#include "qat_launch.h"
+
+namespace qat {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int k) { g_launches.fetch_add((uint64_t)k, std::memory_order_relaxed); }
+
+qat_status launch_status() { return cudaGetLastError() == cudaSuccess ? QAT_OK : QAT_ERR_CUDA; }
+
+Dev device_info() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];  // 0 = unknown
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+  Dev d{0};
+  if (dev < kMaxDev) d.sms = cache[dev].load(std::memory_order_relaxed);
+  if (d.sms <= 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      sms = 1;
+    d.sms = sms;
+    if (dev < kMaxDev) cache[dev].store(sms, std::memory_order_relaxed);
+  }
+  return d;
+}
+
+}  // namespace qat
+
+using namespace qat;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// x, y, grad, grad_in: 32-byte vectors; codes, mask, data, qscales, workspace: 16 bytes
+constexpr uintptr_t kAlignVec = 32;
+constexpr uintptr_t kAlignBuf = 16;
+
+bool valid_dtype(qat_dtype d) { return d == QAT_F32 || d == QAT_BF16; }
+
+// number of elements with overflow / sign checks
+bool elems(int64_t rows, int64_t cols, int64_t* n) {
+  if (rows < 0 || cols < 0) return false;
+  if (cols != 0 && rows > (INT64_C(1) << 50) / cols) return false;
+  *n = rows * cols;
+  return true;
+}
+
+size_t ws_bytes_for(int64_t rows, int64_t cols, qat_granularity g, int64_t group) {
+  if (g == QAT_PER_TENSOR) return (size_t)kMaxPartials * sizeof(uint4);
+  int64_t n;
+  if (!elems(rows, cols, &n)) return 0;
+  int64_t units = 0;
+  if (g == QAT_PER_ROW) units = rows;
+  else if (g == QAT_PER_GROUP && group > 0) units = n / group;
+  return (size_t)((units + 15) / 16 * 16);
+}
+
+// Unit length and count of a granularity; false on an invalid combination.
+bool unit_shape(int64_t rows, int64_t cols, qat_granularity g, int64_t group, int64_t* L,
+                int64_t* units) {
+  int64_t n = rows * cols;
+  if (g == QAT_PER_TENSOR) {
+    *L = n;
+    *units = n > 0 ? 1 : 0;
+    return true;
+  }
+  if (g == QAT_PER_ROW) {
+    *L = cols;
+    *units = rows;
+    return true;
+  }
+  if (g == QAT_PER_GROUP) {
+    if (group <= 0 || cols % group != 0) return false;
+    *L = group;
+    *units = n / group;
+    return true;
+  }
+  return false;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qat_status_string(qat_status s) {
+  switch (s) {
+    case QAT_OK: return "ok";
+    case QAT_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case QAT_ERR_DIMENSION_MISMATCH: return "dimension mismatch";
+    case QAT_ERR_UNSUPPORTED: return "unsupported (bit width, dtype, scheme or format)";
+    case QAT_ERR_CUDA: return "CUDA launch failed";
+    case QAT_ERR_MISALIGNED: return "misaligned pointer";
+    case QAT_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+uint64_t qat_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t qat_workspace_bytes(int64_t rows, int64_t cols, qat_granularity g, int64_t group) {
+  return ws_bytes_for(rows, cols, g, group);
+}
+
+qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t cols,
+                          qat_granularity g, int64_t group, float* absmax, float* minv, float* maxv,
+                          int32_t* flags, void* ws, size_t ws_bytes, qat_stream_t stream) {
+  if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
+  int64_t n, L, units;
+  if (!elems(rows, cols, &n)) return QAT_ERR_INVALID_ARGUMENT;
+  if (!unit_shape(rows, cols, g, group, &L, &units)) return QAT_ERR_INVALID_ARGUMENT;
+  if (n == 0) return QAT_OK;
+  if (!x) return QAT_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, kAlignVec) || (absmax && !aligned(absmax, 4)) || (minv && !aligned(minv, 4)) ||
+      (maxv && !aligned(maxv, 4)))
+    return QAT_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (g == QAT_PER_TENSOR) {
+    if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
+    if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+    int grid = stats_grid(n);
+    qat_status st = launch_stats_tensor(dtype, x, n, true, ws, grid, s);
+    if (st) return st;
+    return launch_stats_finalize(ws, grid, absmax, minv, maxv, flags, s);
+  }
+  if (fused_units_supported(dtype, L))
+    return launch_int_fused(dtype, 8, false, true, x, units, L, nullptr, nullptr, absmax, minv, maxv,
+                            nullptr, nullptr, nullptr, flags, s);
+  return launch_unit_generic(dtype, 0, 8, false, x, units, L, absmax, minv, maxv, nullptr, nullptr,
+                             nullptr, flags, s);
+}
+
+qat_status qat_fake_quant_int(const void* x, qat_dtype dtype, int64_t rows, int64_t cols, int bits,
+                              qat_scheme scheme, qat_granularity g, int64_t group, int params_given,
+                              float* scale, int32_t* zp, void* y, void* codes, uint32_t* mask,
+                              int32_t* flags, void* ws, size_t ws_bytes, qat_stream_t stream) {
+  if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
+  if (bits != 8 && bits != 4) return QAT_ERR_UNSUPPORTED;
+  if (scheme != QAT_SYMMETRIC && scheme != QAT_AFFINE) return QAT_ERR_UNSUPPORTED;
+  const bool affine = scheme == QAT_AFFINE;
+  int64_t n, L, units;
+  if (!elems(rows, cols, &n)) return QAT_ERR_INVALID_ARGUMENT;
+  if (!unit_shape(rows, cols, g, group, &L, &units)) return QAT_ERR_INVALID_ARGUMENT;
+  if (n == 0) return QAT_OK;
+  if (!x || !scale) return QAT_ERR_INVALID_ARGUMENT;
+  if (params_given && affine && !zp) return QAT_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, kAlignVec) || (y && !aligned(y, kAlignVec)) ||
+      (codes && !aligned(codes, kAlignBuf)) || (mask && !aligned(mask, kAlignBuf)) ||
+      !aligned(scale, 4) || (zp && !aligned(zp, 4)))
+    return QAT_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (g == QAT_PER_TENSOR) {
+    if (params_given)
+      return launch_int_tensor(dtype, bits, affine, true, x, n, nullptr, 0, scale, zp, y, codes,
+                               mask, flags, s);
+    if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
+    if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+    int grid = stats_grid(n);
+    qat_status st = launch_stats_tensor(dtype, x, n, affine, ws, grid, s);
+    if (st) return st;
+    return launch_int_tensor(dtype, bits, affine, false, x, n, ws, grid, scale, zp, y, codes, mask,
+                             flags, s);
+  }
+  if (params_given)
+    return launch_int_units(dtype, bits, affine, true, x, n, L, scale, zp, nullptr, y, codes, mask,
+                            flags, s);
+  if (fused_units_supported(dtype, L))
+    return launch_int_fused(dtype, bits, affine, false, x, units, L, scale, zp, nullptr, nullptr,
+                            nullptr, y, codes, mask, flags, s);
+  // fallback: calibrate every unit (warp per unit), then the flat map
+  if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
+  if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+  uint8_t* dead = static_cast<uint8_t*>(ws);
+  qat_status st = launch_unit_generic(dtype, 1, bits, affine, x, units, L, nullptr, nullptr, nullptr,
+                                      scale, zp, dead, flags, s);
+  if (st) return st;
+  return launch_int_units(dtype, bits, affine, false, x, n, L, scale, zp, dead, y, codes, mask,
+                          flags, s);
+}
+
+qat_status qat_fake_quant_fp8(const void* x, qat_dtype dtype, int64_t n, qat_fp8_format fmt,
+                              int scale_given, float* scale, void* y, uint8_t* codes,
+                              uint32_t* mask, int32_t* flags, void* ws, size_t ws_bytes,
+                              qat_stream_t stream) {
+  if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
+  if (fmt != QAT_E4M3 && fmt != QAT_E5M2) return QAT_ERR_UNSUPPORTED;
+  if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;
+  if (n == 0) return QAT_OK;
+  if (!x || !y || !scale) return QAT_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, kAlignVec) || !aligned(y, kAlignVec) || (codes && !aligned(codes, kAlignBuf)) ||
+      (mask && !aligned(mask, kAlignBuf)) || !aligned(scale, 4))
+    return QAT_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (scale_given)
+    return launch_fp8_tensor(dtype, fmt, true, x, n, nullptr, 0, scale, y, codes, mask, flags, s);
+  if (!ws || ws_bytes < ws_bytes_for(1, n, QAT_PER_TENSOR, 0)) return QAT_ERR_WORKSPACE;
+  if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+  int grid = stats_grid(n);
+  qat_status st = launch_stats_tensor(dtype, x, n, false, ws, grid, s);
+  if (st) return st;
+  return launch_fp8_tensor(dtype, fmt, false, x, n, ws, grid, scale, y, codes, mask, flags, s);
+}
+
+qat_status qat_ste_backward(const void* grad, qat_dtype dtype, int64_t n, const uint32_t* mask,
+                            void* grad_in, qat_stream_t stream) {
+  if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
+  if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;
+  if (n == 0) return QAT_OK;
+  if (!grad || !mask || !grad_in) return QAT_ERR_INVALID_ARGUMENT;
+  if (!aligned(grad, kAlignVec) || !aligned(grad_in, kAlignVec) || !aligned(mask, kAlignBuf))
+    return QAT_ERR_MISALIGNED;
+  return launch_ste(dtype, grad, n, mask, grad_in, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qat_status qat_quant4_double(const float* x, int64_t n, uint8_t* data, uint8_t* qscales,
+                             float* super_scales, float* y, qat_stream_t stream) {
+  if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;
+  if (n == 0) return QAT_OK;
+  if (!x || !data || !qscales || !super_scales) return QAT_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, kAlignVec) || !aligned(data, kAlignBuf) || !aligned(qscales, kAlignBuf) ||
+      !aligned(super_scales, 4) || (y && !aligned(y, kAlignVec)))
+    return QAT_ERR_MISALIGNED;
+  return launch_q4_quant(x, n, data, qscales, super_scales, y,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+qat_status qat_dequant4_double(const uint8_t* data, const uint8_t* qscales, const float* super_scales,
+                               int64_t n, float* y, qat_stream_t stream) {
+  if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;
+  if (n == 0) return QAT_OK;
+  if (!data || !qscales || !super_scales || !y) return QAT_ERR_INVALID_ARGUMENT;
+  if (!aligned(data, kAlignBuf) || !aligned(qscales, kAlignBuf) || !aligned(super_scales, 4) ||
+      !aligned(y, kAlignVec))
+    return QAT_ERR_MISALIGNED;
+  return launch_q4_dequant(data, qscales, super_scales, n, y,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,430 @@
+// qat_device.cuh -- device-side building blocks shared by the library's kernels.
+//
+// Data movement: every lane moves 32-byte vectors (ld/st .v8.b32, the 256-bit
+// global accesses of sm_100-class GPUs), so a warp instruction covers 1 KiB of
+// contiguous memory.  A "tile" is 1024 consecutive elements handled by one
+// warp: it owns exactly 32 mask words, which a warp writes with one coalesced
+// 128-byte store.
+//
+// Arithmetic: every floating-point operation that decides an output bit uses
+// an explicitly rounded intrinsic (__fdiv_rn, __fmul_rn, __fsub_rn), so the
+// results do not depend on FMA contraction; no flush-to-zero anywhere.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "qat.h"
+
+namespace qat {
+
+constexpr int kTile = 1024;  // elements per warp tile
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr int kMaxPartials = 1024;  // cross-CTA partial statistics slots
+
+// ---------------------------------------------------------------------------
+// element types: 32-byte vectors of VEC elements
+// ---------------------------------------------------------------------------
+struct F32 {
+  static constexpr int VEC = 8;
+  static constexpr int BYTES = 4;
+  static constexpr qat_dtype kDtype = QAT_F32;
+};
+struct BF16 {
+  static constexpr int VEC = 16;
+  static constexpr int BYTES = 2;
+  static constexpr qat_dtype kDtype = QAT_BF16;
+};
+
+struct V32 {
+  uint32_t w[8];
+};
+
+__device__ __forceinline__ V32 ld_v32(const void* p) {
+  V32 v;
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+        "=r"(v.w[6]), "=r"(v.w[7])
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_v32(void* p, const V32& v) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]),
+               "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
+               "r"(v.w[7])
+               : "memory");
+}
+
+// element e of a vector, widened to fp32 bits
+template <typename T>
+__device__ __forceinline__ uint32_t elem_bits(const V32& v, int e);
+template <>
+__device__ __forceinline__ uint32_t elem_bits<F32>(const V32& v, int e) {
+  return v.w[e];
+}
+template <>
+__device__ __forceinline__ uint32_t elem_bits<BF16>(const V32& v, int e) {
+  uint32_t w = v.w[e >> 1];
+  return (e & 1) ? (w & 0xffff0000u) : (w << 16);
+}
+
+template <typename T>
+__device__ __forceinline__ float elem(const V32& v, int e) {
+  return __uint_as_float(elem_bits<T>(v, e));
+}
+
+// scalar element i of a tensor (tails only)
+template <typename T>
+__device__ __forceinline__ uint32_t load_elem_bits(const void* x, int64_t i);
+template <>
+__device__ __forceinline__ uint32_t load_elem_bits<F32>(const void* x, int64_t i) {
+  return static_cast<const uint32_t*>(x)[i];
+}
+template <>
+__device__ __forceinline__ uint32_t load_elem_bits<BF16>(const void* x, int64_t i) {
+  return static_cast<uint32_t>(static_cast<const uint16_t*>(x)[i]) << 16;
+}
+
+// Load the VEC elements starting at element `base`; `cnt` of them exist
+// (cnt == VEC is the fast path; missing elements read as +0).  The tail loop
+// is fully unrolled with predicates so the vector stays in registers.
+template <typename T>
+__device__ __forceinline__ V32 load_vec(const void* x, int64_t base, int cnt) {
+  if (cnt >= T::VEC) return ld_v32(static_cast<const char*>(x) + base * T::BYTES);
+  V32 v;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v.w[j] = 0u;
+#pragma unroll
+  for (int e = 0; e < T::VEC; ++e) {
+    if (e < cnt) {
+      uint32_t b = load_elem_bits<T>(x, base + e);
+      if (T::BYTES == 4) {
+        v.w[e] = b;
+      } else {
+        v.w[e >> 1] |= (e & 1) ? (b & 0xffff0000u) : (b >> 16);
+      }
+    }
+  }
+  return v;
+}
+
+// fp32 -> bf16 bits, round to nearest even (cvt.rn.bf16x2.f32 packs hi, lo)
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Output vector builder: y values (fp32) -> the output dtype's 32 bytes.
+template <typename T>
+struct OutVec;
+template <>
+struct OutVec<F32> {
+  V32 v;
+  __device__ __forceinline__ void set(int e, float y) { v.w[e] = __float_as_uint(y); }
+};
+template <>
+struct OutVec<BF16> {
+  V32 v;
+  float pend;
+  __device__ __forceinline__ void set(int e, float y) {
+    if ((e & 1) == 0) {
+      pend = y;
+    } else {
+      v.w[e >> 1] = pack_bf16x2(pend, y);
+    }
+  }
+};
+
+// Store the first `cnt` elements of an output vector at element `base`.
+template <typename T>
+__device__ __forceinline__ void store_vec(void* y, int64_t base, const V32& v, int cnt) {
+  if (cnt >= T::VEC) {
+    st_v32(static_cast<char*>(y) + base * T::BYTES, v);
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < T::VEC; ++e) {
+    if (e < cnt) {
+      if (T::BYTES == 4) {
+        static_cast<uint32_t*>(y)[base + e] = v.w[e];
+      } else {
+        uint32_t w = v.w[e >> 1];
+        static_cast<uint16_t*>(y)[base + e] = (uint16_t)((e & 1) ? (w >> 16) : (w & 0xffffu));
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// codes: int8 (VEC bytes per lane) or packed int4 (VEC/2 bytes per lane,
+// element 2j in the high nibble of byte j)
+// ---------------------------------------------------------------------------
+template <int BITS, int VEC>
+struct CodeVec {
+  static constexpr int NBYTES = BITS == 8 ? VEC : VEC / 2;
+  static constexpr int NW = (NBYTES + 3) / 4;
+  uint32_t w[NW];
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int j = 0; j < NW; ++j) w[j] = 0u;
+  }
+  // q: the integer code of element e (two's complement, low BITS bits used)
+  __device__ __forceinline__ void set(int e, int q) {
+    if (BITS == 8) {
+      w[e >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << ((e & 3) * 8);
+    } else {
+      int byte = e >> 1;
+      int shift = (byte & 3) * 8 + ((e & 1) ? 0 : 4);
+      w[byte >> 2] |= (static_cast<uint32_t>(q) & 0xfu) << shift;
+    }
+  }
+  // store at element offset `base` (codes buffer byte offset base*BITS/8);
+  // `cnt` elements present
+  __device__ __forceinline__ void store(void* codes, int64_t base, int cnt) const {
+    uint8_t* p = static_cast<uint8_t*>(codes) + (BITS == 8 ? base : base / 2);
+    if (cnt >= VEC) {
+      if (NBYTES == 16) {
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else if (NBYTES == 8) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+      } else {
+        *reinterpret_cast<uint32_t*>(p) = w[0];
+      }
+      return;
+    }
+    const int nb = BITS == 8 ? cnt : (cnt + 1) / 2;
+#pragma unroll
+    for (int b = 0; b < NBYTES; ++b)
+      if (b < nb) p[b] = (uint8_t)(w[b >> 2] >> ((b & 3) * 8));
+  }
+};
+
+// ---------------------------------------------------------------------------
+// mask assembly: per slot a lane holds VEC mask bits; the 32/VEC lanes that
+// share a mask word OR their shifted bits together.  After all slots of a
+// tile, lane L holds tile word L.
+// ---------------------------------------------------------------------------
+template <int VEC>
+__device__ __forceinline__ uint32_t mask_word_of_slot(uint32_t bits, int lane) {
+  constexpr int LPW = 32 / VEC;  // lanes per mask word
+  uint32_t w = bits << ((lane % LPW) * VEC);
+#pragma unroll
+  for (int o = 1; o < LPW; o <<= 1) w |= __shfl_xor_sync(kFull, w, o);
+  return w;
+}
+
+template <int VEC, int SLOTS>
+__device__ __forceinline__ uint32_t gather_tile_word(const uint32_t (&mw)[SLOTS], int lane) {
+  constexpr int LPW = 32 / VEC;
+  uint32_t out = 0u;
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+    uint32_t v = __shfl_sync(kFull, mw[j], (lane % VEC) * LPW);
+    if (lane / VEC == j) out = v;
+  }
+  return out;
+}
+
+// ---------------------------------------------------------------------------
+// statistics on fp32 bit patterns: finite absmax (as bits of |x|), min / max
+// as order-preserving keys (-0 below +0), non-finite detection
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t order_key(uint32_t u) {
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ uint32_t key_to_bits(uint32_t k) {
+  return (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+}
+constexpr uint32_t kKeyPosInf = 0xff800000u;  // order_key(+inf)
+constexpr uint32_t kKeyNegInf = 0x007fffffu;  // order_key(-inf)
+
+struct Stats {
+  uint32_t amax;       // bits of the finite absmax
+  uint32_t kmin;       // key of the finite min
+  uint32_t kmax;       // key of the finite max
+  uint32_t nonfinite;  // 1 if a NaN/Inf was seen
+  __device__ __forceinline__ void init() {
+    amax = 0u;
+    kmin = kKeyPosInf;
+    kmax = kKeyNegInf;
+    nonfinite = 0u;
+  }
+  template <bool MINMAX>
+  __device__ __forceinline__ void add(uint32_t u) {
+    uint32_t a = u & 0x7fffffffu;
+    bool fin = a < 0x7f800000u;
+    amax = max(amax, fin ? a : 0u);
+    nonfinite |= fin ? 0u : 1u;
+    if (MINMAX) {
+      uint32_t k = order_key(u);
+      kmin = min(kmin, fin ? k : kKeyPosInf);
+      kmax = max(kmax, fin ? k : kKeyNegInf);
+    }
+  }
+  template <bool MINMAX>
+  __device__ __forceinline__ void merge(const Stats& o) {
+    amax = max(amax, o.amax);
+    nonfinite |= o.nonfinite;
+    if (MINMAX) {
+      kmin = min(kmin, o.kmin);
+      kmax = max(kmax, o.kmax);
+    }
+  }
+  // reduce over `width` consecutive lanes (a power of two <= 32)
+  template <bool MINMAX>
+  __device__ __forceinline__ void reduce_lanes(int width) {
+    for (int o = 1; o < width; o <<= 1) {
+      amax = max(amax, __shfl_xor_sync(kFull, amax, o));
+      nonfinite |= __shfl_xor_sync(kFull, nonfinite, o);
+      if (MINMAX) {
+        kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+      }
+    }
+  }
+  __device__ __forceinline__ float absmax_f() const { return __uint_as_float(amax); }
+  __device__ __forceinline__ float min_f() const { return __uint_as_float(key_to_bits(kmin)); }
+  __device__ __forceinline__ float max_f() const { return __uint_as_float(key_to_bits(kmax)); }
+};
+
+// Block-wide reduction of Stats (all threads get the result).  `red` needs
+// 4 * (blockDim.x / 32) words of shared memory.
+template <bool MINMAX>
+__device__ __forceinline__ Stats block_reduce_stats(Stats s, uint32_t* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  s.reduce_lanes<MINMAX>(32);
+  __syncthreads();  // red may still be read from a previous use
+  if (lane == 0) {
+    red[4 * warp + 0] = s.amax;
+    red[4 * warp + 1] = s.kmin;
+    red[4 * warp + 2] = s.kmax;
+    red[4 * warp + 3] = s.nonfinite;
+  }
+  __syncthreads();
+  Stats t;
+  t.init();
+  for (int w = 0; w < nw; ++w) {
+    Stats o;
+    o.amax = red[4 * w + 0];
+    o.kmin = red[4 * w + 1];
+    o.kmax = red[4 * w + 2];
+    o.nonfinite = red[4 * w + 3];
+    t.merge<MINMAX>(o);
+  }
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// integer grid parameters of one unit
+// ---------------------------------------------------------------------------
+struct IntParams {
+  float s;         // scale
+  float wlo, whi;  // STE window [(qmin-zp)*s, (qmax-zp)*s]
+  int klo, khi;    // clamp range of k = q - zp
+  int zp;
+  int dead;        // unit outputs are codes 0, y +0, mask 0
+};
+
+template <int BITS, bool AFFINE>
+struct QRange {
+  static constexpr int qmin = AFFINE ? (BITS == 8 ? -128 : -8) : (BITS == 8 ? -127 : -7);
+  static constexpr int qmax = BITS == 8 ? 127 : 7;
+};
+
+__device__ __forceinline__ void finish_params(IntParams& p, int qmin, int qmax) {
+  p.klo = qmin - p.zp;
+  p.khi = qmax - p.zp;
+  p.wlo = __fmul_rn(__int2float_rn(qmin - p.zp), p.s);
+  p.whi = __fmul_rn(__int2float_rn(qmax - p.zp), p.s);
+}
+
+// Calibration (QuantParams::from_absmax / from_minmax).  Returns the flag bit
+// (0, QAT_FLAG_NONFINITE_CALIB or QAT_FLAG_DEGENERATE).
+template <int BITS, bool AFFINE>
+__device__ __forceinline__ int calibrate(const Stats& st, IntParams& p) {
+  constexpr int qmin = QRange<BITS, AFFINE>::qmin, qmax = QRange<BITS, AFFINE>::qmax;
+  int degenerate = 0;
+  p.zp = 0;
+  if (!AFFINE) {
+    float A = st.absmax_f();
+    p.s = __fdiv_rn(A, (float)qmax);
+    degenerate = !(A > 0.0f) || !(p.s > 0.0f) || isinf(p.s);
+  } else {
+    float mn = st.min_f(), mx = st.max_f();
+    float rmin = (mn < 0.0f) ? mn : 0.0f;
+    float rmax = (mx > 0.0f) ? mx : 0.0f;
+    float range = __fsub_rn(rmax, rmin);
+    p.s = __fdiv_rn(range, (float)(qmax - qmin));
+    degenerate = !(range > 0.0f) || !(p.s > 0.0f) || isinf(p.s);
+    if (!degenerate) {
+      float t = __fsub_rn((float)qmin, __fdiv_rn(rmin, p.s));
+      float z = rintf(t);
+      z = fminf(fmaxf(z, (float)qmin), (float)qmax);
+      p.zp = (int)z;
+    }
+  }
+  int flag = st.nonfinite ? QAT_FLAG_NONFINITE_CALIB : (degenerate ? QAT_FLAG_DEGENERATE : 0);
+  p.dead = flag != 0;
+  finish_params(p, qmin, qmax);
+  return flag;
+}
+
+// Given parameters: validity check.
+template <int BITS, bool AFFINE>
+__device__ __forceinline__ int given_params(float s, int zp, IntParams& p) {
+  constexpr int qmin = QRange<BITS, AFFINE>::qmin, qmax = QRange<BITS, AFFINE>::qmax;
+  p.s = s;
+  p.zp = AFFINE ? zp : 0;
+  int bad = !(s > 0.0f) || isinf(s) || p.zp < qmin || p.zp > qmax;
+  p.dead = bad;
+  finish_params(p, qmin, qmax);
+  return bad ? QAT_FLAG_BAD_PARAMS : 0;
+}
+
+// One element: q = clamp(rne(x/s) + zp), y = (q - zp) * s, mask bit.
+// NAN_TO_ZERO: a NaN quotient gives code 0 (given parameters only; a
+// calibrated unit containing NaN is dead).
+template <bool NAN_TO_ZERO>
+__device__ __forceinline__ void int_elem(float x, const IntParams& p, int& q, float& y,
+                                         uint32_t& m) {
+  float r = __fdiv_rn(x, p.s);
+  int k = __float2int_rn(r);  // saturating; NaN -> 0
+  k = min(max(k, p.klo), p.khi);
+  if (NAN_TO_ZERO && isnan(r)) k = -p.zp;
+  q = k + p.zp;
+  y = __fmul_rn(__int2float_rn(k), p.s);
+  m = (x >= p.wlo) && (x <= p.whi);
+}
+
+__device__ __forceinline__ void flag_or(int32_t* flags, int bits) {
+  if (flags && bits) atomicOr(flags, bits);
+}
+
+// Warp-aggregated flag update: one atomic per warp.
+__device__ __forceinline__ void warp_flag_or(int32_t* flags, int bits) {
+  int all = __reduce_or_sync(kFull, bits);
+  if (flags && all && (threadIdx.x & 31) == 0) atomicOr(flags, all);
+}
+
+// Read the cross-CTA partials written by the per-tensor statistics kernel
+// and reduce them (every thread of the block gets the result).
+template <bool MINMAX>
+__device__ __forceinline__ Stats reduce_partials(const uint4* part, int nparts, uint32_t* red) {
+  Stats s;
+  s.init();
+  for (int i = threadIdx.x; i < nparts; i += blockDim.x) {
+    uint4 p = part[i];
+    Stats o;
+    o.amax = p.x;
+    o.kmin = p.y;
+    o.kmax = p.z;
+    o.nonfinite = p.w;
+    s.merge<MINMAX>(o);
+  }
+  return block_reduce_stats<MINMAX>(s, red);
+}
+
+}  // namespace qat

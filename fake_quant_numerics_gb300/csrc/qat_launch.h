@@ -1,0 +1,71 @@
+// qat_launch.h -- host-side launchers shared by the library's translation
+// units (internal; not part of the C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "qat.h"
+
+namespace qat {
+
+struct Dev {
+  int sms;  // streaming multiprocessors of the current device
+};
+Dev device_info();           // cached per device
+void count_launch(int k);    // diagnostic launch counter
+qat_status launch_status();  // QAT_OK or QAT_ERR_CUDA after a <<<>>> launch
+
+// Grid for a per-tensor statistics pass (<= kMaxPartials blocks).
+int stats_grid(int64_t n);
+
+// per-tensor statistics -> workspace partials (uint4 per block)
+qat_status launch_stats_tensor(qat_dtype dt, const void* x, int64_t n, bool minmax, void* ws,
+                               int grid, cudaStream_t s);
+// partials -> absmax / min / max (one thread block)
+qat_status launch_stats_finalize(const void* ws, int nparts, float* absmax, float* minv, float* maxv,
+                                 int32_t* flags, cudaStream_t s);
+
+// integer fake quant, one parameter set for the whole tensor
+qat_status launch_int_tensor(qat_dtype dt, int bits, bool affine, bool given, const void* x,
+                             int64_t n, const void* ws, int nparts, float* scale, int32_t* zp,
+                             void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s);
+
+// integer fake quant with per-unit parameter arrays (unit = i / L)
+qat_status launch_int_units(qat_dtype dt, int bits, bool affine, bool given, const void* x,
+                            int64_t n, int64_t L, const float* scale, const int32_t* zp,
+                            const uint8_t* dead, void* y, void* codes, uint32_t* mask,
+                            int32_t* flags, cudaStream_t s);
+
+// warp-per-unit statistics / calibration for any unit length (fallback)
+// mode 0: absmax/minv/maxv outputs; mode 1: int params -> scale, zp, dead
+qat_status launch_unit_generic(qat_dtype dt, int mode, int bits, bool affine, const void* x,
+                               int64_t units, int64_t L, float* absmax, float* minv, float* maxv,
+                               float* scale, int32_t* zp, uint8_t* dead, int32_t* flags,
+                               cudaStream_t s);
+
+// fused single-pass per-unit calibration + fake quant (or statistics only)
+// for units of L elements.  Returns QAT_ERR_UNSUPPORTED when L does not fit
+// either fused kernel (the caller then takes the fallback).
+bool fused_units_supported(qat_dtype dt, int64_t L);
+qat_status launch_int_fused(qat_dtype dt, int bits, bool affine, bool stats_only, const void* x,
+                            int64_t units, int64_t L, float* scale, int32_t* zp, float* absmax,
+                            float* minv, float* maxv, void* y, void* codes, uint32_t* mask,
+                            int32_t* flags, cudaStream_t s);
+
+// FP8
+qat_status launch_fp8_tensor(qat_dtype dt, qat_fp8_format fmt, bool given, const void* x, int64_t n,
+                             const void* ws, int nparts, float* scale, void* y, uint8_t* codes,
+                             uint32_t* mask, int32_t* flags, cudaStream_t s);
+
+// STE backward
+qat_status launch_ste(qat_dtype dt, const void* g, int64_t n, const uint32_t* mask, void* dx,
+                      cudaStream_t s);
+
+// two-level 4-bit
+qat_status launch_q4_quant(const float* x, int64_t n, uint8_t* data, uint8_t* qscales, float* sup,
+                           float* y, cudaStream_t s);
+qat_status launch_q4_dequant(const uint8_t* data, const uint8_t* qscales, const float* sup,
+                             int64_t n, float* y, cudaStream_t s);
+
+}  // namespace qat

@@ -1,0 +1,213 @@
+/*
+ * qat.h -- C ABI of the GB300 fake-quant library (libqat.so).
+ *
+ * Quantization-aware-training fake quantization and its straight-through
+ * estimator, plus the QLoRA two-level 4-bit block format, as CUDA kernels for
+ * sm_103a.  Sources of the operations (cited by page and item):
+ *
+ *   [QAT] optirs-gpu 0.3.2, src/optirs_gpu/quantization.rs -- module docs
+ *         ("What fake quantization means", "Integer quantization",
+ *         "fp8 quantization", "Straight-through estimator"), IntDtype::q_range,
+ *         QuantParams::{from_minmax, from_absmax, quantize, dequantize,
+ *         real_min, real_max}, finite_min_max, fake_quant_int,
+ *         per_channel_params, fake_quant_int_per_channel,
+ *         fp8_quantize_magnitude, fake_quant_fp8, fake_quant_backward.
+ *   [DQ]  aprender-train 0.32.0, src/entrenar/quant/double_quant.rs --
+ *         quantize_4bit_double, reconstruct_scales, dequantize_4bit_double,
+ *         DoubleQuantized4Bit.
+ *   [MAR] ferrum-kernels 0.8.0, src/marlin_repack.rs -- per-channel E4M3
+ *         scale absmax / 448, a zero scale encodes as byte 0.
+ *   [EDU] cs349e 05_quantization_basics.py, demo 3 -- groups run along the
+ *         last dimension.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is a DEVICE pointer.  x, y, grad, grad_in and
+ *   y_roundtrip must be 32-byte aligned (each lane moves 32-byte vectors);
+ *   codes, mask, data, qscales and workspace 16-byte aligned; per-unit arrays
+ *   (scale, zero_point, absmax, minv, maxv, super_scales) 4-byte aligned.
+ *   A violation returns QAT_ERR_MISALIGNED.  dev_flags is an int32.
+ * - Tensors are row-major and contiguous; n = rows * cols.  A "unit" is the
+ *   whole tensor (per tensor), one row of `cols` elements (per row, the axis-0
+ *   channel of [QAT] per_channel_params) or one run of `group` consecutive
+ *   elements of a row (per group; `group` must divide `cols`).
+ * - Outputs y have the dtype of x; they are computed in fp32 and rounded once
+ *   (round to nearest even) to bf16 when x is bf16.
+ * - mask: uint32 words, bit (i % 32) of word (i / 32) is element i; bits past
+ *   n in the last word are 0.  Length ceil(n / 32) words.
+ * - 4-bit codes are packed two per byte: element 2j in the HIGH nibble and
+ *   element 2j+1 in the LOW nibble of byte j, two's complement (the nibble
+ *   order of [DQ] dequantize_4bit_double); an odd tail leaves the last low
+ *   nibble 0.  Length ceil(n / 2) bytes.  8-bit codes are int8[n].
+ * - Ownership: the caller owns every buffer.  The library allocates nothing,
+ *   keeps no state between calls (apart from a diagnostic launch counter and a
+ *   per-device SM-count cache) and is re-entrant.  All work is enqueued on
+ *   `stream` and is asynchronous with respect to the host; results are valid
+ *   once the stream has reached the end of the call.
+ * - Synchronous errors (returned before anything is enqueued): a required
+ *   pointer that is NULL or a negative size -> QAT_ERR_INVALID_ARGUMENT;
+ *   a bit width other than 4 or 8, an unknown dtype / scheme / format ->
+ *   QAT_ERR_UNSUPPORTED ([QAT] IntDtype::from_bits); a misaligned pointer ->
+ *   QAT_ERR_MISALIGNED; a workspace smaller than qat_workspace_bytes() where
+ *   the call needs one -> QAT_ERR_WORKSPACE; a failed CUDA launch ->
+ *   QAT_ERR_CUDA.  n == 0 is a no-op that returns QAT_OK.
+ * - Data errors are only known on the device.  Kernels OR the QAT_FLAG_* bits
+ *   into *dev_flags (nullable; the caller zeroes it and reads it after the
+ *   stream has passed the call).  A unit whose calibration fails, or whose
+ *   given parameters are invalid, gets codes 0, y = +0 and mask bits 0; its
+ *   scale is still written.
+ */
+#ifndef QAT_H
+#define QAT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t / CUstream handle; NULL is the legacy default stream. */
+typedef struct CUstream_st* qat_stream_t;
+
+typedef enum {
+  QAT_OK = 0,
+  QAT_ERR_INVALID_ARGUMENT = 1, /* NULL required pointer, negative size, bad granularity/group */
+  QAT_ERR_DIMENSION_MISMATCH = 2,
+  QAT_ERR_UNSUPPORTED = 3,      /* bits not in {4, 8}; unknown dtype, scheme or format */
+  QAT_ERR_CUDA = 4,             /* a CUDA launch or query failed */
+  QAT_ERR_MISALIGNED = 5,       /* a pointer violates the alignment rule above */
+  QAT_ERR_WORKSPACE = 6         /* workspace NULL or smaller than qat_workspace_bytes() */
+} qat_status;
+
+/* Device-side data flags (bitwise OR into *dev_flags). */
+#define QAT_FLAG_NONFINITE_CALIB 1 /* NaN/Inf inside a unit being calibrated ([QAT] finite_min_max) */
+#define QAT_FLAG_DEGENERATE 2      /* absmax == 0, zero range, or a scale that is 0 or inf
+                                      ([QAT] from_absmax / from_minmax) */
+#define QAT_FLAG_BAD_PARAMS 4      /* given scale not finite and > 0 (int) or not finite and >= 0
+                                      (fp8), or given zero point outside [qmin, qmax] */
+#define QAT_FLAG_NONFINITE_INPUT 8 /* NaN/Inf seen by an FP8 amax or by qat_amax_stats; informational */
+
+typedef enum { QAT_F32 = 0, QAT_BF16 = 1 } qat_dtype;
+typedef enum { QAT_SYMMETRIC = 0, QAT_AFFINE = 1 } qat_scheme;
+typedef enum { QAT_PER_TENSOR = 0, QAT_PER_ROW = 1, QAT_PER_GROUP = 2 } qat_granularity;
+typedef enum { QAT_E4M3 = 0, QAT_E5M2 = 1 } qat_fp8_format;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* qat_status_string(qat_status status);
+
+/*
+ * Bytes of device workspace a call may need: per tensor, the cross-block
+ * partial statistics (16 KiB); per row / per group, one byte per unit
+ * (rounded up to 16), used only by the fallback for unit lengths the fused
+ * single-pass kernels do not cover.  The workspace is scratch: its contents on
+ * entry do not matter and are overwritten.  Two calls that use the same
+ * workspace must be ordered on one stream.
+ */
+size_t qat_workspace_bytes(int64_t rows, int64_t cols, qat_granularity granularity, int64_t group);
+
+/*
+ * Scale statistics of every unit ([QAT] finite_min_max; symmetric_from_absmax;
+ * [MAR] absmax per channel): absmax = max |x|, minv / maxv = min / max, all
+ * over the FINITE elements of the unit, with -0 ordered below +0.  A unit
+ * without finite elements gives absmax 0, minv +inf, maxv -inf.  Outputs are
+ * float[units], each nullable.  Any NaN/Inf sets QAT_FLAG_NONFINITE_INPUT.
+ * workspace: qat_workspace_bytes(rows, cols, granularity, group) bytes
+ * (per tensor only).
+ */
+qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t cols,
+                          qat_granularity granularity, int64_t group, float* absmax, float* minv,
+                          float* maxv, int32_t* dev_flags, void* workspace, size_t workspace_bytes,
+                          qat_stream_t stream);
+
+/*
+ * Integer fake quantization ([QAT] module docs "Integer quantization",
+ * QuantParams::quantize / dequantize, fake_quant_int,
+ * fake_quant_int_per_channel) fused with the STE window mask
+ * ([QAT] real_min / real_max, fake_quant_backward).
+ *
+ *   bits 8 or 4; symmetric: [qmin,qmax] = [-127,127] / [-7,7], zp = 0;
+ *   affine: [-128,127] / [-8,7].
+ *   params_given == 0: calibrate every unit.  symmetric: scale = absmax / qmax;
+ *     affine: rmin = min(min,0), rmax = max(max,0),
+ *     scale = (rmax - rmin) / (qmax - qmin), zp = clamp(rne(qmin - rmin/scale)).
+ *     scale[u] (and zero_point[u] if non-NULL) are written.
+ *   params_given == 1: scale[u], zero_point[u] are read (zero_point may be
+ *     NULL for symmetric).
+ *   q = clamp(rne(x / scale) + zp, qmin, qmax)   (documented form: zp added
+ *     after rounding);  y = (q - zp) * scale;
+ *   mask bit = (x >= (qmin - zp) * scale) && (x <= (qmax - zp) * scale).
+ *   With given parameters a NaN input gets code 0 and +-Inf the clamp ends;
+ *   both get mask 0.
+ * y, codes, mask are each nullable.  scale / zero_point have one entry per
+ * unit.  workspace: qat_workspace_bytes(...) bytes.
+ */
+qat_status qat_fake_quant_int(const void* x, qat_dtype dtype, int64_t rows, int64_t cols, int bits,
+                              qat_scheme scheme, qat_granularity granularity, int64_t group,
+                              int params_given, float* scale, int32_t* zero_point, void* y,
+                              void* codes, uint32_t* mask, int32_t* dev_flags, void* workspace,
+                              size_t workspace_bytes, qat_stream_t stream);
+
+/*
+ * Per-tensor amax-scaled FP8 fake quantization ([QAT] fake_quant_fp8 /
+ * fp8_quantize_magnitude; scale as in [MAR]).
+ *   scale_given == 0: s = (max |x| over finite x) / fmt_max, written to *scale
+ *     (fmt_max = 448 for E4M3, 57344 for E5M2); NaN/Inf in x set
+ *     QAT_FLAG_NONFINITE_INPUT but are not an error.
+ *   scale_given == 1: s = *scale (s = 1 gives the unscaled cast).
+ *   t = x / s;  c = saturating round-to-nearest-even cast of t to the format
+ *   (NaN -> NaN, +-Inf -> +-fmt_max, signed zero kept);  y = c * s;
+ *   codes[i] = FP8 encoding of c (NaN encoded 0x7F);
+ *   mask bit = |x| <= fmt_max * s (NaN -> 0).
+ *   s == 0: non-NaN elements get code 0x00 and y = +0 (a zero scale encodes as
+ *   byte 0); NaN stays NaN.  A given s that is negative, NaN or inf sets
+ *   QAT_FLAG_BAD_PARAMS.
+ * y is required; codes and mask are nullable.  scale: one device float.
+ * workspace: qat_workspace_bytes(1, n, QAT_PER_TENSOR, 0) bytes when
+ * scale_given == 0.
+ */
+qat_status qat_fake_quant_fp8(const void* x, qat_dtype dtype, int64_t n, qat_fp8_format format,
+                              int scale_given, float* scale, void* y, uint8_t* codes,
+                              uint32_t* mask, int32_t* dev_flags, void* workspace,
+                              size_t workspace_bytes, qat_stream_t stream);
+
+/*
+ * Straight-through-estimator backward ([QAT] fake_quant_backward) with the
+ * window precomputed as the mask of a forward call: grad_in[i] = grad[i]
+ * (bit copy) where the mask bit is set, +0 elsewhere.  grad and grad_in have
+ * dtype `dtype` and n elements; mask has ceil(n / 32) words.
+ */
+qat_status qat_ste_backward(const void* grad, qat_dtype dtype, int64_t n, const uint32_t* mask,
+                            void* grad_in, qat_stream_t stream);
+
+/*
+ * Two-level 4-bit quantization ([DQ] quantize_4bit_double).
+ *   Level 1, per 64-element block (the last one may be short):
+ *     scale = (max |x| over the block) / 7, code = clamp(round(x / scale), -8, 7)
+ *     with round half away from zero; a zero scale gives code 0; NaN -> 0.
+ *   Level 2, per 256 block scales (the last group may be short):
+ *     super = max(max scale, 1e-8), qscale = clamp(round(scale / super * 255), 0, 255).
+ *   data: ceil(n/2) bytes of packed codes; qscales: ceil(n/64) bytes;
+ *   super_scales: ceil(ceil(n/64) / 256) floats.
+ *   y_roundtrip (nullable): n floats receiving dequantize_4bit_double of the
+ *   result, produced in the same pass.
+ */
+qat_status qat_quant4_double(const float* x, int64_t n, uint8_t* data, uint8_t* qscales,
+                             float* super_scales, float* y_roundtrip, qat_stream_t stream);
+
+/*
+ * Dequantization of the two-level 4-bit format ([DQ] reconstruct_scales,
+ * dequantize_4bit_double): scale = f32(qscale) / 255 * super (two roundings,
+ * in that order), y = f32(code) * scale.
+ */
+qat_status qat_dequant4_double(const uint8_t* data, const uint8_t* qscales,
+                               const float* super_scales, int64_t n, float* y, qat_stream_t stream);
+
+/* Number of kernels this library has launched in this process (diagnostic). */
+uint64_t qat_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QAT_H */
