@@ -1,0 +1,539 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the fake-quant hot path on GB300.
+
+One step runs every operation of the path once, each on its own synthetic
+workload at full size (all resident in HBM):
+
+  w1  per-tensor symmetric int8 fake quant + STE backward, fp32 [1,048,576]
+  w2  per-row affine int8 and per-row symmetric int4 fake quant, fp32 [4096, 4096]
+  w3  per-tensor amax-scaled FP8 fake quant, E4M3 and E5M2, bf16 [8192, 8192]
+  w4  per-group (128) symmetric int4 fake quant + STE backward, bf16 [14336, 4096]
+  w5  two-level 4-bit quantize + dequantize round trip, fp32 [268,435,456]
+
+The metric is algorithmic bytes moved per second (each input read once per
+dependent pass, each output written once; per-tensor calibration needs two
+reads of x), i.e. GB/s, with Gelem/s and the fraction of the measured HBM
+copy bandwidth beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same suite on its own GPU (the
+path shards into independent units, so there is no data-path collective);
+value = bytes of all ranks / max time over ranks.  --impl reference times
+the CPU oracle on a bounded sample of the same workloads (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fake-quant fwd+STE-bwd GB/s and Gelem/s per format, % of GB300 HBM peak"
+WORKLOAD = ("qat fake-quant suite: w1 int8 per-tensor fwd+STE fp32[1048576]; "
+            "w2 per-row affine-int8 + sym-int4 fp32[4096x4096]; "
+            "w3 fp8 e4m3+e5m2 per-tensor amax bf16[8192x8192]; "
+            "w4 per-group-128 sym-int4 fwd+STE bf16[14336x4096]; "
+            "w5 QLoRA double-quant round trip fp32[268435456]")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (per element unless stated)
+# ---------------------------------------------------------------------------
+def workload_bytes(n1=1 << 20, r2=4096, c2=4096, n3=8192 * 8192, r4=14336, c4=4096,
+                   n5=268_435_456):
+    """(name, elements, algorithmic bytes, launches) of every call of one step.
+
+    Per element: per-tensor calibration reads x twice (statistics, then the
+    map); y has the dtype of x; masks are 1 bit; int8 codes 1 byte, int4 codes
+    half a byte; per-unit scales (and zero points) 4 bytes each; the 4-bit
+    format stores half a byte per element, one byte per 64-element block and
+    4 bytes per 256 blocks."""
+    n2, n4 = r2 * c2, r4 * c4
+    nb5 = (n5 + 63) // 64
+    ns5 = (nb5 + 255) // 256
+    m = lambda n: (n + 31) // 32 * 4  # noqa: E731
+    return [
+        ("w1_int8_tensor_fwd", n1, n1 * (4 + 4 + 4) + m(n1) + 4, 2),
+        ("w1_ste_bwd", n1, n1 * (4 + 4) + m(n1), 1),
+        ("w2_affine_int8_row", n2, n2 * (4 + 1 + 4) + m(n2) + r2 * 8, 1),
+        ("w2_sym_int4_row", n2, n2 * 4 + (n2 + 1) // 2 + n2 * 4 + m(n2) + r2 * 4, 1),
+        ("w3_fp8_e4m3_tensor", n3, n3 * (2 + 2 + 2) + m(n3) + 4, 2),
+        ("w3_fp8_e5m2_tensor", n3, n3 * (2 + 2 + 2) + m(n3) + 4, 2),
+        ("w4_int4_group_fwd", n4, n4 * 2 + (n4 + 1) // 2 + n4 * 2 + m(n4) + (n4 // 128) * 4, 1),
+        ("w4_ste_bwd", n4, n4 * (2 + 2) + m(n4), 1),
+        ("w5_quant4_double", n5, n5 * 4 + (n5 + 1) // 2 + nb5 + ns5 * 4, 1),
+        ("w5_dequant4_double", n5, (n5 + 1) // 2 + nb5 + ns5 * 4 + n5 * 4, 1),
+    ]
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (torchrun), kept free of CUDA so they run on gloo
+# ---------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def reduce_max_sum(seconds: float, units: float):
+    """(max seconds over ranks, sum of units over ranks); identity without a process group."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return seconds, units
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        def parse(rows):
+            sm, mx, reasons = [], [], set()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for _, r in rows:
+                try:
+                    sm.append(float(r[2]))
+                    mx.append(float(r[3]))
+                except (ValueError, IndexError):
+                    continue
+                for k, name in enumerate(names):
+                    if len(r) > 6 + k and r[6 + k].lower().startswith("active"):
+                        reasons.add(name)
+            return sm, mx, reasons
+
+        inside = [r for r in self.rows if t0 <= r[0] <= t1]
+        window = "timed"
+        if len(inside) < 3:
+            inside, window = self.rows, "run"
+        sm, mx, reasons = parse(inside)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "unavailable"}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# the GPU suite
+# ---------------------------------------------------------------------------
+class Suite:
+    """All workloads resident on one GPU, outputs preallocated; step() issues
+    every call of the path once through the C ABI binding."""
+
+    def __init__(self, dev, fq, inputs):
+        self.fq = fq
+        f = torch.float32
+        x1, g1, w2, a3, w4, g4, x5 = inputs
+        self.inputs = [t.to(dev) for t in inputs]
+        self.x1, self.g1, self.w2, self.a3, self.w4, self.g4, self.x5 = self.inputs
+        e = lambda n, dt=torch.uint8: torch.empty(n, dtype=dt, device=dev)  # noqa: E731
+        n1, n2, n3, n4, n5 = x1.numel(), w2.numel(), a3.numel(), w4.numel(), x5.numel()
+        self.ws = e(16 * 1024 * 2)
+        self.flags = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.o = dict(
+            s1=e(1, f), y1=e(n1, f), m1=e((n1 + 31) // 32, torch.int32), dx1=e(n1, f),
+            s2a=e(4096, f), z2a=e(4096, torch.int32), y2a=e(n2, f), c2a=e(n2, torch.int8),
+            m2a=e(n2 // 32, torch.int32),
+            s2b=e(4096, f), y2b=e(n2, f), c2b=e(n2 // 2), m2b=e(n2 // 32, torch.int32),
+            s3=e(2, f), y3a=e(n3, torch.bfloat16), m3a=e(n3 // 32, torch.int32),
+            y3b=e(n3, torch.bfloat16), m3b=e(n3 // 32, torch.int32),
+            s4=e(n4 // 128, f), y4=e(n4, torch.bfloat16), c4=e(n4 // 2), m4=e(n4 // 32, torch.int32),
+            dx4=e(n4, torch.bfloat16),
+            d5=e(n5 // 2), q5=e((n5 + 63) // 64), u5=e(((n5 + 63) // 64 + 255) // 256, f),
+            y5=e(n5, f),
+        )
+        self.n = (n1, n2, n3, n4, n5)
+
+    def calls(self):
+        fq, o, ws, fl = self.fq, self.o, self.ws, self.flags
+        n1, n2, n3, n4, n5 = self.n
+        return [
+            lambda: fq.qat_fake_quant_int(self.x1, 1, n1, 8, 0, 0, 0, False, o["s1"], None, o["y1"],
+                                          None, o["m1"], fl, ws),
+            lambda: fq.qat_ste_backward(self.g1, n1, o["m1"], o["dx1"]),
+            lambda: fq.qat_fake_quant_int(self.w2, 4096, 4096, 8, 1, 1, 0, False, o["s2a"], o["z2a"],
+                                          o["y2a"], o["c2a"], o["m2a"], fl, ws),
+            lambda: fq.qat_fake_quant_int(self.w2, 4096, 4096, 4, 0, 1, 0, False, o["s2b"], None,
+                                          o["y2b"], o["c2b"], o["m2b"], fl, ws),
+            lambda: fq.qat_fake_quant_fp8(self.a3, n3, 0, False, o["s3"][0:1], o["y3a"], None,
+                                          o["m3a"], fl, ws),
+            lambda: fq.qat_fake_quant_fp8(self.a3, n3, 1, False, o["s3"][1:2], o["y3b"], None,
+                                          o["m3b"], fl, ws),
+            lambda: fq.qat_fake_quant_int(self.w4, 14336, 4096, 4, 0, 2, 128, False, o["s4"], None,
+                                          o["y4"], o["c4"], o["m4"], fl, ws),
+            lambda: fq.qat_ste_backward(self.g4, n4, o["m4"], o["dx4"]),
+            lambda: fq.qat_quant4_double(self.x5, n5, o["d5"], o["q5"], o["u5"], None),
+            lambda: fq.qat_dequant4_double(o["d5"], o["q5"], o["u5"], n5, o["y5"]),
+        ]
+
+    def outputs_for_host(self):
+        o = self.o
+        return [o[k] for k in ("y1", "m1", "dx1", "s1", "s2a", "z2a", "y2a", "c2a", "m2a", "s2b", "y2b",
+                               "c2b", "m2b", "s3", "y3a", "m3a", "y3b", "m3b", "s4", "y4", "c4", "m4",
+                               "dx4", "d5", "q5", "u5", "y5")]
+
+
+def make_inputs():
+    from fake_quant_numerics_gb300 import workloads as W
+
+    x1, g1 = W.cfg1()
+    w2 = W.cfg2()
+    a3 = W.cfg3()
+    w4, g4 = W.cfg4()
+    x5 = W.cfg5()
+    return [x1, g1, w2, a3, w4, g4, x5]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel: str, source: str):
+    """DRAM bytes per launch of `kernel` at full size from the committed ncu
+    summary, or None when the kernel's source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(os.path.join(ROOT, "fake_quant_numerics_gb300", "csrc", source), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and parts[0] == kernel and parts[1] == sha:
+                    return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+KERNEL_OF_CALL = {
+    "w5_quant4_double": ("k_q4_quant", "kernels_misc.cu"),
+    "w5_dequant4_double": ("k_q4_dequant", "kernels_misc.cu"),
+    "w4_int4_group_fwd": ("k_int_groups", "kernels_fused.cu"),
+    "w4_ste_bwd": ("k_ste", "kernels_misc.cu"),
+    "w2_affine_int8_row": ("k_int_rows", "kernels_fused.cu"),
+    "w2_sym_int4_row": ("k_int_rows", "kernels_fused.cu"),
+    "w1_ste_bwd": ("k_ste", "kernels_misc.cu"),
+}
+
+
+def run_ours(args, rank, world, local):
+    import fake_quant_numerics_gb300 as fq
+
+    fq.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inputs = make_inputs()
+    suite = Suite(dev, fq, inputs)
+    calls = suite.calls()
+    wb = workload_bytes()
+    step_bytes = sum(b for _, _, b, _ in wb)
+    step_elems = sum(e for _, e, _, _ in wb)
+    stream = torch.cuda.current_stream()
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    for _ in range(args.warmup):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, events around every call (same stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+          for _ in range(args.steps)]
+    l0 = fq.qat_kernel_launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        for i, c in enumerate(calls):
+            c()
+            ev[k][i + 1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall1 = time.time()
+    launches = fq.qat_kernel_launch_count() - l0
+    local_s = start.elapsed_time(end) / 1e3
+    max_s, total_bytes = reduce_max_sum(local_s, step_bytes * args.steps)
+    _, total_elems = reduce_max_sum(local_s, step_elems * args.steps)
+    per_call_ms = np.array([[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(len(calls))]
+                            for k in range(args.steps)])
+    mean_ms = per_call_ms.mean(axis=0)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    e2e = run_e2e(args, suite, calls, step_bytes)
+
+    peak, peak_kind = measured_peak()
+    per_wl = {}
+    for (name, elems, b, nl), ms in zip(wb, mean_ms):
+        per_wl[name] = {"ms": round(float(ms), 5), "GB_s": round(b / (ms * 1e-3) / 1e9, 1),
+                        "Gelem_s": round(elems / (ms * 1e-3) / 1e9, 2),
+                        "frac_of_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peak, 4),
+                        "launches": nl, "bytes": b}
+    # dominant kernel: the single-launch call with the largest time
+    dom = max((i for i, w in enumerate(wb) if w[3] == 1), key=lambda i: mean_ms[i])
+    dname, _, dbytes, _ = wb[dom]
+    achieved = dbytes / (mean_ms[dom] * 1e-3) / 1e9
+    kern, src = KERNEL_OF_CALL.get(dname, (dname, ""))
+    traffic = recorded_traffic(kern, src) if src else None
+    value = total_bytes / max_s / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_s / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32/bf16 in, fp32 arithmetic",
+        "data": "synthetic (seeded numpy generators, distributions of the five workloads)",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world} (independent units)",
+                   "l2": "inputs larger than L2: a step streams ~4.1 GB, every input is evicted "
+                         "before it is read again",
+                   "Gelem_s": round(total_elems / max_s / 1e9, 2),
+                   "frac_of_measured_hbm": round(value / peak, 4),
+                   "frac_of_nominal_8TBs": round(value / 8000.0, 4),
+                   "per_workload": per_wl},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "e2e": e2e,
+        "roofline": {"bound": "hbm", "kernel": kern, "call": dname,
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": dbytes},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_fraction)
+    return line
+
+
+def run_e2e(args, suite, calls, step_bytes):
+    """The same step with host inputs: pinned H2D copies of every input, the
+    calls, and D2H copies of every output, all inside the timed region."""
+    host_in = [t.cpu().pin_memory() for t in suite.inputs]
+    outs = suite.outputs_for_host()
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    k = max(2, min(args.steps, args.e2e_steps))
+
+    def step():
+        for d, h in zip(suite.inputs, host_in):
+            d.copy_(h, non_blocking=True)
+        for c in calls:
+            c()
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(k):
+        step()
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    secs, tot = reduce_max_sum(t1 - t0, step_bytes * k)
+    return {"value": round(tot / secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": k}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm
+# ---------------------------------------------------------------------------
+def oracle_sample(frac: float):
+    """Inputs of every workload at a fraction of its rows (same distributions)."""
+    from fake_quant_numerics_gb300 import workloads as W
+
+    def rows(r):
+        return max(1, int(round(r * frac)))
+
+    n1 = max(1024, int((1 << 20) * frac))
+    x1, g1 = W.cfg1(n=n1)
+    w2 = W.cfg2(rows=rows(4096))
+    a3 = W.cfg3(rows=rows(8192))
+    w4, g4 = W.cfg4(rows=rows(14336))
+    n5 = max(16384, int(268_435_456 * frac) // 16384 * 16384)
+    x5 = W.cfg5(n=n5)
+    return x1, g1, w2, a3, w4, g4, x5
+
+
+def oracle_step(inputs):
+    """One pass of the path through the oracle; returns (seconds, bytes, elems)."""
+    import oracle
+    from fake_quant_numerics_gb300 import workloads as W
+
+    x1, g1, w2, a3, w4, g4, x5 = inputs
+    x1n, g1n, w2n, x5n = x1.numpy(), g1.numpy(), w2.numpy(), x5.numpy()
+    a3b, w4b, g4b = W.bf16_bits(a3), W.bf16_bits(w4), W.bf16_bits(g4)
+    n1, n2, n3, n4, n5 = x1n.size, w2n.size, a3b.size, w4b.size, x5n.size
+    r2, r4 = w2.shape[0], w4.shape[0]
+    t0 = time.perf_counter()
+    o1 = oracle.fake_quant_int(x1n, 1, n1, 8, 0, 0, want_codes=False)
+    oracle.ste_backward(g1n, o1["mask"])
+    oracle.fake_quant_int(w2n, r2, 4096, 8, 1, 1)
+    oracle.fake_quant_int(w2n, r2, 4096, 4, 0, 1)
+    oracle.fake_quant_fp8(a3b, 0, want_codes=False)
+    oracle.fake_quant_fp8(a3b, 1, want_codes=False)
+    o4 = oracle.fake_quant_int(w4b, r4, 4096, 4, 0, 2, 128)
+    oracle.ste_backward(g4b, o4["mask"])
+    q = oracle.quant4_double(x5n)
+    oracle.dequant4_double(q["data"], q["qscales"], q["super_scales"], n5)
+    secs = time.perf_counter() - t0
+    wb = workload_bytes(n1, r2, 4096, n3, r4, 4096, n5)
+    return secs, sum(b for _, _, b, _ in wb), sum(e for _, e, _, _ in wb)
+
+
+def cpu_baseline(frac: float):
+    inputs = oracle_sample(frac)
+    secs, nbytes, elems = oracle_step(inputs)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "Gelem_s": round(elems / secs / 1e9, 4), "seconds": round(secs, 2),
+            "sample": f"every workload at {frac:g} of its rows/elements (same distributions), "
+                      f"one pass of the whole path, single-threaded C oracle"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    frac = args.ref_fraction
+    if frac <= 0:
+        # size each step so the whole run stays within about two minutes
+        probe = 1 / 256
+        secs, _, _ = oracle_step(oracle_sample(probe))
+        per_full = secs / probe
+        frac = 120.0 / max(1, args.steps + args.warmup) / per_full
+        frac = float(min(1 / 8, max(1 / 4096, frac)))
+    inputs = oracle_sample(frac)
+    for _ in range(args.warmup):
+        oracle_step(inputs)
+    tot_s, tot_b, tot_e = 0.0, 0.0, 0.0
+    for _ in range(args.steps):
+        s, b, e = oracle_step(inputs)
+        tot_s += s
+        tot_b += b
+        tot_e += e
+    value = tot_b / tot_s / 1e9
+    sample = (f"every workload at {frac:g} of its rows/elements (same distributions), "
+              f"single-threaded C oracle, one pass of the whole path per step")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_s / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32/bf16 in, fp32 arithmetic",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample_fraction": frac},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample, "Gelem_s": round(tot_e / tot_s / 1e9, 4)},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-fraction", type=float, default=1 / 2,
+                    help="fraction of every workload the CPU-baseline oracle pass covers")
+    ap.add_argument("--ref-fraction", type=float, default=0.0,
+                    help="per-step sample of the reference arm (0: sized to ~2 min in total)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    rank, world, local = dist_env()
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

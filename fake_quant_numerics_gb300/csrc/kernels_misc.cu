@@ -118,6 +118,25 @@ __device__ __forceinline__ int nibble_value(uint32_t packed, int e) {
   return nib >= 8 ? nib - 16 : nib;
 }
 
+// y = code * rs for the 8 codes of one 32-bit word.  A NaN product (only
+// possible when rs is inf or NaN: 0 * inf, x * NaN) is written as the
+// canonical quiet NaN 0x7fc00000.
+__device__ __forceinline__ V32 dequant8(uint32_t packed, float rs) {
+  V32 o;
+  if (isfinite(rs)) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      o.w[e] = __float_as_uint(__fmul_rn((float)nibble_value(packed, e), rs));
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float v = __fmul_rn((float)nibble_value(packed, e), rs);
+      o.w[e] = isnan(v) ? 0x7fc00000u : __float_as_uint(v);
+    }
+  }
+  return o;
+}
+
 template <bool ROUNDTRIP>
 __global__ void __launch_bounds__(kQ4Threads) k_q4_quant(const float* __restrict__ x, int64_t n,
                                                          uint8_t* __restrict__ data,
@@ -208,10 +227,7 @@ __global__ void __launch_bounds__(kQ4Threads) k_q4_quant(const float* __restrict
 #pragma unroll
       for (int j = 0; j < kQ4Slots; ++j) {
         const float rs = __fmul_rn(__fdiv_rn(s_q[j * (kQ4Threads / 8) + (tid >> 3)], 255.0f), super);
-        V32 o;
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          o.w[e] = __float_as_uint(__fmul_rn((float)nibble_value(packed[j], e), rs));
+        const V32 o = dequant8(packed[j], rs);
         const int64_t base = e0 + (int64_t)(j * kQ4Threads + tid) * 8;
         if (cnt[j] > 0) store_vec<F32>(y, base, o, cnt[j]);
       }
@@ -269,10 +285,7 @@ __global__ void __launch_bounds__(256) k_q4_dequant(const uint8_t* __restrict__ 
       const int64_t blk = e0 / kQ4Block;
       const float rs =
           __fmul_rn(__fdiv_rn((float)__ldg(qscales + blk), 255.0f), __ldg(sup + blk / kQ4Super));
-      V32 o;
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        o.w[e] = __float_as_uint(__fmul_rn((float)nibble_value(pk[k], e), rs));
+      const V32 o = dequant8(pk[k], rs);
       int64_t c = n - e0;
       store_vec<F32>(y, e0, o, c >= 8 ? 8 : (int)c);
     }

@@ -77,6 +77,7 @@ def lib():
         L.or_reconstruct_scale.restype = f32
         L.or64_fake_quant_int.argtypes = [vp, i32, i64, i64, i32, i32, i32, i64, vp, vp, vp]
         L.or64_fake_quant_fp8.argtypes = [vp, i32, i64, i32, vp, vp]
+        L.or_unit_stats.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp]
     return _lib
 
 
@@ -86,6 +87,22 @@ def _dtype_code(x: np.ndarray) -> int:
     if x.dtype == np.uint16:
         return BF16
     raise TypeError("oracle inputs are float32 arrays or uint16 bf16 bit patterns")
+
+
+def unit_stats(x: np.ndarray, L: int):
+    """(min, max, absmax, nonfinite count) of each run of L elements (finite values only)."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    dt = _dtype_code(x)
+    u = x.size // L if L else 0
+    out = np.zeros((u, 3), np.float32)
+    bad = np.zeros(u, np.int64)
+    mn, mx, am, nb = ctypes.c_float(), ctypes.c_float(), ctypes.c_float(), ctypes.c_int64()
+    for k in range(u):
+        lib().or_unit_stats(_p(x), dt, k * L, L, ctypes.byref(mn), ctypes.byref(mx), ctypes.byref(am),
+                            ctypes.byref(nb))
+        out[k] = (mn.value, mx.value, am.value)
+        bad[k] = nb.value
+    return out[:, 0], out[:, 1], out[:, 2], bad
 
 
 def q_range(bits: int, scheme: int):

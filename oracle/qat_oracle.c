@@ -480,8 +480,13 @@ static int32_t nibble_value(const uint8_t* data, int64_t i) {
   return (nib & 0x08) ? (int32_t)nib - 16 : (int32_t)nib;
 }
 
+/* reading: a NaN result (0 * inf or a NaN scale) is written as the canonical
+ * quiet NaN, as for every other floating-point output of this file. */
+static float canon_nan(float v) { return isnan(v) ? u2f(0x7FC00000u) : v; }
+
 int or_dequant4_single(const uint8_t* data, const float* scales, int64_t n, float* y) {
-  for (int64_t i = 0; i < n; ++i) y[i] = (float)nibble_value(data, i) * scales[i / OR_Q4_BLOCK];
+  for (int64_t i = 0; i < n; ++i)
+    y[i] = canon_nan((float)nibble_value(data, i) * scales[i / OR_Q4_BLOCK]);
   return OR_OK;
 }
 
@@ -530,7 +535,7 @@ int or_dequant4_double(const uint8_t* data, const uint8_t* qscales, const float*
   for (int64_t b = 0; b < nb; ++b) {
     float s = or_reconstruct_scale(qscales[b], supers[b / OR_Q4_SUPER]);
     int64_t s0 = b * OR_Q4_BLOCK, e0 = s0 + OR_Q4_BLOCK < n ? s0 + OR_Q4_BLOCK : n;
-    for (int64_t i = s0; i < e0; ++i) y[i] = (float)nibble_value(data, i) * s;
+    for (int64_t i = s0; i < e0; ++i) y[i] = canon_nan((float)nibble_value(data, i) * s);
   }
   return OR_OK;
 }
