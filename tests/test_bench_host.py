@@ -1,0 +1,81 @@
+"""Host-side pieces of bench.py: byte accounting, the cross-rank timing
+reduction (two gloo ranks on the CPU) and the JSON of the reference arm."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_workload_bytes_match_the_per_element_accounting():
+    wb = {name: (e, b, nl) for name, e, b, nl in bench.workload_bytes()}
+    n1 = 1 << 20
+    assert wb["w1_int8_tensor_fwd"][1] == n1 * 12 + n1 // 8 + 4     # two reads of x, y, mask
+    assert wb["w1_ste_bwd"][1] == n1 * 8 + n1 // 8
+    n5 = 268_435_456
+    assert wb["w5_quant4_double"][1] == n5 * 4 + n5 // 2 + n5 // 64 + 4 * (n5 // 16384)
+    total = sum(b for _, b, _ in wb.values())
+    assert 4.0e9 < total < 4.2e9
+    assert sum(nl for _, _, nl in wb.values()) == 13
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank(rank, world, port, q):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    secs, units = bench.reduce_max_sum(1.0 + rank, 100.0 * (rank + 1))
+    bench.barrier()
+    q.put((rank, secs, units))
+    dist.destroy_process_group()
+
+
+def test_reduce_max_sum_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert out == [(0, 2.0, 300.0), (1, 2.0, 300.0)]
+
+
+def test_reduce_without_process_group_is_identity():
+    assert bench.reduce_max_sum(3.5, 7.0) == (3.5, 7.0)
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3", "--ref-fraction", "0.002"],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_non_zero_rank_prints_nothing():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=300, env=env)
+    assert r.returncode == 0 and r.stdout.strip() == ""
