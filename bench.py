@@ -379,7 +379,7 @@ def run_ours(args, rank, world, local):
                      "traffic": traffic, "algorithmic_bytes": dbytes},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_fraction)
+        line["cpu_baseline"] = cpu_baseline(inputs, args.cpu_passes)
     return line
 
 
@@ -460,13 +460,16 @@ def oracle_step(inputs):
     return secs, sum(b for _, _, b, _ in wb), sum(e for _, e, _, _ in wb)
 
 
-def cpu_baseline(frac: float):
-    inputs = oracle_sample(frac)
-    secs, nbytes, elems = oracle_step(inputs)
+def cpu_baseline(inputs, passes: int):
+    """The oracle, single-threaded, over the benchmark's own full-size inputs."""
+    secs = nbytes = elems = 0.0
+    for _ in range(passes):
+        s, b, e = oracle_step(inputs)
+        secs, nbytes, elems = secs + s, nbytes + b, elems + e
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "Gelem_s": round(elems / secs / 1e9, 4), "seconds": round(secs, 2),
-            "sample": f"every workload at {frac:g} of its rows/elements (same distributions), "
-                      f"one pass of the whole path, single-threaded C oracle"}
+            "sample": f"the five workloads at full size (the GPU run's own inputs), {passes} "
+                      f"pass(es) of the whole path, single-threaded C oracle"}
 
 
 def run_reference(args, rank, world):
@@ -506,12 +509,12 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--cpu-fraction", type=float, default=1 / 2,
-                    help="fraction of every workload the CPU-baseline oracle pass covers")
+    ap.add_argument("--cpu-passes", type=int, default=3,
+                    help="oracle passes over the full workloads for cpu_baseline")
     ap.add_argument("--ref-fraction", type=float, default=0.0,
                     help="per-step sample of the reference arm (0: sized to ~2 min in total)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
