@@ -190,13 +190,16 @@ class Suite:
         self.x1, self.g1, self.w2, self.a3, self.w4, self.g4, self.x5 = self.inputs
         e = lambda n, dt=torch.uint8: torch.empty(n, dtype=dt, device=dev)  # noqa: E731
         n1, n2, n3, n4, n5 = x1.numel(), w2.numel(), a3.numel(), w4.numel(), x5.numel()
+        self.r2, self.c2 = w2.shape
+        self.r4, self.c4 = w4.shape
+        r2 = self.r2
         self.ws = e(16 * 1024 * 2)
         self.flags = torch.zeros(1, dtype=torch.int32, device=dev)
         self.o = dict(
             s1=e(1, f), y1=e(n1, f), m1=e((n1 + 31) // 32, torch.int32), dx1=e(n1, f),
-            s2a=e(4096, f), z2a=e(4096, torch.int32), y2a=e(n2, f), c2a=e(n2, torch.int8),
+            s2a=e(r2, f), z2a=e(r2, torch.int32), y2a=e(n2, f), c2a=e(n2, torch.int8),
             m2a=e(n2 // 32, torch.int32),
-            s2b=e(4096, f), y2b=e(n2, f), c2b=e(n2 // 2), m2b=e(n2 // 32, torch.int32),
+            s2b=e(r2, f), y2b=e(n2, f), c2b=e(n2 // 2), m2b=e(n2 // 32, torch.int32),
             s3=e(2, f), y3a=e(n3, torch.bfloat16), m3a=e(n3 // 32, torch.int32),
             y3b=e(n3, torch.bfloat16), m3b=e(n3 // 32, torch.int32),
             s4=e(n4 // 128, f), y4=e(n4, torch.bfloat16), c4=e(n4 // 2), m4=e(n4 // 32, torch.int32),
@@ -209,19 +212,20 @@ class Suite:
     def calls(self):
         fq, o, ws, fl = self.fq, self.o, self.ws, self.flags
         n1, n2, n3, n4, n5 = self.n
+        r2, c2, r4, c4 = self.r2, self.c2, self.r4, self.c4
         return [
             lambda: fq.qat_fake_quant_int(self.x1, 1, n1, 8, 0, 0, 0, False, o["s1"], None, o["y1"],
                                           None, o["m1"], fl, ws),
             lambda: fq.qat_ste_backward(self.g1, n1, o["m1"], o["dx1"]),
-            lambda: fq.qat_fake_quant_int(self.w2, 4096, 4096, 8, 1, 1, 0, False, o["s2a"], o["z2a"],
+            lambda: fq.qat_fake_quant_int(self.w2, r2, c2, 8, 1, 1, 0, False, o["s2a"], o["z2a"],
                                           o["y2a"], o["c2a"], o["m2a"], fl, ws),
-            lambda: fq.qat_fake_quant_int(self.w2, 4096, 4096, 4, 0, 1, 0, False, o["s2b"], None,
+            lambda: fq.qat_fake_quant_int(self.w2, r2, c2, 4, 0, 1, 0, False, o["s2b"], None,
                                           o["y2b"], o["c2b"], o["m2b"], fl, ws),
             lambda: fq.qat_fake_quant_fp8(self.a3, n3, 0, False, o["s3"][0:1], o["y3a"], None,
                                           o["m3a"], fl, ws),
             lambda: fq.qat_fake_quant_fp8(self.a3, n3, 1, False, o["s3"][1:2], o["y3b"], None,
                                           o["m3b"], fl, ws),
-            lambda: fq.qat_fake_quant_int(self.w4, 14336, 4096, 4, 0, 2, 128, False, o["s4"], None,
+            lambda: fq.qat_fake_quant_int(self.w4, r4, c4, 4, 0, 2, 128, False, o["s4"], None,
                                           o["y4"], o["c4"], o["m4"], fl, ws),
             lambda: fq.qat_ste_backward(self.g4, n4, o["m4"], o["dx4"]),
             lambda: fq.qat_quant4_double(self.x5, n5, o["d5"], o["q5"], o["u5"], None),
@@ -235,15 +239,19 @@ class Suite:
                                "dx4", "d5", "q5", "u5", "y5")]
 
 
-def make_inputs():
-    from fake_quant_numerics_gb300 import workloads as W
+def make_inputs(frac: float = 1.0):
+    """Inputs of the five workloads; frac < 1 keeps that fraction of the rows
+    (elements) of each, with the same distributions (profiling runs only)."""
+    if frac >= 1.0:
+        from fake_quant_numerics_gb300 import workloads as W
 
-    x1, g1 = W.cfg1()
-    w2 = W.cfg2()
-    a3 = W.cfg3()
-    w4, g4 = W.cfg4()
-    x5 = W.cfg5()
-    return [x1, g1, w2, a3, w4, g4, x5]
+        x1, g1 = W.cfg1()
+        w2 = W.cfg2()
+        a3 = W.cfg3()
+        w4, g4 = W.cfg4()
+        x5 = W.cfg5()
+        return [x1, g1, w2, a3, w4, g4, x5]
+    return list(oracle_sample(frac))
 
 
 def measured_peak():
@@ -289,10 +297,15 @@ def run_ours(args, rank, world, local):
     fq.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    inputs = make_inputs()
+    inputs = make_inputs(args.fraction)
     suite = Suite(dev, fq, inputs)
     calls = suite.calls()
-    wb = workload_bytes()
+    n1, n2, n3, n4, n5 = suite.n
+    wb = workload_bytes(n1, suite.r2, suite.c2, n3, suite.r4, suite.c4, n5)
+    if args.only:
+        keep = [i for i, w in enumerate(wb) if any(w[0].startswith(p) for p in args.only.split(","))]
+        calls = [calls[i] for i in keep]
+        wb = [wb[i] for i in keep]
     step_bytes = sum(b for _, _, b, _ in wb)
     step_elems = sum(e for _, e, _, _ in wb)
     stream = torch.cuda.current_stream()
@@ -378,6 +391,8 @@ def run_ours(args, rank, world, local):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": dbytes},
     }
+    if args.fraction < 1.0 or args.only:
+        line["config"]["subset"] = {"only": args.only, "fraction": args.fraction}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inputs, args.cpu_passes)
     return line
@@ -518,6 +533,10 @@ def main(argv=None):
     ap.add_argument("--ref-fraction", type=float, default=0.0,
                     help="per-step sample of the reference arm (0: sized to ~2 min in total)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="",
+                    help="profiling: comma-separated call-name prefixes to run (e.g. w5,w4_int4)")
+    ap.add_argument("--fraction", type=float, default=1.0,
+                    help="profiling: fraction of every workload's rows to generate")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_env()
