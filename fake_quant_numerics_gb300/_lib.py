@@ -41,6 +41,7 @@ PROTOTYPES = {
     "qat_fake_quant_int": ([_vp, _int, _i64, _i64, _int, _int, _int, _i64, _int, _vp, _vp, _vp, _vp,
                             _vp, _vp, _vp, _sz, _vp], _int),
     "qat_fake_quant_fp8": ([_vp, _int, _i64, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _int),
+    "qat_fake_quant_fp8_noalloc": ([_vp, _int, _i64, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp], _int),
     "qat_ste_backward": ([_vp, _int, _i64, _vp, _vp, _vp], _int),
     "qat_quant4_double": ([_vp, _i64, _vp, _vp, _vp, _vp, _vp], _int),
     "qat_dequant4_double": ([_vp, _vp, _vp, _i64, _vp, _vp], _int),

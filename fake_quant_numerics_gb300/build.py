@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqat.so")
 
 SOURCES = ["qat_abi.cu", "kernels_tensor.cu", "kernels_fused.cu", "kernels_fp8.cu",
-           "kernels_misc.cu"]
+           "kernels_misc.cu", "qat_noalloc.cu"]
 HEADERS = ["qat_device.cuh", "qat_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-fmad=false",

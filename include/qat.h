@@ -203,6 +203,32 @@ qat_status qat_quant4_double(const float* x, int64_t n, uint8_t* data, uint8_t* 
 qat_status qat_dequant4_double(const uint8_t* data, const uint8_t* qscales,
                                const float* super_scales, int64_t n, float* y, qat_stream_t stream);
 
+/*
+ * qat_fake_quant_fp8 without a workspace, for callers that cannot allocate
+ * device memory: code embedded in a host framework that owns every device
+ * allocation and passes the library only the tensors it works on, or a
+ * latency-critical loop that must not call cudaMalloc (which can synchronise
+ * the device).  There is no counterpart on the source pages; the arithmetic
+ * and the outputs are exactly those of qat_fake_quant_fp8.
+ *
+ * The amax pass keeps its cross-block partials in a fixed file-scope device
+ * array of 1024 slots x 16 bytes (16 KiB), reserved on every GPU that loads the
+ * library until the process exits.  The statistics pass never needs more than
+ * 2 x (number of SMs) slots; a device that would need more than 1024 gets
+ * QAT_ERR_WORKSPACE.  Nothing is allocated and nothing needs clearing: every
+ * slot a call reads is written earlier in the same call.  All calls share the
+ * array, so calls whose kernels overlap on the GPU (other streams, other host
+ * threads on the same device) race and must be ordered by the caller.  The
+ * first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture begins.  Arguments and errors as qat_fake_quant_fp8, minus the
+ * workspace.
+ */
+qat_status qat_fake_quant_fp8_noalloc(const void* x, qat_dtype dtype, int64_t n,
+                                      qat_fp8_format format, int scale_given, float* scale,
+                                      void* y, uint8_t* codes, uint32_t* mask, int32_t* dev_flags,
+                                      qat_stream_t stream);
+
 /* Number of kernels this library has launched in this process (diagnostic). */
 uint64_t qat_kernel_launch_count(void);
 
