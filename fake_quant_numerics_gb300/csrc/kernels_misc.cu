@@ -171,21 +171,45 @@ __global__ void __launch_bounds__(kQ4Threads) k_q4_quant(const float* __restrict
 #pragma unroll
     for (int j = 0; j < kQ4Slots; ++j) {
       // level 1: absmax over the 64-element block = 8 lanes x 8 elements
-      uint32_t a = 0u;
+      // (fmaxf ignores NaN and keeps +inf, the fold of the definition)
+      float a = 0.0f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        uint32_t ab = v[j].w[e] & 0x7fffffffu;
-        a = max(a, ab <= 0x7f800000u ? ab : 0u);  // NaN does not take part
-      }
-      a = max(a, __shfl_xor_sync(kFull, a, 1));
-      a = max(a, __shfl_xor_sync(kFull, a, 2));
-      a = max(a, __shfl_xor_sync(kFull, a, 4));
-      const float s = __fdiv_rn(__uint_as_float(a), 7.0f);
+      for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(__uint_as_float(v[j].w[e])));
+      a = fmaxf(a, __shfl_xor_sync(kFull, a, 1));
+      a = fmaxf(a, __shfl_xor_sync(kFull, a, 2));
+      a = fmaxf(a, __shfl_xor_sync(kFull, a, 4));
+      const float s = __fdiv_rn(a, 7.0f);
       uint32_t pk = 0u;
+      if (quot_scale_ok(s)) {
+        // |x| <= absmax, so |x/s| <= 7 (1 + 2^-23): |q0| < 8, the band 2^-16
+        // covers 2^(3-22); the clamp to [-8, 7] can never act here; absent
+        // tail elements read +0 and give code 0
+        const float rcp = __frcp_rn(s);
+        uint32_t nearbits = 0u;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        int c = (full || e < cnt[j]) ? q4_code(__uint_as_float(v[j].w[e]), s) : 0;
-        pk |= ((uint32_t)c & 0xfu) << ((e >> 1) * 8 + ((e & 1) ? 0 : 4));
+        for (int e = 0; e < 8; ++e) {
+          bool nr;
+          const float k = rint_quot(__uint_as_float(v[j].w[e]), rcp, 0x1p-16f, nr);
+          nearbits |= (uint32_t)nr << e;
+          const int c = __float2int_rz(k);  // NaN -> 0
+          pk |= ((uint32_t)c & 0xfu) << ((e >> 1) * 8 + ((e & 1) ? 0 : 4));
+        }
+        if (nearbits) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if ((nearbits >> e) & 1u) {
+              const int sh = (e >> 1) * 8 + ((e & 1) ? 0 : 4);
+              const int c = q4_code(__uint_as_float(v[j].w[e]), s);
+              pk = (pk & ~(0xfu << sh)) | (((uint32_t)c & 0xfu) << sh);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          int c = (full || e < cnt[j]) ? q4_code(__uint_as_float(v[j].w[e]), s) : 0;
+          pk |= ((uint32_t)c & 0xfu) << ((e >> 1) * 8 + ((e & 1) ? 0 : 4));
+        }
       }
       packed[j] = pk;
       const int64_t base = e0 + (int64_t)(j * kQ4Threads + tid) * 8;

@@ -399,6 +399,30 @@ __device__ __forceinline__ void int_elem(float x, const IntParams& p, int& q, fl
   m = (x >= p.wlo) && (x <= p.whi);
 }
 
+// ---------------------------------------------------------------------------
+// rounding of a quotient to an integer without a per-element division
+//
+// q0 = RN(x * RN(1/s)) differs from x/s by less than 1.5 ulp(q0) (the
+// reciprocal's relative error is at most 2^-24, the product's rounding half an
+// ulp), and RN(x/s) differs from x/s by at most half an ulp: so while q0 is
+// more than 2.5 ulp(q0) away from every half-integer, RN(x/s) lies in the same
+// open interval between consecutive half-integers as q0, and any rounding of
+// RN(x/s) to an integer (ties to even or away from zero) equals rint(q0).
+// For |q0| < 2^m that distance is below 2^(m-22); `band` must be at least
+// that.  `near` marks the elements that are not covered: the caller
+// recomputes them from the correctly rounded quotient __fdiv_rn(x, s).
+// Safe scales: s and 1/s normal and far from overflow, s in [2^-80, 2^100].
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool quot_scale_ok(float s) { return s >= 0x1p-80f && s <= 0x1p100f; }
+
+__device__ __forceinline__ float rint_quot(float x, float rcp, float band, bool& near) {
+  const float q0 = __fmul_rn(x, rcp);
+  const float k = rintf(q0);
+  // q0 - k is exact (|q0 - k| <= 1/2); its distance to +-1/2 decides
+  near = fabsf(__fsub_rn(fabsf(__fsub_rn(q0, k)), 0.5f)) < band;
+  return k;
+}
+
 __device__ __forceinline__ void flag_or(int32_t* flags, int bits) {
   if (flags && bits) atomicOr(flags, bits);
 }
