@@ -54,7 +54,7 @@ struct Fp8Params {
 constexpr uint32_t kNaN32 = 0x7fc00000u;
 constexpr uint32_t kNaN16 = 0x7fc0u;
 
-template <typename T, int FMT, bool FULL>
+template <typename T, int FMT, bool CODES, bool FULL>
 __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, int64_t tile,
                                          const Fp8Params& p, void* __restrict__ y,
                                          uint8_t* __restrict__ codes, uint32_t* __restrict__ mask,
@@ -108,8 +108,10 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
         mb |= (uint32_t)(fabsf(x0) <= p.lim) << e;
         mb |= (uint32_t)(fabsf(x1) <= p.lim) << (e + 1);
       }
-      if (FULL || e < cnt[j]) cv.set(e, (int)c0);
-      if (FULL || e + 1 < cnt[j]) cv.set(e + 1, (int)c1);
+      if (CODES) {
+        if (FULL || e < cnt[j]) cv.set(e, (int)(int8_t)c0);
+        if (FULL || e + 1 < cnt[j]) cv.set(e + 1, (int)(int8_t)c1);
+      }
       if (T::BYTES == 4) {
         out.w[e] = (p.mode != 2 && n0) ? kNaN32 : __float_as_uint(y0);
         out.w[e + 1] = (p.mode != 2 && n1) ? kNaN32 : __float_as_uint(y1);
@@ -125,7 +127,7 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
     if (!FULL) mb &= (cnt[j] >= 32) ? 0xffffffffu : ((1u << cnt[j]) - 1u);
     if (cnt[j] > 0) {
       store_vec<T>(y, base, out, cnt[j]);
-      if (codes) cv.store(codes, base, cnt[j]);
+      if (CODES) cv.store(codes, base, cnt[j]);
     }
     mw[j] = mask_word_of_slot<VEC>(mb, lane);
   }
@@ -136,13 +138,13 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
   }
 }
 
-template <typename T, int FMT, bool GIVEN>
+template <typename T, int FMT, bool GIVEN, bool CODES>
 __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, int64_t n,
                                                     const uint4* __restrict__ part, int nparts,
                                                     float* scale, void* y, uint8_t* codes,
                                                     uint32_t* mask, int32_t* flags) {
   constexpr float kMax = FMT == QAT_E4M3 ? 448.0f : 57344.0f;
-  __shared__ uint32_t red[4 * 8];
+  __shared__ __align__(16) uint32_t red[4 * 8];
   __shared__ Fp8Params sp;
   if (GIVEN) {
     if (threadIdx.x == 0) {
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, 
       sp.lim = __fmul_rn(kMax, s);
       if (blockIdx.x == 0) {
         scale[0] = s;
-        flag_or(flags, st.nonfinite ? QAT_FLAG_NONFINITE_INPUT : 0);
+        flag_or(flags, st.nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
       }
     }
   }
@@ -174,8 +176,8 @@ __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, 
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
        t += wstride) {
     const int64_t tile = GIVEN ? t : ntiles - 1 - t;
-    if (tile < nfull) fp8_tile<T, FMT, true>(x, n, tile, p, y, codes, mask, lane);
-    else fp8_tile<T, FMT, false>(x, n, tile, p, y, codes, mask, lane);
+    if (tile < nfull) fp8_tile<T, FMT, CODES, true>(x, n, tile, p, y, codes, mask, lane);
+    else fp8_tile<T, FMT, CODES, false>(x, n, tile, p, y, codes, mask, lane);
   }
 }
 
@@ -187,10 +189,13 @@ static void fp8_t(bool given, const void* x, int64_t n, const void* ws, int npar
   int64_t cap = (int64_t)device_info().sms * 8;
   int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
   const uint4* part = static_cast<const uint4*>(ws);
-  if (given)
-    k_fp8_tensor<T, FMT, true><<<grid, 256, 0, s>>>(x, n, part, nparts, scale, y, codes, mask, flags);
-  else
-    k_fp8_tensor<T, FMT, false><<<grid, 256, 0, s>>>(x, n, part, nparts, scale, y, codes, mask, flags);
+#define QAT_K(G, C) k_fp8_tensor<T, FMT, G, C><<<grid, 256, 0, s>>>(x, n, part, nparts, scale, y, codes, mask, flags)
+  if (given) {
+    if (codes) QAT_K(true, true); else QAT_K(true, false);
+  } else {
+    if (codes) QAT_K(false, true); else QAT_K(false, false);
+  }
+#undef QAT_K
 }
 
 qat_status launch_fp8_tensor(qat_dtype dt, qat_fp8_format fmt, bool given, const void* x, int64_t n,

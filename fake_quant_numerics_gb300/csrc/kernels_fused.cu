@@ -63,7 +63,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
         if (minv) minv[u] = st.min_f();
         if (maxv) maxv[u] = st.max_f();
       }
-      if (present[j] && st.nonfinite) fl |= QAT_FLAG_NONFINITE_INPUT;
+      if (present[j] && st.nonfinite()) fl |= QAT_FLAG_NONFINITE_INPUT;
       mw[j] = 0u;
       continue;
     }
@@ -78,7 +78,18 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
     CodeVec<BITS, VEC> cv;
     cv.clear();
     uint32_t mb = 0u;
-    if (!p.dead) {
+    if (p.fast) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        int k;
+        float yv;
+        uint32_t m;
+        int_elem_cal<AFFINE>(elem<T>(v[j], e), p, k, yv, m);
+        ov.set(e, yv);
+        cv.set(e, k + p.zp);
+        mb |= m << e;
+      }
+    } else if (!p.dead) {
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         int q;
@@ -139,24 +150,31 @@ __global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, in
   constexpr int VEC = T::VEC, NT = 256;
   constexpr int LPW = 32 / VEC;
   constexpr bool NEED_MINMAX = AFFINE || STATS_ONLY;
-  __shared__ uint32_t red[4 * 8];
+  __shared__ __align__(16) uint32_t red[4 * 8];
   const int lane = threadIdx.x & 31;
   const int nvec = (int)(L / VEC);
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    const int64_t ub = u * L;
-    V32 v[NV];
-    Stats st;
-    st.init();
+  // the next unit's vectors are requested before the current one is
+  // processed, so each block keeps a unit's worth of loads in flight
+  auto load_unit = [&](int64_t uu, V32 (&dst)[NV]) {
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
-      int vi = threadIdx.x + j * NT;
-      if (vi < nvec) {
-        v[j] = ld_v32(static_cast<const char*>(x) + (ub + (int64_t)vi * VEC) * T::BYTES);
+      const int vi = threadIdx.x + j * NT;
+      if (uu < units && vi < nvec) {
+        dst[j] = ld_v32(static_cast<const char*>(x) + (uu * L + (int64_t)vi * VEC) * T::BYTES);
       } else {
 #pragma unroll
-        for (int w = 0; w < 8; ++w) v[j].w[w] = 0u;
+        for (int w = 0; w < 8; ++w) dst[j].w[w] = 0u;
       }
     }
+  };
+  V32 v[NV];
+  load_unit(blockIdx.x, v);
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int64_t ub = u * L;
+    V32 vn[NV];
+    load_unit(u + gridDim.x, vn);
+    Stats st;
+    st.init();
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       int vi = threadIdx.x + j * NT;
@@ -171,8 +189,10 @@ __global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, in
         if (absmax) absmax[u] = b.absmax_f();
         if (minv) minv[u] = b.min_f();
         if (maxv) maxv[u] = b.max_f();
-        flag_or(flags, b.nonfinite ? QAT_FLAG_NONFINITE_INPUT : 0);
+        flag_or(flags, b.nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
       }
+#pragma unroll
+      for (int j = 0; j < NV; ++j) v[j] = vn[j];
       continue;
     }
     IntParams p;
@@ -191,7 +211,18 @@ __global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, in
       CodeVec<BITS, VEC> cv;
       cv.clear();
       uint32_t mb = 0u;
-      if (!p.dead) {
+      if (p.fast) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          int k;
+          float yv;
+          uint32_t m;
+          int_elem_cal<AFFINE>(elem<T>(v[j], e), p, k, yv, m);
+          ov.set(e, yv);
+          cv.set(e, k + p.zp);
+          mb |= m << e;
+        }
+      } else if (!p.dead) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
           int q;
@@ -214,6 +245,8 @@ __global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, in
       uint32_t w = mask_word_of_slot<VEC>(present ? mb : 0u, lane);
       if (mask && present && (lane % LPW) == 0) mask[base >> 5] = w;
     }
+#pragma unroll
+    for (int j = 0; j < NV; ++j) v[j] = vn[j];
   }
 }
 

@@ -17,8 +17,7 @@
 namespace qat {
 
 // ---------------------------------------------------------------------------
-// per-tensor statistics: one uint4 partial {absmax bits, min key, max key,
-// nonfinite} per block
+// per-tensor statistics: one uint4 partial (Stats::pack) per block
 // ---------------------------------------------------------------------------
 template <typename T, bool MINMAX, bool FULL>
 __device__ __forceinline__ void stats_tile(const void* __restrict__ x, int64_t n, int64_t tile,
@@ -50,7 +49,7 @@ __device__ __forceinline__ void stats_tile(const void* __restrict__ x, int64_t n
 template <typename T, bool MINMAX>
 __global__ void __launch_bounds__(512) k_stats_tensor(const void* __restrict__ x, int64_t n,
                                                       uint4* __restrict__ part) {
-  __shared__ uint32_t red[4 * 16];
+  __shared__ __align__(16) uint32_t red[4 * 16];
   const int lane = threadIdx.x & 31;
   const int64_t ntiles = (n + kTile - 1) / kTile;
   const int64_t nfull = n / kTile;
@@ -63,19 +62,19 @@ __global__ void __launch_bounds__(512) k_stats_tensor(const void* __restrict__ x
     else stats_tile<T, MINMAX, false>(x, n, t, st, lane);
   }
   Stats b = block_reduce_stats<MINMAX>(st, red);
-  if (threadIdx.x == 0) part[blockIdx.x] = make_uint4(b.amax, b.kmin, b.kmax, b.nonfinite);
+  if (threadIdx.x == 0) part[blockIdx.x] = b.pack();
 }
 
 __global__ void __launch_bounds__(256) k_stats_finalize(const uint4* __restrict__ part, int nparts,
                                                         float* absmax, float* minv, float* maxv,
                                                         int32_t* flags) {
-  __shared__ uint32_t red[4 * 8];
+  __shared__ __align__(16) uint32_t red[4 * 8];
   Stats s = reduce_partials<true>(part, nparts, red);
   if (threadIdx.x == 0) {
     if (absmax) absmax[0] = s.absmax_f();
     if (minv) minv[0] = s.min_f();
     if (maxv) maxv[0] = s.max_f();
-    flag_or(flags, s.nonfinite ? QAT_FLAG_NONFINITE_INPUT : 0);
+    flag_or(flags, s.nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
   }
 }
 
@@ -111,7 +110,18 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
     CodeVec<BITS, VEC> cv;
     cv.clear();
     uint32_t mb = 0u;
-    if (!p.dead) {
+    if (!GIVEN && p.fast) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        int k;
+        float yv;
+        uint32_t m;
+        int_elem_cal<AFFINE>(elem<T>(v[j], e), p, k, yv, m);
+        ov.set(e, yv);
+        if (FULL || e < cnt[j]) cv.set(e, k + p.zp);
+        mb |= m << e;
+      }
+    } else if (!p.dead) {
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         int q;
@@ -145,7 +155,7 @@ __global__ void __launch_bounds__(256) k_int_tensor(const void* __restrict__ x, 
                                                     const uint4* __restrict__ part, int nparts,
                                                     float* scale, int32_t* zp, void* y, void* codes,
                                                     uint32_t* mask, int32_t* flags) {
-  __shared__ uint32_t red[4 * 8];
+  __shared__ __align__(16) uint32_t red[4 * 8];
   __shared__ IntParams sp;
   if (GIVEN) {
     if (threadIdx.x == 0) {
@@ -279,7 +289,7 @@ __global__ void __launch_bounds__(256) k_unit_generic(const void* __restrict__ x
         if (absmax) absmax[u] = st.absmax_f();
         if (minv) minv[u] = st.min_f();
         if (maxv) maxv[u] = st.max_f();
-        flag_or(flags, st.nonfinite ? QAT_FLAG_NONFINITE_INPUT : 0);
+        flag_or(flags, st.nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
       } else {
         IntParams p;
         int f = calibrate<BITS, AFFINE>(st, p);

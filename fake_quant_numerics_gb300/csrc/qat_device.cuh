@@ -160,31 +160,50 @@ __device__ __forceinline__ void store_vec(void* y, int64_t base, const V32& v, i
 
 // ---------------------------------------------------------------------------
 // codes: int8 (VEC bytes per lane) or packed int4 (VEC/2 bytes per lane,
-// element 2j in the high nibble of byte j)
+// element 2j in the high nibble of byte j).  Packing uses
+// cvt.pack.sat.{s8,s4}.s32.b32 d, a, b, c  ->  d = c << 2w | sat(a) << w | sat(b)
+// (w = 8 or 4); the codes are already in range, so the saturation never acts.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_s8x2(int a, int b, uint32_t c) {
+  uint32_t d;
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t pack_s4x2(int a, int b, uint32_t c) {
+  uint32_t d;
+  asm("cvt.pack.sat.s4.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 template <int BITS, int VEC>
 struct CodeVec {
   static constexpr int NBYTES = BITS == 8 ? VEC : VEC / 2;
   static constexpr int NW = (NBYTES + 3) / 4;
-  uint32_t w[NW];
+  int q[VEC];
   __device__ __forceinline__ void clear() {
 #pragma unroll
-    for (int j = 0; j < NW; ++j) w[j] = 0u;
+    for (int e = 0; e < VEC; ++e) q[e] = 0;
   }
   // q: the integer code of element e (two's complement, low BITS bits used)
-  __device__ __forceinline__ void set(int e, int q) {
+  __device__ __forceinline__ void set(int e, int qv) { q[e] = qv; }
+  // word j: bytes 4j..4j+3, little endian
+  __device__ __forceinline__ uint32_t word(int j) const {
     if (BITS == 8) {
-      w[e >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << ((e & 3) * 8);
+      return pack_s8x2(q[4 * j + 1], q[4 * j], pack_s8x2(q[4 * j + 3], q[4 * j + 2], 0u));
     } else {
-      int byte = e >> 1;
-      int shift = (byte & 3) * 8 + ((e & 1) ? 0 : 4);
-      w[byte >> 2] |= (static_cast<uint32_t>(q) & 0xfu) << shift;
+      uint32_t d = pack_s4x2(q[8 * j + 6], q[8 * j + 7], 0u);
+      d = pack_s4x2(q[8 * j + 4], q[8 * j + 5], d);
+      d = pack_s4x2(q[8 * j + 2], q[8 * j + 3], d);
+      return pack_s4x2(q[8 * j], q[8 * j + 1], d);
     }
   }
   // store at element offset `base` (codes buffer byte offset base*BITS/8);
-  // `cnt` elements present
+  // `cnt` elements present (absent ones must hold code 0)
   __device__ __forceinline__ void store(void* codes, int64_t base, int cnt) const {
     uint8_t* p = static_cast<uint8_t*>(codes) + (BITS == 8 ? base : base / 2);
+    uint32_t w[NW];
+#pragma unroll
+    for (int j = 0; j < NW; ++j) w[j] = word(j);
     if (cnt >= VEC) {
       if (NBYTES == 16) {
         *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -229,8 +248,14 @@ __device__ __forceinline__ uint32_t gather_tile_word(const uint32_t (&mw)[SLOTS]
 }
 
 // ---------------------------------------------------------------------------
-// statistics on fp32 bit patterns: finite absmax (as bits of |x|), min / max
-// as order-preserving keys (-0 below +0), non-finite detection
+// statistics on fp32 bit patterns
+//
+// absmax: every element maps to t = (bits << 1) + 2^24 (unsigned, wrapping).
+// For a finite value t - 2^24 = 2|bits| lies in [0, 0xfeffffff], so finite
+// values land in [2^24, 2^32 - 2] in the order of |x|; +-inf and NaN (|bits| >=
+// 0x7f800000) wrap around below 2^24.  max(t) is then the finite absmax and
+// min(t) < 2^24 says a NaN/Inf was seen -- two integer min/max per element.
+// min / max: order-preserving keys (-0 below +0) of the finite elements.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t order_key(uint32_t u) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -240,34 +265,37 @@ __device__ __forceinline__ uint32_t key_to_bits(uint32_t k) {
 }
 constexpr uint32_t kKeyPosInf = 0xff800000u;  // order_key(+inf)
 constexpr uint32_t kKeyNegInf = 0x007fffffu;  // order_key(-inf)
+constexpr uint32_t kAbsBias = 0x01000000u;
+
+__device__ __forceinline__ uint32_t abs_key(uint32_t u) { return (u << 1) + kAbsBias; }
 
 struct Stats {
-  uint32_t amax;       // bits of the finite absmax
-  uint32_t kmin;       // key of the finite min
-  uint32_t kmax;       // key of the finite max
-  uint32_t nonfinite;  // 1 if a NaN/Inf was seen
+  uint32_t tmax;  // max abs_key: the finite absmax
+  uint32_t tmin;  // min abs_key: below kAbsBias iff a NaN/Inf was seen
+  uint32_t kmin;  // key of the finite min
+  uint32_t kmax;  // key of the finite max
   __device__ __forceinline__ void init() {
-    amax = 0u;
+    tmax = 0u;
+    tmin = 0xffffffffu;
     kmin = kKeyPosInf;
     kmax = kKeyNegInf;
-    nonfinite = 0u;
   }
   template <bool MINMAX>
   __device__ __forceinline__ void add(uint32_t u) {
-    uint32_t a = u & 0x7fffffffu;
-    bool fin = a < 0x7f800000u;
-    amax = max(amax, fin ? a : 0u);
-    nonfinite |= fin ? 0u : 1u;
+    const uint32_t t = abs_key(u);
+    tmax = max(tmax, t);
+    tmin = min(tmin, t);
     if (MINMAX) {
-      uint32_t k = order_key(u);
+      const bool fin = t >= kAbsBias;
+      const uint32_t k = order_key(u);
       kmin = min(kmin, fin ? k : kKeyPosInf);
       kmax = max(kmax, fin ? k : kKeyNegInf);
     }
   }
   template <bool MINMAX>
   __device__ __forceinline__ void merge(const Stats& o) {
-    amax = max(amax, o.amax);
-    nonfinite |= o.nonfinite;
+    tmax = max(tmax, o.tmax);
+    tmin = min(tmin, o.tmin);
     if (MINMAX) {
       kmin = min(kmin, o.kmin);
       kmax = max(kmax, o.kmax);
@@ -277,17 +305,27 @@ struct Stats {
   template <bool MINMAX>
   __device__ __forceinline__ void reduce_lanes(int width) {
     for (int o = 1; o < width; o <<= 1) {
-      amax = max(amax, __shfl_xor_sync(kFull, amax, o));
-      nonfinite |= __shfl_xor_sync(kFull, nonfinite, o);
+      tmax = max(tmax, __shfl_xor_sync(kFull, tmax, o));
+      tmin = min(tmin, __shfl_xor_sync(kFull, tmin, o));
       if (MINMAX) {
         kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
         kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
       }
     }
   }
-  __device__ __forceinline__ float absmax_f() const { return __uint_as_float(amax); }
+  __device__ __forceinline__ bool nonfinite() const { return tmin < kAbsBias; }
+  __device__ __forceinline__ float absmax_f() const {
+    return __uint_as_float(tmax >= kAbsBias ? (tmax - kAbsBias) >> 1 : 0u);
+  }
   __device__ __forceinline__ float min_f() const { return __uint_as_float(key_to_bits(kmin)); }
   __device__ __forceinline__ float max_f() const { return __uint_as_float(key_to_bits(kmax)); }
+  __device__ __forceinline__ uint4 pack() const { return make_uint4(tmax, tmin, kmin, kmax); }
+  __device__ __forceinline__ void unpack(const uint4& p) {
+    tmax = p.x;
+    tmin = p.y;
+    kmin = p.z;
+    kmax = p.w;
+  }
 };
 
 // Block-wide reduction of Stats (all threads get the result).  `red` needs
@@ -297,24 +335,40 @@ __device__ __forceinline__ Stats block_reduce_stats(Stats s, uint32_t* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   s.reduce_lanes<MINMAX>(32);
   __syncthreads();  // red may still be read from a previous use
-  if (lane == 0) {
-    red[4 * warp + 0] = s.amax;
-    red[4 * warp + 1] = s.kmin;
-    red[4 * warp + 2] = s.kmax;
-    red[4 * warp + 3] = s.nonfinite;
-  }
+  if (lane == 0) reinterpret_cast<uint4*>(red)[warp] = s.pack();
   __syncthreads();
   Stats t;
   t.init();
   for (int w = 0; w < nw; ++w) {
     Stats o;
-    o.amax = red[4 * w + 0];
-    o.kmin = red[4 * w + 1];
-    o.kmax = red[4 * w + 2];
-    o.nonfinite = red[4 * w + 3];
+    o.unpack(reinterpret_cast<const uint4*>(red)[w]);
     t.merge<MINMAX>(o);
   }
   return t;
+}
+
+// ---------------------------------------------------------------------------
+// rounding of a quotient to an integer without a per-element division
+//
+// q0 = RN(x * RN(1/s)) differs from x/s by less than 1.5 ulp(q0) (the
+// reciprocal's relative error is at most 2^-24, the product's rounding half an
+// ulp), and RN(x/s) differs from x/s by at most half an ulp: so while q0 is
+// more than 2.5 ulp(q0) away from every half-integer, RN(x/s) lies in the same
+// open interval between consecutive half-integers as q0, and any rounding of
+// RN(x/s) to an integer (ties to even or away from zero) equals rint(q0).
+// For |q0| < 2^m that distance is below 2^(m-22); `band` must be at least
+// that.  `near` marks the elements that are not covered: the caller
+// recomputes them from the correctly rounded quotient __fdiv_rn(x, s).
+// Safe scales: s and 1/s normal and far from overflow, s in [2^-80, 2^100].
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool quot_scale_ok(float s) { return s >= 0x1p-80f && s <= 0x1p100f; }
+
+__device__ __forceinline__ float rint_quot(float x, float rcp, float band, bool& near) {
+  const float q0 = __fmul_rn(x, rcp);
+  const float k = rintf(q0);
+  // q0 - k is exact (|q0 - k| <= 1/2); its distance to +-1/2 decides
+  near = fabsf(__fsub_rn(fabsf(__fsub_rn(q0, k)), 0.5f)) < band;
+  return k;
 }
 
 // ---------------------------------------------------------------------------
@@ -322,10 +376,12 @@ __device__ __forceinline__ Stats block_reduce_stats(Stats s, uint32_t* red) {
 // ---------------------------------------------------------------------------
 struct IntParams {
   float s;         // scale
+  float rcp;       // RN(1/s), used when `fast`
   float wlo, whi;  // STE window [(qmin-zp)*s, (qmax-zp)*s]
   int klo, khi;    // clamp range of k = q - zp
   int zp;
   int dead;        // unit outputs are codes 0, y +0, mask 0
+  int fast;        // calibrated unit with a scale in the safe range of rint_quot
 };
 
 template <int BITS, bool AFFINE>
@@ -366,8 +422,10 @@ __device__ __forceinline__ int calibrate(const Stats& st, IntParams& p) {
       p.zp = (int)z;
     }
   }
-  int flag = st.nonfinite ? QAT_FLAG_NONFINITE_CALIB : (degenerate ? QAT_FLAG_DEGENERATE : 0);
+  int flag = st.nonfinite() ? QAT_FLAG_NONFINITE_CALIB : (degenerate ? QAT_FLAG_DEGENERATE : 0);
   p.dead = flag != 0;
+  p.fast = !p.dead && quot_scale_ok(p.s);
+  p.rcp = p.fast ? __frcp_rn(p.s) : 0.0f;
   finish_params(p, qmin, qmax);
   return flag;
 }
@@ -380,6 +438,8 @@ __device__ __forceinline__ int given_params(float s, int zp, IntParams& p) {
   p.zp = AFFINE ? zp : 0;
   int bad = !(s > 0.0f) || isinf(s) || p.zp < qmin || p.zp > qmax;
   p.dead = bad;
+  p.fast = 0;
+  p.rcp = 0.0f;
   finish_params(p, qmin, qmax);
   return bad ? QAT_FLAG_BAD_PARAMS : 0;
 }
@@ -399,28 +459,22 @@ __device__ __forceinline__ void int_elem(float x, const IntParams& p, int& q, fl
   m = (x >= p.wlo) && (x <= p.whi);
 }
 
-// ---------------------------------------------------------------------------
-// rounding of a quotient to an integer without a per-element division
-//
-// q0 = RN(x * RN(1/s)) differs from x/s by less than 1.5 ulp(q0) (the
-// reciprocal's relative error is at most 2^-24, the product's rounding half an
-// ulp), and RN(x/s) differs from x/s by at most half an ulp: so while q0 is
-// more than 2.5 ulp(q0) away from every half-integer, RN(x/s) lies in the same
-// open interval between consecutive half-integers as q0, and any rounding of
-// RN(x/s) to an integer (ties to even or away from zero) equals rint(q0).
-// For |q0| < 2^m that distance is below 2^(m-22); `band` must be at least
-// that.  `near` marks the elements that are not covered: the caller
-// recomputes them from the correctly rounded quotient __fdiv_rn(x, s).
-// Safe scales: s and 1/s normal and far from overflow, s in [2^-80, 2^100].
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ bool quot_scale_ok(float s) { return s >= 0x1p-80f && s <= 0x1p100f; }
-
-__device__ __forceinline__ float rint_quot(float x, float rcp, float band, bool& near) {
-  const float q0 = __fmul_rn(x, rcp);
-  const float k = rintf(q0);
-  // q0 - k is exact (|q0 - k| <= 1/2); its distance to +-1/2 decides
-  near = fabsf(__fsub_rn(fabsf(__fsub_rn(q0, k)), 0.5f)) < band;
-  return k;
+// One element of a calibrated unit with p.fast set: the quotient from the
+// reciprocal (rint_quot; |q| <= qmax - qmin <= 255 < 2^9, band 2^-12 > 2^(9-22)),
+// near-ties from the correctly rounded quotient.  Returns k = q - zp.
+// Symmetric: |x| <= absmax bounds |x/s| by qmax (1 + 2^-24)^3 < qmax + 1/2, so
+// k never leaves [-qmax, qmax] and needs no clamp, and the window
+// [-qmax*s, qmax*s] is |x| <= qmax*s.
+template <bool AFFINE>
+__device__ __forceinline__ void int_elem_cal(float x, const IntParams& p, int& k, float& y,
+                                             uint32_t& m) {
+  bool nr;
+  float kf = rint_quot(x, p.rcp, 0x1p-12f, nr);
+  if (nr) kf = rintf(__fdiv_rn(x, p.s));
+  k = __float2int_rz(kf);
+  if (AFFINE) k = min(max(k, p.klo), p.khi);
+  y = __fmul_rn(__int2float_rn(k), p.s);
+  m = AFFINE ? ((x >= p.wlo) && (x <= p.whi)) : (fabsf(x) <= p.whi);
 }
 
 __device__ __forceinline__ void flag_or(int32_t* flags, int bits) {
@@ -440,12 +494,8 @@ __device__ __forceinline__ Stats reduce_partials(const uint4* part, int nparts, 
   Stats s;
   s.init();
   for (int i = threadIdx.x; i < nparts; i += blockDim.x) {
-    uint4 p = part[i];
     Stats o;
-    o.amax = p.x;
-    o.kmin = p.y;
-    o.kmax = p.z;
-    o.nonfinite = p.w;
+    o.unpack(part[i]);
     s.merge<MINMAX>(o);
   }
   return block_reduce_stats<MINMAX>(s, red);
