@@ -45,11 +45,30 @@ __device__ __forceinline__ void fp8x2_decode(uint32_t c2, float& lo, float& hi) 
   hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
 }
 
+// Exact cast without a per-element division.  With rcp = RN(1/s),
+// rlo = RN(rcp (1 - 2^-21)) and rhi = RN(rcp (1 + 2^-21)), the products
+// lo = RN(x rlo) and hi = RN(x rhi) satisfy |lo| < |RN(x/s)| < |hi| (each of
+// rcp, rlo / rhi and the product carries at most 2^-24 relative error, the
+// margin is 8 * 2^-24) with the sign of x, whenever s is in [2^-80, 2^100]
+// (below the normal range all three are far under half the smallest FP8
+// subnormal and cast to the same signed zero; above FP8's range all saturate).
+// The saturating FP8 rounding is monotone in magnitude, so when lo and hi
+// cast to the same code, that is the code of RN(x/s); otherwise the pair is
+// recomputed from the correctly rounded quotient.
 struct Fp8Params {
-  float s;    // scale
-  float lim;  // fmt_max * s: the STE window |x| <= lim
-  int mode;   // 0 normal, 1 zero scale, 2 invalid given scale
+  float s;         // scale
+  float lim;       // fmt_max * s: the STE window |x| <= lim
+  float rlo, rhi;  // bracketing reciprocals (fast == 1)
+  int mode;        // 0 normal, 1 zero scale, 2 invalid given scale
+  int fast;
 };
+
+__device__ __forceinline__ void fp8_params_finish(Fp8Params& p) {
+  p.fast = p.mode == 0 && quot_scale_ok(p.s);
+  const float rcp = p.fast ? __frcp_rn(p.s) : 1.0f;
+  p.rlo = __fmul_rn(rcp, 1.0f - 0x1p-21f);
+  p.rhi = __fmul_rn(rcp, 1.0f + 0x1p-21f);
+}
 
 constexpr uint32_t kNaN32 = 0x7fc00000u;
 constexpr uint32_t kNaN16 = 0x7fc0u;
@@ -90,8 +109,14 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
       uint32_t c0, c1;
       float y0, y1;
       if (p.mode == 0) {
-        const float t0 = __fdiv_rn(x0, p.s), t1 = __fdiv_rn(x1, p.s);
-        const uint32_t c2 = fp8x2_encode<FMT>(t0, t1);
+        uint32_t c2;
+        if (p.fast) {
+          c2 = fp8x2_encode<FMT>(__fmul_rn(x0, p.rlo), __fmul_rn(x1, p.rlo));
+          const uint32_t h2 = fp8x2_encode<FMT>(__fmul_rn(x0, p.rhi), __fmul_rn(x1, p.rhi));
+          if (c2 != h2) c2 = fp8x2_encode<FMT>(__fdiv_rn(x0, p.s), __fdiv_rn(x1, p.s));
+        } else {
+          c2 = fp8x2_encode<FMT>(__fdiv_rn(x0, p.s), __fdiv_rn(x1, p.s));
+        }
         float d0, d1;
         fp8x2_decode<FMT>(c2, d0, d1);
         c0 = c2 & 0xffu;
@@ -152,6 +177,7 @@ __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, 
       sp.s = s;
       sp.mode = (isnan(s) || isinf(s) || s < 0.0f) ? 2 : (s == 0.0f ? 1 : 0);
       sp.lim = __fmul_rn(kMax, s);
+      fp8_params_finish(sp);
       if (blockIdx.x == 0) flag_or(flags, sp.mode == 2 ? QAT_FLAG_BAD_PARAMS : 0);
     }
   } else {
@@ -161,6 +187,7 @@ __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, 
       sp.s = s;
       sp.mode = s == 0.0f ? 1 : 0;
       sp.lim = __fmul_rn(kMax, s);
+      fp8_params_finish(sp);
       if (blockIdx.x == 0) {
         scale[0] = s;
         flag_or(flags, st.nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);

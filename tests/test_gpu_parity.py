@@ -233,6 +233,29 @@ def test_fp8_all_fp32_bit_patterns_unscaled(qat, orc, fmt):
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
+def test_fp8_random_scales_random_bit_patterns(qat, orc, fmt):
+    """Given scales across the whole fast range and its edges, each over 2^20
+    random fp32 bit patterns plus values placed on and next to the cast's
+    rounding boundaries (scaled FP8 midpoints +- a few ulps)."""
+    rng = np.random.default_rng(31 + fmt)
+    scales = [float(np.float32(2.0 ** e * m)) for e, m in
+              zip(rng.integers(-80, 100, size=10), rng.uniform(1, 2, size=10))]
+    scales += [float(np.float32(v)) for v in (2.0 ** -80, 2.0 ** 100, 1 - 2 ** -24, 1.9999999, 3.0,
+                                              448 / 7, 2.0 ** -81, 2.0 ** 101)]
+    probe = np.concatenate([[0.0], np.geomspace(2.0 ** -20, 6.0e4, 400_000)]).astype(np.float32)
+    grid = np.unique(np.abs(orc.fake_quant_fp8(probe, fmt, scale=1.0)["y"].astype(np.float64)))
+    mids = (grid[:-1] + grid[1:]) / 2
+    for sc in scales:
+        bits_ = rng.integers(0, 1 << 32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+        x = bits_.view(np.float32).copy()
+        near = (mids * sc).astype(np.float32)
+        near = np.concatenate([near, -near])
+        for d in (-2, -1, 0, 1, 2):
+            x[: near.size] = (near.view(np.int32) + d).view(np.float32)
+            run_fp8(qat, orc, torch.from_numpy(x.copy()), fmt, scale=sc, want_codes=True)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
 def test_fp8_zero_and_invalid_scale(qat, orc, fmt):
     x = make_input(2, 300, torch.float32, seed=5, specials=True)
     for s in (0.0, -1.0, float("nan"), float("inf"), 2.5e-3):
