@@ -75,25 +75,14 @@ constexpr uint32_t kNaN16 = 0x7fc0u;
 
 template <typename T, int FMT, bool CODES, bool FULL>
 __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, int64_t tile,
+                                         V32 (&v)[kTile / (32 * T::VEC)], bool have, int64_t next,
                                          const Fp8Params& p, void* __restrict__ y,
                                          uint8_t* __restrict__ codes, uint32_t* __restrict__ mask,
                                          int lane) {
   constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
   const int64_t tb = tile * kTile;
-  V32 v[SLOTS];
   int cnt[SLOTS];
-#pragma unroll
-  for (int j = 0; j < SLOTS; ++j) {
-    int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
-    if (FULL) {
-      cnt[j] = VEC;
-      v[j] = ld_v32(static_cast<const char*>(x) + base * T::BYTES);
-    } else {
-      int64_t c = n - base;
-      cnt[j] = c >= VEC ? VEC : (c > 0 ? (int)c : 0);
-      v[j] = load_vec<T>(x, cnt[j] > 0 ? base : 0, cnt[j]);
-    }
-  }
+  tile_load<T, FULL>(x, n, tile, v, cnt, have, lane);
   uint32_t mw[SLOTS];
 #pragma unroll
   for (int j = 0; j < SLOTS; ++j) {
@@ -111,8 +100,11 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
       if (p.mode == 0) {
         uint32_t c2;
         if (p.fast) {
-          c2 = fp8x2_encode<FMT>(__fmul_rn(x0, p.rlo), __fmul_rn(x1, p.rlo));
-          const uint32_t h2 = fp8x2_encode<FMT>(__fmul_rn(x0, p.rhi), __fmul_rn(x1, p.rhi));
+          float l0, l1, h0, h1;
+          mul2(x0, x1, p.rlo, p.rlo, l0, l1);
+          mul2(x0, x1, p.rhi, p.rhi, h0, h1);
+          c2 = fp8x2_encode<FMT>(l0, l1);
+          const uint32_t h2 = fp8x2_encode<FMT>(h0, h1);
           if (c2 != h2) c2 = fp8x2_encode<FMT>(__fdiv_rn(x0, p.s), __fdiv_rn(x1, p.s));
         } else {
           c2 = fp8x2_encode<FMT>(__fdiv_rn(x0, p.s), __fdiv_rn(x1, p.s));
@@ -121,8 +113,7 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
         fp8x2_decode<FMT>(c2, d0, d1);
         c0 = c2 & 0xffu;
         c1 = (c2 >> 8) & 0xffu;
-        y0 = __fmul_rn(d0, p.s);
-        y1 = __fmul_rn(d1, p.s);
+        mul2(d0, d1, p.s, p.s, y0, y1);
       } else {
         c0 = c1 = 0u;
         y0 = y1 = 0.0f;
@@ -149,6 +140,7 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
         out.w[e >> 1] = w;
       }
     }
+    slot_prefetch<T>(x, next, j, v[j], lane);
     if (!FULL) mb &= (cnt[j] >= 32) ? 0xffffffffu : ((1u << cnt[j]) - 1u);
     if (cnt[j] > 0) {
       store_vec<T>(y, base, out, cnt[j]);
@@ -190,7 +182,7 @@ __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, 
       fp8_params_finish(sp);
       if (blockIdx.x == 0) {
         scale[0] = s;
-        flag_or(flags, st.nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
+        flag_or(flags, st.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
       }
     }
   }
@@ -200,11 +192,20 @@ __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, 
   const int64_t ntiles = (n + kTile - 1) / kTile;
   const int64_t nfull = n / kTile;
   const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  V32 v[kTile / (32 * T::VEC)];
+  bool have = false;
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
        t += wstride) {
     const int64_t tile = GIVEN ? t : ntiles - 1 - t;
-    if (tile < nfull) fp8_tile<T, FMT, CODES, true>(x, n, tile, p, y, codes, mask, lane);
-    else fp8_tile<T, FMT, CODES, false>(x, n, tile, p, y, codes, mask, lane);
+    const int64_t nt = t + wstride;
+    const int64_t ntile = GIVEN ? nt : ntiles - 1 - nt;
+    // no rolling prefetch here: the extra live vectors cost more occupancy
+    // than the overlap gains for this arithmetic-heavy map
+    const int64_t next = -1;
+    (void)ntile;
+    if (tile < nfull) fp8_tile<T, FMT, CODES, true>(x, n, tile, v, have, next, p, y, codes, mask, lane);
+    else fp8_tile<T, FMT, CODES, false>(x, n, tile, v, have, next, p, y, codes, mask, lane);
+    have = next >= 0;
   }
 }
 

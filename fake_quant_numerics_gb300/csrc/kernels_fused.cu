@@ -22,22 +22,24 @@ namespace qat {
 
 template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY, bool FULL>
 __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n, int64_t tile,
-                                           float* scale, int32_t* zp, float* absmax, float* minv,
-                                           float* maxv, void* __restrict__ y,
+                                           V32 (&v)[kTile / (32 * T::VEC)], bool have,
+                                           int64_t next, float* scale, int32_t* zp, float* absmax,
+                                           float* minv, float* maxv, void* __restrict__ y,
                                            void* __restrict__ codes, uint32_t* __restrict__ mask,
                                            int lane, int& fl) {
   constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
   constexpr int L = VEC * LPG;
   constexpr bool NEED_MINMAX = AFFINE || STATS_ONLY;
   const int64_t tb = tile * kTile;
-  V32 v[SLOTS];
   bool present[SLOTS];
 #pragma unroll
   for (int j = 0; j < SLOTS; ++j) {
     int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
     // n is a multiple of L, so a lane's vector is entirely present or absent
     present[j] = FULL || base < n;
-    if (present[j]) {
+    if (FULL) {
+      if (!have) v[j] = ld_v32(static_cast<const char*>(x) + base * T::BYTES);
+    } else if (present[j]) {
       v[j] = ld_v32(static_cast<const char*>(x) + base * T::BYTES);
     } else {
 #pragma unroll
@@ -52,8 +54,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
     Stats st;
     st.init();
     if (present[j]) {
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) st.add<NEED_MINMAX>(elem_bits<T>(v[j], e));
+      stats_add_vec<T, NEED_MINMAX>(st, v[j]);
     }
     st.reduce_lanes<NEED_MINMAX>(LPG);
     const bool leader = present[j] && (lane % LPG) == 0;
@@ -63,8 +64,9 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
         if (minv) minv[u] = st.min_f();
         if (maxv) maxv[u] = st.max_f();
       }
-      if (present[j] && st.nonfinite()) fl |= QAT_FLAG_NONFINITE_INPUT;
+      if (present[j] && st.has_nonfinite()) fl |= QAT_FLAG_NONFINITE_INPUT;
       mw[j] = 0u;
+      slot_prefetch<T>(x, next, j, v[j], lane);
       continue;
     }
     IntParams p;
@@ -80,14 +82,17 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
     uint32_t mb = 0u;
     if (p.fast) {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        int k;
-        float yv;
-        uint32_t m;
-        int_elem_cal<AFFINE>(elem<T>(v[j], e), p, k, yv, m);
-        ov.set(e, yv);
-        cv.set(e, k + p.zp);
-        mb |= m << e;
+      for (int e = 0; e < VEC; e += 2) {
+        int ka, kb;
+        float ya, yb;
+        uint32_t ma, mb2;
+        int_pair_cal<AFFINE>(elem<T>(v[j], e), elem<T>(v[j], e + 1), p, ka, kb, ya, yb, ma,
+                             mb2);
+        ov.set(e, ya);
+        ov.set(e + 1, yb);
+        cv.set(e, AFFINE ? ka + p.zp : ka);
+        cv.set(e + 1, AFFINE ? kb + p.zp : kb);
+        mb |= (ma << e) | (mb2 << (e + 1));
       }
     } else if (!p.dead) {
 #pragma unroll
@@ -104,6 +109,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
 #pragma unroll
       for (int e = 0; e < VEC; ++e) ov.set(e, 0.0f);
     }
+    slot_prefetch<T>(x, next, j, v[j], lane);
     if (!present[j]) mb = 0u;
     if (present[j]) {
       if (y) st_v32(static_cast<char*>(y) + base * T::BYTES, ov.v);
@@ -119,7 +125,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
 }
 
 template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY>
-__global__ void __maxnreg__(80) k_int_groups(const void* __restrict__ x, int64_t n, float* scale,
+__global__ void __maxnreg__(T::BYTES == 4 ? 96 : 80) k_int_groups(const void* __restrict__ x, int64_t n, float* scale,
                                              int32_t* zp, float* absmax, float* minv, float* maxv,
                                              void* y, void* codes, uint32_t* mask, int32_t* flags) {
   const int lane = threadIdx.x & 31;
@@ -127,14 +133,19 @@ __global__ void __maxnreg__(80) k_int_groups(const void* __restrict__ x, int64_t
   const int64_t nfull = n / kTile;
   const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
   int fl = 0;
+  V32 v[kTile / (32 * T::VEC)];
+  bool have = false;
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
        t += wstride) {
+    const int64_t next = -1;  // no rolling prefetch: occupancy matters more here
     if (t < nfull)
-      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, true>(x, n, t, scale, zp, absmax, minv, maxv, y,
-                                                         codes, mask, lane, fl);
+      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, true>(x, n, t, v, have, next, scale, zp, absmax,
+                                                         minv, maxv, y, codes, mask, lane, fl);
     else
-      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, false>(x, n, t, scale, zp, absmax, minv, maxv,
-                                                          y, codes, mask, lane, fl);
+      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, false>(x, n, t, v, have, next, scale, zp,
+                                                          absmax, minv, maxv, y, codes, mask, lane,
+                                                          fl);
+    have = next >= 0;
   }
   warp_flag_or(flags, fl);
 }
@@ -179,8 +190,7 @@ __global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, in
     for (int j = 0; j < NV; ++j) {
       int vi = threadIdx.x + j * NT;
       if (vi < nvec) {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) st.add<NEED_MINMAX>(elem_bits<T>(v[j], e));
+        stats_add_vec<T, NEED_MINMAX>(st, v[j]);
       }
     }
     Stats b = block_reduce_stats<NEED_MINMAX>(st, red);
@@ -189,7 +199,7 @@ __global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, in
         if (absmax) absmax[u] = b.absmax_f();
         if (minv) minv[u] = b.min_f();
         if (maxv) maxv[u] = b.max_f();
-        flag_or(flags, b.nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
+        flag_or(flags, b.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
       }
 #pragma unroll
       for (int j = 0; j < NV; ++j) v[j] = vn[j];
@@ -213,14 +223,17 @@ __global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, in
       uint32_t mb = 0u;
       if (p.fast) {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          int k;
-          float yv;
-          uint32_t m;
-          int_elem_cal<AFFINE>(elem<T>(v[j], e), p, k, yv, m);
-          ov.set(e, yv);
-          cv.set(e, k + p.zp);
-          mb |= m << e;
+        for (int e = 0; e < VEC; e += 2) {
+          int ka, kb;
+          float ya, yb;
+          uint32_t ma, mb2;
+          int_pair_cal<AFFINE>(elem<T>(v[j], e), elem<T>(v[j], e + 1), p, ka, kb, ya, yb, ma,
+                               mb2);
+          ov.set(e, ya);
+          ov.set(e + 1, yb);
+          cv.set(e, AFFINE ? ka + p.zp : ka);
+          cv.set(e + 1, AFFINE ? kb + p.zp : kb);
+          mb |= (ma << e) | (mb2 << (e + 1));
         }
       } else if (!p.dead) {
 #pragma unroll

@@ -25,32 +25,22 @@ namespace qat {
 // ---------------------------------------------------------------------------
 template <typename T, bool FULL>
 __device__ __forceinline__ void ste_tile(const void* __restrict__ g, int64_t n, int64_t tile,
-                                         const uint32_t* __restrict__ mask, void* __restrict__ dx,
-                                         int lane) {
+                                         V32 (&v)[kTile / (32 * T::VEC)], uint32_t& word,
+                                         bool have, int64_t next, const uint32_t* __restrict__ mask,
+                                         void* __restrict__ dx, int lane) {
   constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC), LPW = 32 / VEC;
   const int64_t tb = tile * kTile;
   const int64_t nwords = (n + 31) / 32;
   const int64_t wi = tile * 32 + lane;
-  uint32_t word = 0u;
-  if (FULL || wi < nwords) word = __ldg(mask + wi);
-  V32 v[SLOTS];
+  if (!FULL || !have) word = (FULL || wi < nwords) ? __ldg(mask + wi) : 0u;
   int cnt[SLOTS];
-#pragma unroll
-  for (int j = 0; j < SLOTS; ++j) {
-    int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
-    if (FULL) {
-      cnt[j] = VEC;
-      v[j] = ld_v32(static_cast<const char*>(g) + base * T::BYTES);
-    } else {
-      int64_t c = n - base;
-      cnt[j] = c >= VEC ? VEC : (c > 0 ? (int)c : 0);
-      v[j] = load_vec<T>(g, cnt[j] > 0 ? base : 0, cnt[j]);
-    }
-  }
+  tile_load<T, FULL>(g, n, tile, v, cnt, have, lane);
+  const uint32_t cur = word;
+  if (next >= 0) word = __ldg(mask + next * 32 + lane);
 #pragma unroll
   for (int j = 0; j < SLOTS; ++j) {
     const int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
-    const uint32_t w = __shfl_sync(kFull, word, j * VEC + lane / LPW);
+    const uint32_t w = __shfl_sync(kFull, cur, j * VEC + lane / LPW);
     const uint32_t bits = (w >> ((lane % LPW) * VEC)) & ((1u << VEC) - 1u);
     V32 o;
 #pragma unroll
@@ -64,6 +54,7 @@ __device__ __forceinline__ void ste_tile(const void* __restrict__ g, int64_t n, 
       }
       o.w[k] = v[j].w[k] & sel;
     }
+    slot_prefetch<T>(g, next, j, v[j], lane);
     if (cnt[j] > 0) store_vec<T>(dx, base, o, cnt[j]);
   }
 }
@@ -75,10 +66,15 @@ __global__ void __launch_bounds__(256) k_ste(const void* __restrict__ g, int64_t
   const int64_t ntiles = (n + kTile - 1) / kTile;
   const int64_t nfull = n / kTile;
   const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  V32 v[kTile / (32 * T::VEC)];
+  uint32_t word = 0u;
+  bool have = false;
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
        t += wstride) {
-    if (t < nfull) ste_tile<T, true>(g, n, t, mask, dx, lane);
-    else ste_tile<T, false>(g, n, t, mask, dx, lane);
+    const int64_t next = -1;  // no rolling prefetch: occupancy matters more here
+    if (t < nfull) ste_tile<T, true>(g, n, t, v, word, have, next, mask, dx, lane);
+    else ste_tile<T, false>(g, n, t, v, word, have, next, mask, dx, lane);
+    have = next >= 0;
   }
 }
 
@@ -138,7 +134,7 @@ __device__ __forceinline__ V32 dequant8(uint32_t packed, float rs) {
 }
 
 template <bool ROUNDTRIP>
-__global__ void __launch_bounds__(kQ4Threads) k_q4_quant(const float* __restrict__ x, int64_t n,
+__global__ void __launch_bounds__(kQ4Threads, 2) k_q4_quant(const float* __restrict__ x, int64_t n,
                                                          uint8_t* __restrict__ data,
                                                          uint8_t* __restrict__ qscales,
                                                          float* __restrict__ sup,
@@ -150,17 +146,21 @@ __global__ void __launch_bounds__(kQ4Threads) k_q4_quant(const float* __restrict
   const int64_t nsuper = (n + kQ4SuperElems - 1) / kQ4SuperElems;
   const int64_t nblocks = (n + kQ4Block - 1) / kQ4Block;
   const int64_t nbytes = (n + 1) / 2;
+  // The vectors of the next super-block are requested as soon as the level-1
+  // codes of the current one are computed, so they are in flight while
+  // level 2 (two block barriers) and the stores run.
+  V32 v[kQ4Slots];
+  bool have = false;  // v already holds this super-block (a full one)
   for (int64_t sb = blockIdx.x; sb < nsuper; sb += gridDim.x) {
     const int64_t e0 = sb * kQ4SuperElems;
     const bool full = e0 + kQ4SuperElems <= n;
-    V32 v[kQ4Slots];
     int cnt[kQ4Slots];
 #pragma unroll
     for (int j = 0; j < kQ4Slots; ++j) {
       int64_t base = e0 + (int64_t)(j * kQ4Threads + tid) * 8;
       if (full) {
         cnt[j] = 8;
-        v[j] = ld_v32(x + base);
+        if (!have) v[j] = ld_v32(x + base);
       } else {
         int64_t c = n - base;
         cnt[j] = c >= 8 ? 8 : (c > 0 ? (int)c : 0);
@@ -184,15 +184,25 @@ __global__ void __launch_bounds__(kQ4Threads) k_q4_quant(const float* __restrict
         // |x| <= absmax, so |x/s| <= 7 (1 + 2^-23): |q0| < 8, the band 2^-16
         // covers 2^(3-22); the clamp to [-8, 7] can never act here; absent
         // tail elements read +0 and give code 0
+        // quotient from the reciprocal, rounded with the magic constant (see
+        // int_pair_cal); the low four bits of RN(q + M) are the code
         const float rcp = __frcp_rn(s);
+        constexpr float kLim = 0.5f - 0x1p-16f;
         uint32_t nearbits = 0u;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          bool nr;
-          const float k = rint_quot(__uint_as_float(v[j].w[e]), rcp, 0x1p-16f, nr);
-          nearbits |= (uint32_t)nr << e;
-          const int c = __float2int_rz(k);  // NaN -> 0
-          pk |= ((uint32_t)c & 0xfu) << ((e >> 1) * 8 + ((e & 1) ? 0 : 4));
+        for (int e = 0; e < 8; e += 2) {
+          float q0, q1, t0, t1, f0, f1, d0, d1;
+          mul2(__uint_as_float(v[j].w[e]), __uint_as_float(v[j].w[e + 1]), rcp, rcp, q0, q1);
+          add2(q0, q1, kRintMagic, kRintMagic, t0, t1);
+          sub2(t0, t1, kRintMagic, kRintMagic, f0, f1);
+          sub2(q0, q1, f0, f1, d0, d1);
+          nearbits |= ((uint32_t)(fabsf(d0) > kLim) << e) | ((uint32_t)(fabsf(d1) > kLim) << (e + 1));
+          // NaN elements: t is NaN, its low bits are not a code; they are near
+          // by the NaN test below and get code 0 from the exact path
+          if (isnan(q0)) nearbits |= 1u << e;
+          if (isnan(q1)) nearbits |= 1u << (e + 1);
+          pk |= ((__float_as_uint(t0) & 0xfu) << ((e >> 1) * 8 + 4)) |
+                ((__float_as_uint(t1) & 0xfu) << ((e >> 1) * 8));
         }
         if (nearbits) {
 #pragma unroll
@@ -221,6 +231,15 @@ __global__ void __launch_bounds__(kQ4Threads) k_q4_quant(const float* __restrict
           if (base / 2 + b < nbytes) data[base / 2 + b] = (uint8_t)(pk >> (8 * b));
       }
       if ((lane & 7) == 0) s_scale[j * (kQ4Threads / 8) + (tid >> 3)] = cnt[j] > 0 ? s : 0.0f;
+    }
+    {
+      const int64_t nsb = sb + gridDim.x;
+      have = nsb < nsuper && nsb * kQ4SuperElems + kQ4SuperElems <= n;
+      if (have) {
+#pragma unroll
+        for (int j = 0; j < kQ4Slots; ++j)
+          v[j] = ld_v32(x + nsb * kQ4SuperElems + (int64_t)(j * kQ4Threads + tid) * 8);
+      }
     }
     __syncthreads();
     // level 2: super = max(max scale, 1e-8); q = clamp(round(scale / super * 255), 0, 255)
@@ -276,41 +295,73 @@ qat_status launch_q4_quant(const float* x, int64_t n, uint8_t* data, uint8_t* qs
 // into 8 floats (one 32-byte store); a warp covers 256 contiguous elements
 // per store instruction
 // ---------------------------------------------------------------------------
+// The next step's code words, block scales and super-scales are requested
+// before the current step's arithmetic and stores (rolling prefetch).
+struct Q4Step {
+  static constexpr int K = 4;  // octets per lane per step
+  uint32_t pk[K];
+  float qs[K], sup[K];
+};
+
+template <bool FULL>
+__device__ __forceinline__ void q4_step_load(const uint8_t* __restrict__ data,
+                                             const uint8_t* __restrict__ qscales,
+                                             const float* __restrict__ sup, int64_t n, int64_t st,
+                                             int lane, Q4Step& d) {
+  const int64_t nbytes = (n + 1) / 2;
+#pragma unroll
+  for (int k = 0; k < Q4Step::K; ++k) {
+    const int64_t oct = st * (32 * Q4Step::K) + k * 32 + lane;
+    if (FULL || oct * 8 + 8 <= n) {
+      d.pk[k] = __ldg(reinterpret_cast<const uint32_t*>(data) + oct);
+    } else {
+      d.pk[k] = 0u;
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        if (oct * 4 + b < nbytes) d.pk[k] |= (uint32_t)data[oct * 4 + b] << (8 * b);
+    }
+    if (FULL || oct * 8 < n) {
+      const int64_t blk = oct >> 3;  // 8 octets per 64-element block
+      d.qs[k] = (float)__ldg(qscales + blk);
+      d.sup[k] = __ldg(sup + blk / kQ4Super);
+    } else {
+      d.qs[k] = 0.0f;
+      d.sup[k] = 0.0f;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) k_q4_dequant(const uint8_t* __restrict__ data,
                                                     const uint8_t* __restrict__ qscales,
                                                     const float* __restrict__ sup, int64_t n,
                                                     float* __restrict__ y) {
-  constexpr int K = 4;  // octets per lane per step
+  constexpr int K = Q4Step::K;
   const int lane = threadIdx.x & 31;
   const int64_t noct = (n + 7) / 8;
-  const int64_t nbytes = (n + 1) / 2;
   const int64_t nsteps = (noct + 32 * K - 1) / (32 * K);
+  const int64_t nfull = n / (256 * K);  // steps whose 32*K octets are all complete
   const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  Q4Step cur, nxt;
+  bool have = false;
   for (int64_t st = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); st < nsteps;
        st += wstride) {
-    uint32_t pk[K];
-    int64_t oct[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      oct[k] = st * (32 * K) + k * 32 + lane;
-      if (oct[k] * 8 + 8 <= n) {
-        pk[k] = __ldg(reinterpret_cast<const uint32_t*>(data) + oct[k]);
-      } else {
-        pk[k] = 0u;
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-          if (oct[k] * 4 + b < nbytes) pk[k] |= (uint32_t)data[oct[k] * 4 + b] << (8 * b);
-      }
+    if (have) {
+      cur = nxt;
+    } else if (st < nfull) {
+      q4_step_load<true>(data, qscales, sup, n, st, lane, cur);
+    } else {
+      q4_step_load<false>(data, qscales, sup, n, st, lane, cur);
     }
+    const int64_t ns = st + wstride;
+    have = ns < nfull;
+    if (have) q4_step_load<true>(data, qscales, sup, n, ns, lane, nxt);
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-      const int64_t e0 = oct[k] * 8;
+      const int64_t e0 = (st * (32 * K) + k * 32 + lane) * 8;
       if (e0 >= n) continue;
-      const int64_t blk = e0 / kQ4Block;
-      const float rs =
-          __fmul_rn(__fdiv_rn((float)__ldg(qscales + blk), 255.0f), __ldg(sup + blk / kQ4Super));
-      const V32 o = dequant8(pk[k], rs);
-      int64_t c = n - e0;
+      const float rs = __fmul_rn(__fdiv_rn(cur.qs[k], 255.0f), cur.sup[k]);
+      const V32 o = dequant8(cur.pk[k], rs);
+      const int64_t c = n - e0;
       store_vec<F32>(y, e0, o, c >= 8 ? 8 : (int)c);
     }
   }

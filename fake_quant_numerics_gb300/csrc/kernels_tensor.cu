@@ -21,28 +21,21 @@ namespace qat {
 // ---------------------------------------------------------------------------
 template <typename T, bool MINMAX, bool FULL>
 __device__ __forceinline__ void stats_tile(const void* __restrict__ x, int64_t n, int64_t tile,
-                                           Stats& st, int lane) {
+                                           V32 (&v)[kTile / (32 * T::VEC)], bool have,
+                                           int64_t next, Stats& st, int lane) {
   constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
-  const int64_t tb = tile * kTile;
-  V32 v[SLOTS];
   int cnt[SLOTS];
+  tile_load<T, FULL>(x, n, tile, v, cnt, have, lane);
 #pragma unroll
   for (int j = 0; j < SLOTS; ++j) {
-    int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
-    if (FULL) {
-      cnt[j] = VEC;
-      v[j] = ld_v32(static_cast<const char*>(x) + base * T::BYTES);
+    if (MINMAX) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e)
+        if (FULL || e < cnt[j]) st.add<true>(elem_bits<T>(v[j], e));
     } else {
-      int64_t c = n - base;
-      cnt[j] = c >= VEC ? VEC : (c > 0 ? (int)c : 0);
-      v[j] = load_vec<T>(x, cnt[j] > 0 ? base : 0, cnt[j]);
+      st.add_absmax<T>(v[j]);  // absent tail elements read +0
     }
-  }
-#pragma unroll
-  for (int j = 0; j < SLOTS; ++j) {
-#pragma unroll
-    for (int e = 0; e < VEC; ++e)
-      if (FULL || e < cnt[j]) st.add<MINMAX>(elem_bits<T>(v[j], e));
+    slot_prefetch<T>(x, next, j, v[j], lane);
   }
 }
 
@@ -56,10 +49,14 @@ __global__ void __launch_bounds__(512) k_stats_tensor(const void* __restrict__ x
   const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
   Stats st;
   st.init();
+  V32 v[kTile / (32 * T::VEC)];
+  bool have = false;
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
        t += wstride) {
-    if (t < nfull) stats_tile<T, MINMAX, true>(x, n, t, st, lane);
-    else stats_tile<T, MINMAX, false>(x, n, t, st, lane);
+    const int64_t next = -1;  // no rolling prefetch: occupancy matters more here
+    if (t < nfull) stats_tile<T, MINMAX, true>(x, n, t, v, have, next, st, lane);
+    else stats_tile<T, MINMAX, false>(x, n, t, v, have, next, st, lane);
+    have = next >= 0;
   }
   Stats b = block_reduce_stats<MINMAX>(st, red);
   if (threadIdx.x == 0) part[blockIdx.x] = b.pack();
@@ -74,7 +71,7 @@ __global__ void __launch_bounds__(256) k_stats_finalize(const uint4* __restrict_
     if (absmax) absmax[0] = s.absmax_f();
     if (minv) minv[0] = s.min_f();
     if (maxv) maxv[0] = s.max_f();
-    flag_or(flags, s.nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
+    flag_or(flags, s.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
   }
 }
 
@@ -83,25 +80,14 @@ __global__ void __launch_bounds__(256) k_stats_finalize(const uint4* __restrict_
 // ---------------------------------------------------------------------------
 template <typename T, int BITS, bool AFFINE, bool GIVEN, bool FULL>
 __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, int64_t tile,
+                                         V32 (&v)[kTile / (32 * T::VEC)], bool have, int64_t next,
                                          const IntParams& p, void* __restrict__ y,
                                          void* __restrict__ codes, uint32_t* __restrict__ mask,
                                          int lane) {
   constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
   const int64_t tb = tile * kTile;
-  V32 v[SLOTS];
   int cnt[SLOTS];
-#pragma unroll
-  for (int j = 0; j < SLOTS; ++j) {
-    int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
-    if (FULL) {
-      cnt[j] = VEC;
-      v[j] = ld_v32(static_cast<const char*>(x) + base * T::BYTES);
-    } else {
-      int64_t c = n - base;
-      cnt[j] = c >= VEC ? VEC : (c > 0 ? (int)c : 0);
-      v[j] = load_vec<T>(x, cnt[j] > 0 ? base : 0, cnt[j]);
-    }
-  }
+  tile_load<T, FULL>(x, n, tile, v, cnt, have, lane);
   uint32_t mw[SLOTS];
 #pragma unroll
   for (int j = 0; j < SLOTS; ++j) {
@@ -112,14 +98,16 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
     uint32_t mb = 0u;
     if (!GIVEN && p.fast) {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        int k;
-        float yv;
-        uint32_t m;
-        int_elem_cal<AFFINE>(elem<T>(v[j], e), p, k, yv, m);
-        ov.set(e, yv);
-        if (FULL || e < cnt[j]) cv.set(e, k + p.zp);
-        mb |= m << e;
+      for (int e = 0; e < VEC; e += 2) {
+        int ka, kb;
+        float ya, yb;
+        uint32_t ma, mb2;
+        int_pair_cal<AFFINE>(elem<T>(v[j], e), elem<T>(v[j], e + 1), p, ka, kb, ya, yb, ma, mb2);
+        ov.set(e, ya);
+        ov.set(e + 1, yb);
+        if (FULL || e < cnt[j]) cv.set(e, AFFINE ? ka + p.zp : ka);
+        if (FULL || e + 1 < cnt[j]) cv.set(e + 1, AFFINE ? kb + p.zp : kb);
+        mb |= (ma << e) | (mb2 << (e + 1));
       }
     } else if (!p.dead) {
 #pragma unroll
@@ -136,6 +124,7 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
 #pragma unroll
       for (int e = 0; e < VEC; ++e) ov.set(e, 0.0f);
     }
+    slot_prefetch<T>(x, next, j, v[j], lane);
     if (!FULL) mb &= (cnt[j] >= 32) ? 0xffffffffu : ((1u << cnt[j]) - 1u);
     if (cnt[j] > 0) {
       if (y) store_vec<T>(y, base, ov.v, cnt[j]);
@@ -179,13 +168,21 @@ __global__ void __launch_bounds__(256) k_int_tensor(const void* __restrict__ x, 
   const int64_t ntiles = (n + kTile - 1) / kTile;
   const int64_t nfull = n / kTile;
   const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  V32 v[kTile / (32 * T::VEC)];
+  bool have = false;
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
        t += wstride) {
     // calibrated: reverse order, so the first tiles read are the ones the
     // statistics pass touched last (still in L2)
     const int64_t tile = GIVEN ? t : ntiles - 1 - t;
-    if (tile < nfull) int_tile<T, BITS, AFFINE, GIVEN, true>(x, n, tile, p, y, codes, mask, lane);
-    else int_tile<T, BITS, AFFINE, GIVEN, false>(x, n, tile, p, y, codes, mask, lane);
+    const int64_t nt = t + wstride;
+    const int64_t ntile = GIVEN ? nt : ntiles - 1 - nt;
+    const int64_t next = (nt < ntiles && ntile < nfull) ? ntile : -1;
+    if (tile < nfull)
+      int_tile<T, BITS, AFFINE, GIVEN, true>(x, n, tile, v, have, next, p, y, codes, mask, lane);
+    else
+      int_tile<T, BITS, AFFINE, GIVEN, false>(x, n, tile, v, have, next, p, y, codes, mask, lane);
+    have = next >= 0;
   }
 }
 
@@ -289,7 +286,7 @@ __global__ void __launch_bounds__(256) k_unit_generic(const void* __restrict__ x
         if (absmax) absmax[u] = st.absmax_f();
         if (minv) minv[u] = st.min_f();
         if (maxv) maxv[u] = st.max_f();
-        flag_or(flags, st.nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
+        flag_or(flags, st.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
       } else {
         IntParams p;
         int f = calibrate<BITS, AFFINE>(st, p);

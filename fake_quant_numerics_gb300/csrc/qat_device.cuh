@@ -110,6 +110,40 @@ __device__ __forceinline__ V32 load_vec(const void* x, int64_t base, int cnt) {
   return v;
 }
 
+// ---------------------------------------------------------------------------
+// tile loads with a rolling prefetch
+// ---------------------------------------------------------------------------
+// `v` may already hold this tile (have, full tiles only); after a slot is
+// consumed, the same slot of the warp's next full tile (next >= 0) is
+// requested into it, so loads stay in flight while the warp computes.
+template <typename T, bool FULL>
+__device__ __forceinline__ void tile_load(const void* __restrict__ x, int64_t n, int64_t tile,
+                                          V32 (&v)[kTile / (32 * T::VEC)],
+                                          int (&cnt)[kTile / (32 * T::VEC)], bool have, int lane) {
+  constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
+  const int64_t tb = tile * kTile;
+#pragma unroll
+  for (int j = 0; j < SLOTS; ++j) {
+    const int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+    if (FULL) {
+      cnt[j] = VEC;
+      if (!have) v[j] = ld_v32(static_cast<const char*>(x) + base * T::BYTES);
+    } else {
+      const int64_t c = n - base;
+      cnt[j] = c >= VEC ? VEC : (c > 0 ? (int)c : 0);
+      v[j] = load_vec<T>(x, cnt[j] > 0 ? base : 0, cnt[j]);
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void slot_prefetch(const void* __restrict__ x, int64_t next, int j,
+                                              V32& vj, int lane) {
+  if (next >= 0)
+    vj = ld_v32(static_cast<const char*>(x) +
+                (next * kTile + (int64_t)(j * 32 + lane) * T::VEC) * T::BYTES);
+}
+
 // fp32 -> bf16 bits, round to nearest even (cvt.rn.bf16x2.f32 packs hi, lo)
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -248,14 +282,40 @@ __device__ __forceinline__ uint32_t gather_tile_word(const uint32_t (&mw)[SLOTS]
 }
 
 // ---------------------------------------------------------------------------
-// statistics on fp32 bit patterns
-//
-// absmax: every element maps to t = (bits << 1) + 2^24 (unsigned, wrapping).
-// For a finite value t - 2^24 = 2|bits| lies in [0, 0xfeffffff], so finite
-// values land in [2^24, 2^32 - 2] in the order of |x|; +-inf and NaN (|bits| >=
-// 0x7f800000) wrap around below 2^24.  max(t) is then the finite absmax and
-// min(t) < 2^24 says a NaN/Inf was seen -- two integer min/max per element.
-// min / max: order-preserving keys (-0 below +0) of the finite elements.
+// packed fp32 pairs: Blackwell f32x2 arithmetic, one IEEE round-to-nearest
+// operation per lane of the pair (the same results as two scalar ops)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mul2(float a0, float a1, float b0, float b1, float& r0, float& r1) {
+  asm("{ .reg .b64 x, y, r;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n"
+      " mul.rn.f32x2 r, x, y;\n mov.b64 {%0, %1}, r; }"
+      : "=f"(r0), "=f"(r1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void add2(float a0, float a1, float b0, float b1, float& r0, float& r1) {
+  asm("{ .reg .b64 x, y, r;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n"
+      " add.rn.f32x2 r, x, y;\n mov.b64 {%0, %1}, r; }"
+      : "=f"(r0), "=f"(r1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub2(float a0, float a1, float b0, float b1, float& r0, float& r1) {
+  asm("{ .reg .b64 x, y, r;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n"
+      " sub.rn.f32x2 r, x, y;\n mov.b64 {%0, %1}, r; }"
+      : "=f"(r0), "=f"(r1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// max with NaN propagation (max.NaN): NaN if either input is NaN
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// statistics on fp32 bit patterns: finite absmax (as bits of |x|), min / max
+// as order-preserving keys (-0 below +0), non-finite detection
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t order_key(uint32_t u) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -265,37 +325,60 @@ __device__ __forceinline__ uint32_t key_to_bits(uint32_t k) {
 }
 constexpr uint32_t kKeyPosInf = 0xff800000u;  // order_key(+inf)
 constexpr uint32_t kKeyNegInf = 0x007fffffu;  // order_key(-inf)
-constexpr uint32_t kAbsBias = 0x01000000u;
-
-__device__ __forceinline__ uint32_t abs_key(uint32_t u) { return (u << 1) + kAbsBias; }
 
 struct Stats {
-  uint32_t tmax;  // max abs_key: the finite absmax
-  uint32_t tmin;  // min abs_key: below kAbsBias iff a NaN/Inf was seen
-  uint32_t kmin;  // key of the finite min
-  uint32_t kmax;  // key of the finite max
+  uint32_t amax;       // bits of the finite absmax
+  uint32_t nonfinite;  // 1 if a NaN/Inf was seen
+  uint32_t kmin;       // key of the finite min
+  uint32_t kmax;       // key of the finite max
   __device__ __forceinline__ void init() {
-    tmax = 0u;
-    tmin = 0xffffffffu;
+    amax = 0u;
+    nonfinite = 0u;
     kmin = kKeyPosInf;
     kmax = kKeyNegInf;
   }
+  // one element, NaN/Inf filtered out (the general path)
   template <bool MINMAX>
   __device__ __forceinline__ void add(uint32_t u) {
-    const uint32_t t = abs_key(u);
-    tmax = max(tmax, t);
-    tmin = min(tmin, t);
+    const uint32_t a = u & 0x7fffffffu;
+    const bool fin = a < 0x7f800000u;
+    amax = max(amax, fin ? a : 0u);
+    nonfinite |= fin ? 0u : 1u;
     if (MINMAX) {
-      const bool fin = t >= kAbsBias;
       const uint32_t k = order_key(u);
       kmin = min(kmin, fin ? k : kKeyPosInf);
       kmax = max(kmax, fin ? k : kKeyNegInf);
     }
   }
+  // absmax of one 32-byte vector (absent tail elements read +0).  Fast fold:
+  // max.NaN of |x| -- one operation per element (per two for bf16).  Its
+  // result is the finite absmax unless the vector holds NaN or Inf; only then
+  // the filtered per-element fold runs.
+  template <typename T>
+  __device__ __forceinline__ void add_absmax(const V32& v) {
+    uint32_t r;
+    if (T::BYTES == 2) {
+      uint32_t m2 = 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m2 = bf16x2_max_nan(m2, v.w[k] & 0x7fff7fffu);
+      r = __float_as_uint(fmax_nan(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u)));
+    } else {
+      float m = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m = fmax_nan(m, fabsf(__uint_as_float(v.w[k])));
+      r = __float_as_uint(m);
+    }
+    if (r < 0x7f800000u) {
+      amax = max(amax, r);
+    } else {
+#pragma unroll
+      for (int e = 0; e < T::VEC; ++e) add<false>(elem_bits<T>(v, e));
+    }
+  }
   template <bool MINMAX>
   __device__ __forceinline__ void merge(const Stats& o) {
-    tmax = max(tmax, o.tmax);
-    tmin = min(tmin, o.tmin);
+    amax = max(amax, o.amax);
+    nonfinite |= o.nonfinite;
     if (MINMAX) {
       kmin = min(kmin, o.kmin);
       kmax = max(kmax, o.kmax);
@@ -305,28 +388,37 @@ struct Stats {
   template <bool MINMAX>
   __device__ __forceinline__ void reduce_lanes(int width) {
     for (int o = 1; o < width; o <<= 1) {
-      tmax = max(tmax, __shfl_xor_sync(kFull, tmax, o));
-      tmin = min(tmin, __shfl_xor_sync(kFull, tmin, o));
+      amax = max(amax, __shfl_xor_sync(kFull, amax, o));
+      nonfinite |= __shfl_xor_sync(kFull, nonfinite, o);
       if (MINMAX) {
         kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
         kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
       }
     }
   }
-  __device__ __forceinline__ bool nonfinite() const { return tmin < kAbsBias; }
-  __device__ __forceinline__ float absmax_f() const {
-    return __uint_as_float(tmax >= kAbsBias ? (tmax - kAbsBias) >> 1 : 0u);
-  }
+  __device__ __forceinline__ bool has_nonfinite() const { return nonfinite != 0u; }
+  __device__ __forceinline__ float absmax_f() const { return __uint_as_float(amax); }
   __device__ __forceinline__ float min_f() const { return __uint_as_float(key_to_bits(kmin)); }
   __device__ __forceinline__ float max_f() const { return __uint_as_float(key_to_bits(kmax)); }
-  __device__ __forceinline__ uint4 pack() const { return make_uint4(tmax, tmin, kmin, kmax); }
+  __device__ __forceinline__ uint4 pack() const { return make_uint4(amax, nonfinite, kmin, kmax); }
   __device__ __forceinline__ void unpack(const uint4& p) {
-    tmax = p.x;
-    tmin = p.y;
+    amax = p.x;
+    nonfinite = p.y;
     kmin = p.z;
     kmax = p.w;
   }
 };
+
+// statistics of one vector: the fast absmax fold when min / max are not needed
+template <typename T, bool MINMAX>
+__device__ __forceinline__ void stats_add_vec(Stats& st, const V32& v) {
+  if (MINMAX) {
+#pragma unroll
+    for (int e = 0; e < T::VEC; ++e) st.add<true>(elem_bits<T>(v, e));
+  } else {
+    st.add_absmax<T>(v);
+  }
+}
 
 // Block-wide reduction of Stats (all threads get the result).  `red` needs
 // 4 * (blockDim.x / 32) words of shared memory.
@@ -378,6 +470,7 @@ struct IntParams {
   float s;         // scale
   float rcp;       // RN(1/s), used when `fast`
   float wlo, whi;  // STE window [(qmin-zp)*s, (qmax-zp)*s]
+  float klof, khif;  // the clamp range as floats
   int klo, khi;    // clamp range of k = q - zp
   int zp;
   int dead;        // unit outputs are codes 0, y +0, mask 0
@@ -393,6 +486,8 @@ struct QRange {
 __device__ __forceinline__ void finish_params(IntParams& p, int qmin, int qmax) {
   p.klo = qmin - p.zp;
   p.khi = qmax - p.zp;
+  p.klof = (float)p.klo;
+  p.khif = (float)p.khi;
   p.wlo = __fmul_rn(__int2float_rn(qmin - p.zp), p.s);
   p.whi = __fmul_rn(__int2float_rn(qmax - p.zp), p.s);
 }
@@ -422,7 +517,7 @@ __device__ __forceinline__ int calibrate(const Stats& st, IntParams& p) {
       p.zp = (int)z;
     }
   }
-  int flag = st.nonfinite() ? QAT_FLAG_NONFINITE_CALIB : (degenerate ? QAT_FLAG_DEGENERATE : 0);
+  int flag = st.has_nonfinite() ? QAT_FLAG_NONFINITE_CALIB : (degenerate ? QAT_FLAG_DEGENERATE : 0);
   p.dead = flag != 0;
   p.fast = !p.dead && quot_scale_ok(p.s);
   p.rcp = p.fast ? __frcp_rn(p.s) : 0.0f;
@@ -475,6 +570,48 @@ __device__ __forceinline__ void int_elem_cal(float x, const IntParams& p, int& k
   if (AFFINE) k = min(max(k, p.klo), p.khi);
   y = __fmul_rn(__int2float_rn(k), p.s);
   m = AFFINE ? ((x >= p.wlo) && (x <= p.whi)) : (fabsf(x) <= p.whi);
+}
+
+// rint without the conversion unit: for |q| < 2^22, RN(q + M) with M = 1.5*2^23
+// lies in [2^23, 2^24) where the spacing is 1, so it is M + rint(q) (ties to
+// even, M being even); subtracting M back is exact and gives +0 for zero.  The
+// bit pattern of M + k is 0x4b400000 + k, so the integer comes for free.
+constexpr float kRintMagic = 12582912.0f;
+constexpr uint32_t kRintMagicBits = 0x4b400000u;
+
+// A pair of elements of a calibrated unit with p.fast set: the quotient from
+// the reciprocal, rounded with the magic constant, near-ties (see rint_quot)
+// decided from the correctly rounded quotient; k = q - zp, y = k * s, mask.
+template <bool AFFINE>
+__device__ __forceinline__ void int_pair_cal(float xa, float xb, const IntParams& p, int& ka,
+                                             int& kb, float& ya, float& yb, uint32_t& ma,
+                                             uint32_t& mb) {
+  constexpr float kLim = 0.5f - 0x1p-12f;  // |q| < 2^9: band 2^-12 > 2^(9-22)
+  float qa, qb, ta, tb, fa, fb, da, db;
+  mul2(xa, xb, p.rcp, p.rcp, qa, qb);
+  add2(qa, qb, kRintMagic, kRintMagic, ta, tb);
+  sub2(ta, tb, kRintMagic, kRintMagic, fa, fb);
+  sub2(qa, qb, fa, fb, da, db);  // exact, |d| <= 1/2
+  const bool na = fabsf(da) > kLim, nb = fabsf(db) > kLim;
+  if (na || nb) {
+    if (na) fa = __fadd_rn(rintf(__fdiv_rn(xa, p.s)), 0.0f);
+    if (nb) fb = __fadd_rn(rintf(__fdiv_rn(xb, p.s)), 0.0f);
+  }
+  if (AFFINE) {
+    fa = fminf(fmaxf(fa, p.klof), p.khif);
+    fb = fminf(fmaxf(fb, p.klof), p.khif);
+  }
+  mul2(fa, fb, p.s, p.s, ya, yb);
+  add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
+  ka = (int)(__float_as_uint(ta) - kRintMagicBits);
+  kb = (int)(__float_as_uint(tb) - kRintMagicBits);
+  if (AFFINE) {
+    ma = (xa >= p.wlo) && (xa <= p.whi);
+    mb = (xb >= p.wlo) && (xb <= p.whi);
+  } else {
+    ma = fabsf(xa) <= p.whi;
+    mb = fabsf(xb) <= p.whi;
+  }
 }
 
 __device__ __forceinline__ void flag_or(int32_t* flags, int bits) {
