@@ -92,7 +92,7 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
     cv.clear();
     uint32_t mb = 0u;
 #pragma unroll
-    for (int e = 0; e < VEC; e += 2) {
+    for (int e = VEC - 2; e >= 0; e -= 2) {
       const float x0 = elem<T>(v[j], e), x1 = elem<T>(v[j], e + 1);
       const bool n0 = isnan(x0), n1 = isnan(x1);
       uint32_t c0, c1;
@@ -125,8 +125,8 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
         mb |= (uint32_t)(fabsf(x1) <= p.lim) << (e + 1);
       }
       if (CODES) {
-        if (FULL || e < cnt[j]) cv.set(e, (int)(int8_t)c0);
-        if (FULL || e + 1 < cnt[j]) cv.set(e + 1, (int)(int8_t)c1);
+        cv.set2(e, (FULL || e < cnt[j]) ? (int)(int8_t)c0 : 0,
+                (FULL || e + 1 < cnt[j]) ? (int)(int8_t)c1 : 0);
       }
       if (T::BYTES == 4) {
         out.w[e] = (p.mode != 2 && n0) ? kNaN32 : __float_as_uint(y0);
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, 
       if (blockIdx.x == 0) flag_or(flags, sp.mode == 2 ? QAT_FLAG_BAD_PARAMS : 0);
     }
   } else {
-    Stats st = reduce_partials<false>(part, nparts, red);
+    Stats st = reduce_partials<kMMNone>(part, nparts, red);
     if (threadIdx.x == 0) {
       float s = __fdiv_rn(st.absmax_f(), kMax);
       sp.s = s;

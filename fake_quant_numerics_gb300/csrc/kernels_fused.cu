@@ -29,7 +29,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
                                            int lane, int& fl) {
   constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
   constexpr int L = VEC * LPG;
-  constexpr bool NEED_MINMAX = AFFINE || STATS_ONLY;
+  constexpr int MM = STATS_ONLY ? kMMKeys : (AFFINE ? kMMFloat : kMMNone);
   const int64_t tb = tile * kTile;
   bool present[SLOTS];
 #pragma unroll
@@ -52,17 +52,17 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
     const int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
     const int64_t u = base / L;
     Stats st;
-    st.init();
+    st.init<MM>();
     if (present[j]) {
-      stats_add_vec<T, NEED_MINMAX>(st, v[j]);
+      stats_add_vec<T, MM>(st, v[j]);
     }
-    st.reduce_lanes<NEED_MINMAX>(LPG);
+    st.reduce_lanes<MM>(LPG);
     const bool leader = present[j] && (lane % LPG) == 0;
     if (STATS_ONLY) {
       if (leader) {
         if (absmax) absmax[u] = st.absmax_f();
-        if (minv) minv[u] = st.min_f();
-        if (maxv) maxv[u] = st.max_f();
+        if (minv) minv[u] = st.min_f<MM>();
+        if (maxv) maxv[u] = st.max_f<MM>();
       }
       if (present[j] && st.has_nonfinite()) fl |= QAT_FLAG_NONFINITE_INPUT;
       mw[j] = 0u;
@@ -70,7 +70,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
       continue;
     }
     IntParams p;
-    int f = calibrate<BITS, AFFINE>(st, p);
+    int f = calibrate<BITS, AFFINE, MM>(st, p);
     if (leader) {
       scale[u] = p.s;
       if (zp) zp[u] = p.zp;
@@ -82,16 +82,14 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
     uint32_t mb = 0u;
     if (p.fast) {
 #pragma unroll
-      for (int e = 0; e < VEC; e += 2) {
+      for (int e = VEC - 2; e >= 0; e -= 2) {
         int ka, kb;
         float ya, yb;
         uint32_t ma, mb2;
         int_pair_cal<AFFINE>(elem<T>(v[j], e), elem<T>(v[j], e + 1), p, ka, kb, ya, yb, ma,
                              mb2);
-        ov.set(e, ya);
-        ov.set(e + 1, yb);
-        cv.set(e, AFFINE ? ka + p.zp : ka);
-        cv.set(e + 1, AFFINE ? kb + p.zp : kb);
+        ov.set2(e, ya, yb);
+        cv.set2(e, AFFINE ? ka + p.zp : ka, AFFINE ? kb + p.zp : kb);
         mb |= (ma << e) | (mb2 << (e + 1));
       }
     } else if (!p.dead) {
@@ -154,13 +152,13 @@ __global__ void __maxnreg__(T::BYTES == 4 ? 96 : 80) k_int_groups(const void* __
 // one thread block (256 threads) per unit of L elements, NV vectors / thread
 // ---------------------------------------------------------------------------
 template <typename T, int BITS, bool AFFINE, int NV, bool STATS_ONLY>
-__global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, int64_t units,
+__global__ void __launch_bounds__(256, (NV <= 2 && !AFFINE) ? 3 : 1) k_int_rows(const void* __restrict__ x, int64_t units,
                                                   int64_t L, float* scale, int32_t* zp,
                                                   float* absmax, float* minv, float* maxv, void* y,
                                                   void* codes, uint32_t* mask, int32_t* flags) {
   constexpr int VEC = T::VEC, NT = 256;
   constexpr int LPW = 32 / VEC;
-  constexpr bool NEED_MINMAX = AFFINE || STATS_ONLY;
+  constexpr int MM = STATS_ONLY ? kMMKeys : (AFFINE ? kMMFloat : kMMNone);
   __shared__ __align__(16) uint32_t red[4 * 8];
   const int lane = threadIdx.x & 31;
   const int nvec = (int)(L / VEC);
@@ -185,20 +183,20 @@ __global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, in
     V32 vn[NV];
     load_unit(u + gridDim.x, vn);
     Stats st;
-    st.init();
+    st.init<MM>();
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       int vi = threadIdx.x + j * NT;
       if (vi < nvec) {
-        stats_add_vec<T, NEED_MINMAX>(st, v[j]);
+        stats_add_vec<T, MM>(st, v[j]);
       }
     }
-    Stats b = block_reduce_stats<NEED_MINMAX>(st, red);
+    Stats b = block_reduce_stats<MM>(st, red);
     if (STATS_ONLY) {
       if (threadIdx.x == 0) {
         if (absmax) absmax[u] = b.absmax_f();
-        if (minv) minv[u] = b.min_f();
-        if (maxv) maxv[u] = b.max_f();
+        if (minv) minv[u] = b.min_f<MM>();
+        if (maxv) maxv[u] = b.max_f<MM>();
         flag_or(flags, b.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
       }
 #pragma unroll
@@ -206,7 +204,7 @@ __global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, in
       continue;
     }
     IntParams p;
-    int f = calibrate<BITS, AFFINE>(b, p);
+    int f = calibrate<BITS, AFFINE, MM>(b, p);
     if (threadIdx.x == 0) {
       scale[u] = p.s;
       if (zp) zp[u] = p.zp;
@@ -223,16 +221,14 @@ __global__ void __launch_bounds__(256) k_int_rows(const void* __restrict__ x, in
       uint32_t mb = 0u;
       if (p.fast) {
 #pragma unroll
-        for (int e = 0; e < VEC; e += 2) {
+        for (int e = VEC - 2; e >= 0; e -= 2) {
           int ka, kb;
           float ya, yb;
           uint32_t ma, mb2;
           int_pair_cal<AFFINE>(elem<T>(v[j], e), elem<T>(v[j], e + 1), p, ka, kb, ya, yb, ma,
                                mb2);
-          ov.set(e, ya);
-          ov.set(e + 1, yb);
-          cv.set(e, AFFINE ? ka + p.zp : ka);
-          cv.set(e + 1, AFFINE ? kb + p.zp : kb);
+          ov.set2(e, ya, yb);
+          cv.set2(e, AFFINE ? ka + p.zp : ka, AFFINE ? kb + p.zp : kb);
           mb |= (ma << e) | (mb2 << (e + 1));
         }
       } else if (!p.dead) {

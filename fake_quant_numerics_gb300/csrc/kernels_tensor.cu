@@ -19,7 +19,7 @@ namespace qat {
 // ---------------------------------------------------------------------------
 // per-tensor statistics: one uint4 partial (Stats::pack) per block
 // ---------------------------------------------------------------------------
-template <typename T, bool MINMAX, bool FULL>
+template <typename T, int MM, bool FULL>
 __device__ __forceinline__ void stats_tile(const void* __restrict__ x, int64_t n, int64_t tile,
                                            V32 (&v)[kTile / (32 * T::VEC)], bool have,
                                            int64_t next, Stats& st, int lane) {
@@ -28,18 +28,20 @@ __device__ __forceinline__ void stats_tile(const void* __restrict__ x, int64_t n
   tile_load<T, FULL>(x, n, tile, v, cnt, have, lane);
 #pragma unroll
   for (int j = 0; j < SLOTS; ++j) {
-    if (MINMAX) {
+    if (MM == kMMNone) {
+      st.add_absmax<T>(v[j]);  // absent tail elements read +0
+    } else if (FULL) {
+      stats_add_vec<T, MM>(st, v[j]);
+    } else {
 #pragma unroll
       for (int e = 0; e < VEC; ++e)
-        if (FULL || e < cnt[j]) st.add<true>(elem_bits<T>(v[j], e));
-    } else {
-      st.add_absmax<T>(v[j]);  // absent tail elements read +0
+        if (e < cnt[j]) st.add<MM>(elem_bits<T>(v[j], e));
     }
     slot_prefetch<T>(x, next, j, v[j], lane);
   }
 }
 
-template <typename T, bool MINMAX>
+template <typename T, int MM>
 __global__ void __launch_bounds__(512) k_stats_tensor(const void* __restrict__ x, int64_t n,
                                                       uint4* __restrict__ part) {
   __shared__ __align__(16) uint32_t red[4 * 16];
@@ -48,17 +50,17 @@ __global__ void __launch_bounds__(512) k_stats_tensor(const void* __restrict__ x
   const int64_t nfull = n / kTile;
   const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
   Stats st;
-  st.init();
+  st.init<MM>();
   V32 v[kTile / (32 * T::VEC)];
   bool have = false;
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
        t += wstride) {
     const int64_t next = -1;  // no rolling prefetch: occupancy matters more here
-    if (t < nfull) stats_tile<T, MINMAX, true>(x, n, t, v, have, next, st, lane);
-    else stats_tile<T, MINMAX, false>(x, n, t, v, have, next, st, lane);
+    if (t < nfull) stats_tile<T, MM, true>(x, n, t, v, have, next, st, lane);
+    else stats_tile<T, MM, false>(x, n, t, v, have, next, st, lane);
     have = next >= 0;
   }
-  Stats b = block_reduce_stats<MINMAX>(st, red);
+  Stats b = block_reduce_stats<MM>(st, red);
   if (threadIdx.x == 0) part[blockIdx.x] = b.pack();
 }
 
@@ -66,11 +68,11 @@ __global__ void __launch_bounds__(256) k_stats_finalize(const uint4* __restrict_
                                                         float* absmax, float* minv, float* maxv,
                                                         int32_t* flags) {
   __shared__ __align__(16) uint32_t red[4 * 8];
-  Stats s = reduce_partials<true>(part, nparts, red);
+  Stats s = reduce_partials<kMMKeys>(part, nparts, red);
   if (threadIdx.x == 0) {
     if (absmax) absmax[0] = s.absmax_f();
-    if (minv) minv[0] = s.min_f();
-    if (maxv) maxv[0] = s.max_f();
+    if (minv) minv[0] = s.min_f<kMMKeys>();
+    if (maxv) maxv[0] = s.max_f<kMMKeys>();
     flag_or(flags, s.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
   }
 }
@@ -98,15 +100,17 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
     uint32_t mb = 0u;
     if (!GIVEN && p.fast) {
 #pragma unroll
-      for (int e = 0; e < VEC; e += 2) {
+      for (int e = VEC - 2; e >= 0; e -= 2) {
         int ka, kb;
         float ya, yb;
         uint32_t ma, mb2;
         int_pair_cal<AFFINE>(elem<T>(v[j], e), elem<T>(v[j], e + 1), p, ka, kb, ya, yb, ma, mb2);
-        ov.set(e, ya);
-        ov.set(e + 1, yb);
-        if (FULL || e < cnt[j]) cv.set(e, AFFINE ? ka + p.zp : ka);
-        if (FULL || e + 1 < cnt[j]) cv.set(e + 1, AFFINE ? kb + p.zp : kb);
+        ov.set2(e, ya, yb);
+        if (AFFINE) {
+          ka += p.zp;
+          kb += p.zp;
+        }
+        cv.set2(e, (FULL || e < cnt[j]) ? ka : 0, (FULL || e + 1 < cnt[j]) ? kb : 0);
         mb |= (ma << e) | (mb2 << (e + 1));
       }
     } else if (!p.dead) {
@@ -152,9 +156,10 @@ __global__ void __launch_bounds__(256) k_int_tensor(const void* __restrict__ x, 
       if (blockIdx.x == 0) flag_or(flags, f);
     }
   } else {
-    Stats st = reduce_partials<AFFINE>(part, nparts, red);
+    constexpr int MM = AFFINE ? kMMFloat : kMMNone;
+    Stats st = reduce_partials<MM>(part, nparts, red);
     if (threadIdx.x == 0) {
-      int f = calibrate<BITS, AFFINE>(st, sp);
+      int f = calibrate<BITS, AFFINE, MM>(st, sp);
       if (blockIdx.x == 0) {
         scale[0] = sp.s;
         if (zp) zp[0] = sp.zp;
@@ -277,19 +282,19 @@ __global__ void __launch_bounds__(256) k_unit_generic(const void* __restrict__ x
   for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units;
        u += wstride) {
     Stats st;
-    st.init();
+    st.init<kMMKeys>();
     const int64_t off = u * L;
-    for (int64_t i = lane; i < L; i += 32) st.add<true>(load_elem_bits<T>(x, off + i));
-    st.reduce_lanes<true>(32);
+    for (int64_t i = lane; i < L; i += 32) st.add<kMMKeys>(load_elem_bits<T>(x, off + i));
+    st.reduce_lanes<kMMKeys>(32);
     if (lane == 0) {
       if (MODE == 0) {
         if (absmax) absmax[u] = st.absmax_f();
-        if (minv) minv[u] = st.min_f();
-        if (maxv) maxv[u] = st.max_f();
+        if (minv) minv[u] = st.min_f<kMMKeys>();
+        if (maxv) maxv[u] = st.max_f<kMMKeys>();
         flag_or(flags, st.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
       } else {
         IntParams p;
-        int f = calibrate<BITS, AFFINE>(st, p);
+        int f = calibrate<BITS, AFFINE, kMMKeys>(st, p);
         scale[u] = p.s;
         if (zp) zp[u] = p.zp;
         dead[u] = (uint8_t)p.dead;
@@ -320,16 +325,20 @@ static int map_grid(int64_t n, int per_sm) {
   return (int)(g < 1 ? 1 : g);
 }
 
-qat_status launch_stats_tensor(qat_dtype dt, const void* x, int64_t n, bool minmax, void* ws,
+qat_status launch_stats_tensor(qat_dtype dt, const void* x, int64_t n, int mm, void* ws,
                                int grid, cudaStream_t s) {
   uint4* part = static_cast<uint4*>(ws);
+#define QAT_ST(T, M) k_stats_tensor<T, M><<<grid, 512, 0, s>>>(x, n, part)
   if (dt == QAT_F32) {
-    if (minmax) k_stats_tensor<F32, true><<<grid, 512, 0, s>>>(x, n, part);
-    else k_stats_tensor<F32, false><<<grid, 512, 0, s>>>(x, n, part);
+    if (mm == kMMKeys) QAT_ST(F32, kMMKeys);
+    else if (mm == kMMFloat) QAT_ST(F32, kMMFloat);
+    else QAT_ST(F32, kMMNone);
   } else {
-    if (minmax) k_stats_tensor<BF16, true><<<grid, 512, 0, s>>>(x, n, part);
-    else k_stats_tensor<BF16, false><<<grid, 512, 0, s>>>(x, n, part);
+    if (mm == kMMKeys) QAT_ST(BF16, kMMKeys);
+    else if (mm == kMMFloat) QAT_ST(BF16, kMMFloat);
+    else QAT_ST(BF16, kMMNone);
   }
+#undef QAT_ST
   count_launch(1);
   return launch_status();
 }

@@ -125,7 +125,7 @@ qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t 
     if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
     if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
     int grid = stats_grid(n);
-    qat_status st = launch_stats_tensor(dtype, x, n, true, ws, grid, s);
+    qat_status st = launch_stats_tensor(dtype, x, n, kMMKeys, ws, grid, s);
     if (st) return st;
     return launch_stats_finalize(ws, grid, absmax, minv, maxv, flags, s);
   }
@@ -162,7 +162,7 @@ qat_status qat_fake_quant_int(const void* x, qat_dtype dtype, int64_t rows, int6
     if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
     if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
     int grid = stats_grid(n);
-    qat_status st = launch_stats_tensor(dtype, x, n, affine, ws, grid, s);
+    qat_status st = launch_stats_tensor(dtype, x, n, affine ? kMMFloat : kMMNone, ws, grid, s);
     if (st) return st;
     return launch_int_tensor(dtype, bits, affine, false, x, n, ws, grid, scale, zp, y, codes, mask,
                              flags, s);
@@ -202,7 +202,7 @@ qat_status qat_fake_quant_fp8(const void* x, qat_dtype dtype, int64_t n, qat_fp8
   if (!ws || ws_bytes < ws_bytes_for(1, n, QAT_PER_TENSOR, 0)) return QAT_ERR_WORKSPACE;
   if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
   int grid = stats_grid(n);
-  qat_status st = launch_stats_tensor(dtype, x, n, false, ws, grid, s);
+  qat_status st = launch_stats_tensor(dtype, x, n, kMMNone, ws, grid, s);
   if (st) return st;
   return launch_fp8_tensor(dtype, fmt, false, x, n, ws, grid, scale, y, codes, mask, flags, s);
 }

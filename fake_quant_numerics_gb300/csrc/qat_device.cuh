@@ -158,6 +158,10 @@ template <>
 struct OutVec<F32> {
   V32 v;
   __device__ __forceinline__ void set(int e, float y) { v.w[e] = __float_as_uint(y); }
+  __device__ __forceinline__ void set2(int e, float ya, float yb) {
+    v.w[e] = __float_as_uint(ya);
+    v.w[e + 1] = __float_as_uint(yb);
+  }
 };
 template <>
 struct OutVec<BF16> {
@@ -170,6 +174,7 @@ struct OutVec<BF16> {
       v.w[e >> 1] = pack_bf16x2(pend, y);
     }
   }
+  __device__ __forceinline__ void set2(int e, float ya, float yb) { v.w[e >> 1] = pack_bf16x2(ya, yb); }
 };
 
 // Store the first `cnt` elements of an output vector at element `base`.
@@ -213,31 +218,34 @@ template <int BITS, int VEC>
 struct CodeVec {
   static constexpr int NBYTES = BITS == 8 ? VEC : VEC / 2;
   static constexpr int NW = (NBYTES + 3) / 4;
-  int q[VEC];
+  uint32_t w[NW];
   __device__ __forceinline__ void clear() {
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) q[e] = 0;
+    for (int j = 0; j < NW; ++j) w[j] = 0u;
   }
-  // q: the integer code of element e (two's complement, low BITS bits used)
-  __device__ __forceinline__ void set(int e, int qv) { q[e] = qv; }
-  // word j: bytes 4j..4j+3, little endian
-  __device__ __forceinline__ uint32_t word(int j) const {
+  // codes of elements e and e + 1 (e even), packed into their word with the
+  // cvt.pack chain; within a word, pairs must come in descending order
+  // (the earlier bytes are shifted up by the later calls)
+  __device__ __forceinline__ void set2(int e, int qa, int qb) {
     if (BITS == 8) {
-      return pack_s8x2(q[4 * j + 1], q[4 * j], pack_s8x2(q[4 * j + 3], q[4 * j + 2], 0u));
+      w[e >> 2] = pack_s8x2(qb, qa, w[e >> 2]);
     } else {
-      uint32_t d = pack_s4x2(q[8 * j + 6], q[8 * j + 7], 0u);
-      d = pack_s4x2(q[8 * j + 4], q[8 * j + 5], d);
-      d = pack_s4x2(q[8 * j + 2], q[8 * j + 3], d);
-      return pack_s4x2(q[8 * j], q[8 * j + 1], d);
+      w[e >> 3] = pack_s4x2(qa, qb, w[e >> 3]);
+    }
+  }
+  // one code, any order (OR-ed into a cleared word)
+  __device__ __forceinline__ void set(int e, int q) {
+    if (BITS == 8) {
+      w[e >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << ((e & 3) * 8);
+    } else {
+      const int byte = e >> 1;
+      w[byte >> 2] |= (static_cast<uint32_t>(q) & 0xfu) << ((byte & 3) * 8 + ((e & 1) ? 0 : 4));
     }
   }
   // store at element offset `base` (codes buffer byte offset base*BITS/8);
   // `cnt` elements present (absent ones must hold code 0)
   __device__ __forceinline__ void store(void* codes, int64_t base, int cnt) const {
     uint8_t* p = static_cast<uint8_t*>(codes) + (BITS == 8 ? base : base / 2);
-    uint32_t w[NW];
-#pragma unroll
-    for (int j = 0; j < NW; ++j) w[j] = word(j);
     if (cnt >= VEC) {
       if (NBYTES == 16) {
         *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -326,80 +334,126 @@ __device__ __forceinline__ uint32_t key_to_bits(uint32_t k) {
 constexpr uint32_t kKeyPosInf = 0xff800000u;  // order_key(+inf)
 constexpr uint32_t kKeyNegInf = 0x007fffffu;  // order_key(-inf)
 
+// What a Stats fold tracks besides the finite absmax:
+//   kMMNone  -- nothing (symmetric grids, FP8);
+//   kMMFloat -- finite min / max as floats (calibration of affine grids, where
+//               the sign of a zero extreme cannot matter: only min(m, 0) and
+//               max(M, 0) are used);
+//   kMMKeys  -- finite min / max as order keys with -0 below +0 (the
+//               statistics entry point, whose outputs expose the zero sign).
+constexpr int kMMNone = 0, kMMFloat = 1, kMMKeys = 2;
+
 struct Stats {
   uint32_t amax;       // bits of the finite absmax
   uint32_t nonfinite;  // 1 if a NaN/Inf was seen
-  uint32_t kmin;       // key of the finite min
-  uint32_t kmax;       // key of the finite max
+  uint32_t kmin;       // finite min: key (kMMKeys) or float bits (kMMFloat)
+  uint32_t kmax;       // finite max: key (kMMKeys) or float bits (kMMFloat)
+  template <int MM>
   __device__ __forceinline__ void init() {
     amax = 0u;
     nonfinite = 0u;
-    kmin = kKeyPosInf;
-    kmax = kKeyNegInf;
+    kmin = MM == kMMFloat ? 0x7f800000u : kKeyPosInf;  // +inf
+    kmax = MM == kMMFloat ? 0xff800000u : kKeyNegInf;  // -inf
   }
   // one element, NaN/Inf filtered out (the general path)
-  template <bool MINMAX>
+  template <int MM>
   __device__ __forceinline__ void add(uint32_t u) {
     const uint32_t a = u & 0x7fffffffu;
     const bool fin = a < 0x7f800000u;
     amax = max(amax, fin ? a : 0u);
     nonfinite |= fin ? 0u : 1u;
-    if (MINMAX) {
+    if (MM == kMMKeys) {
       const uint32_t k = order_key(u);
       kmin = min(kmin, fin ? k : kKeyPosInf);
       kmax = max(kmax, fin ? k : kKeyNegInf);
+    } else if (MM == kMMFloat && fin) {
+      kmin = __float_as_uint(fminf(__uint_as_float(kmin), __uint_as_float(u)));
+      kmax = __float_as_uint(fmaxf(__uint_as_float(kmax), __uint_as_float(u)));
     }
   }
-  // absmax of one 32-byte vector (absent tail elements read +0).  Fast fold:
-  // max.NaN of |x| -- one operation per element (per two for bf16).  Its
-  // result is the finite absmax unless the vector holds NaN or Inf; only then
-  // the filtered per-element fold runs.
+  // max.NaN of |x| over a 32-byte vector: the finite absmax bits, or a value
+  // >= 0x7f800000 when the vector holds NaN or Inf
   template <typename T>
-  __device__ __forceinline__ void add_absmax(const V32& v) {
-    uint32_t r;
+  __device__ __forceinline__ uint32_t vec_absmax_nan(const V32& v) const {
     if (T::BYTES == 2) {
       uint32_t m2 = 0u;
 #pragma unroll
       for (int k = 0; k < 8; ++k) m2 = bf16x2_max_nan(m2, v.w[k] & 0x7fff7fffu);
-      r = __float_as_uint(fmax_nan(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u)));
-    } else {
-      float m = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) m = fmax_nan(m, fabsf(__uint_as_float(v.w[k])));
-      r = __float_as_uint(m);
+      return __float_as_uint(fmax_nan(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u)));
     }
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m = fmax_nan(m, fabsf(__uint_as_float(v.w[k])));
+    return __float_as_uint(m);
+  }
+  // absmax of one 32-byte vector (absent tail elements read +0): one max.NaN
+  // per element (per two for bf16); only a vector holding NaN or Inf takes
+  // the filtered per-element fold.
+  template <typename T>
+  __device__ __forceinline__ void add_absmax(const V32& v) {
+    const uint32_t r = vec_absmax_nan<T>(v);
     if (r < 0x7f800000u) {
       amax = max(amax, r);
     } else {
 #pragma unroll
-      for (int e = 0; e < T::VEC; ++e) add<false>(elem_bits<T>(v, e));
+      for (int e = 0; e < T::VEC; ++e) add<kMMNone>(elem_bits<T>(v, e));
     }
   }
-  template <bool MINMAX>
+  // finite min / max as floats of one full 32-byte vector (kMMFloat): plain
+  // fminf / fmaxf unless the vector holds NaN or Inf
+  template <typename T>
+  __device__ __forceinline__ void add_minmax_float(const V32& v) {
+    if (vec_absmax_nan<T>(v) < 0x7f800000u) {
+      float mn = __uint_as_float(kmin), mx = __uint_as_float(kmax);
+#pragma unroll
+      for (int e = 0; e < T::VEC; ++e) {
+        const float x = __uint_as_float(elem_bits<T>(v, e));
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+      }
+      kmin = __float_as_uint(mn);
+      kmax = __float_as_uint(mx);
+    } else {
+#pragma unroll
+      for (int e = 0; e < T::VEC; ++e) add<kMMFloat>(elem_bits<T>(v, e));
+    }
+  }
+  template <int MM>
   __device__ __forceinline__ void merge(const Stats& o) {
     amax = max(amax, o.amax);
     nonfinite |= o.nonfinite;
-    if (MINMAX) {
+    if (MM == kMMKeys) {
       kmin = min(kmin, o.kmin);
       kmax = max(kmax, o.kmax);
+    } else if (MM == kMMFloat) {
+      kmin = __float_as_uint(fminf(__uint_as_float(kmin), __uint_as_float(o.kmin)));
+      kmax = __float_as_uint(fmaxf(__uint_as_float(kmax), __uint_as_float(o.kmax)));
     }
   }
   // reduce over `width` consecutive lanes (a power of two <= 32)
-  template <bool MINMAX>
+  template <int MM>
   __device__ __forceinline__ void reduce_lanes(int width) {
     for (int o = 1; o < width; o <<= 1) {
-      amax = max(amax, __shfl_xor_sync(kFull, amax, o));
-      nonfinite |= __shfl_xor_sync(kFull, nonfinite, o);
-      if (MINMAX) {
-        kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
-        kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+      Stats t;
+      t.amax = __shfl_xor_sync(kFull, amax, o);
+      t.nonfinite = __shfl_xor_sync(kFull, nonfinite, o);
+      if (MM != kMMNone) {
+        t.kmin = __shfl_xor_sync(kFull, kmin, o);
+        t.kmax = __shfl_xor_sync(kFull, kmax, o);
       }
+      merge<MM>(t);
     }
   }
   __device__ __forceinline__ bool has_nonfinite() const { return nonfinite != 0u; }
   __device__ __forceinline__ float absmax_f() const { return __uint_as_float(amax); }
-  __device__ __forceinline__ float min_f() const { return __uint_as_float(key_to_bits(kmin)); }
-  __device__ __forceinline__ float max_f() const { return __uint_as_float(key_to_bits(kmax)); }
+  template <int MM>
+  __device__ __forceinline__ float min_f() const {
+    return __uint_as_float(MM == kMMKeys ? key_to_bits(kmin) : kmin);
+  }
+  template <int MM>
+  __device__ __forceinline__ float max_f() const {
+    return __uint_as_float(MM == kMMKeys ? key_to_bits(kmax) : kmax);
+  }
   __device__ __forceinline__ uint4 pack() const { return make_uint4(amax, nonfinite, kmin, kmax); }
   __device__ __forceinline__ void unpack(const uint4& p) {
     amax = p.x;
@@ -409,12 +463,14 @@ struct Stats {
   }
 };
 
-// statistics of one vector: the fast absmax fold when min / max are not needed
-template <typename T, bool MINMAX>
+// statistics of one full vector
+template <typename T, int MM>
 __device__ __forceinline__ void stats_add_vec(Stats& st, const V32& v) {
-  if (MINMAX) {
+  if (MM == kMMKeys) {
 #pragma unroll
-    for (int e = 0; e < T::VEC; ++e) st.add<true>(elem_bits<T>(v, e));
+    for (int e = 0; e < T::VEC; ++e) st.add<kMMKeys>(elem_bits<T>(v, e));
+  } else if (MM == kMMFloat) {
+    st.add_minmax_float<T>(v);
   } else {
     st.add_absmax<T>(v);
   }
@@ -422,19 +478,19 @@ __device__ __forceinline__ void stats_add_vec(Stats& st, const V32& v) {
 
 // Block-wide reduction of Stats (all threads get the result).  `red` needs
 // 4 * (blockDim.x / 32) words of shared memory.
-template <bool MINMAX>
+template <int MM>
 __device__ __forceinline__ Stats block_reduce_stats(Stats s, uint32_t* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  s.reduce_lanes<MINMAX>(32);
+  s.reduce_lanes<MM>(32);
   __syncthreads();  // red may still be read from a previous use
   if (lane == 0) reinterpret_cast<uint4*>(red)[warp] = s.pack();
   __syncthreads();
   Stats t;
-  t.init();
+  t.init<MM>();
   for (int w = 0; w < nw; ++w) {
     Stats o;
     o.unpack(reinterpret_cast<const uint4*>(red)[w]);
-    t.merge<MINMAX>(o);
+    t.merge<MM>(o);
   }
   return t;
 }
@@ -448,20 +504,12 @@ __device__ __forceinline__ Stats block_reduce_stats(Stats s, uint32_t* red) {
 // more than 2.5 ulp(q0) away from every half-integer, RN(x/s) lies in the same
 // open interval between consecutive half-integers as q0, and any rounding of
 // RN(x/s) to an integer (ties to even or away from zero) equals rint(q0).
-// For |q0| < 2^m that distance is below 2^(m-22); `band` must be at least
-// that.  `near` marks the elements that are not covered: the caller
-// recomputes them from the correctly rounded quotient __fdiv_rn(x, s).
+// For |q0| < 2^m that distance is below 2^(m-22); the band used must be at
+// least that.  Elements inside the band are recomputed by the caller from the
+// correctly rounded quotient __fdiv_rn(x, s).
 // Safe scales: s and 1/s normal and far from overflow, s in [2^-80, 2^100].
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool quot_scale_ok(float s) { return s >= 0x1p-80f && s <= 0x1p100f; }
-
-__device__ __forceinline__ float rint_quot(float x, float rcp, float band, bool& near) {
-  const float q0 = __fmul_rn(x, rcp);
-  const float k = rintf(q0);
-  // q0 - k is exact (|q0 - k| <= 1/2); its distance to +-1/2 decides
-  near = fabsf(__fsub_rn(fabsf(__fsub_rn(q0, k)), 0.5f)) < band;
-  return k;
-}
 
 // ---------------------------------------------------------------------------
 // integer grid parameters of one unit
@@ -474,7 +522,7 @@ struct IntParams {
   int klo, khi;    // clamp range of k = q - zp
   int zp;
   int dead;        // unit outputs are codes 0, y +0, mask 0
-  int fast;        // calibrated unit with a scale in the safe range of rint_quot
+  int fast;        // calibrated unit with a scale in the safe range (quot_scale_ok)
 };
 
 template <int BITS, bool AFFINE>
@@ -494,7 +542,7 @@ __device__ __forceinline__ void finish_params(IntParams& p, int qmin, int qmax) 
 
 // Calibration (QuantParams::from_absmax / from_minmax).  Returns the flag bit
 // (0, QAT_FLAG_NONFINITE_CALIB or QAT_FLAG_DEGENERATE).
-template <int BITS, bool AFFINE>
+template <int BITS, bool AFFINE, int MM>
 __device__ __forceinline__ int calibrate(const Stats& st, IntParams& p) {
   constexpr int qmin = QRange<BITS, AFFINE>::qmin, qmax = QRange<BITS, AFFINE>::qmax;
   int degenerate = 0;
@@ -504,7 +552,7 @@ __device__ __forceinline__ int calibrate(const Stats& st, IntParams& p) {
     p.s = __fdiv_rn(A, (float)qmax);
     degenerate = !(A > 0.0f) || !(p.s > 0.0f) || isinf(p.s);
   } else {
-    float mn = st.min_f(), mx = st.max_f();
+    float mn = st.min_f<MM>(), mx = st.max_f<MM>();
     float rmin = (mn < 0.0f) ? mn : 0.0f;
     float rmax = (mx > 0.0f) ? mx : 0.0f;
     float range = __fsub_rn(rmax, rmin);
@@ -554,24 +602,6 @@ __device__ __forceinline__ void int_elem(float x, const IntParams& p, int& q, fl
   m = (x >= p.wlo) && (x <= p.whi);
 }
 
-// One element of a calibrated unit with p.fast set: the quotient from the
-// reciprocal (rint_quot; |q| <= qmax - qmin <= 255 < 2^9, band 2^-12 > 2^(9-22)),
-// near-ties from the correctly rounded quotient.  Returns k = q - zp.
-// Symmetric: |x| <= absmax bounds |x/s| by qmax (1 + 2^-24)^3 < qmax + 1/2, so
-// k never leaves [-qmax, qmax] and needs no clamp, and the window
-// [-qmax*s, qmax*s] is |x| <= qmax*s.
-template <bool AFFINE>
-__device__ __forceinline__ void int_elem_cal(float x, const IntParams& p, int& k, float& y,
-                                             uint32_t& m) {
-  bool nr;
-  float kf = rint_quot(x, p.rcp, 0x1p-12f, nr);
-  if (nr) kf = rintf(__fdiv_rn(x, p.s));
-  k = __float2int_rz(kf);
-  if (AFFINE) k = min(max(k, p.klo), p.khi);
-  y = __fmul_rn(__int2float_rn(k), p.s);
-  m = AFFINE ? ((x >= p.wlo) && (x <= p.whi)) : (fabsf(x) <= p.whi);
-}
-
 // rint without the conversion unit: for |q| < 2^22, RN(q + M) with M = 1.5*2^23
 // lies in [2^23, 2^24) where the spacing is 1, so it is M + rint(q) (ties to
 // even, M being even); subtracting M back is exact and gives +0 for zero.  The
@@ -580,8 +610,9 @@ constexpr float kRintMagic = 12582912.0f;
 constexpr uint32_t kRintMagicBits = 0x4b400000u;
 
 // A pair of elements of a calibrated unit with p.fast set: the quotient from
-// the reciprocal, rounded with the magic constant, near-ties (see rint_quot)
+// the reciprocal, rounded with the magic constant, near-ties
 // decided from the correctly rounded quotient; k = q - zp, y = k * s, mask.
+// (see the quotient note above quot_scale_ok)
 template <bool AFFINE>
 __device__ __forceinline__ void int_pair_cal(float xa, float xb, const IntParams& p, int& ka,
                                              int& kb, float& ya, float& yb, uint32_t& ma,
@@ -626,16 +657,16 @@ __device__ __forceinline__ void warp_flag_or(int32_t* flags, int bits) {
 
 // Read the cross-CTA partials written by the per-tensor statistics kernel
 // and reduce them (every thread of the block gets the result).
-template <bool MINMAX>
+template <int MM>
 __device__ __forceinline__ Stats reduce_partials(const uint4* part, int nparts, uint32_t* red) {
   Stats s;
-  s.init();
+  s.init<MM>();
   for (int i = threadIdx.x; i < nparts; i += blockDim.x) {
     Stats o;
     o.unpack(part[i]);
-    s.merge<MINMAX>(o);
+    s.merge<MM>(o);
   }
-  return block_reduce_stats<MINMAX>(s, red);
+  return block_reduce_stats<MM>(s, red);
 }
 
 }  // namespace qat

@@ -19,8 +19,9 @@ qat_status launch_status();  // QAT_OK or QAT_ERR_CUDA after a <<<>>> launch
 // Grid for a per-tensor statistics pass (<= kMaxPartials blocks).
 int stats_grid(int64_t n);
 
-// per-tensor statistics -> workspace partials (uint4 per block)
-qat_status launch_stats_tensor(qat_dtype dt, const void* x, int64_t n, bool minmax, void* ws,
+// per-tensor statistics -> workspace partials (uint4 per block); mm is the
+// min / max mode of Stats (kMMNone, kMMFloat, kMMKeys)
+qat_status launch_stats_tensor(qat_dtype dt, const void* x, int64_t n, int mm, void* ws,
                                int grid, cudaStream_t s);
 // partials -> absmax / min / max (one thread block)
 qat_status launch_stats_finalize(const void* ws, int nparts, float* absmax, float* minv, float* maxv,

@@ -77,7 +77,7 @@ extern "C" qat_status qat_fake_quant_fp8_noalloc(const void* x, qat_dtype dtype,
   void* ws = nullptr;
   qat_status st = scratch_of_current_device(&ws);
   if (st) return st;
-  st = qat::launch_stats_tensor(dtype, x, n, false, ws, grid, s);
+  st = qat::launch_stats_tensor(dtype, x, n, qat::kMMNone, ws, grid, s);
   if (st) return st;
   return qat::launch_fp8_tensor(dtype, fmt, false, x, n, ws, grid, scale, y, codes, mask, flags, s);
 }
