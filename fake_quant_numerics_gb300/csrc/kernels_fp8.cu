@@ -56,10 +56,11 @@ __device__ __forceinline__ void fp8x2_decode(uint32_t c2, float& lo, float& hi) 
 // cast to the same code, that is the code of RN(x/s); otherwise the pair is
 // recomputed from the correctly rounded quotient.
 struct Fp8Params {
-  float s;         // scale
-  float lim;       // fmt_max * s: the STE window |x| <= lim
-  float rlo, rhi;  // bracketing reciprocals (fast == 1)
-  int mode;        // 0 normal, 1 zero scale, 2 invalid given scale
+  float s;          // scale
+  float lim;        // fmt_max * s: the STE window |x| <= lim
+  float rlo, rhi;   // bracketing reciprocals (fast == 1)
+  uint32_t limh2;   // (bf16 magnitude bits of the largest bf16 <= lim) | 0x8000, in both halves
+  int mode;         // 0 normal, 1 zero scale, 2 invalid given scale
   int fast;
 };
 
@@ -68,10 +69,51 @@ __device__ __forceinline__ void fp8_params_finish(Fp8Params& p) {
   const float rcp = p.fast ? __frcp_rn(p.s) : 1.0f;
   p.rlo = __fmul_rn(rcp, 1.0f - 0x1p-21f);
   p.rhi = __fmul_rn(rcp, 1.0f + 0x1p-21f);
+  // lim >= 0 is finite when fast; truncating its bits to 16 rounds toward 0
+  p.limh2 = ((__float_as_uint(p.lim) >> 16) | 0x8000u) * 0x00010001u;
 }
 
 constexpr uint32_t kNaN32 = 0x7fc00000u;
 constexpr uint32_t kNaN16 = 0x7fc0u;
+
+// One bf16 vector (16 elements, 8 bf16x2 words) on the bracketing path,
+// with the element tests done on the packed words: a = w & 0x7fff7fff holds
+// both magnitudes; a half above 0x7f80 is a NaN (adding 0x7f carries into
+// its top bit), and |x| <= lim is (0x8000 | L) - a >= 0x8000 per half, L the
+// magnitude bits of the largest bf16 not above lim (no borrow crosses the
+// halves since every a <= 0x7fff).  Returns false, leaving the vector to the
+// element-wise path, when a NaN is present or a bracket splits.
+template <int FMT, bool CODES>
+__device__ __forceinline__ bool fp8_vec_bf16_fast(const V32& v, const Fp8Params& p, V32& out,
+                                                  CodeVec<8, 16>& cv, uint32_t& mb) {
+  uint32_t bad = 0u, macc = 0u, pend = 0u;
+#pragma unroll
+  for (int e = 14; e >= 0; e -= 2) {
+    const uint32_t w = v.w[e >> 1];
+    const uint32_t a = w & 0x7fff7fffu;
+    bad |= (a + 0x007f007fu) & 0x80008000u;
+    // window bits of elements e and e + 1 land on bits e and 16 + e
+    macc |= ((p.limh2 - a) & 0x80008000u) >> (15 - e);
+    const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xffff0000u);
+    float l0, l1, h0, h1;
+    mul2(x0, x1, p.rlo, p.rlo, l0, l1);
+    mul2(x0, x1, p.rhi, p.rhi, h0, h1);
+    const uint32_t c2 = fp8x2_encode<FMT>(l0, l1);
+    bad |= c2 ^ fp8x2_encode<FMT>(h0, h1);
+    float d0, d1, y0, y1;
+    fp8x2_decode<FMT>(c2, d0, d1);
+    mul2(d0, d1, p.s, p.s, y0, y1);
+    out.w[e >> 1] = pack_bf16x2(y0, y1);
+    if (CODES) {
+      if (e & 2)
+        pend = c2;
+      else
+        cv.w[e >> 2] = __byte_perm(c2, pend, 0x5410);  // codes e .. e + 3
+    }
+  }
+  mb = (macc & 0x5555u) | ((macc >> 15) & 0xaaaau);
+  return bad == 0u;
+}
 
 template <typename T, int FMT, bool CODES, bool FULL>
 __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, int64_t tile,
@@ -89,55 +131,62 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
     const int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
     V32 out;
     CodeVec<8, VEC> cv;
-    cv.clear();
     uint32_t mb = 0u;
-#pragma unroll
-    for (int e = VEC - 2; e >= 0; e -= 2) {
-      const float x0 = elem<T>(v[j], e), x1 = elem<T>(v[j], e + 1);
-      const bool n0 = isnan(x0), n1 = isnan(x1);
-      uint32_t c0, c1;
-      float y0, y1;
-      if (p.mode == 0) {
-        uint32_t c2;
-        if (p.fast) {
-          float l0, l1, h0, h1;
-          mul2(x0, x1, p.rlo, p.rlo, l0, l1);
-          mul2(x0, x1, p.rhi, p.rhi, h0, h1);
-          c2 = fp8x2_encode<FMT>(l0, l1);
-          const uint32_t h2 = fp8x2_encode<FMT>(h0, h1);
-          if (c2 != h2) c2 = fp8x2_encode<FMT>(__fdiv_rn(x0, p.s), __fdiv_rn(x1, p.s));
+    bool done = false;
+    if constexpr (T::BYTES == 2) {
+      if (p.fast) done = fp8_vec_bf16_fast<FMT, CODES>(v[j], p, out, cv, mb);
+    }
+    if (!done) {
+      cv.clear();
+      mb = 0u;
+  #pragma unroll
+      for (int e = VEC - 2; e >= 0; e -= 2) {
+        const float x0 = elem<T>(v[j], e), x1 = elem<T>(v[j], e + 1);
+        const bool n0 = isnan(x0), n1 = isnan(x1);
+        uint32_t c0, c1;
+        float y0, y1;
+        if (p.mode == 0) {
+          uint32_t c2;
+          if (p.fast) {
+            float l0, l1, h0, h1;
+            mul2(x0, x1, p.rlo, p.rlo, l0, l1);
+            mul2(x0, x1, p.rhi, p.rhi, h0, h1);
+            c2 = fp8x2_encode<FMT>(l0, l1);
+            const uint32_t h2 = fp8x2_encode<FMT>(h0, h1);
+            if (c2 != h2) c2 = fp8x2_encode<FMT>(__fdiv_rn(x0, p.s), __fdiv_rn(x1, p.s));
+          } else {
+            c2 = fp8x2_encode<FMT>(__fdiv_rn(x0, p.s), __fdiv_rn(x1, p.s));
+          }
+          float d0, d1;
+          fp8x2_decode<FMT>(c2, d0, d1);
+          c0 = c2 & 0xffu;
+          c1 = (c2 >> 8) & 0xffu;
+          mul2(d0, d1, p.s, p.s, y0, y1);
         } else {
-          c2 = fp8x2_encode<FMT>(__fdiv_rn(x0, p.s), __fdiv_rn(x1, p.s));
+          c0 = c1 = 0u;
+          y0 = y1 = 0.0f;
         }
-        float d0, d1;
-        fp8x2_decode<FMT>(c2, d0, d1);
-        c0 = c2 & 0xffu;
-        c1 = (c2 >> 8) & 0xffu;
-        mul2(d0, d1, p.s, p.s, y0, y1);
-      } else {
-        c0 = c1 = 0u;
-        y0 = y1 = 0.0f;
-      }
-      if (p.mode != 2) {
-        if (n0) c0 = 0x7fu;
-        if (n1) c1 = 0x7fu;
-        mb |= (uint32_t)(fabsf(x0) <= p.lim) << e;
-        mb |= (uint32_t)(fabsf(x1) <= p.lim) << (e + 1);
-      }
-      if (CODES) {
-        cv.set2(e, (FULL || e < cnt[j]) ? (int)(int8_t)c0 : 0,
-                (FULL || e + 1 < cnt[j]) ? (int)(int8_t)c1 : 0);
-      }
-      if (T::BYTES == 4) {
-        out.w[e] = (p.mode != 2 && n0) ? kNaN32 : __float_as_uint(y0);
-        out.w[e + 1] = (p.mode != 2 && n1) ? kNaN32 : __float_as_uint(y1);
-      } else {
-        uint32_t w = pack_bf16x2(y0, y1);
         if (p.mode != 2) {
-          if (n0) w = (w & 0xffff0000u) | kNaN16;
-          if (n1) w = (w & 0x0000ffffu) | (kNaN16 << 16);
+          if (n0) c0 = 0x7fu;
+          if (n1) c1 = 0x7fu;
+          mb |= (uint32_t)(fabsf(x0) <= p.lim) << e;
+          mb |= (uint32_t)(fabsf(x1) <= p.lim) << (e + 1);
         }
-        out.w[e >> 1] = w;
+        if (CODES) {
+          cv.set2(e, (FULL || e < cnt[j]) ? (int)(int8_t)c0 : 0,
+                  (FULL || e + 1 < cnt[j]) ? (int)(int8_t)c1 : 0);
+        }
+        if (T::BYTES == 4) {
+          out.w[e] = (p.mode != 2 && n0) ? kNaN32 : __float_as_uint(y0);
+          out.w[e + 1] = (p.mode != 2 && n1) ? kNaN32 : __float_as_uint(y1);
+        } else {
+          uint32_t w = pack_bf16x2(y0, y1);
+          if (p.mode != 2) {
+            if (n0) w = (w & 0xffff0000u) | kNaN16;
+            if (n1) w = (w & 0x0000ffffu) | (kNaN16 << 16);
+          }
+          out.w[e >> 1] = w;
+        }
       }
     }
     slot_prefetch<T>(x, next, j, v[j], lane);

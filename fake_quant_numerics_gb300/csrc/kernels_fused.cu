@@ -47,73 +47,99 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
     }
   }
   uint32_t mw[SLOTS];
+  // groups per slot and per tile; with at most 32 groups in a tile, lane i
+  // calibrates group i once instead of every lane of every group
+  constexpr int G = 32 / LPG, NG = SLOTS * G;
+  if constexpr (!STATS_ONLY && NG <= 32) {
+    Stats sj[SLOTS];
 #pragma unroll
-  for (int j = 0; j < SLOTS; ++j) {
-    const int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
-    const int64_t u = base / L;
-    Stats st;
-    st.init<MM>();
-    if (present[j]) {
-      stats_add_vec<T, MM>(st, v[j]);
+    for (int j = 0; j < SLOTS; ++j) {
+      Stats& sr = sj[j];
+      sr.init<MM>();
+      if (present[j]) stats_add_vec<T, MM>(sr, v[j]);
+      sr.reduce_lanes<MM>(LPG);
     }
-    st.reduce_lanes<MM>(LPG);
-    const bool leader = present[j] && (lane % LPG) == 0;
-    if (STATS_ONLY) {
-      if (leader) {
-        if (absmax) absmax[u] = st.absmax_f();
-        if (minv) minv[u] = st.min_f<MM>();
-        if (maxv) maxv[u] = st.max_f<MM>();
+    // group i lives in slot i / G on lanes (i % G) * LPG ...
+    Stats g;
+    g.init<MM>();
+    const int src = (lane % G) * LPG;
+#pragma unroll
+    for (int j = 0; j < SLOTS; ++j) {
+      Stats t;
+      t.amax = __shfl_sync(kFull, sj[j].amax, src);
+      t.nonfinite = __shfl_sync(kFull, sj[j].nonfinite, src);
+      if (MM != kMMNone) {
+        t.kmin = __shfl_sync(kFull, sj[j].kmin, src);
+        t.kmax = __shfl_sync(kFull, sj[j].kmax, src);
       }
-      if (present[j] && st.has_nonfinite()) fl |= QAT_FLAG_NONFINITE_INPUT;
-      mw[j] = 0u;
+      if (lane / G == j) g = t;
+    }
+    IntParams q;
+    const int f = calibrate<BITS, AFFINE, MM>(g, q);
+    const int64_t ug = tb / L + lane;
+    if (lane < NG && ug * L < n) {
+      scale[ug] = q.s;
+      if (zp) zp[ug] = q.zp;
+      fl |= f;
+    }
+#pragma unroll
+    for (int j = 0; j < SLOTS; ++j) {
+      const int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+      const IntParams p = shfl_params<BITS, AFFINE>(q, j * G + lane / LPG);
+      OutVec<T> ov;
+      CodeVec<BITS, VEC> cv;
+      uint32_t mb;
+      int_map_vec<T, BITS, AFFINE>(v[j], p, ov, cv, mb);
       slot_prefetch<T>(x, next, j, v[j], lane);
-      continue;
-    }
-    IntParams p;
-    int f = calibrate<BITS, AFFINE, MM>(st, p);
-    if (leader) {
-      scale[u] = p.s;
-      if (zp) zp[u] = p.zp;
-    }
-    if (present[j]) fl |= f;
-    OutVec<T> ov;
-    CodeVec<BITS, VEC> cv;
-    cv.clear();
-    uint32_t mb = 0u;
-    if (p.fast) {
-#pragma unroll
-      for (int e = VEC - 2; e >= 0; e -= 2) {
-        int ka, kb;
-        float ya, yb;
-        uint32_t ma, mb2;
-        int_pair_cal<AFFINE>(elem<T>(v[j], e), elem<T>(v[j], e + 1), p, ka, kb, ya, yb, ma,
-                             mb2);
-        ov.set2(e, ya, yb);
-        cv.set2(e, AFFINE ? ka + p.zp : ka, AFFINE ? kb + p.zp : kb);
-        mb |= (ma << e) | (mb2 << (e + 1));
+      if (!present[j]) mb = 0u;
+      if (present[j]) {
+        if (y) st_v32(static_cast<char*>(y) + base * T::BYTES, ov.v);
+        if (codes) cv.store(codes, base, VEC);
       }
-    } else if (!p.dead) {
+      mw[j] = mask_word_of_slot<VEC>(mb, lane);
+    }
+  } else {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        int q;
-        float yv;
-        uint32_t m;
-        int_elem<false>(elem<T>(v[j], e), p, q, yv, m);
-        ov.set(e, yv);
-        cv.set(e, q);
-        mb |= m << e;
+    for (int j = 0; j < SLOTS; ++j) {
+      const int64_t base = tb + (int64_t)(j * 32 + lane) * VEC;
+      const int64_t u = base / L;
+      Stats st;
+      st.init<MM>();
+      if (present[j]) {
+        stats_add_vec<T, MM>(st, v[j]);
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) ov.set(e, 0.0f);
+      st.reduce_lanes<MM>(LPG);
+      const bool leader = present[j] && (lane % LPG) == 0;
+      if (STATS_ONLY) {
+        if (leader) {
+          if (absmax) absmax[u] = st.absmax_f();
+          if (minv) minv[u] = st.min_f<MM>();
+          if (maxv) maxv[u] = st.max_f<MM>();
+        }
+        if (present[j] && st.has_nonfinite()) fl |= QAT_FLAG_NONFINITE_INPUT;
+        mw[j] = 0u;
+        slot_prefetch<T>(x, next, j, v[j], lane);
+        continue;
+      }
+      IntParams p;
+      int f = calibrate<BITS, AFFINE, MM>(st, p);
+      if (leader) {
+        scale[u] = p.s;
+        if (zp) zp[u] = p.zp;
+      }
+      if (present[j]) fl |= f;
+      OutVec<T> ov;
+      CodeVec<BITS, VEC> cv;
+      uint32_t mb;
+      int_map_vec<T, BITS, AFFINE>(v[j], p, ov, cv, mb);
+      slot_prefetch<T>(x, next, j, v[j], lane);
+      if (!present[j]) mb = 0u;
+      if (present[j]) {
+        if (y) st_v32(static_cast<char*>(y) + base * T::BYTES, ov.v);
+        if (codes) cv.store(codes, base, VEC);
+      }
+      mw[j] = mask_word_of_slot<VEC>(mb, lane);
     }
-    slot_prefetch<T>(x, next, j, v[j], lane);
-    if (!present[j]) mb = 0u;
-    if (present[j]) {
-      if (y) st_v32(static_cast<char*>(y) + base * T::BYTES, ov.v);
-      if (codes) cv.store(codes, base, VEC);
-    }
-    mw[j] = mask_word_of_slot<VEC>(mb, lane);
   }
   if (!STATS_ONLY && mask) {
     uint32_t w = gather_tile_word<VEC, SLOTS>(mw, lane);
@@ -135,7 +161,8 @@ __global__ void __maxnreg__(T::BYTES == 4 ? 96 : 80) k_int_groups(const void* __
   bool have = false;
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
        t += wstride) {
-    const int64_t next = -1;  // no rolling prefetch: occupancy matters more here
+    const int64_t nt = t + wstride;
+    const int64_t next = nt < nfull ? nt : -1;  // rolling prefetch of the next full tile
     if (t < nfull)
       group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, true>(x, n, t, v, have, next, scale, zp, absmax,
                                                          minv, maxv, y, codes, mask, lane, fl);
@@ -217,35 +244,8 @@ __global__ void __launch_bounds__(256, (NV <= 2 && !AFFINE) ? 3 : 1) k_int_rows(
       const int64_t base = ub + (int64_t)vi * VEC;
       OutVec<T> ov;
       CodeVec<BITS, VEC> cv;
-      cv.clear();
-      uint32_t mb = 0u;
-      if (p.fast) {
-#pragma unroll
-        for (int e = VEC - 2; e >= 0; e -= 2) {
-          int ka, kb;
-          float ya, yb;
-          uint32_t ma, mb2;
-          int_pair_cal<AFFINE>(elem<T>(v[j], e), elem<T>(v[j], e + 1), p, ka, kb, ya, yb, ma,
-                               mb2);
-          ov.set2(e, ya, yb);
-          cv.set2(e, AFFINE ? ka + p.zp : ka, AFFINE ? kb + p.zp : kb);
-          mb |= (ma << e) | (mb2 << (e + 1));
-        }
-      } else if (!p.dead) {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          int q;
-          float yv;
-          uint32_t m;
-          int_elem<false>(elem<T>(v[j], e), p, q, yv, m);
-          ov.set(e, yv);
-          cv.set(e, q);
-          mb |= m << e;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) ov.set(e, 0.0f);
-      }
+      uint32_t mb;
+      int_map_vec<T, BITS, AFFINE>(v[j], p, ov, cv, mb);
       if (present) {
         if (y) st_v32(static_cast<char*>(y) + base * T::BYTES, ov.v);
         if (codes) cv.store(codes, base, VEC);
@@ -281,9 +281,9 @@ static int nv_of(qat_dtype dt, int64_t L) {
 bool fused_units_supported(qat_dtype dt, int64_t L) { return lpg_of(dt, L) || nv_of(dt, L); }
 
 template <typename T, int BITS, bool AFFINE, bool SO>
-static void groups_t(int lpg, const void* x, int64_t n, float* scale, int32_t* zp, float* absmax,
-                     float* minv, float* maxv, void* y, void* codes, uint32_t* mask, int32_t* flags,
-                     cudaStream_t s) {
+static qat_status groups_t(int lpg, const void* x, int64_t n, float* scale, int32_t* zp,
+                           float* absmax, float* minv, float* maxv, void* y, void* codes,
+                           uint32_t* mask, int32_t* flags, cudaStream_t s) {
   const int64_t ntiles = (n + kTile - 1) / kTile;
   int64_t g = (ntiles + 7) / 8;
   int64_t cap = (int64_t)device_info().sms * 8;
@@ -298,6 +298,7 @@ static void groups_t(int lpg, const void* x, int64_t n, float* scale, int32_t* z
     default: QAT_G(32); break;
   }
 #undef QAT_G
+  return launch_status();
 }
 
 template <typename T, int BITS, bool AFFINE, bool SO>
@@ -318,17 +319,17 @@ static void rows_t(int nv, const void* x, int64_t units, int64_t L, float* scale
 }
 
 template <typename T, int BITS, bool AFFINE, bool SO>
-static void fused_t(const void* x, int64_t units, int64_t L, float* scale, int32_t* zp,
-                    float* absmax, float* minv, float* maxv, void* y, void* codes, uint32_t* mask,
-                    int32_t* flags, cudaStream_t s) {
+static qat_status fused_t(const void* x, int64_t units, int64_t L, float* scale, int32_t* zp,
+                          float* absmax, float* minv, float* maxv, void* y, void* codes,
+                          uint32_t* mask, int32_t* flags, cudaStream_t s) {
   const qat_dtype dt = T::kDtype;
   int lpg = lpg_of(dt, L);
   if (lpg)
-    groups_t<T, BITS, AFFINE, SO>(lpg, x, units * L, scale, zp, absmax, minv, maxv, y, codes, mask,
-                                  flags, s);
-  else
-    rows_t<T, BITS, AFFINE, SO>(nv_of(dt, L), x, units, L, scale, zp, absmax, minv, maxv, y, codes,
-                                mask, flags, s);
+    return groups_t<T, BITS, AFFINE, SO>(lpg, x, units * L, scale, zp, absmax, minv, maxv, y,
+                                         codes, mask, flags, s);
+  rows_t<T, BITS, AFFINE, SO>(nv_of(dt, L), x, units, L, scale, zp, absmax, minv, maxv, y, codes,
+                              mask, flags, s);
+  return launch_status();
 }
 
 qat_status launch_int_fused(qat_dtype dt, int bits, bool affine, bool stats_only, const void* x,
@@ -336,8 +337,9 @@ qat_status launch_int_fused(qat_dtype dt, int bits, bool affine, bool stats_only
                             float* minv, float* maxv, void* y, void* codes, uint32_t* mask,
                             int32_t* flags, cudaStream_t s) {
   if (!fused_units_supported(dt, L)) return QAT_ERR_UNSUPPORTED;
+  qat_status st;
 #define QAT_F(T, B, A, SO) \
-  fused_t<T, B, A, SO>(x, units, L, scale, zp, absmax, minv, maxv, y, codes, mask, flags, s)
+  st = fused_t<T, B, A, SO>(x, units, L, scale, zp, absmax, minv, maxv, y, codes, mask, flags, s)
   if (stats_only) {
     if (dt == QAT_F32) QAT_F(F32, 8, false, true);
     else QAT_F(BF16, 8, false, true);
@@ -349,8 +351,8 @@ qat_status launch_int_fused(qat_dtype dt, int bits, bool affine, bool stats_only
     else { if (affine) QAT_F(BF16, 4, true, false); else QAT_F(BF16, 4, false, false); }
   }
 #undef QAT_F
-  count_launch(1);
-  return launch_status();
+  if (st == QAT_OK) count_launch(1);
+  return st;
 }
 
 }  // namespace qat

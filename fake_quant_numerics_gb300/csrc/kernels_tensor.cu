@@ -99,20 +99,7 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
     cv.clear();
     uint32_t mb = 0u;
     if (!GIVEN && p.fast) {
-#pragma unroll
-      for (int e = VEC - 2; e >= 0; e -= 2) {
-        int ka, kb;
-        float ya, yb;
-        uint32_t ma, mb2;
-        int_pair_cal<AFFINE>(elem<T>(v[j], e), elem<T>(v[j], e + 1), p, ka, kb, ya, yb, ma, mb2);
-        ov.set2(e, ya, yb);
-        if (AFFINE) {
-          ka += p.zp;
-          kb += p.zp;
-        }
-        cv.set2(e, (FULL || e < cnt[j]) ? ka : 0, (FULL || e + 1 < cnt[j]) ? kb : 0);
-        mb |= (ma << e) | (mb2 << (e + 1));
-      }
+      int_vec_cal<T, BITS, AFFINE, FULL>(v[j], p, cnt[j], ov, cv, mb);
     } else if (!p.dead) {
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
@@ -144,7 +131,7 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
 }
 
 template <typename T, int BITS, bool AFFINE, bool GIVEN>
-__global__ void __launch_bounds__(256) k_int_tensor(const void* __restrict__ x, int64_t n,
+__global__ void __maxnreg__(80) k_int_tensor(const void* __restrict__ x, int64_t n,
                                                     const uint4* __restrict__ part, int nparts,
                                                     float* scale, int32_t* zp, void* y, void* codes,
                                                     uint32_t* mask, int32_t* flags) {
@@ -197,7 +184,7 @@ __global__ void __launch_bounds__(256) k_int_tensor(const void* __restrict__ x, 
 // lengths the fused kernels do not cover)
 // ---------------------------------------------------------------------------
 template <typename T, int BITS, bool AFFINE, bool GIVEN>
-__global__ void __launch_bounds__(256) k_int_units(const void* __restrict__ x, int64_t n, int64_t L,
+__global__ void __maxnreg__(80) k_int_units(const void* __restrict__ x, int64_t n, int64_t L,
                                                    const float* __restrict__ scale,
                                                    const int32_t* __restrict__ zp,
                                                    const uint8_t* __restrict__ dead, void* y,

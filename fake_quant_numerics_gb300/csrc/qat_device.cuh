@@ -308,6 +308,13 @@ __device__ __forceinline__ void sub2(float a0, float a1, float b0, float b1, flo
       " sub.rn.f32x2 r, x, y;\n mov.b64 {%0, %1}, r; }"
       : "=f"(r0), "=f"(r1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
+// r = a * b + c, one rounding per lane
+__device__ __forceinline__ void fma2(float a0, float a1, float b0, float b1, float c0, float c1,
+                                     float& r0, float& r1) {
+  asm("{ .reg .b64 x, y, z, r;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n"
+      " mov.b64 z, {%6, %7};\n fma.rn.f32x2 r, x, y, z;\n mov.b64 {%0, %1}, r; }"
+      : "=f"(r0), "=f"(r1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
 
 // max with NaN propagation (max.NaN): NaN if either input is NaN
 __device__ __forceinline__ float fmax_nan(float a, float b) {
@@ -430,9 +437,23 @@ struct Stats {
       kmax = __float_as_uint(fmaxf(__uint_as_float(kmax), __uint_as_float(o.kmax)));
     }
   }
-  // reduce over `width` consecutive lanes (a power of two <= 32)
+  // reduce over `width` consecutive lanes (a power of two <= 32); the whole
+  // warp takes one redux.sync per field (amax bits of a non-negative float
+  // and order keys are monotone as unsigned integers)
   template <int MM>
   __device__ __forceinline__ void reduce_lanes(int width) {
+    if (width == 32) {
+      amax = __reduce_max_sync(kFull, amax);
+      nonfinite = __reduce_or_sync(kFull, nonfinite);
+      if (MM == kMMKeys) {
+        kmin = __reduce_min_sync(kFull, kmin);
+        kmax = __reduce_max_sync(kFull, kmax);
+      } else if (MM == kMMFloat) {
+        kmin = key_to_bits(__reduce_min_sync(kFull, order_key(kmin)));
+        kmax = key_to_bits(__reduce_max_sync(kFull, order_key(kmax)));
+      }
+      return;
+    }
     for (int o = 1; o < width; o <<= 1) {
       Stats t;
       t.amax = __shfl_xor_sync(kFull, amax, o);
@@ -496,19 +517,41 @@ __device__ __forceinline__ Stats block_reduce_stats(Stats s, uint32_t* red) {
 }
 
 // ---------------------------------------------------------------------------
-// rounding of a quotient to an integer without a per-element division
+// the correctly rounded quotient without a per-element division
 //
-// q0 = RN(x * RN(1/s)) differs from x/s by less than 1.5 ulp(q0) (the
-// reciprocal's relative error is at most 2^-24, the product's rounding half an
-// ulp), and RN(x/s) differs from x/s by at most half an ulp: so while q0 is
-// more than 2.5 ulp(q0) away from every half-integer, RN(x/s) lies in the same
-// open interval between consecutive half-integers as q0, and any rounding of
-// RN(x/s) to an integer (ties to even or away from zero) equals rint(q0).
-// For |q0| < 2^m that distance is below 2^(m-22); the band used must be at
-// least that.  Elements inside the band are recomputed by the caller from the
-// correctly rounded quotient __fdiv_rn(x, s).
+// With y = RN(1/s) (within half an ulp of 1/s) and Q = x/s:
+//   q0 = RN(x y) is within 2^-24 |Q| + ulp/2 < 2 ulp(Q) of Q;
+//   r0 = RN(x - q0 s) (one fma) is s (Q - q0)(1 + eta), |eta| <= 2^-24;
+//   q1 = RN(q0 + r0 y) (one fma) rounds Q + (Q - q0)(eta + delta + eta delta),
+//   |delta| = |s y - 1| <= 2^-24, i.e. Q moved by less than 2^-22 ulp(Q), so
+//   q1 is within one ulp of Q (faithful);
+//   r1 = x - q1 s is then exactly representable and one fma gives it, and
+//   q2 = RN(q1 + r1 y) = RN(Q) by Markstein's theorem (y correctly rounded,
+//   q1 within one ulp; P. Markstein, IBM J. Res. Dev. 34(1), 1990).
+// q2 is the IEEE quotient RN(x/s) itself, so rint(q2) and an FP8 cast of q2
+// equal those of the divided value.  Preconditions: no overflow and no
+// underflow of the products and remainders, which the scale range below
+// guarantees for |Q| >= 2^-20 (smaller quotients round to 0 under rint
+// whatever the last bits are).
 // Safe scales: s and 1/s normal and far from overflow, s in [2^-80, 2^100].
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float quotient_rn(float x, float rcp, float ns) {
+  const float q0 = __fmul_rn(x, rcp);
+  const float q1 = __fmaf_rn(__fmaf_rn(q0, ns, x), rcp, q0);
+  return __fmaf_rn(__fmaf_rn(q1, ns, x), rcp, q1);
+}
+
+// the same for a pair (f32x2 arithmetic); ns = -s
+__device__ __forceinline__ void quotient_rn2(float xa, float xb, float rcp, float ns, float& qa,
+                                             float& qb) {
+  float ra, rb;
+  mul2(xa, xb, rcp, rcp, qa, qb);
+  fma2(qa, qb, ns, ns, xa, xb, ra, rb);
+  fma2(ra, rb, rcp, rcp, qa, qb, qa, qb);
+  fma2(qa, qb, ns, ns, xa, xb, ra, rb);
+  fma2(ra, rb, rcp, rcp, qa, qb, qa, qb);
+}
+
 __device__ __forceinline__ bool quot_scale_ok(float s) { return s >= 0x1p-80f && s <= 0x1p100f; }
 
 // ---------------------------------------------------------------------------
@@ -573,6 +616,34 @@ __device__ __forceinline__ int calibrate(const Stats& st, IntParams& p) {
   return flag;
 }
 
+// The parameters of lane `src` (calibrated there), as the map needs them:
+// s, rcp, the window, zp and the dead / fast bits travel; the clamp range is
+// rebuilt from zp.  For the symmetric grid wlo = RN(qmin s) = -RN(qmax s).
+template <int BITS, bool AFFINE>
+__device__ __forceinline__ IntParams shfl_params(const IntParams& q, int src) {
+  constexpr int qmin = QRange<BITS, AFFINE>::qmin, qmax = QRange<BITS, AFFINE>::qmax;
+  IntParams p;
+  p.s = __shfl_sync(kFull, q.s, src);
+  p.rcp = __shfl_sync(kFull, q.rcp, src);
+  p.whi = __shfl_sync(kFull, q.whi, src);
+  const int bitsw =
+      __shfl_sync(kFull, q.dead | (q.fast << 1) | (AFFINE ? ((q.zp & 0xff) << 2) : 0), src);
+  p.dead = bitsw & 1;
+  p.fast = (bitsw >> 1) & 1;
+  if (AFFINE) {
+    p.zp = (int)(int8_t)(uint8_t)((bitsw >> 2) & 0xff);
+    p.wlo = __shfl_sync(kFull, q.wlo, src);
+  } else {
+    p.zp = 0;
+    p.wlo = -p.whi;
+  }
+  p.klo = qmin - p.zp;
+  p.khi = qmax - p.zp;
+  p.klof = (float)p.klo;
+  p.khif = (float)p.khi;
+  return p;
+}
+
 // Given parameters: validity check.
 template <int BITS, bool AFFINE>
 __device__ __forceinline__ int given_params(float s, int zp, IntParams& p) {
@@ -609,39 +680,90 @@ __device__ __forceinline__ void int_elem(float x, const IntParams& p, int& q, fl
 constexpr float kRintMagic = 12582912.0f;
 constexpr uint32_t kRintMagicBits = 0x4b400000u;
 
-// A pair of elements of a calibrated unit with p.fast set: the quotient from
-// the reciprocal, rounded with the magic constant, near-ties
-// decided from the correctly rounded quotient; k = q - zp, y = k * s, mask.
-// (see the quotient note above quot_scale_ok)
-template <bool AFFINE>
-__device__ __forceinline__ void int_pair_cal(float xa, float xb, const IntParams& p, int& ka,
-                                             int& kb, float& ya, float& yb, uint32_t& ma,
-                                             uint32_t& mb) {
-  constexpr float kLim = 0.5f - 0x1p-12f;  // |q| < 2^9: band 2^-12 > 2^(9-22)
-  float qa, qb, ta, tb, fa, fb, da, db;
-  mul2(xa, xb, p.rcp, p.rcp, qa, qb);
-  add2(qa, qb, kRintMagic, kRintMagic, ta, tb);
-  sub2(ta, tb, kRintMagic, kRintMagic, fa, fb);
-  sub2(qa, qb, fa, fb, da, db);  // exact, |d| <= 1/2
-  const bool na = fabsf(da) > kLim, nb = fabsf(db) > kLim;
-  if (na || nb) {
-    if (na) fa = __fadd_rn(rintf(__fdiv_rn(xa, p.s)), 0.0f);
-    if (nb) fb = __fadd_rn(rintf(__fdiv_rn(xb, p.s)), 0.0f);
+// One vector of a calibrated unit with p.fast set.  A calibrated unit with
+// p.fast holds only finite values (a NaN or Inf makes it dead), which the
+// window test below relies on.
+//   quotient: q = RN(x/s) by quotient_rn2, f = rint(q) by the magic constant;
+//   k = clamp(f) (affine), y = k * s, code k + zp from the bits of k + M;
+//   STE window: whi - |x| >= 0 (symmetric), whi - x >= 0 and x - wlo >= 0
+//     (affine); RN never changes the sign of a difference and an exact zero
+//     difference is +0, except (-0) - (+0) = -0: a lower bound of +0 is used
+//     as -0 (x - (-0) is +0 for both zeros), and the whi side never meets
+//     that case (whi >= +0, and whi - |x| has |x| >= +0).  So the sign bits
+//     are the window test; they are shifted into the mask with funnel
+//     shifts, highest element first.
+// FULL == false: elements e >= cnt are absent (read as +0) and get code 0.
+template <typename T, int BITS, bool AFFINE, bool FULL>
+__device__ __forceinline__ void int_vec_cal(const V32& v, const IntParams& p, int cnt,
+                                            OutVec<T>& ov, CodeVec<BITS, T::VEC>& cv,
+                                            uint32_t& mb) {
+  constexpr int VEC = T::VEC;
+  const float ns = -p.s;
+  const float wlo = p.wlo == 0.0f ? -0.0f : p.wlo;
+  cv.clear();
+  uint32_t out = 0u;  // out-of-window bits
+#pragma unroll
+  for (int e = VEC - 2; e >= 0; e -= 2) {
+    const float xa = elem<T>(v, e), xb = elem<T>(v, e + 1);
+    float fa, fb, ta, tb, ya, yb;
+    quotient_rn2(xa, xb, p.rcp, ns, fa, fb);
+    add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
+    sub2(ta, tb, kRintMagic, kRintMagic, fa, fb);
+    if (AFFINE) {
+      fa = fminf(fmaxf(fa, p.klof), p.khif);
+      fb = fminf(fmaxf(fb, p.klof), p.khif);
+      add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
+    }
+    mul2(fa, fb, p.s, p.s, ya, yb);
+    ov.set2(e, ya, yb);
+    int qa = (int)(__float_as_uint(ta) - kRintMagicBits) + (AFFINE ? p.zp : 0);
+    int qb = (int)(__float_as_uint(tb) - kRintMagicBits) + (AFFINE ? p.zp : 0);
+    if (!FULL) {
+      if (e >= cnt) qa = 0;
+      if (e + 1 >= cnt) qb = 0;
+    }
+    cv.set2(e, qa, qb);
+    uint32_t oa, ob;
+    if (AFFINE) {
+      float ha, hb, la, lb;
+      sub2(p.whi, p.whi, xa, xb, ha, hb);
+      sub2(xa, xb, wlo, wlo, la, lb);
+      oa = __float_as_uint(ha) | __float_as_uint(la);
+      ob = __float_as_uint(hb) | __float_as_uint(lb);
+    } else {
+      oa = __float_as_uint(__fsub_rn(p.whi, fabsf(xa)));
+      ob = __float_as_uint(__fsub_rn(p.whi, fabsf(xb)));
+    }
+    out = __funnelshift_l(ob, out, 1);
+    out = __funnelshift_l(oa, out, 1);
   }
-  if (AFFINE) {
-    fa = fminf(fmaxf(fa, p.klof), p.khif);
-    fb = fminf(fmaxf(fb, p.klof), p.khif);
-  }
-  mul2(fa, fb, p.s, p.s, ya, yb);
-  add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
-  ka = (int)(__float_as_uint(ta) - kRintMagicBits);
-  kb = (int)(__float_as_uint(tb) - kRintMagicBits);
-  if (AFFINE) {
-    ma = (xa >= p.wlo) && (xa <= p.whi);
-    mb = (xb >= p.wlo) && (xb <= p.whi);
+  mb = ~out & (VEC == 32 ? 0xffffffffu : ((1u << VEC) - 1u));
+}
+
+// Element map of one full vector with calibrated or given parameters: the
+// reciprocal path when p.fast, the IEEE path otherwise, zeros for a dead unit.
+template <typename T, int BITS, bool AFFINE>
+__device__ __forceinline__ void int_map_vec(const V32& v, const IntParams& p, OutVec<T>& ov,
+                                            CodeVec<BITS, T::VEC>& cv, uint32_t& mb) {
+  constexpr int VEC = T::VEC;
+  cv.clear();
+  mb = 0u;
+  if (p.fast) {
+    int_vec_cal<T, BITS, AFFINE, true>(v, p, VEC, ov, cv, mb);
+  } else if (!p.dead) {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      int q;
+      float yv;
+      uint32_t m;
+      int_elem<false>(elem<T>(v, e), p, q, yv, m);
+      ov.set(e, yv);
+      cv.set(e, q);
+      mb |= m << e;
+    }
   } else {
-    ma = fabsf(xa) <= p.whi;
-    mb = fabsf(xb) <= p.whi;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) ov.set(e, 0.0f);
   }
 }
 

@@ -85,8 +85,10 @@ def run_int(qat, orc, x, rows, cols, bits_, scheme, gran, group=0, scale=None, z
 
 
 TENSOR_SHAPES = [(1, 1), (1, 31), (1, 1023), (3, 1025), (1, 16385), (7, 9999)]
+# (5000, 96): every block of the per-row kernel takes many rows; (2, 16384):
+# the largest rows of the per-row kernel (8 vectors per thread for f32)
 ROW_SHAPES = [(3, 64), (2, 256), (5, 4096), (3, 8192), (7, 96), (4, 40), (3, 1000), (2, 33),
-              (1, 32768)]
+              (1, 32768), (2, 16384), (5000, 96)]
 GROUP_SHAPES = [(8, 512, 128), (3, 384, 128), (5, 96, 32), (4, 300, 100), (2, 1024, 1024),
                 (4, 64, 16), (6, 256, 256), (2, 2048, 512)]
 
@@ -117,6 +119,28 @@ def test_int_per_group(qat, orc, dt, bits_, scheme):
     for i, (r, c, g) in enumerate(GROUP_SHAPES):
         x = make_input(r, c, DT[dt], seed=300 + i, zero_unit=1, nan_unit=3, L=g)
         run_int(qat, orc, x, r, c, bits_, SCHEMES[scheme], 2, g)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("bits_", [8, 4])
+def test_int_affine_zero_window_ends(qat, orc, dt, bits_):
+    """Affine units whose window ends at 0 (all values >= 0 gives zp = qmin and
+    wlo = +0; all values <= 0 gives zp = qmax and whi = +0) holding both signed
+    zeros: -0 and +0 are inside the window."""
+    rng = np.random.default_rng(61)
+    for gran, (r, c, g) in ((0, (1, 4096, 0)), (1, (4, 4096, 0)), (1, (4, 96, 0)),
+                            (2, (4, 512, 128)), (2, (4, 512, 64))):
+        a = np.abs(rng.standard_normal((r, c)).astype(np.float32)) + np.float32(0.01)
+        if gran == 0:
+            a = a if rng.integers(2) else -a
+        else:
+            a[1::2] *= -1  # odd rows non-positive, even rows non-negative
+        flat = a.reshape(-1)
+        flat[rng.integers(0, flat.size, size=flat.size // 9)] = -0.0
+        flat[rng.integers(0, flat.size, size=flat.size // 9)] = 0.0
+        x = torch.from_numpy(a)
+        x = x.to(DT[dt]) if dt != "f32" else x
+        run_int(qat, orc, x, r, c, bits_, 1, gran, g)
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
@@ -288,6 +312,7 @@ def test_ste_backward(qat, orc, dt):
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_amax_stats(qat, orc, dt):
     cases = [(0, 3, 1025, 0), (0, 1, 1, 0), (1, 5, 4096, 0), (1, 3, 96, 0), (1, 4, 40, 0),
+             (1, 5000, 96, 0), (1, 2, 16384, 0),
              (2, 8, 512, 128), (2, 4, 300, 100), (2, 3, 64, 32)]
     for i, (gran, r, c, g) in enumerate(cases):
         x = make_input(r, c, DT[dt], seed=500 + i, specials=True)
