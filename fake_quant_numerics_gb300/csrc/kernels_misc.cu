@@ -97,7 +97,9 @@ constexpr int kQ4Block = 64;
 constexpr int kQ4Super = 256;                       // block scales per super-block
 constexpr int kQ4SuperElems = kQ4Block * kQ4Super;  // 16384
 constexpr int kQ4Threads = 512;
-constexpr int kQ4Slots = kQ4SuperElems / (kQ4Threads * 8);  // 4 vectors of 8 fp32 per thread
+// each lane holds 16 elements (two 32-byte vectors) of one 64-element block,
+// four lanes per block; a thread covers kQ4Pairs such blocks per super-block
+constexpr int kQ4Pairs = kQ4SuperElems / (kQ4Threads * 16);  // 2
 
 // code = clamp(round_half_away(x / s), -8, 7); s == 0 or NaN -> 0
 __device__ __forceinline__ int q4_code(float x, float s) {
@@ -133,6 +135,64 @@ __device__ __forceinline__ V32 dequant8(uint32_t packed, float rs) {
   return o;
 }
 
+// Level 1 of one lane's 16 elements (block scale s, 4-bit codes in two
+// words, element 8h + e of the lane in word h).  For a block scale in the
+// safe range the quotient is the IEEE RN(x/s) (quotient_rn2, exact), rounded
+// to nearest even by the magic constant; the definition rounds half away from
+// zero, so an exact half-integer quotient (and a NaN element, code 0) sends
+// the lane through the element-wise code of q4_code.  Absent tail elements
+// read +0 and give code 0.
+__device__ __forceinline__ void q4_codes16(const V32 (&v)[2], float s, bool has_nan, bool full,
+                                           const int (&cnt)[2], uint32_t (&w)[2]) {
+  if (quot_scale_ok(s)) {
+    const float rcp = __frcp_rn(s), ns = -s;
+    bool fix = has_nan;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t pk = 0u;
+#pragma unroll
+      for (int e = 6; e >= 0; e -= 2) {
+        float qa, qb, ta, tb, fa, fb, da, db;
+        quotient_rn2(__uint_as_float(v[h].w[e]), __uint_as_float(v[h].w[e + 1]), rcp, ns, qa, qb);
+        add2(qa, qb, kRintMagic, kRintMagic, ta, tb);
+        sub2(ta, tb, kRintMagic, kRintMagic, fa, fb);
+        sub2(qa, qb, fa, fb, da, db);  // exact
+        fix |= (fabsf(da) == 0.5f) | (fabsf(db) == 0.5f);
+        // |x/s| <= 7 (1 + 2^-23): k = rint(q) in [-7, 7], the low nibble of
+        // the two's complement k is the code
+        pk = pack_s4x2((int)(__float_as_uint(ta) - kRintMagicBits),
+                       (int)(__float_as_uint(tb) - kRintMagicBits), pk);
+      }
+      w[h] = pk;
+    }
+    if (fix) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float x = __uint_as_float(v[h].w[e]);
+          const float q = quotient_rn(x, rcp, ns);
+          if (isnan(x) || fabsf(__fsub_rn(q, rintf(q))) == 0.5f) {
+            const int sh = (e >> 1) * 8 + ((e & 1) ? 0 : 4);
+            w[h] = (w[h] & ~(0xfu << sh)) | (((uint32_t)q4_code(x, s) & 0xfu) << sh);
+          }
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t pk = 0u;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = (full || e < cnt[h]) ? q4_code(__uint_as_float(v[h].w[e]), s) : 0;
+        pk |= ((uint32_t)c & 0xfu) << ((e >> 1) * 8 + ((e & 1) ? 0 : 4));
+      }
+      w[h] = pk;
+    }
+  }
+}
+
 template <bool ROUNDTRIP>
 __global__ void __launch_bounds__(kQ4Threads, 2) k_q4_quant(const float* __restrict__ x, int64_t n,
                                                          uint8_t* __restrict__ data,
@@ -146,112 +206,88 @@ __global__ void __launch_bounds__(kQ4Threads, 2) k_q4_quant(const float* __restr
   const int64_t nsuper = (n + kQ4SuperElems - 1) / kQ4SuperElems;
   const int64_t nblocks = (n + kQ4Block - 1) / kQ4Block;
   const int64_t nbytes = (n + 1) / 2;
-  // The vectors of the next super-block are requested as soon as the level-1
-  // codes of the current one are computed, so they are in flight while
-  // level 2 (two block barriers) and the stores run.
-  V32 v[kQ4Slots];
+  // thread tid, pair j: elements e0 + j * 8192 + 16 tid .. + 15, block
+  // j * 128 + tid / 4 of the super-block.  The vectors of the next
+  // super-block are requested as soon as the level-1 codes of the current one
+  // are computed, so they are in flight while level 2 (two block barriers)
+  // and the stores run.
+  V32 v[kQ4Pairs][2];
   bool have = false;  // v already holds this super-block (a full one)
   for (int64_t sb = blockIdx.x; sb < nsuper; sb += gridDim.x) {
     const int64_t e0 = sb * kQ4SuperElems;
     const bool full = e0 + kQ4SuperElems <= n;
-    int cnt[kQ4Slots];
+    int cnt[kQ4Pairs][2];
 #pragma unroll
-    for (int j = 0; j < kQ4Slots; ++j) {
-      int64_t base = e0 + (int64_t)(j * kQ4Threads + tid) * 8;
-      if (full) {
-        cnt[j] = 8;
-        if (!have) v[j] = ld_v32(x + base);
-      } else {
-        int64_t c = n - base;
-        cnt[j] = c >= 8 ? 8 : (c > 0 ? (int)c : 0);
-        v[j] = load_vec<F32>(x, cnt[j] > 0 ? base : 0, cnt[j]);
+    for (int j = 0; j < kQ4Pairs; ++j) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t base = e0 + (int64_t)j * (kQ4Threads * 16) + tid * 16 + h * 8;
+        if (full) {
+          cnt[j][h] = 8;
+          if (!have) v[j][h] = ld_v32(x + base);
+        } else {
+          const int64_t c = n - base;
+          cnt[j][h] = c >= 8 ? 8 : (c > 0 ? (int)c : 0);
+          v[j][h] = load_vec<F32>(x, cnt[j][h] > 0 ? base : 0, cnt[j][h]);
+        }
       }
     }
-    uint32_t packed[kQ4Slots];
+    uint32_t packed[kQ4Pairs][2];
 #pragma unroll
-    for (int j = 0; j < kQ4Slots; ++j) {
-      // level 1: absmax over the 64-element block = 8 lanes x 8 elements
-      // (fmaxf ignores NaN and keeps +inf, the fold of the definition)
-      float a = 0.0f;
+    for (int j = 0; j < kQ4Pairs; ++j) {
+      // level 1: absmax over the 64-element block = 4 lanes x 16 elements.
+      // max.NaN flags a NaN in the lane's elements; the definition's fold
+      // (fmaxf: NaN ignored, +inf kept) is then redone element by element.
+      float m = 0.0f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(__uint_as_float(v[j].w[e])));
-      a = fmaxf(a, __shfl_xor_sync(kFull, a, 1));
-      a = fmaxf(a, __shfl_xor_sync(kFull, a, 2));
-      a = fmaxf(a, __shfl_xor_sync(kFull, a, 4));
-      const float s = __fdiv_rn(a, 7.0f);
-      uint32_t pk = 0u;
-      if (quot_scale_ok(s)) {
-        // |x| <= absmax, so |x/s| <= 7 (1 + 2^-23): |q0| < 8, the band 2^-16
-        // covers 2^(3-22); the clamp to [-8, 7] can never act here; absent
-        // tail elements read +0 and give code 0
-        // quotient from the reciprocal, rounded with the magic constant (see
-        // int_pair_cal); the low four bits of RN(q + M) are the code
-        const float rcp = __frcp_rn(s);
-        constexpr float kLim = 0.5f - 0x1p-16f;
-        uint32_t nearbits = 0u;
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          float q0, q1, t0, t1, f0, f1, d0, d1;
-          mul2(__uint_as_float(v[j].w[e]), __uint_as_float(v[j].w[e + 1]), rcp, rcp, q0, q1);
-          add2(q0, q1, kRintMagic, kRintMagic, t0, t1);
-          sub2(t0, t1, kRintMagic, kRintMagic, f0, f1);
-          sub2(q0, q1, f0, f1, d0, d1);
-          nearbits |= ((uint32_t)(fabsf(d0) > kLim) << e) | ((uint32_t)(fabsf(d1) > kLim) << (e + 1));
-          // NaN elements: t is NaN, its low bits are not a code; they are near
-          // by the NaN test below and get code 0 from the exact path
-          if (isnan(q0)) nearbits |= 1u << e;
-          if (isnan(q1)) nearbits |= 1u << (e + 1);
-          pk |= ((__float_as_uint(t0) & 0xfu) << ((e >> 1) * 8 + 4)) |
-                ((__float_as_uint(t1) & 0xfu) << ((e >> 1) * 8));
-        }
-        if (nearbits) {
+        for (int e = 0; e < 8; ++e) m = fmax_nan(m, fabsf(__uint_as_float(v[j][h].w[e])));
+      const bool has_nan = isnan(m);
+      if (has_nan) {
+        m = 0.0f;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            if ((nearbits >> e) & 1u) {
-              const int sh = (e >> 1) * 8 + ((e & 1) ? 0 : 4);
-              const int c = q4_code(__uint_as_float(v[j].w[e]), s);
-              pk = (pk & ~(0xfu << sh)) | (((uint32_t)c & 0xfu) << sh);
-            }
-          }
-        }
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(__uint_as_float(v[j][h].w[e])));
+      }
+      m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+      const float s = __fdiv_rn(m, 7.0f);
+      q4_codes16(v[j], s, has_nan, full, cnt[j], packed[j]);
+      const int64_t base = e0 + (int64_t)j * (kQ4Threads * 16) + tid * 16;
+      if (full) {
+        *reinterpret_cast<uint2*>(data + base / 2) = make_uint2(packed[j][0], packed[j][1]);
       } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          int c = (full || e < cnt[j]) ? q4_code(__uint_as_float(v[j].w[e]), s) : 0;
-          pk |= ((uint32_t)c & 0xfu) << ((e >> 1) * 8 + ((e & 1) ? 0 : 4));
-        }
+        for (int b = 0; b < 8; ++b)
+          if (base / 2 + b < nbytes) data[base / 2 + b] = (uint8_t)(packed[j][b >> 2] >> (8 * (b & 3)));
       }
-      packed[j] = pk;
-      const int64_t base = e0 + (int64_t)(j * kQ4Threads + tid) * 8;
-      if (cnt[j] == 8) {
-        *reinterpret_cast<uint32_t*>(data + base / 2) = pk;
-      } else if (cnt[j] > 0) {
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-          if (base / 2 + b < nbytes) data[base / 2 + b] = (uint8_t)(pk >> (8 * b));
-      }
-      if ((lane & 7) == 0) s_scale[j * (kQ4Threads / 8) + (tid >> 3)] = cnt[j] > 0 ? s : 0.0f;
+      if ((tid & 3) == 0) s_scale[j * (kQ4Threads / 4) + (tid >> 2)] = base < n ? s : 0.0f;
     }
     {
       const int64_t nsb = sb + gridDim.x;
       have = nsb < nsuper && nsb * kQ4SuperElems + kQ4SuperElems <= n;
       if (have) {
 #pragma unroll
-        for (int j = 0; j < kQ4Slots; ++j)
-          v[j] = ld_v32(x + nsb * kQ4SuperElems + (int64_t)(j * kQ4Threads + tid) * 8);
+        for (int j = 0; j < kQ4Pairs; ++j)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            v[j][h] = ld_v32(x + nsb * kQ4SuperElems + (int64_t)j * (kQ4Threads * 16) + tid * 16 +
+                             h * 8);
       }
     }
     __syncthreads();
     // level 2: super = max(max scale, 1e-8); q = clamp(round(scale / super * 255), 0, 255)
     const int64_t b0 = sb * kQ4Super;
-    float sc = 0.0f, m = 0.0f;
+    float sc = 0.0f, mm = 0.0f;
     if (tid < kQ4Super) {
       sc = s_scale[tid];
-      m = sc;
+      mm = sc;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-    if (lane == 0) s_red[tid >> 5] = m;
+    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(kFull, mm, o));
+    if (lane == 0) s_red[tid >> 5] = mm;
     __syncthreads();
     float mx = 0.0f;
 #pragma unroll
@@ -268,11 +304,15 @@ __global__ void __launch_bounds__(kQ4Threads, 2) k_q4_quant(const float* __restr
     if (ROUNDTRIP) {
       __syncthreads();
 #pragma unroll
-      for (int j = 0; j < kQ4Slots; ++j) {
-        const float rs = __fmul_rn(__fdiv_rn(s_q[j * (kQ4Threads / 8) + (tid >> 3)], 255.0f), super);
-        const V32 o = dequant8(packed[j], rs);
-        const int64_t base = e0 + (int64_t)(j * kQ4Threads + tid) * 8;
-        if (cnt[j] > 0) store_vec<F32>(y, base, o, cnt[j]);
+      for (int j = 0; j < kQ4Pairs; ++j) {
+        const float rs =
+            __fmul_rn(__fdiv_rn(s_q[j * (kQ4Threads / 4) + (tid >> 2)], 255.0f), super);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const V32 o = dequant8(packed[j][h], rs);
+          const int64_t base = e0 + (int64_t)j * (kQ4Threads * 16) + tid * 16 + h * 8;
+          if (cnt[j][h] > 0) store_vec<F32>(y, base, o, cnt[j][h]);
+        }
       }
     }
     __syncthreads();  // shared arrays are reused by the next super-block

@@ -385,6 +385,24 @@ def test_q4_double_specials(qat, orc):
     run_q4(qat, orc, (np.sin(np.arange(4096, dtype=np.float32) * np.float32(0.1)) * 2).astype(np.float32))
 
 
+def test_q4_double_exact_ties(qat, orc):
+    """Blocks whose absmax is 7 * 2^k give the scale 2^k exactly, so x / s of
+    half-integer multiples of 2^k are exact ties, which the codes round half
+    away from zero; one block also holds a NaN, one a negative absmax."""
+    rng = np.random.default_rng(15)
+    nblk = 3 * 256 + 5
+    x = np.empty(nblk * 64, np.float32)
+    halves = np.arange(-13, 14, dtype=np.float32) / 2  # -6.5 .. 6.5 in steps of 1/2
+    for b in range(nblk):
+        k = int(rng.integers(-30, 30))
+        blk = rng.choice(halves, size=64) * np.float32(2.0 ** k)
+        blk[rng.integers(64)] = np.float32(7 * 2.0 ** k) * (1 if b % 5 else -1)
+        blk[rng.integers(64, size=3)] = [0.0, -0.0, np.float32(2.0 ** k)]
+        x[b * 64:(b + 1) * 64] = blk
+    x[64 * 7 + 9] = np.nan
+    run_q4(qat, orc, x)
+
+
 # ---------------------------------------------------------------------------
 # binding behaviour
 # ---------------------------------------------------------------------------

@@ -436,6 +436,15 @@ def test_q4_nibble_order_and_codes(orc):
     assert list(decode_nibbles(r["data"], 5)) == [7, 1, -7, 2, -3]
 
 
+def test_q4_exact_ties_round_half_away_from_zero(orc):
+    # absmax 7 -> scale exactly 1, so every x below is its own quotient; the
+    # block code rounds like Rust's f32::round (half away from zero), unlike
+    # the integer grid's ties-to-even
+    x = np.array([7.0, 2.5, -2.5, 0.5, -0.5, 6.5, -6.5, 1.5], np.float32)
+    r = orc.quant4_double(x)
+    assert list(decode_nibbles(r["data"], 8)) == [7, 3, -3, 1, -1, 7, -7, 2]
+
+
 def test_q4_accounting(orc):
     rows = {r[0]: r[1:] for r in golden_lines("double_quant_accounting.txt")}
     n = 1 << 28
