@@ -109,28 +109,32 @@ __device__ __forceinline__ int q4_code(float x, float s) {
   return min(max(k, -8), 7);
 }
 
-__device__ __forceinline__ int nibble_value(uint32_t packed, int e) {
-  // element e of 8: byte e/2, even element in the high nibble
-  int shift = (e >> 1) * 8 + ((e & 1) ? 0 : 4);
-  int nib = (int)((packed >> shift) & 0xfu);
-  return nib >= 8 ? nib - 16 : nib;
-}
-
-// y = code * rs for the 8 codes of one 32-bit word.  A NaN product (only
-// possible when rs is inf or NaN: 0 * inf, x * NaN) is written as the
-// canonical quiet NaN 0x7fc00000.
+// y = code * rs for the 8 codes of one 32-bit word (element e in byte e / 2,
+// even element in the high nibble).  The code k of a nibble u is (u ^ 8) - 8,
+// and the float bits 0x4b400000 | (u ^ 8) are the value M + k + 8 with
+// M = 1.5 * 2^23, so subtracting M + 8 gives k exactly without an
+// integer-to-float conversion; y = RN(k * rs).  A NaN product (only possible
+// when rs is inf or NaN: 0 * inf, x * NaN) is written as the canonical quiet
+// NaN 0x7fc00000.
 __device__ __forceinline__ V32 dequant8(uint32_t packed, float rs) {
+  constexpr float kBias = 12582920.0f;  // M + 8
+  const uint32_t w = packed ^ 0x88888888u;
   V32 o;
-  if (isfinite(rs)) {
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    const int sh = (e >> 1) * 8;
+    const float ta = __uint_as_float(((w >> (sh + 4)) & 0xfu) | 0x4b400000u);
+    const float tb = __uint_as_float(((w >> sh) & 0xfu) | 0x4b400000u);
+    float ka, kb, ya, yb;
+    sub2(ta, tb, kBias, kBias, ka, kb);
+    mul2(ka, kb, rs, rs, ya, yb);
+    o.w[e] = __float_as_uint(ya);
+    o.w[e + 1] = __float_as_uint(yb);
+  }
+  if (!isfinite(rs)) {
 #pragma unroll
     for (int e = 0; e < 8; ++e)
-      o.w[e] = __float_as_uint(__fmul_rn((float)nibble_value(packed, e), rs));
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float v = __fmul_rn((float)nibble_value(packed, e), rs);
-      o.w[e] = isnan(v) ? 0x7fc00000u : __float_as_uint(v);
-    }
+      if (isnan(__uint_as_float(o.w[e]))) o.w[e] = 0x7fc00000u;
   }
   return o;
 }
@@ -331,86 +335,84 @@ qat_status launch_q4_quant(const float* x, int64_t n, uint8_t* data, uint8_t* qs
 }
 
 // ---------------------------------------------------------------------------
-// two-level 4-bit dequantization: each lane turns 8 codes (one 32-bit word)
-// into 8 floats (one 32-byte store); a warp covers 256 contiguous elements
-// per store instruction
+// two-level 4-bit dequantization: a warp step is 128 octets (1024 elements,
+// 16 blocks, inside one super-block); lane l takes octets 32 k + l (k < 4),
+// so each 32-byte store instruction of the warp covers 1 KiB of contiguous
+// output.  Loads per lane and step: four code words (128 contiguous bytes per
+// warp instruction), the step's 16 block scales as one broadcast 16-byte
+// load, and the super-scale.  The next step's loads are issued before the
+// current step's arithmetic and stores (rolling prefetch).  RN(q / 255)
+// comes from a 256-entry table of the same correctly rounded quotients.
 // ---------------------------------------------------------------------------
-// The next step's code words, block scales and super-scales are requested
-// before the current step's arithmetic and stores (rolling prefetch).
 struct Q4Step {
-  static constexpr int K = 4;  // octets per lane per step
-  uint32_t pk[K];
-  float qs[K], sup[K];
+  uint32_t pk[4];
+  uint4 q;  // block scales 16 st .. 16 st + 15, byte b of word w = block 16 st + 4 w + b
+  float sup;
 };
 
-template <bool FULL>
-__device__ __forceinline__ void q4_step_load(const uint8_t* __restrict__ data,
+__device__ __forceinline__ void q4_step_full(const uint8_t* __restrict__ data,
                                              const uint8_t* __restrict__ qscales,
-                                             const float* __restrict__ sup, int64_t n, int64_t st,
-                                             int lane, Q4Step& d) {
-  const int64_t nbytes = (n + 1) / 2;
+                                             const float* __restrict__ sup, int64_t st, int lane,
+                                             Q4Step& d) {
+  const uint32_t* words = reinterpret_cast<const uint32_t*>(data) + st * 128 + lane;
 #pragma unroll
-  for (int k = 0; k < Q4Step::K; ++k) {
-    const int64_t oct = st * (32 * Q4Step::K) + k * 32 + lane;
-    if (FULL || oct * 8 + 8 <= n) {
-      d.pk[k] = __ldg(reinterpret_cast<const uint32_t*>(data) + oct);
-    } else {
-      d.pk[k] = 0u;
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-        if (oct * 4 + b < nbytes) d.pk[k] |= (uint32_t)data[oct * 4 + b] << (8 * b);
-    }
-    if (FULL || oct * 8 < n) {
-      const int64_t blk = oct >> 3;  // 8 octets per 64-element block
-      d.qs[k] = (float)__ldg(qscales + blk);
-      d.sup[k] = __ldg(sup + blk / kQ4Super);
-    } else {
-      d.qs[k] = 0.0f;
-      d.sup[k] = 0.0f;
-    }
-  }
+  for (int k = 0; k < 4; ++k) d.pk[k] = __ldg(words + 32 * k);
+  d.q = __ldg(reinterpret_cast<const uint4*>(qscales) + st);
+  d.sup = __ldg(sup + (st >> 4));
 }
 
 __global__ void __launch_bounds__(256) k_q4_dequant(const uint8_t* __restrict__ data,
                                                     const uint8_t* __restrict__ qscales,
                                                     const float* __restrict__ sup, int64_t n,
                                                     float* __restrict__ y) {
-  constexpr int K = Q4Step::K;
+  __shared__ float s_inv255[256];
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) s_inv255[i] = __fdiv_rn((float)i, 255.0f);
+  __syncthreads();
   const int lane = threadIdx.x & 31;
-  const int64_t noct = (n + 7) / 8;
-  const int64_t nsteps = (noct + 32 * K - 1) / (32 * K);
-  const int64_t nfull = n / (256 * K);  // steps whose 32*K octets are all complete
+  const int64_t nsteps = (n + 1023) / 1024;
+  const int64_t nfull = n / 1024;
   const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
   Q4Step cur, nxt;
   bool have = false;
   for (int64_t st = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); st < nsteps;
        st += wstride) {
-    if (have) {
-      cur = nxt;
-    } else if (st < nfull) {
-      q4_step_load<true>(data, qscales, sup, n, st, lane, cur);
-    } else {
-      q4_step_load<false>(data, qscales, sup, n, st, lane, cur);
+    if (st >= nfull) {
+      // the partial last step: element-wise bounds
+      const int64_t nbytes = (n + 1) / 2;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t e0 = (st * 128 + k * 32 + lane) * 8;
+        if (e0 >= n) continue;
+        uint32_t pk = 0u;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          if (e0 / 2 + b < nbytes) pk |= (uint32_t)data[e0 / 2 + b] << (8 * b);
+        const float rs = __fmul_rn(s_inv255[qscales[e0 / kQ4Block]], sup[e0 / kQ4SuperElems]);
+        const int64_t c = n - e0;
+        store_vec<F32>(y, e0, dequant8(pk, rs), c >= 8 ? 8 : (int)c);
+      }
+      continue;
     }
+    if (have)
+      cur = nxt;
+    else
+      q4_step_full(data, qscales, sup, st, lane, cur);
     const int64_t ns = st + wstride;
     have = ns < nfull;
-    if (have) q4_step_load<true>(data, qscales, sup, n, ns, lane, nxt);
+    if (have) q4_step_full(data, qscales, sup, ns, lane, nxt);
+    const int qb = 8 * (lane >> 3);  // octet 32 k + l lies in block 16 st + 4 k + l / 8
+    const uint32_t qw[4] = {cur.q.x, cur.q.y, cur.q.z, cur.q.w};
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      const int64_t e0 = (st * (32 * K) + k * 32 + lane) * 8;
-      if (e0 >= n) continue;
-      const float rs = __fmul_rn(__fdiv_rn(cur.qs[k], 255.0f), cur.sup[k]);
-      const V32 o = dequant8(cur.pk[k], rs);
-      const int64_t c = n - e0;
-      store_vec<F32>(y, e0, o, c >= 8 ? 8 : (int)c);
+    for (int k = 0; k < 4; ++k) {
+      const float rs = __fmul_rn(s_inv255[(qw[k] >> qb) & 0xffu], cur.sup);
+      st_v32(y + (st * 128 + k * 32 + lane) * 8, dequant8(cur.pk[k], rs));
     }
   }
 }
 
 qat_status launch_q4_dequant(const uint8_t* data, const uint8_t* qscales, const float* sup,
                              int64_t n, float* y, cudaStream_t s) {
-  const int64_t noct = (n + 7) / 8;
-  const int64_t nsteps = (noct + 127) / 128;
+  const int64_t nsteps = (n + 1023) / 1024;
   int64_t g = (nsteps + 7) / 8;
   int64_t cap = (int64_t)device_info().sms * 8;
   int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
