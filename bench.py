@@ -263,17 +263,26 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def source_key(source: str) -> str:
+    """sha256[:16] of a kernel's source file followed by the shared device
+    header it includes (the key under which profiles/traffic.txt records it)."""
+    h = hashlib.sha256()
+    for f in (source, "qat_device.cuh"):
+        with open(os.path.join(ROOT, "fake_quant_numerics_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(kernel: str, source: str):
     """DRAM bytes per launch of `kernel` at full size from the committed ncu
-    summary, or None when the kernel's source changed since the capture."""
+    summary, or None when the kernel's sources changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
-        with open(os.path.join(ROOT, "fake_quant_numerics_gb300", "csrc", source), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        key = source_key(source)
         with open(path) as f:
             for line in f:
                 parts = line.split()
-                if len(parts) >= 3 and parts[0] == kernel and parts[1] == sha:
+                if len(parts) >= 3 and parts[0] == kernel and parts[1] == key:
                     return float(parts[2])
     except OSError:
         pass
