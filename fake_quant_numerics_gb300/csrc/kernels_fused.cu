@@ -179,7 +179,7 @@ __global__ void __maxnreg__(T::BYTES == 4 ? 96 : 80) k_int_groups(const void* __
 // one thread block (256 threads) per unit of L elements, NV vectors / thread
 // ---------------------------------------------------------------------------
 template <typename T, int BITS, bool AFFINE, int NV, bool STATS_ONLY>
-__global__ void __launch_bounds__(256, (NV <= 2 && !AFFINE) ? 3 : 1) k_int_rows(const void* __restrict__ x, int64_t units,
+__global__ void __launch_bounds__(256, NV <= 2 ? 3 : 1) k_int_rows(const void* __restrict__ x, int64_t units,
                                                   int64_t L, float* scale, int32_t* zp,
                                                   float* absmax, float* minv, float* maxv, void* y,
                                                   void* codes, uint32_t* mask, int32_t* flags) {
@@ -187,8 +187,14 @@ __global__ void __launch_bounds__(256, (NV <= 2 && !AFFINE) ? 3 : 1) k_int_rows(
   constexpr int LPW = 32 / VEC;
   constexpr int MM = STATS_ONLY ? kMMKeys : (AFFINE ? kMMFloat : kMMNone);
   __shared__ __align__(16) uint32_t red[4 * 8];
-  const int lane = threadIdx.x & 31;
+  __shared__ IntParams sp;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nvec = (int)(L / VEC);
+  // The row's statistics are folded per warp (redux.sync), the 8 warp
+  // partials by warp 0, whose lane 0 calibrates and publishes the parameters
+  // in shared memory: once per row, not once per thread.  `red` and `sp` are
+  // rewritten by the next row only after its first barrier, by which time
+  // every thread has read them.
   // the next unit's vectors are requested before the current one is
   // processed, so each block keeps a unit's worth of loads in flight
   auto load_unit = [&](int64_t uu, V32 (&dst)[NV]) {
@@ -218,25 +224,37 @@ __global__ void __launch_bounds__(256, (NV <= 2 && !AFFINE) ? 3 : 1) k_int_rows(
         stats_add_vec<T, MM>(st, v[j]);
       }
     }
-    Stats b = block_reduce_stats<MM>(st, red);
-    if (STATS_ONLY) {
-      if (threadIdx.x == 0) {
-        if (absmax) absmax[u] = b.absmax_f();
-        if (minv) minv[u] = b.min_f<MM>();
-        if (maxv) maxv[u] = b.max_f<MM>();
-        flag_or(flags, b.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
+    st.reduce_lanes<MM>(32);
+    if (lane == 0) reinterpret_cast<uint4*>(red)[warp] = st.pack();
+    __syncthreads();
+    if (warp == 0) {
+      Stats b;
+      b.init<MM>();
+      if (lane < NT / 32) b.unpack(reinterpret_cast<const uint4*>(red)[lane]);
+      b.reduce_lanes<MM>(NT / 32);
+      if (lane == 0) {
+        if (STATS_ONLY) {
+          if (absmax) absmax[u] = b.absmax_f();
+          if (minv) minv[u] = b.min_f<MM>();
+          if (maxv) maxv[u] = b.max_f<MM>();
+          flag_or(flags, b.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
+        } else {
+          IntParams q;
+          const int f = calibrate<BITS, AFFINE, MM>(b, q);
+          sp = q;
+          scale[u] = q.s;
+          if (zp) zp[u] = q.zp;
+          flag_or(flags, f);
+        }
       }
+    }
+    if (STATS_ONLY) {
 #pragma unroll
       for (int j = 0; j < NV; ++j) v[j] = vn[j];
       continue;
     }
-    IntParams p;
-    int f = calibrate<BITS, AFFINE, MM>(b, p);
-    if (threadIdx.x == 0) {
-      scale[u] = p.s;
-      if (zp) zp[u] = p.zp;
-      flag_or(flags, f);
-    }
+    __syncthreads();
+    const IntParams p = sp;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int vi = threadIdx.x + j * NT;
