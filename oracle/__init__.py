@@ -78,6 +78,19 @@ def lib():
         L.or64_fake_quant_int.argtypes = [vp, i32, i64, i64, i32, i32, i32, i64, vp, vp, vp]
         L.or64_fake_quant_fp8.argtypes = [vp, i32, i64, i32, vp, vp]
         L.or_unit_stats.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp]
+        u64 = ctypes.c_uint64
+        L.or_philox4x32_10.argtypes = [vp, vp, vp]
+        L.or_sr_uniform.argtypes = [u64, u64, i64]
+        L.or_sr_uniform.restype = f32
+        L.or_sr_round.argtypes = [f32, f32]
+        L.or_sr_round.restype = f32
+        L.or_quantize_sr.argtypes = [f32, f32, i32, i32, i32, f32]
+        L.or_quantize_sr.restype = i32
+        L.or_fp8_cast_sr.argtypes = [f32, i32, f32]
+        L.or_fp8_cast_sr.restype = f32
+        L.or_fake_quant_int_sr.argtypes = [vp, i32, i64, i64, i32, i32, i32, i64, i32, vp, vp, u64,
+                                           u64, vp, vp, vp, vp]
+        L.or_fake_quant_fp8_sr.argtypes = [vp, i32, i64, i32, i32, vp, u64, u64, vp, vp, vp, vp]
     return _lib
 
 
@@ -165,6 +178,78 @@ def fake_quant_int(x: np.ndarray, rows: int, cols: int, bits: int, scheme: int, 
     if st:
         raise ValueError(f"oracle fake_quant_int status {st}")
     return dict(y=y, codes=codes, mask=mask, scale=sc[:u], zero_point=zp[:u], flags=flags.value)
+
+
+def philox4x32_10(counter, key) -> np.ndarray:
+    """One Philox-4x32-10 block: counter (4 x uint32), key (2 x uint32) -> 4 x uint32."""
+    c = np.ascontiguousarray(counter, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.empty(4, np.uint32)
+    lib().or_philox4x32_10(_p(c), _p(k), _p(out))
+    return out
+
+
+def sr_uniform(seed: int, offset: int, n: int) -> np.ndarray:
+    """The stochastic-rounding draws u_0 .. u_{n-1} of a call with (seed, offset)."""
+    f = lib().or_sr_uniform
+    return np.array([f(seed, offset, i) for i in range(n)], np.float32)
+
+
+def sr_round(r: float, u: float) -> float:
+    return lib().or_sr_round(r, u)
+
+
+def quantize_sr(x: float, scale: float, zp: int, qmin: int, qmax: int, u: float) -> int:
+    return lib().or_quantize_sr(x, scale, zp, qmin, qmax, u)
+
+
+def fp8_cast_sr(t: float, fmt: int, u: float) -> float:
+    return lib().or_fp8_cast_sr(t, fmt, u)
+
+
+def fake_quant_int_sr(x: np.ndarray, rows: int, cols: int, bits: int, scheme: int,
+                      granularity: int, group: int = 0, seed: int = 0, offset: int = 0,
+                      scale=None, zero_point=None, want_y=True, want_codes=True, want_mask=True):
+    """fake_quant_int with stochastic rounding; returns dict(y, codes, mask, scale,
+    zero_point, flags)."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    dt = _dtype_code(x)
+    n = rows * cols
+    u = n_units(rows, cols, granularity, group) if (granularity != PER_GROUP or group > 0) else 0
+    given = scale is not None
+    sc = np.ascontiguousarray(scale, dtype=np.float32).copy() if given else np.zeros(max(u, 1), np.float32)
+    zp = (np.ascontiguousarray(zero_point, dtype=np.int32).copy() if zero_point is not None
+          else np.zeros(max(u, 1), np.int32))
+    y = np.empty(n, dtype=x.dtype) if want_y else None
+    codes = None
+    if want_codes:
+        codes = np.empty(n, np.int8) if bits == 8 else np.empty((n + 1) // 2, np.uint8)
+    mask = np.empty((n + 31) // 32, np.uint32) if want_mask else None
+    flags = ctypes.c_int32(0)
+    st = lib().or_fake_quant_int_sr(_p(x), dt, rows, cols, bits, scheme, granularity, group,
+                                    int(given), _p(sc), _p(zp), seed, offset, _p(y), _p(codes),
+                                    _p(mask), ctypes.byref(flags))
+    if st:
+        raise ValueError(f"oracle fake_quant_int_sr status {st}")
+    return dict(y=y, codes=codes, mask=mask, scale=sc[:u], zero_point=zp[:u], flags=flags.value)
+
+
+def fake_quant_fp8_sr(x: np.ndarray, fmt: int, seed: int = 0, offset: int = 0, scale=None,
+                      want_codes=True, want_mask=True):
+    """fake_quant_fp8 with stochastic rounding; returns dict(y, codes, mask, scale, flags)."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    dt = _dtype_code(x)
+    n = x.size
+    s = ctypes.c_float(0.0 if scale is None else float(scale))
+    y = np.empty(n, dtype=x.dtype)
+    codes = np.empty(n, np.uint8) if want_codes else None
+    mask = np.empty((n + 31) // 32, np.uint32) if want_mask else None
+    flags = ctypes.c_int32(0)
+    st = lib().or_fake_quant_fp8_sr(_p(x), dt, n, fmt, int(scale is not None), ctypes.byref(s),
+                                    seed, offset, _p(y), _p(codes), _p(mask), ctypes.byref(flags))
+    if st:
+        raise ValueError(f"oracle fake_quant_fp8_sr status {st}")
+    return dict(y=y, codes=codes, mask=mask, scale=np.float32(s.value), flags=flags.value)
 
 
 def fake_quant_fp8(x: np.ndarray, fmt: int, scale=None, want_codes=True, want_mask=True):

@@ -27,6 +27,11 @@
  *          absmax/448, zero scale -> code 0)
  *   [EDU]  cs349e 05_quantization_basics.py, demo 3 (groups run along the last
  *          dimension)
+ *   [QAT] RoundingMode::{Nearest, Stochastic}::round_to_int (stochastic
+ *          rounding), with the uniform draws from a counter-based generator:
+ *   [PHX]  Philox-4x32-10, J. Salmon, M. Moraes, R. Dror, D. Shaw, "Parallel
+ *          random numbers: as easy as 1, 2, 3", SC 2011 (the round function
+ *          and the Weyl key schedule as published)
  *
  * Every place where the sources are silent and a reading was taken is marked
  * "reading:" below.
@@ -217,6 +222,77 @@ static int in_window(float x, float scale, int32_t zp, int32_t qmin, int32_t qma
   return (x >= lo && x <= hi) ? 1 : 0;
 }
 
+/* ------------------------------------------------------------------------- */
+/* Stochastic rounding.                                                       */
+/* [QAT] RoundingMode::Stochastic: lower = floor(r), frac = r - lower, the    */
+/* result is lower + 1 when the draw u < frac and lower otherwise, so that    */
+/* E[round(r)] = r.  reading: the module draws u in [0, 1) from a caller's    */
+/* Rng in element order; here the draw of element i of a call is a function   */
+/* of (seed, offset, i) alone, so that any evaluation order gives the same    */
+/* result:                                                                    */
+/*   w = word (i mod 4) of Philox-4x32-10 [PHX] with key (lo32 seed,          */
+/*       hi32 seed) and counter (lo32 j, hi32 j, 0, 0), j = offset + i / 4;   */
+/*   u = (w >> 9) * 2^-23, a multiple of 2^-23 in [0, 1).                     */
+/* A caller advances offset by ceil(n / 4) per call for fresh draws.  In      */
+/* binary32, frac = r - floor(r) is exact (Sterbenz) and so is u, so the      */
+/* decision u < frac is exact.                                                */
+/* ------------------------------------------------------------------------- */
+void or_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    /* [PHX] Philox S-box: two 32x32 -> 64-bit products with the round
+     * multipliers, high halves mixed with the other words and the key. */
+    uint64_t p0 = (uint64_t)0xD2511F53u * x0;
+    uint64_t p1 = (uint64_t)0xCD9E8D57u * x2;
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t n0 = hi1 ^ x1 ^ k0;
+    uint32_t n2 = hi0 ^ x3 ^ k1;
+    x0 = n0;
+    x1 = lo1;
+    x2 = n2;
+    x3 = lo0;
+    /* [PHX] Weyl sequence key schedule */
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  out[0] = x0;
+  out[1] = x1;
+  out[2] = x2;
+  out[3] = x3;
+}
+
+float or_sr_uniform(uint64_t seed, uint64_t offset, int64_t i) {
+  uint64_t j = offset + (uint64_t)i / 4u;
+  uint32_t ctr[4] = {(uint32_t)j, (uint32_t)(j >> 32), 0u, 0u};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  or_philox4x32_10(ctr, key, out);
+  return (float)(out[i & 3] >> 9) * 0x1p-23f;
+}
+
+/* [QAT] round_to_int, Stochastic arm, in binary32.  NaN stays NaN; for an
+ * infinite r, frac is NaN and the comparison is false, so r itself is
+ * returned (as floor(+-inf) is +-inf). */
+float or_sr_round(float r, float u) {
+  float lower = floorf(r);
+  float frac = r - lower;
+  return (u < frac) ? lower + 1.0f : lower;
+}
+
+/* QuantParams::quantize with stochastic rounding, in the documented form
+ * (the zero point is added after rounding, as for or_quantize). */
+int32_t or_quantize_sr(float x, float scale, int32_t zp, int32_t qmin, int32_t qmax, float u) {
+  float r = x / scale;
+  if (isnan(r)) return 0;
+  float k = or_sr_round(r, u);
+  float lo = (float)(qmin - zp), hi = (float)(qmax - zp);
+  if (k < lo) k = lo;
+  if (k > hi) k = hi;
+  return (int32_t)k + zp;
+}
+
 static void set_code(void* codes, int bits, int64_t i, int32_t q) {
   if (!codes) return;
   if (bits == 8) {
@@ -251,9 +327,10 @@ static void set_mask(uint32_t* mask, int64_t i, int bit) {
 /* A unit that fails calibration (flag set) or has invalid given params gets  */
 /* codes 0, y = +0, mask 0.  reading: the module returns an error there.      */
 /* ------------------------------------------------------------------------- */
-int or_fake_quant_int(const void* x, int dtype, int64_t rows, int64_t cols, int bits, int scheme,
-                      int gran, int64_t group, int params_given, float* scale, int32_t* zp,
-                      void* y, void* codes, uint32_t* mask, int32_t* flags, int doc_form) {
+static int fq_int(const void* x, int dtype, int64_t rows, int64_t cols, int bits, int scheme,
+                  int gran, int64_t group, int params_given, float* scale, int32_t* zp, void* y,
+                  void* codes, uint32_t* mask, int32_t* flags, int doc_form, int stochastic,
+                  uint64_t seed, uint64_t offset) {
   int32_t qmin, qmax;
   int st = or_q_range(bits, scheme, &qmin, &qmax);
   if (st) return st;
@@ -302,13 +379,33 @@ int or_fake_quant_int(const void* x, int dtype, int64_t rows, int64_t cols, int 
         set_mask(mask, i, 0);
         continue;
       }
-      int32_t q = or_quantize(v, s, z, qmin, qmax, doc_form);
+      int32_t q = stochastic
+                      ? or_quantize_sr(v, s, z, qmin, qmax, or_sr_uniform(seed, offset, i))
+                      : or_quantize(v, s, z, qmin, qmax, doc_form);
       set_code(codes, bits, i, q);
       if (y) store_elem(y, dtype, i, or_dequantize(q, s, z));
       set_mask(mask, i, in_window(v, s, z, qmin, qmax));
     }
   }
   return OR_OK;
+}
+
+int or_fake_quant_int(const void* x, int dtype, int64_t rows, int64_t cols, int bits, int scheme,
+                      int gran, int64_t group, int params_given, float* scale, int32_t* zp,
+                      void* y, void* codes, uint32_t* mask, int32_t* flags, int doc_form) {
+  return fq_int(x, dtype, rows, cols, bits, scheme, gran, group, params_given, scale, zp, y, codes,
+                mask, flags, doc_form, 0, 0, 0);
+}
+
+/* The same with stochastic rounding: element i rounds with the draw
+ * or_sr_uniform(seed, offset, i); calibration and the STE window are those of
+ * the nearest-rounding path. */
+int or_fake_quant_int_sr(const void* x, int dtype, int64_t rows, int64_t cols, int bits,
+                         int scheme, int gran, int64_t group, int params_given, float* scale,
+                         int32_t* zp, uint64_t seed, uint64_t offset, void* y, void* codes,
+                         uint32_t* mask, int32_t* flags) {
+  return fq_int(x, dtype, rows, cols, bits, scheme, gran, group, params_given, scale, zp, y, codes,
+                mask, flags, 1, 1, seed, offset);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -333,6 +430,28 @@ float or_fp8_magnitude(float a, int fmt) {
   float mag = k * step;
   if (mag > fp8_max(fmt)) return fp8_max(fmt);
   return mag;
+}
+
+/* [QAT] fp8_quantize_magnitude with RoundingMode::Stochastic: the ratio a/ulp
+ * (an exact power-of-two scaling) is rounded by or_sr_round with draw u, then
+ * saturated as in the nearest-rounding rule. */
+float or_fp8_magnitude_sr(float a, int fmt, float u) {
+  if (a == 0.0f) return 0.0f;
+  int emin = 1 - fp8_bias(fmt);
+  int e = (int)((f2u(a) >> 23) & 0xFF) - 127;
+  int se = (e > emin ? e : emin) - fp8_mbits(fmt);
+  float step = ldexpf(1.0f, se);
+  float ratio = a / step;
+  float k = or_sr_round(ratio, u);
+  float mag = k * step;
+  if (mag > fp8_max(fmt)) return fp8_max(fmt);
+  return mag;
+}
+
+float or_fp8_cast_sr(float t, int fmt, float u) {
+  if (isnan(t)) return u2f(0x7FC00000u);
+  if (isinf(t)) return copysignf(fp8_max(fmt), t);
+  return copysignf(or_fp8_magnitude_sr(fabsf(t), fmt, u), t);
 }
 
 /* [QAT] fake_quant_fp8, one element: NaN -> NaN, +-Inf -> +-max, otherwise the
@@ -379,8 +498,9 @@ uint8_t or_fp8_encode(float c, int fmt) {
 /* A given s that is negative, NaN or infinite: OR_FLAG_BAD_PARAMS and every  */
 /* element gets code 0, y = +0, mask 0.                                       */
 /* ------------------------------------------------------------------------- */
-int or_fake_quant_fp8(const void* x, int dtype, int64_t n, int fmt, int scale_given, float* scale,
-                      void* y, uint8_t* codes, uint32_t* mask, int32_t* flags) {
+static int fq_fp8(const void* x, int dtype, int64_t n, int fmt, int scale_given, float* scale,
+                  void* y, uint8_t* codes, uint32_t* mask, int32_t* flags, int stochastic,
+                  uint64_t seed, uint64_t offset) {
   if (fmt != OR_E4M3 && fmt != OR_E5M2) return OR_ERR_UNSUPPORTED;
   if (n < 0) return OR_ERR_INVALID;
   if (n == 0) return OR_OK;
@@ -412,7 +532,7 @@ int or_fake_quant_fp8(const void* x, int dtype, int64_t n, int fmt, int scale_gi
       m = (fabsf(v) <= lim) ? 1 : 0;
     } else {
       float t = v / s;
-      c = or_fp8_cast(t, fmt);
+      c = stochastic ? or_fp8_cast_sr(t, fmt, or_sr_uniform(seed, offset, i)) : or_fp8_cast(t, fmt);
       yv = c * s;
       m = (fabsf(v) <= lim) ? 1 : 0;
     }
@@ -421,6 +541,20 @@ int or_fake_quant_fp8(const void* x, int dtype, int64_t n, int fmt, int scale_gi
     set_mask(mask, i, m);
   }
   return OR_OK;
+}
+
+int or_fake_quant_fp8(const void* x, int dtype, int64_t n, int fmt, int scale_given, float* scale,
+                      void* y, uint8_t* codes, uint32_t* mask, int32_t* flags) {
+  return fq_fp8(x, dtype, n, fmt, scale_given, scale, y, codes, mask, flags, 0, 0, 0);
+}
+
+/* The same with stochastic rounding of the FP8 magnitude (draw of element i:
+ * or_sr_uniform(seed, offset, i)); the scale and the STE window are those of
+ * the nearest-rounding path. */
+int or_fake_quant_fp8_sr(const void* x, int dtype, int64_t n, int fmt, int scale_given,
+                         float* scale, uint64_t seed, uint64_t offset, void* y, uint8_t* codes,
+                         uint32_t* mask, int32_t* flags) {
+  return fq_fp8(x, dtype, n, fmt, scale_given, scale, y, codes, mask, flags, 1, seed, offset);
 }
 
 /* ------------------------------------------------------------------------- */
