@@ -1,12 +1,14 @@
 """GB300 fake-quant library: QAT fake quantization (int8/int4 symmetric and
 affine per tensor / row / group, saturating FP8 E4M3/E5M2), its
 straight-through-estimator backward, and the QLoRA two-level 4-bit block
-format, as CUDA kernels for sm_103a behind a C ABI (include/qat.h).
+format, as CUDA kernels for sm_103a behind a C ABI (include/qat.h); the
+integer and FP8 maps also round stochastically with counter-based draws.
 """
 from ._lib import QatError, load  # noqa: F401
 from .api import (DoubleQuantized4Bit, FakeQuantFp8, FakeQuantInt, FakeQuantSTE,  # noqa: F401
                   QatDataError, amax_stats, dequantize_4bit_double, fake_quant_backward,
                   fake_quant_fp8, fake_quant_int, qat_amax_stats, qat_dequant4_double,
-                  qat_fake_quant_fp8, qat_fake_quant_int, qat_kernel_launch_count,
+                  qat_fake_quant_fp8, qat_fake_quant_fp8_sr, qat_fake_quant_int,
+                  qat_fake_quant_int_sr, qat_kernel_launch_count,
                   qat_quant4_double, qat_ste_backward, qat_workspace_bytes, quantize_4bit_double,
                   raise_on_flags)

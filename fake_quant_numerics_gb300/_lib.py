@@ -34,6 +34,8 @@ _lib = None
 
 _vp, _i64, _int, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
 
+_u64 = ctypes.c_uint64
+
 PROTOTYPES = {
     "qat_status_string": ([_int], ctypes.c_char_p),
     "qat_workspace_bytes": ([_i64, _i64, _int, _i64], _sz),
@@ -42,6 +44,10 @@ PROTOTYPES = {
                             _vp, _vp, _vp, _sz, _vp], _int),
     "qat_fake_quant_fp8": ([_vp, _int, _i64, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _int),
     "qat_fake_quant_fp8_noalloc": ([_vp, _int, _i64, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp], _int),
+    "qat_fake_quant_int_sr": ([_vp, _int, _i64, _i64, _int, _int, _int, _i64, _int, _vp, _vp, _u64,
+                               _u64, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _int),
+    "qat_fake_quant_fp8_sr": ([_vp, _int, _i64, _int, _int, _vp, _u64, _u64, _vp, _vp, _vp, _vp, _vp,
+                               _sz, _vp], _int),
     "qat_ste_backward": ([_vp, _int, _i64, _vp, _vp, _vp], _int),
     "qat_quant4_double": ([_vp, _i64, _vp, _vp, _vp, _vp, _vp], _int),
     "qat_dequant4_double": ([_vp, _vp, _vp, _i64, _vp, _vp], _int),

@@ -94,6 +94,26 @@ def qat_fake_quant_fp8(x, n, fmt, scale_given, scale, y, codes, mask, dev_flags,
     _lib.check("qat_fake_quant_fp8", st)
 
 
+def qat_fake_quant_int_sr(x, rows, cols, bits, scheme, granularity, group, params_given, scale,
+                          zero_point, seed, offset, y, codes, mask, dev_flags, workspace,
+                          stream=None):
+    st = _lib.lib().qat_fake_quant_int_sr(_p(x), _dt(x), rows, cols, bits, _SCHEME[scheme],
+                                          _GRAN[granularity], group, int(params_given), _p(scale),
+                                          _p(zero_point), int(seed), int(offset), _p(y), _p(codes),
+                                          _p(mask), _p(dev_flags), _p(workspace),
+                                          _nbytes(workspace), _s(stream))
+    _lib.check("qat_fake_quant_int_sr", st)
+
+
+def qat_fake_quant_fp8_sr(x, n, fmt, scale_given, scale, seed, offset, y, codes, mask, dev_flags,
+                          workspace, stream=None):
+    st = _lib.lib().qat_fake_quant_fp8_sr(_p(x), _dt(x), n, _FMT[fmt], int(scale_given), _p(scale),
+                                          int(seed), int(offset), _p(y), _p(codes), _p(mask),
+                                          _p(dev_flags), _p(workspace), _nbytes(workspace),
+                                          _s(stream))
+    _lib.check("qat_fake_quant_fp8_sr", st)
+
+
 def qat_ste_backward(grad, n, mask, grad_in, stream=None):
     st = _lib.lib().qat_ste_backward(_p(grad), _dt(grad), n, _p(mask), _p(grad_in), _s(stream))
     _lib.check("qat_ste_backward", st)
@@ -191,9 +211,11 @@ class DoubleQuantized4Bit(NamedTuple):
 def fake_quant_int(x: torch.Tensor, bits: int = 8, scheme="symmetric", granularity="tensor",
                    group: int = 0, scale: Optional[torch.Tensor] = None,
                    zero_point: Optional[torch.Tensor] = None, want_codes: bool = True,
-                   want_mask: bool = True, check: bool = False) -> FakeQuantInt:
+                   want_mask: bool = True, check: bool = False, rounding: str = "nearest",
+                   seed: int = 0, offset: int = 0) -> FakeQuantInt:
     """Integer fake quantization of x (float32 or bfloat16, CUDA), calibrated per
-    tensor / row / group, or with the given per-unit scale and zero point."""
+    tensor / row / group, or with the given per-unit scale and zero point.
+    rounding="stochastic" rounds with the counter-based draws of (seed, offset)."""
     x = _ready(x)
     rows, cols = _shape2d(x)
     n = x.numel()
@@ -224,16 +246,24 @@ def fake_quant_int(x: torch.Tensor, bits: int = 8, scheme="symmetric", granulari
     flags = torch.zeros(1, dtype=torch.int32, device=dev)
     wsb = qat_workspace_bytes(rows, cols, gran, group)
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
-    qat_fake_quant_int(x, rows, cols, bits, sch, gran, group, given, scale, zero_point, y, codes, mask,
-                       flags, ws)
+    if rounding == "stochastic":
+        qat_fake_quant_int_sr(x, rows, cols, bits, sch, gran, group, given, scale, zero_point, seed,
+                              offset, y, codes, mask, flags, ws)
+    elif rounding == "nearest":
+        qat_fake_quant_int(x, rows, cols, bits, sch, gran, group, given, scale, zero_point, y, codes,
+                           mask, flags, ws)
+    else:
+        raise ValueError(f"rounding must be 'nearest' or 'stochastic', not {rounding!r}")
     if check:
         raise_on_flags(flags, "fake_quant_int")
     return FakeQuantInt(y, codes, mask, scale, zero_point, flags)
 
 
 def fake_quant_fp8(x: torch.Tensor, fmt="e4m3", scale: Optional[float] = None,
-                   want_codes: bool = False, want_mask: bool = True) -> FakeQuantFp8:
-    """Per-tensor amax-scaled (or given-scale) saturating FP8 fake quantization."""
+                   want_codes: bool = False, want_mask: bool = True, rounding: str = "nearest",
+                   seed: int = 0, offset: int = 0) -> FakeQuantFp8:
+    """Per-tensor amax-scaled (or given-scale) saturating FP8 fake quantization;
+    rounding="stochastic" rounds with the counter-based draws of (seed, offset)."""
     x = _ready(x)
     n = x.numel()
     dev = x.device
@@ -248,7 +278,12 @@ def fake_quant_fp8(x: torch.Tensor, fmt="e4m3", scale: Optional[float] = None,
     ws = None
     if not given:
         ws = torch.empty(qat_workspace_bytes(1, n, PER_TENSOR, 0), dtype=torch.uint8, device=dev)
-    qat_fake_quant_fp8(x, n, fmt, given, s, y, codes, mask, flags, ws)
+    if rounding == "stochastic":
+        qat_fake_quant_fp8_sr(x, n, fmt, given, s, seed, offset, y, codes, mask, flags, ws)
+    elif rounding == "nearest":
+        qat_fake_quant_fp8(x, n, fmt, given, s, y, codes, mask, flags, ws)
+    else:
+        raise ValueError(f"rounding must be 'nearest' or 'stochastic', not {rounding!r}")
     return FakeQuantFp8(y, codes, mask, s, flags)
 
 

@@ -20,7 +20,10 @@ LIB = os.path.join(PKG, "libqat.so")
 
 SOURCES = ["qat_abi.cu", "kernels_tensor.cu", "kernels_fused.cu", "kernels_fp8.cu",
            "kernels_misc.cu", "qat_noalloc.cu"]
-HEADERS = ["qat_device.cuh", "qat_launch.h"]
+# sources compiled a second time with QAT_SR=1: their stochastic-rounding
+# kernels and *_sr launchers (object <name>_sr.o)
+SR_SOURCES = ["kernels_tensor.cu", "kernels_fused.cu", "kernels_fp8.cu"]
+HEADERS = ["qat_device.cuh", "qat_launch.h", "qat_sr.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-fmad=false",
            "-prec-div=true", "-prec-sqrt=true", "-ftz=false", "-I", INCLUDE, "-I", CSRC]
@@ -46,12 +49,16 @@ def build(verbose: bool = False, extra_flags=()) -> str:
     nvcc = _nvcc()
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "qat.h")]
     jobs, objs = [], []
-    for src in SOURCES:
+    units = [(src, src.replace(".cu", ".o"), []) for src in SOURCES]
+    units += [(src, src.replace(".cu", "_sr.o"), ["-DQAT_SR=1"]) for src in SR_SOURCES]
+    # the longest translation units first, so the parallel build ends sooner
+    units.sort(key=lambda u: u[0] != "kernels_fused.cu")
+    for src, oname, defs in units:
         sp = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, oname)
         objs.append(obj)
         if verbose or _stale(obj, [sp, *hdrs, __file__]):
-            cmd = [nvcc, *ARCH, *NVFLAGS, *extra_flags, "-c", sp, "-o", obj]
+            cmd = [nvcc, *ARCH, *NVFLAGS, *defs, *extra_flags, "-c", sp, "-o", obj]
             if verbose:
                 cmd.insert(1, "-Xptxas=-v")
             jobs.append(cmd)

@@ -59,6 +59,7 @@ struct Fp8Params {
   float s;          // scale
   float lim;        // fmt_max * s: the STE window |x| <= lim
   float rlo, rhi;   // bracketing reciprocals (fast == 1)
+  float rcp, ns;    // RN(1/s) and -s for the exact quotient (stochastic rounding, fast == 1)
   uint32_t limh2;   // (bf16 magnitude bits of the largest bf16 <= lim) | 0x8000, in both halves
   int mode;         // 0 normal, 1 zero scale, 2 invalid given scale
   int fast;
@@ -69,6 +70,8 @@ __device__ __forceinline__ void fp8_params_finish(Fp8Params& p) {
   const float rcp = p.fast ? __frcp_rn(p.s) : 1.0f;
   p.rlo = __fmul_rn(rcp, 1.0f - 0x1p-21f);
   p.rhi = __fmul_rn(rcp, 1.0f + 0x1p-21f);
+  p.rcp = rcp;
+  p.ns = -p.s;
   // lim >= 0 is finite when fast; truncating its bits to 16 rounds toward 0
   p.limh2 = ((__float_as_uint(p.lim) >> 16) | 0x8000u) * 0x00010001u;
 }
@@ -115,12 +118,97 @@ __device__ __forceinline__ bool fp8_vec_bf16_fast(const V32& v, const Fp8Params&
   return bad == 0u;
 }
 
+// fp8_quantize_magnitude with stochastic rounding (RoundingMode::Stochastic):
+// e = floor(log2 a) from the exponent field (a binary32 subnormal reads
+// e = -127, below emin), ulp = 2^(max(e, emin) - mbits), a / ulp (an exact
+// power-of-two scaling) rounded by sr_round with draw u, times ulp,
+// saturated at the format maximum; the sign of t.  A NaN t is handled by the
+// caller (canonical NaN, code 0x7F).
+template <int FMT>
+__device__ __forceinline__ float fp8_sr_value(float t, float u) {
+  constexpr int MB = FMT == QAT_E4M3 ? 3 : 2, EMIN = FMT == QAT_E4M3 ? -6 : -14;
+  constexpr float kMaxF = FMT == QAT_E4M3 ? 448.0f : 57344.0f;
+  const float a = fabsf(t);
+  const int e = (int)(__float_as_uint(a) >> 23) - 127;
+  const int se = (e > EMIN ? e : EMIN) - MB;                  // in [EMIN - MB, 128 - MB]
+  const float inv = __uint_as_float((uint32_t)(127 - se) << 23);  // 2^-se, normal
+  const float step = __uint_as_float((uint32_t)(127 + se) << 23); // 2^se, normal
+  const float k = sr_round(__fmul_rn(a, inv), u);
+  const float mag = fminf(__fmul_rn(k, step), kMaxF);
+  return copysignf(mag, t);
+}
+
+// One vector with stochastic rounding: the IEEE quotient t = RN(x/s) (exact
+// residual-step quotient for a safe scale, the division otherwise; its sign
+// is that of x), the grid value of fp8_sr_value, its code by the saturating
+// cast (exact for a grid value), y = c * s; NaN, zero-scale and invalid-scale
+// handling and the window as in the nearest-rounding path.
 template <typename T, int FMT, bool CODES, bool FULL>
+__device__ __forceinline__ void fp8_vec_sr(const V32& v, const Fp8Params& p, const SrCtx& sr,
+                                           int64_t base, int cnt, V32& out,
+                                           CodeVec<8, T::VEC>& cv, uint32_t& mb) {
+  constexpr int VEC = T::VEC;
+  cv.clear();
+  mb = 0u;
+#pragma unroll
+  for (int g = VEC / 4 - 1; g >= 0; --g) {
+    float u[4];
+    sr_draws4(sr, base / 4 + g, u);
+#pragma unroll
+    for (int h = 1; h >= 0; --h) {
+      const int e = 4 * g + 2 * h;
+      const float x0 = elem<T>(v, e), x1 = elem<T>(v, e + 1);
+      const bool n0 = isnan(x0), n1 = isnan(x1);
+      uint32_t c0 = 0u, c1 = 0u;
+      float y0 = 0.0f, y1 = 0.0f;
+      if (p.mode == 0) {
+        float t0, t1;
+        if (p.fast) {
+          quotient_rn2(x0, x1, p.rcp, p.ns, t0, t1);
+          t0 = isfinite(x0) ? copysignf(t0, x0) : x0;  // +-inf / s = +-inf, NaN stays NaN
+          t1 = isfinite(x1) ? copysignf(t1, x1) : x1;
+        } else {
+          t0 = __fdiv_rn(x0, p.s);
+          t1 = __fdiv_rn(x1, p.s);
+        }
+        const float g0 = fp8_sr_value<FMT>(t0, u[2 * h]);
+        const float g1 = fp8_sr_value<FMT>(t1, u[2 * h + 1]);
+        const uint32_t c2 = fp8x2_encode<FMT>(g0, g1);
+        c0 = c2 & 0xffu;
+        c1 = (c2 >> 8) & 0xffu;
+        mul2(g0, g1, p.s, p.s, y0, y1);
+      }
+      if (p.mode != 2) {
+        if (n0) c0 = 0x7fu;
+        if (n1) c1 = 0x7fu;
+        mb |= (uint32_t)(fabsf(x0) <= p.lim) << e;
+        mb |= (uint32_t)(fabsf(x1) <= p.lim) << (e + 1);
+      }
+      if (CODES) {
+        cv.set2(e, (FULL || e < cnt) ? (int)(int8_t)c0 : 0,
+                (FULL || e + 1 < cnt) ? (int)(int8_t)c1 : 0);
+      }
+      if (T::BYTES == 4) {
+        out.w[e] = (p.mode != 2 && n0) ? kNaN32 : __float_as_uint(y0);
+        out.w[e + 1] = (p.mode != 2 && n1) ? kNaN32 : __float_as_uint(y1);
+      } else {
+        uint32_t w = pack_bf16x2(y0, y1);
+        if (p.mode != 2) {
+          if (n0) w = (w & 0xffff0000u) | kNaN16;
+          if (n1) w = (w & 0x0000ffffu) | (kNaN16 << 16);
+        }
+        out.w[e >> 1] = w;
+      }
+    }
+  }
+}
+
+template <typename T, int FMT, bool CODES, bool FULL, bool SR>
 __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, int64_t tile,
                                          V32 (&v)[kTile / (32 * T::VEC)], bool have, int64_t next,
-                                         const Fp8Params& p, void* __restrict__ y,
-                                         uint8_t* __restrict__ codes, uint32_t* __restrict__ mask,
-                                         int lane) {
+                                         const Fp8Params& p, const SrCtx& sr,
+                                         void* __restrict__ y, uint8_t* __restrict__ codes,
+                                         uint32_t* __restrict__ mask, int lane) {
   constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
   const int64_t tb = tile * kTile;
   int cnt[SLOTS];
@@ -133,7 +221,10 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
     CodeVec<8, VEC> cv;
     uint32_t mb = 0u;
     bool done = false;
-    if constexpr (T::BYTES == 2) {
+    if constexpr (SR) {
+      fp8_vec_sr<T, FMT, CODES, FULL>(v[j], p, sr, base, cnt[j], out, cv, mb);
+      done = true;
+    } else if constexpr (T::BYTES == 2) {
       if (p.fast) done = fp8_vec_bf16_fast<FMT, CODES>(v[j], p, out, cv, mb);
     }
     if (!done) {
@@ -204,11 +295,12 @@ __device__ __forceinline__ void fp8_tile(const void* __restrict__ x, int64_t n, 
   }
 }
 
-template <typename T, int FMT, bool GIVEN, bool CODES>
+template <typename T, int FMT, bool GIVEN, bool CODES, bool SR>
 __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, int64_t n,
                                                     const uint4* __restrict__ part, int nparts,
-                                                    float* scale, void* y, uint8_t* codes,
-                                                    uint32_t* mask, int32_t* flags) {
+                                                    float* scale, SrCtx sr, void* y,
+                                                    uint8_t* codes, uint32_t* mask,
+                                                    int32_t* flags) {
   constexpr float kMax = FMT == QAT_E4M3 ? 448.0f : 57344.0f;
   __shared__ __align__(16) uint32_t red[4 * 8];
   __shared__ Fp8Params sp;
@@ -252,21 +344,26 @@ __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, 
     // than the overlap gains for this arithmetic-heavy map
     const int64_t next = -1;
     (void)ntile;
-    if (tile < nfull) fp8_tile<T, FMT, CODES, true>(x, n, tile, v, have, next, p, y, codes, mask, lane);
-    else fp8_tile<T, FMT, CODES, false>(x, n, tile, v, have, next, p, y, codes, mask, lane);
+    if (tile < nfull)
+      fp8_tile<T, FMT, CODES, true, SR>(x, n, tile, v, have, next, p, sr, y, codes, mask, lane);
+    else
+      fp8_tile<T, FMT, CODES, false, SR>(x, n, tile, v, have, next, p, sr, y, codes, mask, lane);
     have = next >= 0;
   }
 }
 
 template <typename T, int FMT>
 static void fp8_t(bool given, const void* x, int64_t n, const void* ws, int nparts, float* scale,
-                  void* y, uint8_t* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
+                  const SrCtx& sr, void* y, uint8_t* codes, uint32_t* mask, int32_t* flags,
+                  cudaStream_t s) {
   const int64_t ntiles = (n + kTile - 1) / kTile;
   int64_t g = (ntiles + 7) / 8;
   int64_t cap = (int64_t)device_info().sms * 8;
   int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
   const uint4* part = static_cast<const uint4*>(ws);
-#define QAT_K(G, C) k_fp8_tensor<T, FMT, G, C><<<grid, 256, 0, s>>>(x, n, part, nparts, scale, y, codes, mask, flags)
+#define QAT_K(G, C)                                                                              \
+  k_fp8_tensor<T, FMT, G, C, QAT_SR><<<grid, 256, 0, s>>>(x, n, part, nparts, scale, sr, y, codes, \
+                                                          mask, flags)
   if (given) {
     if (codes) QAT_K(true, true); else QAT_K(true, false);
   } else {
@@ -275,16 +372,16 @@ static void fp8_t(bool given, const void* x, int64_t n, const void* ws, int npar
 #undef QAT_K
 }
 
-qat_status launch_fp8_tensor(qat_dtype dt, qat_fp8_format fmt, bool given, const void* x, int64_t n,
-                             const void* ws, int nparts, float* scale, void* y, uint8_t* codes,
-                             uint32_t* mask, int32_t* flags, cudaStream_t s) {
+QAT_DECL_FP8_TENSOR(QAT_SR_NAME(launch_fp8_tensor)) {
+#define QAT_F8(T, F) fp8_t<T, F>(given, x, n, ws, nparts, scale, sr, y, codes, mask, flags, s)
   if (dt == QAT_F32) {
-    if (fmt == QAT_E4M3) fp8_t<F32, QAT_E4M3>(given, x, n, ws, nparts, scale, y, codes, mask, flags, s);
-    else fp8_t<F32, QAT_E5M2>(given, x, n, ws, nparts, scale, y, codes, mask, flags, s);
+    if (fmt == QAT_E4M3) QAT_F8(F32, QAT_E4M3);
+    else QAT_F8(F32, QAT_E5M2);
   } else {
-    if (fmt == QAT_E4M3) fp8_t<BF16, QAT_E4M3>(given, x, n, ws, nparts, scale, y, codes, mask, flags, s);
-    else fp8_t<BF16, QAT_E5M2>(given, x, n, ws, nparts, scale, y, codes, mask, flags, s);
+    if (fmt == QAT_E4M3) QAT_F8(BF16, QAT_E4M3);
+    else QAT_F8(BF16, QAT_E5M2);
   }
+#undef QAT_F8
   count_launch(1);
   return launch_status();
 }

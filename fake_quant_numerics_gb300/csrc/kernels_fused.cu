@@ -20,13 +20,13 @@
 
 namespace qat {
 
-template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY, bool FULL>
+template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY, bool FULL, bool SR>
 __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n, int64_t tile,
                                            V32 (&v)[kTile / (32 * T::VEC)], bool have,
                                            int64_t next, float* scale, int32_t* zp, float* absmax,
-                                           float* minv, float* maxv, void* __restrict__ y,
-                                           void* __restrict__ codes, uint32_t* __restrict__ mask,
-                                           int lane, int& fl) {
+                                           float* minv, float* maxv, const SrCtx& sr,
+                                           void* __restrict__ y, void* __restrict__ codes,
+                                           uint32_t* __restrict__ mask, int lane, int& fl) {
   constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
   constexpr int L = VEC * LPG;
   constexpr int MM = STATS_ONLY ? kMMKeys : (AFFINE ? kMMFloat : kMMNone);
@@ -89,7 +89,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
       OutVec<T> ov;
       CodeVec<BITS, VEC> cv;
       uint32_t mb;
-      int_map_vec<T, BITS, AFFINE>(v[j], p, ov, cv, mb);
+      int_map_vec<T, BITS, AFFINE, SR>(v[j], p, ov, cv, mb, sr, base);
       slot_prefetch<T>(x, next, j, v[j], lane);
       if (!present[j]) mb = 0u;
       if (present[j]) {
@@ -131,7 +131,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
       OutVec<T> ov;
       CodeVec<BITS, VEC> cv;
       uint32_t mb;
-      int_map_vec<T, BITS, AFFINE>(v[j], p, ov, cv, mb);
+      int_map_vec<T, BITS, AFFINE, SR>(v[j], p, ov, cv, mb, sr, base);
       slot_prefetch<T>(x, next, j, v[j], lane);
       if (!present[j]) mb = 0u;
       if (present[j]) {
@@ -148,10 +148,11 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
   }
 }
 
-template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY>
-__global__ void __maxnreg__(T::BYTES == 4 ? 96 : 80) k_int_groups(const void* __restrict__ x, int64_t n, float* scale,
-                                             int32_t* zp, float* absmax, float* minv, float* maxv,
-                                             void* y, void* codes, uint32_t* mask, int32_t* flags) {
+template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY, bool SR>
+__global__ void __maxnreg__(SR ? 128 : (T::BYTES == 4 ? 96 : 80))
+    k_int_groups(const void* __restrict__ x, int64_t n, float* scale, int32_t* zp, float* absmax,
+                 float* minv, float* maxv, SrCtx sr, void* y, void* codes, uint32_t* mask,
+                 int32_t* flags) {
   const int lane = threadIdx.x & 31;
   const int64_t ntiles = (n + kTile - 1) / kTile;
   const int64_t nfull = n / kTile;
@@ -162,14 +163,17 @@ __global__ void __maxnreg__(T::BYTES == 4 ? 96 : 80) k_int_groups(const void* __
   for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
        t += wstride) {
     const int64_t nt = t + wstride;
-    const int64_t next = nt < nfull ? nt : -1;  // rolling prefetch of the next full tile
+    // rolling prefetch of the next full tile (not with stochastic rounding,
+    // whose draws need the registers)
+    const int64_t next = (!SR && nt < nfull) ? nt : -1;
     if (t < nfull)
-      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, true>(x, n, t, v, have, next, scale, zp, absmax,
-                                                         minv, maxv, y, codes, mask, lane, fl);
+      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, true, SR>(x, n, t, v, have, next, scale, zp,
+                                                             absmax, minv, maxv, sr, y, codes, mask,
+                                                             lane, fl);
     else
-      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, false>(x, n, t, v, have, next, scale, zp,
-                                                          absmax, minv, maxv, y, codes, mask, lane,
-                                                          fl);
+      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, false, SR>(x, n, t, v, have, next, scale, zp,
+                                                              absmax, minv, maxv, sr, y, codes,
+                                                              mask, lane, fl);
     have = next >= 0;
   }
   warp_flag_or(flags, fl);
@@ -178,11 +182,11 @@ __global__ void __maxnreg__(T::BYTES == 4 ? 96 : 80) k_int_groups(const void* __
 // ---------------------------------------------------------------------------
 // one thread block (256 threads) per unit of L elements, NV vectors / thread
 // ---------------------------------------------------------------------------
-template <typename T, int BITS, bool AFFINE, int NV, bool STATS_ONLY>
-__global__ void __launch_bounds__(256, NV <= 2 ? 3 : 1) k_int_rows(const void* __restrict__ x, int64_t units,
-                                                  int64_t L, float* scale, int32_t* zp,
-                                                  float* absmax, float* minv, float* maxv, void* y,
-                                                  void* codes, uint32_t* mask, int32_t* flags) {
+template <typename T, int BITS, bool AFFINE, int NV, bool STATS_ONLY, bool SR>
+__global__ void __launch_bounds__(256, NV <= 2 ? 3 : 1)
+    k_int_rows(const void* __restrict__ x, int64_t units, int64_t L, float* scale, int32_t* zp,
+               float* absmax, float* minv, float* maxv, SrCtx sr, void* y, void* codes,
+               uint32_t* mask, int32_t* flags) {
   constexpr int VEC = T::VEC, NT = 256;
   constexpr int LPW = 32 / VEC;
   constexpr int MM = STATS_ONLY ? kMMKeys : (AFFINE ? kMMFloat : kMMNone);
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(256, NV <= 2 ? 3 : 1) k_int_rows(const void* _
       OutVec<T> ov;
       CodeVec<BITS, VEC> cv;
       uint32_t mb;
-      int_map_vec<T, BITS, AFFINE>(v[j], p, ov, cv, mb);
+      int_map_vec<T, BITS, AFFINE, SR>(v[j], p, ov, cv, mb, sr, base);
       if (present) {
         if (y) st_v32(static_cast<char*>(y) + base * T::BYTES, ov.v);
         if (codes) cv.store(codes, base, VEC);
@@ -296,18 +300,22 @@ static int nv_of(qat_dtype dt, int64_t L) {
   return 0;
 }
 
+#if !QAT_SR
 bool fused_units_supported(qat_dtype dt, int64_t L) { return lpg_of(dt, L) || nv_of(dt, L); }
+#endif
 
 template <typename T, int BITS, bool AFFINE, bool SO>
 static qat_status groups_t(int lpg, const void* x, int64_t n, float* scale, int32_t* zp,
-                           float* absmax, float* minv, float* maxv, void* y, void* codes,
-                           uint32_t* mask, int32_t* flags, cudaStream_t s) {
+                           float* absmax, float* minv, float* maxv, const SrCtx& sr, void* y,
+                           void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
   const int64_t ntiles = (n + kTile - 1) / kTile;
   int64_t g = (ntiles + 7) / 8;
   int64_t cap = (int64_t)device_info().sms * 8;
   int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
-#define QAT_G(LP) \
-  k_int_groups<T, BITS, AFFINE, LP, SO><<<grid, 256, 0, s>>>(x, n, scale, zp, absmax, minv, maxv, y, codes, mask, flags)
+#define QAT_G(LP)                                                                         \
+  k_int_groups<T, BITS, AFFINE, LP, SO, QAT_SR><<<grid, 256, 0, s>>>(x, n, scale, zp, absmax, \
+                                                                     minv, maxv, sr, y, codes, \
+                                                                     mask, flags)
   switch (lpg) {
     case 2: QAT_G(2); break;
     case 4: QAT_G(4); break;
@@ -321,12 +329,14 @@ static qat_status groups_t(int lpg, const void* x, int64_t n, float* scale, int3
 
 template <typename T, int BITS, bool AFFINE, bool SO>
 static void rows_t(int nv, const void* x, int64_t units, int64_t L, float* scale, int32_t* zp,
-                   float* absmax, float* minv, float* maxv, void* y, void* codes, uint32_t* mask,
-                   int32_t* flags, cudaStream_t s) {
+                   float* absmax, float* minv, float* maxv, const SrCtx& sr, void* y, void* codes,
+                   uint32_t* mask, int32_t* flags, cudaStream_t s) {
   int64_t cap = (int64_t)device_info().sms * 8;
   int grid = (int)(units > cap ? cap : (units < 1 ? 1 : units));
-#define QAT_R(NV) \
-  k_int_rows<T, BITS, AFFINE, NV, SO><<<grid, 256, 0, s>>>(x, units, L, scale, zp, absmax, minv, maxv, y, codes, mask, flags)
+#define QAT_R(NV)                                                                         \
+  k_int_rows<T, BITS, AFFINE, NV, SO, QAT_SR><<<grid, 256, 0, s>>>(x, units, L, scale, zp,     \
+                                                                   absmax, minv, maxv, sr, y,  \
+                                                                   codes, mask, flags)
   switch (nv) {
     case 1: QAT_R(1); break;
     case 2: QAT_R(2); break;
@@ -338,29 +348,30 @@ static void rows_t(int nv, const void* x, int64_t units, int64_t L, float* scale
 
 template <typename T, int BITS, bool AFFINE, bool SO>
 static qat_status fused_t(const void* x, int64_t units, int64_t L, float* scale, int32_t* zp,
-                          float* absmax, float* minv, float* maxv, void* y, void* codes,
-                          uint32_t* mask, int32_t* flags, cudaStream_t s) {
+                          float* absmax, float* minv, float* maxv, const SrCtx& sr, void* y,
+                          void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
   const qat_dtype dt = T::kDtype;
   int lpg = lpg_of(dt, L);
   if (lpg)
-    return groups_t<T, BITS, AFFINE, SO>(lpg, x, units * L, scale, zp, absmax, minv, maxv, y,
+    return groups_t<T, BITS, AFFINE, SO>(lpg, x, units * L, scale, zp, absmax, minv, maxv, sr, y,
                                          codes, mask, flags, s);
-  rows_t<T, BITS, AFFINE, SO>(nv_of(dt, L), x, units, L, scale, zp, absmax, minv, maxv, y, codes,
-                              mask, flags, s);
+  rows_t<T, BITS, AFFINE, SO>(nv_of(dt, L), x, units, L, scale, zp, absmax, minv, maxv, sr, y,
+                              codes, mask, flags, s);
   return launch_status();
 }
 
-qat_status launch_int_fused(qat_dtype dt, int bits, bool affine, bool stats_only, const void* x,
-                            int64_t units, int64_t L, float* scale, int32_t* zp, float* absmax,
-                            float* minv, float* maxv, void* y, void* codes, uint32_t* mask,
-                            int32_t* flags, cudaStream_t s) {
-  if (!fused_units_supported(dt, L)) return QAT_ERR_UNSUPPORTED;
+QAT_DECL_INT_FUSED(QAT_SR_NAME(launch_int_fused)) {
+  if (!(lpg_of(dt, L) || nv_of(dt, L))) return QAT_ERR_UNSUPPORTED;
   qat_status st;
 #define QAT_F(T, B, A, SO) \
-  st = fused_t<T, B, A, SO>(x, units, L, scale, zp, absmax, minv, maxv, y, codes, mask, flags, s)
+  st = fused_t<T, B, A, SO>(x, units, L, scale, zp, absmax, minv, maxv, sr, y, codes, mask, flags, s)
   if (stats_only) {
+#if QAT_SR
+    return QAT_ERR_UNSUPPORTED;
+#else
     if (dt == QAT_F32) QAT_F(F32, 8, false, true);
     else QAT_F(BF16, 8, false, true);
+#endif
   } else if (dt == QAT_F32) {
     if (bits == 8) { if (affine) QAT_F(F32, 8, true, false); else QAT_F(F32, 8, false, false); }
     else { if (affine) QAT_F(F32, 4, true, false); else QAT_F(F32, 4, false, false); }

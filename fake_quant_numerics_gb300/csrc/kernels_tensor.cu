@@ -16,6 +16,7 @@
 
 namespace qat {
 
+#if !QAT_SR
 // ---------------------------------------------------------------------------
 // per-tensor statistics: one uint4 partial (Stats::pack) per block
 // ---------------------------------------------------------------------------
@@ -77,15 +78,17 @@ __global__ void __launch_bounds__(256) k_stats_finalize(const uint4* __restrict_
   }
 }
 
+#endif  // !QAT_SR
+
 // ---------------------------------------------------------------------------
 // integer fake quant, one parameter set (calibrated from partials or given)
 // ---------------------------------------------------------------------------
-template <typename T, int BITS, bool AFFINE, bool GIVEN, bool FULL>
+template <typename T, int BITS, bool AFFINE, bool GIVEN, bool FULL, bool SR>
 __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, int64_t tile,
                                          V32 (&v)[kTile / (32 * T::VEC)], bool have, int64_t next,
-                                         const IntParams& p, void* __restrict__ y,
-                                         void* __restrict__ codes, uint32_t* __restrict__ mask,
-                                         int lane) {
+                                         const IntParams& p, const SrCtx& sr,
+                                         void* __restrict__ y, void* __restrict__ codes,
+                                         uint32_t* __restrict__ mask, int lane) {
   constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
   const int64_t tb = tile * kTile;
   int cnt[SLOTS];
@@ -99,17 +102,29 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
     cv.clear();
     uint32_t mb = 0u;
     if (!GIVEN && p.fast) {
-      int_vec_cal<T, BITS, AFFINE, FULL>(v[j], p, cnt[j], ov, cv, mb);
+      if (SR)
+        int_vec_cal_sr<T, BITS, AFFINE, FULL>(v[j], p, cnt[j], sr, base, ov, cv, mb);
+      else
+        int_vec_cal<T, BITS, AFFINE, FULL>(v[j], p, cnt[j], ov, cv, mb);
     } else if (!p.dead) {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        int q;
-        float yv;
-        uint32_t m;
-        int_elem<GIVEN>(elem<T>(v[j], e), p, q, yv, m);
-        ov.set(e, yv);
-        if (FULL || e < cnt[j]) cv.set(e, q);
-        mb |= m << e;
+      for (int g = 0; g < VEC / 4; ++g) {
+        float u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (SR) sr_draws4(sr, base / 4 + g, u);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int e = 4 * g + c;
+          int q;
+          float yv;
+          uint32_t m;
+          if (SR)
+            int_elem_sr<GIVEN>(elem<T>(v[j], e), u[c], p, q, yv, m);
+          else
+            int_elem<GIVEN>(elem<T>(v[j], e), p, q, yv, m);
+          ov.set(e, yv);
+          if (FULL || e < cnt[j]) cv.set(e, q);
+          mb |= m << e;
+        }
       }
     } else {
 #pragma unroll
@@ -130,11 +145,11 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
   }
 }
 
-template <typename T, int BITS, bool AFFINE, bool GIVEN>
-__global__ void __maxnreg__(80) k_int_tensor(const void* __restrict__ x, int64_t n,
+template <typename T, int BITS, bool AFFINE, bool GIVEN, bool SR>
+__global__ void __maxnreg__(SR ? 128 : 80) k_int_tensor(const void* __restrict__ x, int64_t n,
                                                     const uint4* __restrict__ part, int nparts,
-                                                    float* scale, int32_t* zp, void* y, void* codes,
-                                                    uint32_t* mask, int32_t* flags) {
+                                                    float* scale, int32_t* zp, SrCtx sr, void* y,
+                                                    void* codes, uint32_t* mask, int32_t* flags) {
   __shared__ __align__(16) uint32_t red[4 * 8];
   __shared__ IntParams sp;
   if (GIVEN) {
@@ -171,9 +186,11 @@ __global__ void __maxnreg__(80) k_int_tensor(const void* __restrict__ x, int64_t
     const int64_t ntile = GIVEN ? nt : ntiles - 1 - nt;
     const int64_t next = (nt < ntiles && ntile < nfull) ? ntile : -1;
     if (tile < nfull)
-      int_tile<T, BITS, AFFINE, GIVEN, true>(x, n, tile, v, have, next, p, y, codes, mask, lane);
+      int_tile<T, BITS, AFFINE, GIVEN, true, SR>(x, n, tile, v, have, next, p, sr, y, codes, mask,
+                                                 lane);
     else
-      int_tile<T, BITS, AFFINE, GIVEN, false>(x, n, tile, v, have, next, p, y, codes, mask, lane);
+      int_tile<T, BITS, AFFINE, GIVEN, false, SR>(x, n, tile, v, have, next, p, sr, y, codes, mask,
+                                                  lane);
     have = next >= 0;
   }
 }
@@ -183,12 +200,13 @@ __global__ void __maxnreg__(80) k_int_tensor(const void* __restrict__ x, int64_t
 // (given per-row / per-group parameters, and the calibrated fallback for unit
 // lengths the fused kernels do not cover)
 // ---------------------------------------------------------------------------
-template <typename T, int BITS, bool AFFINE, bool GIVEN>
-__global__ void __maxnreg__(80) k_int_units(const void* __restrict__ x, int64_t n, int64_t L,
+template <typename T, int BITS, bool AFFINE, bool GIVEN, bool SR>
+__global__ void __maxnreg__(SR ? 128 : 80) k_int_units(const void* __restrict__ x, int64_t n, int64_t L,
                                                    const float* __restrict__ scale,
                                                    const int32_t* __restrict__ zp,
-                                                   const uint8_t* __restrict__ dead, void* y,
-                                                   void* codes, uint32_t* mask, int32_t* flags) {
+                                                   const uint8_t* __restrict__ dead, SrCtx sr,
+                                                   void* y, void* codes, uint32_t* mask,
+                                                   int32_t* flags) {
   constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
   constexpr int qmin = QRange<BITS, AFFINE>::qmin, qmax = QRange<BITS, AFFINE>::qmax;
   const int lane = threadIdx.x & 31;
@@ -215,6 +233,14 @@ __global__ void __maxnreg__(80) k_int_units(const void* __restrict__ x, int64_t 
       p.zp = 0;
       p.dead = 1;
       finish_params(p, qmin, qmax);
+      float ud[VEC];  // stochastic-rounding draws of the vector's elements
+#pragma unroll
+      for (int g = 0; g < VEC / 4; ++g) {
+        float w[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (SR) sr_draws4(sr, base / 4 + g, w);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ud[4 * g + c] = w[c];
+      }
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         int q = 0;
@@ -233,7 +259,12 @@ __global__ void __maxnreg__(80) k_int_units(const void* __restrict__ x, int64_t 
               finish_params(p, qmin, qmax);
             }
           }
-          if (!p.dead) int_elem<GIVEN>(elem<T>(v, e), p, q, yv, m);
+          if (!p.dead) {
+            if (SR)
+              int_elem_sr<GIVEN>(elem<T>(v, e), ud[e], p, q, yv, m);
+            else
+              int_elem<GIVEN>(elem<T>(v, e), p, q, yv, m);
+          }
         }
         ov.set(e, yv);
         cv.set(e, q);
@@ -254,6 +285,7 @@ __global__ void __maxnreg__(80) k_int_units(const void* __restrict__ x, int64_t 
   }
 }
 
+#if !QAT_SR
 // ---------------------------------------------------------------------------
 // warp-per-unit statistics for any unit length (scalar loads)
 //   MODE 0: absmax / minv / maxv per unit, QAT_FLAG_NONFINITE_INPUT
@@ -291,9 +323,12 @@ __global__ void __launch_bounds__(256) k_unit_generic(const void* __restrict__ x
   }
 }
 
+#endif  // !QAT_SR
+
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
+#if !QAT_SR
 int stats_grid(int64_t n) {
   const int64_t ntiles = (n + kTile - 1) / kTile;
   const int64_t warps_per_block = 16;  // 512 threads
@@ -304,6 +339,8 @@ int stats_grid(int64_t n) {
   return (int)(g < 1 ? 1 : g);
 }
 
+#endif  // !QAT_SR
+
 static int map_grid(int64_t n, int per_sm) {
   const int64_t ntiles = (n + kTile - 1) / kTile;
   int64_t g = (ntiles + 7) / 8;  // 8 warps per 256-thread block
@@ -312,6 +349,7 @@ static int map_grid(int64_t n, int per_sm) {
   return (int)(g < 1 ? 1 : g);
 }
 
+#if !QAT_SR
 qat_status launch_stats_tensor(qat_dtype dt, const void* x, int64_t n, int mm, void* ws,
                                int grid, cudaStream_t s) {
   uint4* part = static_cast<uint4*>(ws);
@@ -338,24 +376,28 @@ qat_status launch_stats_finalize(const void* ws, int nparts, float* absmax, floa
   return launch_status();
 }
 
+#endif  // !QAT_SR
+
 template <typename T, int BITS, bool AFFINE>
 static void int_tensor_t(bool given, const void* x, int64_t n, const void* ws, int nparts,
-                         float* scale, int32_t* zp, void* y, void* codes, uint32_t* mask,
-                         int32_t* flags, cudaStream_t s) {
+                         float* scale, int32_t* zp, const SrCtx& sr, void* y, void* codes,
+                         uint32_t* mask, int32_t* flags, cudaStream_t s) {
   const int grid = map_grid(n, 8);
   const uint4* part = static_cast<const uint4*>(ws);
   if (given)
-    k_int_tensor<T, BITS, AFFINE, true>
-        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, y, codes, mask, flags);
+    k_int_tensor<T, BITS, AFFINE, true, QAT_SR>
+        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, y, codes, mask, flags);
   else
-    k_int_tensor<T, BITS, AFFINE, false>
-        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, y, codes, mask, flags);
+    k_int_tensor<T, BITS, AFFINE, false, QAT_SR>
+        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, y, codes, mask, flags);
 }
 
-qat_status launch_int_tensor(qat_dtype dt, int bits, bool affine, bool given, const void* x,
-                             int64_t n, const void* ws, int nparts, float* scale, int32_t* zp,
-                             void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
-#define QAT_IT(T, B, A) int_tensor_t<T, B, A>(given, x, n, ws, nparts, scale, zp, y, codes, mask, flags, s)
+qat_status QAT_SR_NAME(launch_int_tensor)(qat_dtype dt, int bits, bool affine, bool given,
+                                          const void* x, int64_t n, const void* ws, int nparts,
+                                          float* scale, int32_t* zp, const SrCtx& sr, void* y,
+                                          void* codes, uint32_t* mask, int32_t* flags,
+                                          cudaStream_t s) {
+#define QAT_IT(T, B, A) int_tensor_t<T, B, A>(given, x, n, ws, nparts, scale, zp, sr, y, codes, mask, flags, s)
   if (dt == QAT_F32) {
     if (bits == 8) { if (affine) QAT_IT(F32, 8, true); else QAT_IT(F32, 8, false); }
     else { if (affine) QAT_IT(F32, 4, true); else QAT_IT(F32, 4, false); }
@@ -370,22 +412,23 @@ qat_status launch_int_tensor(qat_dtype dt, int bits, bool affine, bool given, co
 
 template <typename T, int BITS, bool AFFINE>
 static void int_units_t(bool given, const void* x, int64_t n, int64_t L, const float* scale,
-                        const int32_t* zp, const uint8_t* dead, void* y, void* codes, uint32_t* mask,
-                        int32_t* flags, cudaStream_t s) {
+                        const int32_t* zp, const uint8_t* dead, const SrCtx& sr, void* y,
+                        void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
   const int grid = map_grid(n, 8);
   if (given)
-    k_int_units<T, BITS, AFFINE, true>
-        <<<grid, 256, 0, s>>>(x, n, L, scale, zp, dead, y, codes, mask, flags);
+    k_int_units<T, BITS, AFFINE, true, QAT_SR>
+        <<<grid, 256, 0, s>>>(x, n, L, scale, zp, dead, sr, y, codes, mask, flags);
   else
-    k_int_units<T, BITS, AFFINE, false>
-        <<<grid, 256, 0, s>>>(x, n, L, scale, zp, dead, y, codes, mask, flags);
+    k_int_units<T, BITS, AFFINE, false, QAT_SR>
+        <<<grid, 256, 0, s>>>(x, n, L, scale, zp, dead, sr, y, codes, mask, flags);
 }
 
-qat_status launch_int_units(qat_dtype dt, int bits, bool affine, bool given, const void* x,
-                            int64_t n, int64_t L, const float* scale, const int32_t* zp,
-                            const uint8_t* dead, void* y, void* codes, uint32_t* mask,
-                            int32_t* flags, cudaStream_t s) {
-#define QAT_IU(T, B, A) int_units_t<T, B, A>(given, x, n, L, scale, zp, dead, y, codes, mask, flags, s)
+qat_status QAT_SR_NAME(launch_int_units)(qat_dtype dt, int bits, bool affine, bool given,
+                                         const void* x, int64_t n, int64_t L, const float* scale,
+                                         const int32_t* zp, const uint8_t* dead, const SrCtx& sr,
+                                         void* y, void* codes, uint32_t* mask, int32_t* flags,
+                                         cudaStream_t s) {
+#define QAT_IU(T, B, A) int_units_t<T, B, A>(given, x, n, L, scale, zp, dead, sr, y, codes, mask, flags, s)
   if (dt == QAT_F32) {
     if (bits == 8) { if (affine) QAT_IU(F32, 8, true); else QAT_IU(F32, 8, false); }
     else { if (affine) QAT_IU(F32, 4, true); else QAT_IU(F32, 4, false); }
@@ -398,6 +441,7 @@ qat_status launch_int_units(qat_dtype dt, int bits, bool affine, bool given, con
   return launch_status();
 }
 
+#if !QAT_SR
 template <typename T>
 static void unit_generic_t(int mode, int bits, bool affine, const void* x, int64_t units, int64_t L,
                            float* absmax, float* minv, float* maxv, float* scale, int32_t* zp,
@@ -424,5 +468,7 @@ qat_status launch_unit_generic(qat_dtype dt, int mode, int bits, bool affine, co
   count_launch(1);
   return launch_status();
 }
+
+#endif  // !QAT_SR
 
 }  // namespace qat

@@ -131,15 +131,19 @@ qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t 
   }
   if (fused_units_supported(dtype, L))
     return launch_int_fused(dtype, 8, false, true, x, units, L, nullptr, nullptr, absmax, minv, maxv,
-                            nullptr, nullptr, nullptr, flags, s);
+                            SrCtx{}, nullptr, nullptr, nullptr, flags, s);
   return launch_unit_generic(dtype, 0, 8, false, x, units, L, absmax, minv, maxv, nullptr, nullptr,
                              nullptr, flags, s);
 }
 
-qat_status qat_fake_quant_int(const void* x, qat_dtype dtype, int64_t rows, int64_t cols, int bits,
-                              qat_scheme scheme, qat_granularity g, int64_t group, int params_given,
-                              float* scale, int32_t* zp, void* y, void* codes, uint32_t* mask,
-                              int32_t* flags, void* ws, size_t ws_bytes, qat_stream_t stream) {
+// The integer and FP8 entry points share one body; sr == nullptr rounds to
+// nearest, otherwise stochastically with the call's draws.
+static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t rows, int64_t cols,
+                                      int bits, qat_scheme scheme, qat_granularity g,
+                                      int64_t group, int params_given, float* scale, int32_t* zp,
+                                      const SrCtx* sr, void* y, void* codes, uint32_t* mask,
+                                      int32_t* flags, void* ws, size_t ws_bytes,
+                                      qat_stream_t stream) {
   if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
   if (bits != 8 && bits != 4) return QAT_ERR_UNSUPPORTED;
   if (scheme != QAT_SYMMETRIC && scheme != QAT_AFFINE) return QAT_ERR_UNSUPPORTED;
@@ -155,24 +159,28 @@ qat_status qat_fake_quant_int(const void* x, qat_dtype dtype, int64_t rows, int6
       !aligned(scale, 4) || (zp && !aligned(zp, 4)))
     return QAT_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const SrCtx c = sr ? *sr : SrCtx{};
+  auto map_tensor = sr ? launch_int_tensor_sr : launch_int_tensor;
+  auto map_units = sr ? launch_int_units_sr : launch_int_units;
+  auto map_fused = sr ? launch_int_fused_sr : launch_int_fused;
   if (g == QAT_PER_TENSOR) {
     if (params_given)
-      return launch_int_tensor(dtype, bits, affine, true, x, n, nullptr, 0, scale, zp, y, codes,
-                               mask, flags, s);
+      return map_tensor(dtype, bits, affine, true, x, n, nullptr, 0, scale, zp, c, y, codes, mask,
+                        flags, s);
     if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
     if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
     int grid = stats_grid(n);
     qat_status st = launch_stats_tensor(dtype, x, n, affine ? kMMFloat : kMMNone, ws, grid, s);
     if (st) return st;
-    return launch_int_tensor(dtype, bits, affine, false, x, n, ws, grid, scale, zp, y, codes, mask,
-                             flags, s);
+    return map_tensor(dtype, bits, affine, false, x, n, ws, grid, scale, zp, c, y, codes, mask,
+                      flags, s);
   }
   if (params_given)
-    return launch_int_units(dtype, bits, affine, true, x, n, L, scale, zp, nullptr, y, codes, mask,
-                            flags, s);
+    return map_units(dtype, bits, affine, true, x, n, L, scale, zp, nullptr, c, y, codes, mask,
+                     flags, s);
   if (fused_units_supported(dtype, L))
-    return launch_int_fused(dtype, bits, affine, false, x, units, L, scale, zp, nullptr, nullptr,
-                            nullptr, y, codes, mask, flags, s);
+    return map_fused(dtype, bits, affine, false, x, units, L, scale, zp, nullptr, nullptr, nullptr,
+                     c, y, codes, mask, flags, s);
   // fallback: calibrate every unit (warp per unit), then the flat map
   if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
   if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
@@ -180,14 +188,41 @@ qat_status qat_fake_quant_int(const void* x, qat_dtype dtype, int64_t rows, int6
   qat_status st = launch_unit_generic(dtype, 1, bits, affine, x, units, L, nullptr, nullptr, nullptr,
                                       scale, zp, dead, flags, s);
   if (st) return st;
-  return launch_int_units(dtype, bits, affine, false, x, n, L, scale, zp, dead, y, codes, mask,
-                          flags, s);
+  return map_units(dtype, bits, affine, false, x, n, L, scale, zp, dead, c, y, codes, mask, flags,
+                   s);
 }
 
-qat_status qat_fake_quant_fp8(const void* x, qat_dtype dtype, int64_t n, qat_fp8_format fmt,
-                              int scale_given, float* scale, void* y, uint8_t* codes,
-                              uint32_t* mask, int32_t* flags, void* ws, size_t ws_bytes,
-                              qat_stream_t stream) {
+qat_status qat_fake_quant_int(const void* x, qat_dtype dtype, int64_t rows, int64_t cols, int bits,
+                              qat_scheme scheme, qat_granularity g, int64_t group, int params_given,
+                              float* scale, int32_t* zp, void* y, void* codes, uint32_t* mask,
+                              int32_t* flags, void* ws, size_t ws_bytes, qat_stream_t stream) {
+  return fake_quant_int_impl(x, dtype, rows, cols, bits, scheme, g, group, params_given, scale, zp,
+                             nullptr, y, codes, mask, flags, ws, ws_bytes, stream);
+}
+
+static SrCtx sr_ctx(uint64_t seed, uint64_t offset) {
+  SrCtx c;
+  c.k0 = (uint32_t)seed;
+  c.k1 = (uint32_t)(seed >> 32);
+  c.offset = offset;
+  return c;
+}
+
+qat_status qat_fake_quant_int_sr(const void* x, qat_dtype dtype, int64_t rows, int64_t cols,
+                                 int bits, qat_scheme scheme, qat_granularity g, int64_t group,
+                                 int params_given, float* scale, int32_t* zp, uint64_t seed,
+                                 uint64_t offset, void* y, void* codes, uint32_t* mask,
+                                 int32_t* flags, void* ws, size_t ws_bytes, qat_stream_t stream) {
+  const SrCtx c = sr_ctx(seed, offset);
+  return fake_quant_int_impl(x, dtype, rows, cols, bits, scheme, g, group, params_given, scale, zp,
+                             &c, y, codes, mask, flags, ws, ws_bytes, stream);
+}
+
+static qat_status fake_quant_fp8_impl(const void* x, qat_dtype dtype, int64_t n,
+                                      qat_fp8_format fmt, int scale_given, float* scale,
+                                      const SrCtx* sr, void* y, uint8_t* codes, uint32_t* mask,
+                                      int32_t* flags, void* ws, size_t ws_bytes,
+                                      qat_stream_t stream) {
   if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
   if (fmt != QAT_E4M3 && fmt != QAT_E5M2) return QAT_ERR_UNSUPPORTED;
   if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;
@@ -197,14 +232,33 @@ qat_status qat_fake_quant_fp8(const void* x, qat_dtype dtype, int64_t n, qat_fp8
       (mask && !aligned(mask, kAlignBuf)) || !aligned(scale, 4))
     return QAT_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const SrCtx c = sr ? *sr : SrCtx{};
+  auto map = sr ? launch_fp8_tensor_sr : launch_fp8_tensor;
   if (scale_given)
-    return launch_fp8_tensor(dtype, fmt, true, x, n, nullptr, 0, scale, y, codes, mask, flags, s);
+    return map(dtype, fmt, true, x, n, nullptr, 0, scale, c, y, codes, mask, flags, s);
   if (!ws || ws_bytes < ws_bytes_for(1, n, QAT_PER_TENSOR, 0)) return QAT_ERR_WORKSPACE;
   if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
   int grid = stats_grid(n);
   qat_status st = launch_stats_tensor(dtype, x, n, kMMNone, ws, grid, s);
   if (st) return st;
-  return launch_fp8_tensor(dtype, fmt, false, x, n, ws, grid, scale, y, codes, mask, flags, s);
+  return map(dtype, fmt, false, x, n, ws, grid, scale, c, y, codes, mask, flags, s);
+}
+
+qat_status qat_fake_quant_fp8(const void* x, qat_dtype dtype, int64_t n, qat_fp8_format fmt,
+                              int scale_given, float* scale, void* y, uint8_t* codes,
+                              uint32_t* mask, int32_t* flags, void* ws, size_t ws_bytes,
+                              qat_stream_t stream) {
+  return fake_quant_fp8_impl(x, dtype, n, fmt, scale_given, scale, nullptr, y, codes, mask, flags,
+                             ws, ws_bytes, stream);
+}
+
+qat_status qat_fake_quant_fp8_sr(const void* x, qat_dtype dtype, int64_t n, qat_fp8_format fmt,
+                                 int scale_given, float* scale, uint64_t seed, uint64_t offset,
+                                 void* y, uint8_t* codes, uint32_t* mask, int32_t* flags,
+                                 void* ws, size_t ws_bytes, qat_stream_t stream) {
+  const SrCtx c = sr_ctx(seed, offset);
+  return fake_quant_fp8_impl(x, dtype, n, fmt, scale_given, scale, &c, y, codes, mask, flags, ws,
+                             ws_bytes, stream);
 }
 
 qat_status qat_ste_backward(const void* grad, qat_dtype dtype, int64_t n, const uint32_t* mask,

@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include "qat.h"
+#include "qat_sr.h"
 
 namespace qat {
 
@@ -740,26 +741,157 @@ __device__ __forceinline__ void int_vec_cal(const V32& v, const IntParams& p, in
   mb = ~out & (VEC == 32 ? 0xffffffffu : ((1u << VEC) - 1u));
 }
 
+// ---------------------------------------------------------------------------
+// stochastic rounding (optirs-gpu quantization.rs, RoundingMode::Stochastic:
+// floor(r) + 1 when the draw u < r - floor(r), floor(r) otherwise)
+//
+// The draw of element i of a call: word i % 4 of Philox-4x32-10 (J. Salmon,
+// M. Moraes, R. Dror, D. Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+// SC 2011) with key (low, high word of the seed) and counter (low, high word
+// of offset + i / 4, 0, 0); u = (w >> 9) * 2^-23.  r - floor(r) and u are
+// exact in binary32, so the decision is exact.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint64_t ctr, uint32_t k0, uint32_t k1) {
+  uint32_t x0 = (uint32_t)ctr, x1 = (uint32_t)(ctr >> 32), x2 = 0u, x3 = 0u;
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    // the Philox S-box: 32 x 32 -> 64-bit products by the two round
+    // multipliers, high halves mixed with the other words and the round key
+    const uint32_t hi0 = __umulhi(0xD2511F53u, x0), lo0 = 0xD2511F53u * x0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, x2), lo1 = 0xCD9E8D57u * x2;
+    const uint32_t n0 = hi1 ^ x1 ^ k0, n2 = hi0 ^ x3 ^ k1;
+    x0 = n0;
+    x1 = lo1;
+    x2 = n2;
+    x3 = lo0;
+    k0 += 0x9E3779B9u;  // Weyl key schedule
+    k1 += 0xBB67AE85u;
+  }
+  return make_uint4(x0, x1, x2, x3);
+}
+
+// draws of the four elements 4 g .. 4 g + 3 (g = element index / 4)
+__device__ __forceinline__ void sr_draws4(const SrCtx& sr, int64_t g, float (&u)[4]) {
+  const uint4 w = philox4x32_10(sr.offset + (uint64_t)g, sr.k0, sr.k1);
+  // (w >> 9) * 2^-23 exactly: 1 + (w >> 9) 2^-23 has those bits, minus 1
+  u[0] = __uint_as_float(0x3f800000u | (w.x >> 9)) - 1.0f;
+  u[1] = __uint_as_float(0x3f800000u | (w.y >> 9)) - 1.0f;
+  u[2] = __uint_as_float(0x3f800000u | (w.z >> 9)) - 1.0f;
+  u[3] = __uint_as_float(0x3f800000u | (w.w >> 9)) - 1.0f;
+}
+
+// the stochastic rounding of r with draw u (NaN stays NaN; for +-inf the
+// fraction is NaN, no increment, and r is returned)
+__device__ __forceinline__ float sr_round(float r, float u) {
+  const float lower = floorf(r);
+  const float frac = __fsub_rn(r, lower);  // exact
+  return (u < frac) ? __fadd_rn(lower, 1.0f) : lower;
+}
+
+// One vector of a calibrated unit with p.fast set, stochastic rounding: the
+// quotient is the exact RN(x/s) (quotient_rn2), k = sr_round(q, u) clamped to
+// the code range (a value just above qmax - zp can round up past it), y = k s,
+// the window as in int_vec_cal.  base: element index of element 0 (a
+// multiple of 4).
+template <typename T, int BITS, bool AFFINE, bool FULL>
+__device__ __forceinline__ void int_vec_cal_sr(const V32& v, const IntParams& p, int cnt,
+                                               const SrCtx& sr, int64_t base, OutVec<T>& ov,
+                                               CodeVec<BITS, T::VEC>& cv, uint32_t& mb) {
+  constexpr int VEC = T::VEC;
+  const float ns = -p.s;
+  const float wlo = p.wlo == 0.0f ? -0.0f : p.wlo;
+  cv.clear();
+  uint32_t out = 0u;
+#pragma unroll
+  for (int g = VEC / 4 - 1; g >= 0; --g) {
+    float u[4];
+    sr_draws4(sr, base / 4 + g, u);
+#pragma unroll
+    for (int h = 1; h >= 0; --h) {
+      const int e = 4 * g + 2 * h;
+      const float xa = elem<T>(v, e), xb = elem<T>(v, e + 1);
+      float qa, qb, ta, tb, ya, yb;
+      quotient_rn2(xa, xb, p.rcp, ns, qa, qb);
+      float fa = fminf(fmaxf(sr_round(qa, u[2 * h]), p.klof), p.khif);
+      float fb = fminf(fmaxf(sr_round(qb, u[2 * h + 1]), p.klof), p.khif);
+      add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
+      mul2(fa, fb, p.s, p.s, ya, yb);
+      ov.set2(e, ya, yb);
+      int qa_ = (int)(__float_as_uint(ta) - kRintMagicBits) + (AFFINE ? p.zp : 0);
+      int qb_ = (int)(__float_as_uint(tb) - kRintMagicBits) + (AFFINE ? p.zp : 0);
+      if (!FULL) {
+        if (e >= cnt) qa_ = 0;
+        if (e + 1 >= cnt) qb_ = 0;
+      }
+      cv.set2(e, qa_, qb_);
+      uint32_t oa, ob;
+      if (AFFINE) {
+        float ha, hb, la, lb;
+        sub2(p.whi, p.whi, xa, xb, ha, hb);
+        sub2(xa, xb, wlo, wlo, la, lb);
+        oa = __float_as_uint(ha) | __float_as_uint(la);
+        ob = __float_as_uint(hb) | __float_as_uint(lb);
+      } else {
+        oa = __float_as_uint(__fsub_rn(p.whi, fabsf(xa)));
+        ob = __float_as_uint(__fsub_rn(p.whi, fabsf(xb)));
+      }
+      out = __funnelshift_l(ob, out, 1);
+      out = __funnelshift_l(oa, out, 1);
+    }
+  }
+  mb = ~out & (VEC == 32 ? 0xffffffffu : ((1u << VEC) - 1u));
+}
+
+// One element with the IEEE quotient and stochastic rounding (given
+// parameters, or a calibrated scale outside the reciprocal's safe range):
+// k = clamp(sr_round(x / s, u)), a NaN quotient gives code 0 (NAN_TO_ZERO,
+// given parameters; a calibrated unit with a NaN is dead).
+template <bool NAN_TO_ZERO>
+__device__ __forceinline__ void int_elem_sr(float x, float u, const IntParams& p, int& q, float& y,
+                                            uint32_t& m) {
+  const float r = __fdiv_rn(x, p.s);
+  float kf = fminf(fmaxf(sr_round(r, u), p.klof), p.khif);  // fminf/fmaxf drop a NaN r
+  int k = (int)kf;
+  if (NAN_TO_ZERO && isnan(r)) k = -p.zp;
+  q = k + p.zp;
+  y = __fmul_rn(__int2float_rn(k), p.s);
+  m = (x >= p.wlo) && (x <= p.whi);
+}
+
 // Element map of one full vector with calibrated or given parameters: the
 // reciprocal path when p.fast, the IEEE path otherwise, zeros for a dead unit.
-template <typename T, int BITS, bool AFFINE>
+// SR: stochastic rounding with the draws of elements base .. base + VEC - 1.
+template <typename T, int BITS, bool AFFINE, bool SR = false>
 __device__ __forceinline__ void int_map_vec(const V32& v, const IntParams& p, OutVec<T>& ov,
-                                            CodeVec<BITS, T::VEC>& cv, uint32_t& mb) {
+                                            CodeVec<BITS, T::VEC>& cv, uint32_t& mb,
+                                            const SrCtx& sr = SrCtx{}, int64_t base = 0) {
   constexpr int VEC = T::VEC;
   cv.clear();
   mb = 0u;
   if (p.fast) {
-    int_vec_cal<T, BITS, AFFINE, true>(v, p, VEC, ov, cv, mb);
+    if (SR)
+      int_vec_cal_sr<T, BITS, AFFINE, true>(v, p, VEC, sr, base, ov, cv, mb);
+    else
+      int_vec_cal<T, BITS, AFFINE, true>(v, p, VEC, ov, cv, mb);
   } else if (!p.dead) {
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      int q;
-      float yv;
-      uint32_t m;
-      int_elem<false>(elem<T>(v, e), p, q, yv, m);
-      ov.set(e, yv);
-      cv.set(e, q);
-      mb |= m << e;
+    for (int g = 0; g < VEC / 4; ++g) {
+      float u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (SR) sr_draws4(sr, base / 4 + g, u);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int e = 4 * g + c;
+        int q;
+        float yv;
+        uint32_t m;
+        if (SR)
+          int_elem_sr<false>(elem<T>(v, e), u[c], p, q, yv, m);
+        else
+          int_elem<false>(elem<T>(v, e), p, q, yv, m);
+        ov.set(e, yv);
+        cv.set(e, q);
+        mb |= m << e;
+      }
     }
   } else {
 #pragma unroll

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "qat.h"
+#include "qat_sr.h"
 
 namespace qat {
 
@@ -27,16 +28,26 @@ qat_status launch_stats_tensor(qat_dtype dt, const void* x, int64_t n, int mm, v
 qat_status launch_stats_finalize(const void* ws, int nparts, float* absmax, float* minv, float* maxv,
                                  int32_t* flags, cudaStream_t s);
 
+// Launchers whose rounding can be stochastic come in two builds: the plain
+// name rounds to nearest (sr ignored), the *_sr name rounds stochastically
+// with the draws of sr.
+
 // integer fake quant, one parameter set for the whole tensor
-qat_status launch_int_tensor(qat_dtype dt, int bits, bool affine, bool given, const void* x,
-                             int64_t n, const void* ws, int nparts, float* scale, int32_t* zp,
-                             void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s);
+#define QAT_DECL_INT_TENSOR(name)                                                               \
+  qat_status name(qat_dtype dt, int bits, bool affine, bool given, const void* x, int64_t n,    \
+                  const void* ws, int nparts, float* scale, int32_t* zp, const SrCtx& sr,       \
+                  void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s)
+QAT_DECL_INT_TENSOR(launch_int_tensor);
+QAT_DECL_INT_TENSOR(launch_int_tensor_sr);
 
 // integer fake quant with per-unit parameter arrays (unit = i / L)
-qat_status launch_int_units(qat_dtype dt, int bits, bool affine, bool given, const void* x,
-                            int64_t n, int64_t L, const float* scale, const int32_t* zp,
-                            const uint8_t* dead, void* y, void* codes, uint32_t* mask,
-                            int32_t* flags, cudaStream_t s);
+#define QAT_DECL_INT_UNITS(name)                                                                \
+  qat_status name(qat_dtype dt, int bits, bool affine, bool given, const void* x, int64_t n,    \
+                  int64_t L, const float* scale, const int32_t* zp, const uint8_t* dead,        \
+                  const SrCtx& sr, void* y, void* codes, uint32_t* mask, int32_t* flags,        \
+                  cudaStream_t s)
+QAT_DECL_INT_UNITS(launch_int_units);
+QAT_DECL_INT_UNITS(launch_int_units_sr);
 
 // warp-per-unit statistics / calibration for any unit length (fallback)
 // mode 0: absmax/minv/maxv outputs; mode 1: int params -> scale, zp, dead
@@ -49,15 +60,21 @@ qat_status launch_unit_generic(qat_dtype dt, int mode, int bits, bool affine, co
 // for units of L elements.  Returns QAT_ERR_UNSUPPORTED when L does not fit
 // either fused kernel (the caller then takes the fallback).
 bool fused_units_supported(qat_dtype dt, int64_t L);
-qat_status launch_int_fused(qat_dtype dt, int bits, bool affine, bool stats_only, const void* x,
-                            int64_t units, int64_t L, float* scale, int32_t* zp, float* absmax,
-                            float* minv, float* maxv, void* y, void* codes, uint32_t* mask,
-                            int32_t* flags, cudaStream_t s);
+#define QAT_DECL_INT_FUSED(name)                                                                \
+  qat_status name(qat_dtype dt, int bits, bool affine, bool stats_only, const void* x,          \
+                  int64_t units, int64_t L, float* scale, int32_t* zp, float* absmax,           \
+                  float* minv, float* maxv, const SrCtx& sr, void* y, void* codes,              \
+                  uint32_t* mask, int32_t* flags, cudaStream_t s)
+QAT_DECL_INT_FUSED(launch_int_fused);
+QAT_DECL_INT_FUSED(launch_int_fused_sr);  // stats_only unsupported
 
 // FP8
-qat_status launch_fp8_tensor(qat_dtype dt, qat_fp8_format fmt, bool given, const void* x, int64_t n,
-                             const void* ws, int nparts, float* scale, void* y, uint8_t* codes,
-                             uint32_t* mask, int32_t* flags, cudaStream_t s);
+#define QAT_DECL_FP8_TENSOR(name)                                                               \
+  qat_status name(qat_dtype dt, qat_fp8_format fmt, bool given, const void* x, int64_t n,       \
+                  const void* ws, int nparts, float* scale, const SrCtx& sr, void* y,           \
+                  uint8_t* codes, uint32_t* mask, int32_t* flags, cudaStream_t s)
+QAT_DECL_FP8_TENSOR(launch_fp8_tensor);
+QAT_DECL_FP8_TENSOR(launch_fp8_tensor_sr);
 
 // STE backward
 qat_status launch_ste(qat_dtype dt, const void* g, int64_t n, const uint32_t* mask, void* dx,

@@ -71,7 +71,8 @@ extern "C" qat_status qat_fake_quant_fp8_noalloc(const void* x, qat_dtype dtype,
     return QAT_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (scale_given)
-    return qat::launch_fp8_tensor(dtype, fmt, true, x, n, nullptr, 0, scale, y, codes, mask, flags, s);
+    return qat::launch_fp8_tensor(dtype, fmt, true, x, n, nullptr, 0, scale, qat::SrCtx{}, y, codes,
+                                  mask, flags, s);
   const int grid = qat::stats_grid(n);
   if (grid > kNoAllocSlots) return QAT_ERR_WORKSPACE;  // more partials than the fixed scratch holds
   void* ws = nullptr;
@@ -79,5 +80,6 @@ extern "C" qat_status qat_fake_quant_fp8_noalloc(const void* x, qat_dtype dtype,
   if (st) return st;
   st = qat::launch_stats_tensor(dtype, x, n, qat::kMMNone, ws, grid, s);
   if (st) return st;
-  return qat::launch_fp8_tensor(dtype, fmt, false, x, n, ws, grid, scale, y, codes, mask, flags, s);
+  return qat::launch_fp8_tensor(dtype, fmt, false, x, n, ws, grid, scale, qat::SrCtx{}, y, codes,
+                                mask, flags, s);
 }

@@ -1,0 +1,28 @@
+// qat_sr.h -- the stochastic-rounding call context shared by the host
+// launchers and the kernels (internal; not part of the C ABI).
+#pragma once
+
+#include <cstdint>
+
+namespace qat {
+
+// Philox-4x32-10 key and counter base of one call: element i draws word
+// i % 4 of the block with counter offset + i / 4.
+struct SrCtx {
+  uint32_t k0, k1;  // key: low and high word of the seed
+  uint64_t offset;  // counter base
+};
+
+}  // namespace qat
+
+// Each kernel source is compiled twice: with QAT_SR 0 (nearest rounding, the
+// statistics kernels and every launcher) and with QAT_SR 1 (only the kernels
+// whose rounding is stochastic, behind launchers named *_sr).
+#ifndef QAT_SR
+#define QAT_SR 0
+#endif
+#if QAT_SR
+#define QAT_SR_NAME(f) f##_sr
+#else
+#define QAT_SR_NAME(f) f
+#endif

@@ -172,6 +172,36 @@ qat_status qat_fake_quant_fp8(const void* x, qat_dtype dtype, int64_t n, qat_fp8
                               size_t workspace_bytes, qat_stream_t stream);
 
 /*
+ * Stochastic rounding ([QAT] RoundingMode::Stochastic, round_to_int): the
+ * same operations as qat_fake_quant_int and qat_fake_quant_fp8 (same
+ * arguments, calibration, window, layouts, flags and errors), with the
+ * nearest rounding of r replaced by floor(r) + 1 when the element's draw
+ * u < r - floor(r) and floor(r) otherwise (so E[round(r)] = r).
+ *   int:  r = x / scale (binary32, IEEE); q = clamp(round(r) + zp, qmin, qmax).
+ *   fp8:  r = a / ulp, a = |x / scale|, ulp = 2^(max(floor(log2 a), emin) - mbits)
+ *         (an exact power-of-two scaling); magnitude round(r) * ulp, saturated
+ *         at the format maximum; the sign of x / scale.
+ * Draws: element i (flat index, 0-based) uses word i % 4 of Philox-4x32-10
+ * (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+ * SC 2011; 10 rounds) with key (low, high 32 bits of seed) and counter
+ * (low, high 32 bits of offset + i / 4, 0, 0); u = (word >> 9) * 2^-23, a
+ * multiple of 2^-23 in [0, 1).  The draws depend only on (seed, offset, i):
+ * results are reproducible and independent of the launch shape.  To draw
+ * fresh numbers for a later call on the same seed, advance offset by at
+ * least ceil(n / 4).
+ */
+qat_status qat_fake_quant_int_sr(const void* x, qat_dtype dtype, int64_t rows, int64_t cols,
+                                 int bits, qat_scheme scheme, qat_granularity granularity,
+                                 int64_t group, int params_given, float* scale, int32_t* zero_point,
+                                 uint64_t seed, uint64_t offset, void* y, void* codes,
+                                 uint32_t* mask, int32_t* dev_flags, void* workspace,
+                                 size_t workspace_bytes, qat_stream_t stream);
+qat_status qat_fake_quant_fp8_sr(const void* x, qat_dtype dtype, int64_t n, qat_fp8_format format,
+                                 int scale_given, float* scale, uint64_t seed, uint64_t offset,
+                                 void* y, uint8_t* codes, uint32_t* mask, int32_t* dev_flags,
+                                 void* workspace, size_t workspace_bytes, qat_stream_t stream);
+
+/*
  * Straight-through-estimator backward ([QAT] fake_quant_backward) with the
  * window precomputed as the mask of a forward call: grad_in[i] = grad[i]
  * (bit copy) where the mask bit is set, +0 elsewhere.  grad and grad_in have
