@@ -239,6 +239,97 @@ class Suite:
                                "dx4", "d5", "q5", "u5", "y5")]
 
 
+def run_next_rows(args, suite, wb, peak):
+    """Rows past the headline path, timed like it (CUDA events per call on the
+    launching stream, after warm-up) but reported outside `value`:
+    - stochastic rounding (the *_sr entry points) of the w2, w3 and w4 maps,
+      same inputs, outputs and algorithmic bytes as their nearest-rounding
+      calls;
+    - config 1 (w1 int8 per-tensor fwd + STE) replayed as one CUDA graph
+      against the same two calls issued directly, with a 256 MiB L2 flush
+      before every timed iteration."""
+    fq, o, ws, fl = suite.fq, suite.o, suite.ws, suite.flags
+    n1, n2, n3, n4, n5 = suite.n
+    r2, c2, r4, c4 = suite.r2, suite.c2, suite.r4, suite.c4
+    seed = 0x5EED
+    bytes_of = {name: b for name, _, b, _ in wb}
+    sr = [
+        ("w2_affine_int8_row_sr", "w2_affine_int8_row",
+         lambda: fq.qat_fake_quant_int_sr(suite.w2, r2, c2, 8, 1, 1, 0, False, o["s2a"], o["z2a"],
+                                          seed, 0, o["y2a"], o["c2a"], o["m2a"], fl, ws)),
+        ("w2_sym_int4_row_sr", "w2_sym_int4_row",
+         lambda: fq.qat_fake_quant_int_sr(suite.w2, r2, c2, 4, 0, 1, 0, False, o["s2b"], None, seed,
+                                          0, o["y2b"], o["c2b"], o["m2b"], fl, ws)),
+        ("w3_fp8_e4m3_tensor_sr", "w3_fp8_e4m3_tensor",
+         lambda: fq.qat_fake_quant_fp8_sr(suite.a3, n3, 0, False, o["s3"][0:1], seed, 0, o["y3a"],
+                                          None, o["m3a"], fl, ws)),
+        ("w4_int4_group_fwd_sr", "w4_int4_group_fwd",
+         lambda: fq.qat_fake_quant_int_sr(suite.w4, r4, c4, 4, 0, 2, 128, False, o["s4"], None,
+                                          seed, 0, o["y4"], o["c4"], o["m4"], fl, ws)),
+    ]
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 200))
+    for _ in range(3):
+        for _, _, c in sr:
+            c()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(sr) + 1)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for k in range(steps):
+        for i, (_, _, c) in enumerate(sr):
+            ev[k][i].record(stream)
+            c()
+        ev[k][len(sr)].record(stream)
+    torch.cuda.synchronize()
+    out = {}
+    for i, (name, base, _) in enumerate(sr):
+        ms = sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(steps)) / steps
+        b = bytes_of[base]
+        out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(b / (ms * 1e-3) / 1e9, 1),
+                     "frac_of_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peak, 4),
+                     "bytes": b, "launches": 2 if base.startswith("w3") else 1}
+
+    # config 1: direct calls and one CUDA graph of the same calls
+    calls = suite.calls()[:2]
+    b1 = bytes_of["w1_int8_tensor_fwd"] + bytes_of["w1_ste_bwd"]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=suite.x1.device)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            for c in calls:
+                c()
+    stream.wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in calls:
+            c()
+
+    def timed(run):
+        t = []
+        for _ in range(3):
+            run()
+        for _ in range(steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            z = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run()
+            z.record(stream)
+            t.append((a, z))
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(z) for a, z in t) / len(t)
+
+    direct_ms = timed(lambda: [c() for c in calls])
+    graph_ms = timed(g.replay)
+    w1 = {}
+    for key, ms in (("direct", direct_ms), ("cuda_graph", graph_ms)):
+        w1[key] = {"us": round(ms * 1e3, 2), "GB_s": round(b1 / (ms * 1e-3) / 1e9, 1),
+                   "frac_of_measured_hbm": round(b1 / (ms * 1e-3) / 1e9 / peak, 4)}
+    w1["bytes"] = b1
+    w1["l2"] = "256 MiB memset before every timed iteration"
+    return {"stochastic_rounding": out, "w1_int8_tensor_fwd_ste": w1}
+
+
 def make_inputs(frac: float = 1.0):
     """Inputs of the five workloads; frac < 1 keeps that fraction of the rows
     (elements) of each, with the same distributions (profiling runs only)."""
@@ -359,6 +450,9 @@ def run_ours(args, rank, world, local):
     e2e = run_e2e(args, suite, calls, step_bytes)
 
     peak, peak_kind = measured_peak()
+    next_rows = None
+    if not args.only and args.fraction >= 1.0 and not args.no_next:
+        next_rows = run_next_rows(args, suite, wb, peak)
     per_wl = {}
     for (name, elems, b, nl), ms in zip(wb, mean_ms):
         per_wl[name] = {"ms": round(float(ms), 5), "GB_s": round(b / (ms * 1e-3) / 1e9, 1),
@@ -402,6 +496,8 @@ def run_ours(args, rank, world, local):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": dbytes},
     }
+    if next_rows is not None:
+        line["next_rows"] = next_rows
     if args.fraction < 1.0 or args.only:
         line["config"]["subset"] = {"only": args.only, "fraction": args.fraction}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -544,6 +640,8 @@ def main(argv=None):
     ap.add_argument("--ref-fraction", type=float, default=0.0,
                     help="per-step sample of the reference arm (0: sized to ~2 min in total)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip the stochastic-rounding and CUDA-graph timings (next_rows)")
     ap.add_argument("--only", default="",
                     help="profiling: comma-separated call-name prefixes to run (e.g. w5,w4_int4)")
     ap.add_argument("--fraction", type=float, default=1.0,
