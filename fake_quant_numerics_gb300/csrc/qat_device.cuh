@@ -757,8 +757,10 @@ __device__ __forceinline__ uint4 philox4x32_10(uint64_t ctr, uint32_t k0, uint32
   for (int round = 0; round < 10; ++round) {
     // the Philox S-box: 32 x 32 -> 64-bit products by the two round
     // multipliers, high halves mixed with the other words and the round key
-    const uint32_t hi0 = __umulhi(0xD2511F53u, x0), lo0 = 0xD2511F53u * x0;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, x2), lo1 = 0xCD9E8D57u * x2;
+    const uint64_t p0 = (uint64_t)0xD2511F53u * x0;  // one 32 x 32 -> 64-bit multiply each
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * x2;
+    const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
     const uint32_t n0 = hi1 ^ x1 ^ k0, n2 = hi0 ^ x3 ^ k1;
     x0 = n0;
     x1 = lo1;
