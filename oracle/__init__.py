@@ -91,6 +91,9 @@ def lib():
         L.or_fake_quant_int_sr.argtypes = [vp, i32, i64, i64, i32, i32, i32, i64, i32, vp, vp, u64,
                                            u64, vp, vp, vp, vp]
         L.or_fake_quant_fp8_sr.argtypes = [vp, i32, i64, i32, i32, vp, u64, u64, vp, vp, vp, vp]
+        L.or_adam_update.argtypes = [vp, vp, vp, vp, i64, f32, f32, f32, f32, f32, f32, f32]
+        L.or_qat_optimizer_step.argtypes = [vp, vp, vp, vp, i64, f32, f32, f32, f32, f32, f32, f32,
+                                            i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, vp, vp]
     return _lib
 
 
@@ -250,6 +253,47 @@ def fake_quant_fp8_sr(x: np.ndarray, fmt: int, seed: int = 0, offset: int = 0, s
     if st:
         raise ValueError(f"oracle fake_quant_fp8_sr status {st}")
     return dict(y=y, codes=codes, mask=mask, scale=np.float32(s.value), flags=flags.value)
+
+
+def bias_corrections(beta1: float, beta2: float, t: int):
+    """1 - beta^t of step t, evaluated in binary64 as the QAT module does, then
+    rounded to binary32 (the values a caller hands to the optimizer step)."""
+    b1, b2 = float(np.float32(beta1)), float(np.float32(beta2))
+    return np.float32(1.0 - b1 ** t), np.float32(1.0 - b2 ** t)
+
+
+def adam_update(w, g, m, v, lr, beta1, beta2, eps, wd, bc1, bc2):
+    """The optimizer's element loop on copies; returns (w, m, v)."""
+    w, m, v = (np.array(a, np.float32).reshape(-1).copy() for a in (w, m, v))
+    g = np.ascontiguousarray(g, np.float32).reshape(-1)
+    lib().or_adam_update(_p(w), _p(g), _p(m), _p(v), w.size, lr, beta1, beta2, eps, wd, bc1, bc2)
+    return w, m, v
+
+
+def qat_optimizer_step(w, g, m, v, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
+                       step=1, bits=8, scheme=0, fmt=0, stochastic=False, seed=0, offset=0,
+                       want_codes=True, want_mask=True):
+    """One QatOptimizer::step on copies of (w, m, v): returns dict(w, m, v, view,
+    codes, mask, scale, zero_point, flags); bits = 0 selects the FP8 view."""
+    w, m, v = (np.array(a, np.float32).reshape(-1).copy() for a in (w, m, v))
+    g = np.ascontiguousarray(g, np.float32).reshape(-1)
+    n = w.size
+    bc1, bc2 = bias_corrections(beta1, beta2, step)
+    view = np.empty(n, np.float32)
+    codes = None
+    if want_codes:
+        codes = (np.empty(n, np.int8) if bits == 8 else np.empty((n + 1) // 2, np.uint8) if bits == 4
+                 else np.empty(n, np.uint8))
+    mask = np.empty((n + 31) // 32, np.uint32) if want_mask else None
+    sc, zp, flags = ctypes.c_float(0.0), ctypes.c_int32(0), ctypes.c_int32(0)
+    st = lib().or_qat_optimizer_step(_p(w), _p(g), _p(m), _p(v), n, lr, beta1, beta2, eps,
+                                     weight_decay, bc1, bc2, bits, scheme, fmt, int(stochastic),
+                                     seed, offset, _p(view), _p(codes), _p(mask), ctypes.byref(sc),
+                                     ctypes.byref(zp), ctypes.byref(flags))
+    if st:
+        raise ValueError(f"oracle qat_optimizer_step status {st}")
+    return dict(w=w, m=m, v=v, view=view, codes=codes, mask=mask, scale=np.float32(sc.value),
+                zero_point=zp.value, flags=flags.value, bias_corrections=(bc1, bc2))
 
 
 def fake_quant_fp8(x: np.ndarray, fmt: int, scale=None, want_codes=True, want_mask=True):

@@ -32,6 +32,8 @@
  *   [PHX]  Philox-4x32-10, J. Salmon, M. Moraes, R. Dror, D. Shaw, "Parallel
  *          random numbers: as easy as 1, 2, 3", SC 2011 (the round function
  *          and the Weyl key schedule as published)
+ *   [QAT]  QatConfig, QatOptimizer::{step, requantize} (Adam/AdamW update of
+ *          the master weights, then the fake-quant view)
  *
  * Every place where the sources are silent and a reading was taken is marked
  * "reading:" below.
@@ -555,6 +557,62 @@ int or_fake_quant_fp8_sr(const void* x, int dtype, int64_t n, int fmt, int scale
                          float* scale, uint64_t seed, uint64_t offset, void* y, uint8_t* codes,
                          uint32_t* mask, int32_t* flags) {
   return fq_fp8(x, dtype, n, fmt, scale_given, scale, y, codes, mask, flags, 1, seed, offset);
+}
+
+/* ------------------------------------------------------------------------- */
+/* [QAT] QatOptimizer::step, the element loop, in binary32:                   */
+/*   m = beta1 m + (1 - beta1) g;  v = beta2 v + (1 - beta2) g g;             */
+/*   m_hat = m / bc1;  v_hat = v / bc2;                                       */
+/*   if wd != 0: w = w - lr wd w   (decoupled, AdamW);                        */
+/*   w = w - lr m_hat / (sqrt(v_hat) + eps).                                  */
+/* reading: every quantity is binary32 (master, moments, hyper-parameters),   */
+/* each product / quotient / sum / square root rounded once, in the printed   */
+/* order (left to right: (1 - beta2) g is rounded before the second g, lr wd  */
+/* before w, lr m_hat before the division); 1 - beta is a binary32            */
+/* subtraction; the bias corrections bc = 1 - beta^t of step t are given by   */
+/* the caller (the module evaluates them in binary64).                        */
+/* ------------------------------------------------------------------------- */
+void or_adam_update(float* w, const float* g, float* m, float* v, int64_t n, float lr,
+                    float beta1, float beta2, float eps, float wd, float bc1, float bc2) {
+  const float omb1 = 1.0f - beta1, omb2 = 1.0f - beta2;
+  const float lrwd = lr * wd;
+  for (int64_t i = 0; i < n; ++i) {
+    float gi = g[i];
+    float mi = beta1 * m[i] + omb1 * gi;
+    float vi = beta2 * v[i] + (omb2 * gi) * gi;
+    m[i] = mi;
+    v[i] = vi;
+    float mh = mi / bc1;
+    float vh = vi / bc2;
+    float wi = w[i];
+    if (wd != 0.0f) wi = wi - lrwd * wi;
+    wi = wi - (lr * mh) / (sqrtf(vh) + eps);
+    w[i] = wi;
+  }
+}
+
+/* [QAT] QatOptimizer::step + requantize: the update above, then the view
+ * re-derived from the new master: an integer target (bits 8 or 4) is
+ * calibrated per tensor over the finite values (per_tensor_minmax: absmax
+ * for symmetric, min/max for affine) and fake-quantized; an FP8 target is
+ * the unscaled saturating cast (scale 1).  Rounding nearest or stochastic
+ * (draws or_sr_uniform(seed, offset, i)).  *scale (and *zp) receive the view's
+ * parameters; mask and codes as for the fake-quant calls. */
+int or_qat_optimizer_step(float* w, const float* g, float* m, float* v, int64_t n, float lr,
+                          float beta1, float beta2, float eps, float wd, float bc1, float bc2,
+                          int bits, int scheme, int fmt, int stochastic, uint64_t seed,
+                          uint64_t offset, float* view, void* codes, uint32_t* mask, float* scale,
+                          int32_t* zp, int32_t* flags) {
+  if (n < 0) return OR_ERR_INVALID;
+  or_adam_update(w, g, m, v, n, lr, beta1, beta2, eps, wd, bc1, bc2);
+  if (n == 0) return OR_OK;
+  if (bits == 8 || bits == 4)
+    return fq_int(w, OR_F32, 1, n, bits, scheme, OR_PER_TENSOR, 0, 0, scale, zp, view, codes, mask,
+                  flags, 1, stochastic, seed, offset);
+  if (bits != 0) return OR_ERR_UNSUPPORTED;
+  *scale = 1.0f;
+  return fq_fp8(w, OR_F32, n, fmt, 1, scale, view, (uint8_t*)codes, mask, flags, stochastic, seed,
+                offset);
 }
 
 /* ------------------------------------------------------------------------- */
