@@ -6,7 +6,8 @@ integer and FP8 maps also round stochastically with counter-based draws.
 """
 from ._lib import QatError, load  # noqa: F401
 from .api import (DoubleQuantized4Bit, FakeQuantFp8, FakeQuantInt, FakeQuantSTE,  # noqa: F401
-                  QatDataError, amax_stats, dequantize_4bit_double, fake_quant_backward,
+                  OptimizerStep, QatDataError, adam_hparams, amax_stats, dequantize_4bit_double,
+                  fake_quant_backward, optimizer_step, qat_optimizer_step,
                   fake_quant_fp8, fake_quant_int, qat_amax_stats, qat_dequant4_double,
                   qat_fake_quant_fp8, qat_fake_quant_fp8_sr, qat_fake_quant_int,
                   qat_fake_quant_int_sr, qat_kernel_launch_count,

@@ -36,6 +36,14 @@ _vp, _i64, _int, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_s
 
 _u64 = ctypes.c_uint64
 
+
+class AdamHparams(ctypes.Structure):
+    """qat_adam_hparams (include/qat.h)."""
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("bias_correction1", ctypes.c_float), ("bias_correction2", ctypes.c_float)]
+
+
 PROTOTYPES = {
     "qat_status_string": ([_int], ctypes.c_char_p),
     "qat_workspace_bytes": ([_i64, _i64, _int, _i64], _sz),
@@ -46,6 +54,8 @@ PROTOTYPES = {
     "qat_fake_quant_fp8_noalloc": ([_vp, _int, _i64, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp], _int),
     "qat_fake_quant_int_sr": ([_vp, _int, _i64, _i64, _int, _int, _int, _i64, _int, _vp, _vp, _u64,
                                _u64, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _int),
+    "qat_optimizer_step": ([_vp, _vp, _vp, _vp, _i64, ctypes.POINTER(AdamHparams), _int, _int, _int,
+                            _int, _u64, _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _int),
     "qat_fake_quant_fp8_sr": ([_vp, _int, _i64, _int, _int, _vp, _u64, _u64, _vp, _vp, _vp, _vp, _vp,
                                _sz, _vp], _int),
     "qat_ste_backward": ([_vp, _int, _i64, _vp, _vp, _vp], _int),

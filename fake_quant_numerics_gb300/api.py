@@ -114,6 +114,25 @@ def qat_fake_quant_fp8_sr(x, n, fmt, scale_given, scale, seed, offset, y, codes,
     _lib.check("qat_fake_quant_fp8_sr", st)
 
 
+def adam_hparams(lr, beta1, beta2, eps, weight_decay, step):
+    """qat_adam_hparams of step `step` (>= 1): the bias corrections 1 - beta^t
+    evaluated in binary64 (as QatOptimizer::step does) from the binary32 betas."""
+    b1, b2 = ctypes.c_float(beta1).value, ctypes.c_float(beta2).value
+    return _lib.AdamHparams(lr, beta1, beta2, eps, weight_decay, 1.0 - b1 ** step, 1.0 - b2 ** step)
+
+
+def qat_optimizer_step(master, grad, exp_avg, exp_avg_sq, n, hparams, bits, scheme, fmt, stochastic,
+                       seed, offset, view, codes, mask, scale, zero_point, dev_flags, workspace,
+                       stream=None):
+    st = _lib.lib().qat_optimizer_step(_p(master), _p(grad), _p(exp_avg), _p(exp_avg_sq), n,
+                                       ctypes.byref(hparams), bits, _SCHEME[scheme], _FMT[fmt],
+                                       int(stochastic), int(seed), int(offset), _p(view),
+                                       _p(codes), _p(mask), _p(scale), _p(zero_point),
+                                       _p(dev_flags), _p(workspace), _nbytes(workspace),
+                                       _s(stream))
+    _lib.check("qat_optimizer_step", st)
+
+
 def qat_ste_backward(grad, n, mask, grad_in, stream=None):
     st = _lib.lib().qat_ste_backward(_p(grad), _dt(grad), n, _p(mask), _p(grad_in), _s(stream))
     _lib.check("qat_ste_backward", st)
@@ -285,6 +304,69 @@ def fake_quant_fp8(x: torch.Tensor, fmt="e4m3", scale: Optional[float] = None,
     else:
         raise ValueError(f"rounding must be 'nearest' or 'stochastic', not {rounding!r}")
     return FakeQuantFp8(y, codes, mask, s, flags)
+
+
+class OptimizerStep(NamedTuple):
+    view: torch.Tensor
+    codes: Optional[torch.Tensor]
+    mask: Optional[torch.Tensor]
+    scale: torch.Tensor
+    zero_point: Optional[torch.Tensor]
+    flags: torch.Tensor
+
+
+_TARGETS = {"int8": (8, E4M3), "int4": (4, E4M3), "e4m3": (0, E4M3), "fp8_e4m3": (0, E4M3),
+            "e5m2": (0, E5M2), "fp8_e5m2": (0, E5M2)}
+
+
+def _in_place(t: torch.Tensor, what: str) -> torch.Tensor:
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.data_ptr() % 32:
+        raise ValueError(f"{what} must be a contiguous, 32-byte aligned float32 CUDA tensor "
+                         "(it is updated in place)")
+    return t
+
+
+def optimizer_step(master: torch.Tensor, grad: torch.Tensor, exp_avg: torch.Tensor,
+                   exp_avg_sq: torch.Tensor, step: int, lr: float, betas=(0.9, 0.999),
+                   eps: float = 1e-8, weight_decay: float = 0.0, target: str = "int8",
+                   scheme="symmetric", rounding: str = "nearest", seed: int = 0, offset: int = 0,
+                   want_codes: bool = False, want_mask: bool = False,
+                   check: bool = False) -> OptimizerStep:
+    """One QatOptimizer::step: Adam / AdamW update of the float32 master and its
+    moments in place (step t >= 1), then the fake-quant view of the new master
+    (target int8 / int4 calibrated per tensor, or the unscaled e4m3 / e5m2 cast)."""
+    if step < 1:
+        raise ValueError("step counts from 1")
+    bits, fmt = _TARGETS[target]
+    master = _in_place(master, "master")
+    exp_avg = _in_place(exp_avg, "exp_avg")
+    exp_avg_sq = _in_place(exp_avg_sq, "exp_avg_sq")
+    grad = _ready(grad.to(torch.float32))
+    n = master.numel()
+    if grad.numel() != n or exp_avg.numel() != n or exp_avg_sq.numel() != n:
+        raise QatError("optimizer_step", _lib.QAT_ERR_DIMENSION_MISMATCH)
+    dev = master.device
+    view = torch.empty_like(master)
+    codes = None
+    if want_codes:
+        codes = (torch.empty(n, dtype=torch.int8, device=dev) if bits == 8
+                 else torch.empty((n + 1) // 2, dtype=torch.uint8, device=dev) if bits == 4
+                 else torch.empty(n, dtype=torch.uint8, device=dev))
+    mask = torch.empty((n + 31) // 32, dtype=torch.int32, device=dev) if want_mask else None
+    scale = torch.empty(1, dtype=torch.float32, device=dev)
+    zp = torch.empty(1, dtype=torch.int32, device=dev)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(qat_workspace_bytes(1, n, PER_TENSOR, 0), dtype=torch.uint8, device=dev)
+    if rounding not in ("nearest", "stochastic"):
+        raise ValueError(f"rounding must be 'nearest' or 'stochastic', not {rounding!r}")
+    hp = adam_hparams(lr, betas[0], betas[1], eps, weight_decay, step)
+    qat_optimizer_step(master, grad, exp_avg, exp_avg_sq, n, hp, bits, scheme, fmt,
+                       rounding == "stochastic", seed, offset, view, codes, mask, scale, zp, flags,
+                       ws)
+    if check:
+        raise_on_flags(flags, "optimizer_step")
+    return OptimizerStep(view, codes, mask, scale, zp if bits and _SCHEME[scheme] == AFFINE else None,
+                         flags)
 
 
 def fake_quant_backward(grad: torch.Tensor, mask: torch.Tensor) -> torch.Tensor:

@@ -261,6 +261,61 @@ qat_status qat_fake_quant_fp8_sr(const void* x, qat_dtype dtype, int64_t n, qat_
                              ws_bytes, stream);
 }
 
+qat_status qat_optimizer_step(float* master, const float* grad, float* exp_avg, float* exp_avg_sq,
+                              int64_t n, const qat_adam_hparams* hp, int bits, qat_scheme scheme,
+                              qat_fp8_format format, int stochastic, uint64_t seed,
+                              uint64_t offset, float* view, void* codes, uint32_t* mask,
+                              float* scale, int32_t* zp, int32_t* flags, void* ws,
+                              size_t ws_bytes, qat_stream_t stream) {
+  if (!hp) return QAT_ERR_INVALID_ARGUMENT;
+  if (bits != 0 && bits != 4 && bits != 8) return QAT_ERR_UNSUPPORTED;
+  if (bits == 0 && format != QAT_E4M3 && format != QAT_E5M2) return QAT_ERR_UNSUPPORTED;
+  if (bits != 0 && scheme != QAT_SYMMETRIC && scheme != QAT_AFFINE) return QAT_ERR_UNSUPPORTED;
+  if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;
+  const float bc1 = hp->bias_correction1, bc2 = hp->bias_correction2;
+  if (!(bc1 > 0.0f) || !(bc2 > 0.0f) || isinf(bc1) || isinf(bc2)) return QAT_ERR_INVALID_ARGUMENT;
+  if (n == 0) return QAT_OK;
+  if (!master || !grad || !exp_avg || !exp_avg_sq || !view || !scale)
+    return QAT_ERR_INVALID_ARGUMENT;
+  if (!aligned(master, kAlignVec) || !aligned(grad, kAlignVec) || !aligned(exp_avg, kAlignVec) ||
+      !aligned(exp_avg_sq, kAlignVec) || !aligned(view, kAlignVec) ||
+      (codes && !aligned(codes, kAlignBuf)) || (mask && !aligned(mask, kAlignBuf)) ||
+      !aligned(scale, 4) || (zp && !aligned(zp, 4)))
+    return QAT_ERR_MISALIGNED;
+  const bool int_view = bits != 0;
+  if (int_view) {
+    if (!ws || ws_bytes < ws_bytes_for(1, n, QAT_PER_TENSOR, 0)) return QAT_ERR_WORKSPACE;
+    if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+  }
+  AdamHp a;
+  a.lr = hp->lr;
+  a.beta1 = hp->beta1;
+  a.beta2 = hp->beta2;
+  a.eps = hp->eps;
+  a.omb1 = 1.0f - hp->beta1;
+  a.omb2 = 1.0f - hp->beta2;
+  a.lrwd = hp->lr * hp->weight_decay;
+  a.bc1 = bc1;
+  a.bc2 = bc2;
+  a.decay = hp->weight_decay != 0.0f;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool affine = int_view && scheme == QAT_AFFINE;
+  const int grid = stats_grid(n);
+  qat_status st = launch_adam(master, grad, exp_avg, exp_avg_sq, n, a,
+                              affine ? kMMFloat : kMMNone, int_view, ws, grid,
+                              int_view ? nullptr : scale, s);
+  if (st) return st;
+  const SrCtx c = sr_ctx(seed, offset);
+  if (int_view) {
+    auto map = stochastic ? launch_int_tensor_sr : launch_int_tensor;
+    return map(QAT_F32, bits, affine, false, master, n, ws, grid, scale, zp, c, view, codes, mask,
+               flags, s);
+  }
+  auto map = stochastic ? launch_fp8_tensor_sr : launch_fp8_tensor;
+  return map(QAT_F32, format, true, master, n, nullptr, 0, scale, c, view,
+             static_cast<uint8_t*>(codes), mask, flags, s);
+}
+
 qat_status qat_ste_backward(const void* grad, qat_dtype dtype, int64_t n, const uint32_t* mask,
                             void* grad_in, qat_stream_t stream) {
   if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;

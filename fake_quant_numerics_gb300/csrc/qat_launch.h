@@ -76,6 +76,18 @@ QAT_DECL_INT_FUSED(launch_int_fused_sr);  // stats_only unsupported
 QAT_DECL_FP8_TENSOR(launch_fp8_tensor);
 QAT_DECL_FP8_TENSOR(launch_fp8_tensor_sr);
 
+// QAT optimizer step, the master update (binary32 hyper-parameters; omb =
+// 1 - beta, lrwd = lr * wd, decay = (wd != 0), bc = the bias corrections)
+struct AdamHp {
+  float lr, beta1, beta2, eps, omb1, omb2, lrwd, bc1, bc2;
+  int decay;
+};
+// the update of w, m, v in place; with `stats`, one partial of the new w per
+// block into ws (min / max mode mm, grid <= kMaxPartials); otherwise block 0
+// writes 1.0f to *scale_one when it is not null
+qat_status launch_adam(float* w, const float* g, float* m, float* v, int64_t n, const AdamHp& hp,
+                       int mm, bool stats, void* ws, int grid, float* scale_one, cudaStream_t s);
+
 // STE backward
 qat_status launch_ste(qat_dtype dt, const void* g, int64_t n, const uint32_t* mask, void* dx,
                       cudaStream_t s);

@@ -202,6 +202,49 @@ qat_status qat_fake_quant_fp8_sr(const void* x, qat_dtype dtype, int64_t n, qat_
                                  void* workspace, size_t workspace_bytes, qat_stream_t stream);
 
 /*
+ * One QAT optimizer step ([QAT] QatConfig, QatOptimizer::step + requantize):
+ * an Adam / AdamW update of the fp32 master weights in place, then the
+ * fake-quant view re-derived from the new master.
+ *   master, grad, exp_avg, exp_avg_sq: float32[n] (master, first and second
+ *     moments updated in place; grad read).  32-byte aligned.
+ *   hp: host pointer; lr, beta1, beta2, eps, weight_decay as in QatConfig and
+ *     bias_correction1/2 = 1 - beta1^t, 1 - beta2^t of this step t >= 1 (the
+ *     module evaluates them in binary64; the caller passes them rounded to
+ *     binary32).  Per element, in binary32 with one rounding per operation:
+ *       m = beta1 m + (1 - beta1) g;  v = beta2 v + ((1 - beta2) g) g;
+ *       m_hat = m / bc1;  v_hat = v / bc2;
+ *       if weight_decay != 0: w = w - (lr weight_decay) w;
+ *       w = w - (lr m_hat) / (sqrt(v_hat) + eps).
+ *   view target: bits = 8 or 4 -> integer view calibrated per tensor over the
+ *     new master (QuantParams::per_tensor_minmax with `scheme`), exactly
+ *     qat_fake_quant_int per tensor on the new master (scale, zero_point
+ *     written); bits = 0 -> FP8 view, the unscaled saturating cast in
+ *     `format` (qat_fake_quant_fp8 with scale 1; *scale set to 1).
+ *   stochastic != 0: stochastic rounding of the view with the draws of
+ *     (seed, offset), as qat_fake_quant_int_sr / qat_fake_quant_fp8_sr.
+ *   view: float32[n]; codes / mask (nullable) as the fake-quant calls;
+ *     workspace (integer view only): qat_workspace_bytes(1, n,
+ *     QAT_PER_TENSOR, 0) bytes.
+ * Errors: hp NULL, a bias correction not finite and > 0, a NULL array ->
+ * QAT_ERR_INVALID_ARGUMENT; bits not in {0, 4, 8} or an unknown format ->
+ * QAT_ERR_UNSUPPORTED; alignment / workspace as above.  A non-finite new
+ * master value flags QAT_FLAG_NONFINITE_CALIB for an integer view (the
+ * module's calibration error) and gives codes 0, view +0, mask 0.
+ * Two kernel launches: the update (with the view's statistics) and the view.
+ */
+typedef struct {
+  float lr, beta1, beta2, eps, weight_decay;
+  float bias_correction1, bias_correction2;
+} qat_adam_hparams;
+
+qat_status qat_optimizer_step(float* master, const float* grad, float* exp_avg, float* exp_avg_sq,
+                              int64_t n, const qat_adam_hparams* hp, int bits, qat_scheme scheme,
+                              qat_fp8_format format, int stochastic, uint64_t seed,
+                              uint64_t offset, float* view, void* codes, uint32_t* mask,
+                              float* scale, int32_t* zero_point, int32_t* dev_flags,
+                              void* workspace, size_t workspace_bytes, qat_stream_t stream);
+
+/*
  * Straight-through-estimator backward ([QAT] fake_quant_backward) with the
  * window precomputed as the mask of a forward call: grad_in[i] = grad[i]
  * (bit copy) where the mask bit is set, +0 elsewhere.  grad and grad_in have
