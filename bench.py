@@ -327,7 +327,57 @@ def run_next_rows(args, suite, wb, peak):
                    "frac_of_measured_hbm": round(b1 / (ms * 1e-3) / 1e9 / peak, 4)}
     w1["bytes"] = b1
     w1["l2"] = "256 MiB memset before every timed iteration"
-    return {"stochastic_rounding": out, "w1_int8_tensor_fwd_ste": w1}
+    del flush
+    return {"stochastic_rounding": out, "w1_int8_tensor_fwd_ste": w1,
+            "qat_optimizer_step": run_optimizer_rows(args, suite, peak)}
+
+
+def run_optimizer_rows(args, suite, peak, n=1 << 26):
+    """The QAT optimizer step (AdamW update of an fp32 master with its moments,
+    then the per-tensor int8 view with its mask, or the FP8 view) on a synthetic
+    64M-parameter master (N(0, 0.02), gradients N(0, 1e-3), seeded on the
+    device): 256 MB per array, so no array stays in L2.  Algorithmic bytes per
+    element: update 16 read + 12 written, view 4 read + 4 written + 1/8 mask."""
+    fq = suite.fq
+    dev = suite.x1.device
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    w = torch.randn(n, generator=gen, device=dev) * 0.02
+    g = torch.randn(n, generator=gen, device=dev) * 0.001
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    view = torch.empty(n, device=dev)
+    mask = torch.empty((n + 31) // 32, dtype=torch.int32, device=dev)
+    scale = torch.empty(1, device=dev)
+    zp = torch.empty(1, dtype=torch.int32, device=dev)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(fq.qat_workspace_bytes(1, n, 0, 0), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 100))
+    b = int(n * (28 + 8) + (n + 31) // 32 * 4)
+    res = {"elements": n, "bytes": b, "launches": 2}
+    for name, bits_, sr in (("int8_view", 8, False), ("int8_view_sr", 8, True), ("e4m3_view", 0, False)):
+        t = 0
+        def step():
+            nonlocal t
+            t += 1
+            hp = fq.adam_hparams(1e-3, 0.9, 0.999, 1e-8, 0.01, t)
+            fq.qat_optimizer_step(w, g, m, v, n, hp, bits_, "symmetric", "e4m3", sr, 7, t * n,
+                                  view, None, mask, scale, zp, flags, ws)
+        for _ in range(3):
+            step()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, z in ev:
+            a.record(stream)
+            step()
+            z.record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(z) for a, z in ev) / steps
+        res[name] = {"us": round(ms * 1e3, 1), "GB_s": round(b / (ms * 1e-3) / 1e9, 1),
+                     "frac_of_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peak, 4)}
+    return res
 
 
 def make_inputs(frac: float = 1.0):
