@@ -25,7 +25,7 @@ _CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fno-stric
 
 F32, BF16 = 0, 1
 SYM, AFFINE = 0, 1
-PER_TENSOR, PER_ROW, PER_GROUP = 0, 1, 2
+PER_TENSOR, PER_ROW, PER_GROUP, PER_COLUMN = 0, 1, 2, 3
 E4M3, E5M2 = 0, 1
 FLAG_NONFINITE, FLAG_DEGENERATE, FLAG_BAD_PARAMS, FLAG_NONFINITE_INPUT = 1, 2, 4, 8
 FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
@@ -78,6 +78,7 @@ def lib():
         L.or64_fake_quant_int.argtypes = [vp, i32, i64, i64, i32, i32, i32, i64, vp, vp, vp]
         L.or64_fake_quant_fp8.argtypes = [vp, i32, i64, i32, vp, vp]
         L.or_unit_stats.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp]
+        L.or_unit_stats_strided.argtypes = [vp, i32, i64, i64, i64, vp, vp, vp, vp]
         u64 = ctypes.c_uint64
         L.or_philox4x32_10.argtypes = [vp, vp, vp]
         L.or_sr_uniform.argtypes = [u64, u64, i64]
@@ -121,6 +122,22 @@ def unit_stats(x: np.ndarray, L: int):
     return out[:, 0], out[:, 1], out[:, 2], bad
 
 
+def column_stats(x: np.ndarray, rows: int, cols: int):
+    """(min, max, absmax, nonfinite count) of each column of a row-major
+    [rows, cols] tensor (finite values only)."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    dt = _dtype_code(x)
+    out = np.zeros((cols, 3), np.float32)
+    bad = np.zeros(cols, np.int64)
+    mn, mx, am, nb = ctypes.c_float(), ctypes.c_float(), ctypes.c_float(), ctypes.c_int64()
+    for c in range(cols):
+        lib().or_unit_stats_strided(_p(x), dt, c, rows, cols, ctypes.byref(mn), ctypes.byref(mx),
+                                    ctypes.byref(am), ctypes.byref(nb))
+        out[c] = (mn.value, mx.value, am.value)
+        bad[c] = nb.value
+    return out[:, 0], out[:, 1], out[:, 2], bad
+
+
 def q_range(bits: int, scheme: int):
     lo, hi = ctypes.c_int32(), ctypes.c_int32()
     st = lib().or_q_range(bits, scheme, ctypes.byref(lo), ctypes.byref(hi))
@@ -154,6 +171,8 @@ def n_units(rows: int, cols: int, granularity: int, group: int = 0) -> int:
         return 1 if rows * cols > 0 else 0
     if granularity == PER_ROW:
         return rows
+    if granularity == PER_COLUMN:
+        return cols if rows > 0 else 0
     return rows * cols // group
 
 

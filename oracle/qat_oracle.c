@@ -62,6 +62,7 @@
 #define OR_PER_TENSOR 0
 #define OR_PER_ROW 1
 #define OR_PER_GROUP 2
+#define OR_PER_COLUMN 3
 #define OR_E4M3 0
 #define OR_E5M2 1
 
@@ -136,12 +137,13 @@ int or_q_range(int bits, int scheme, int32_t* qmin, int32_t* qmax) {
 /* error flag; FP8 path: informational).                                      */
 /* An empty fold leaves min=+inf, max=-inf, absmax=0.                         */
 /* ------------------------------------------------------------------------- */
-void or_unit_stats(const void* x, int dtype, int64_t off, int64_t len, float* mn, float* mx,
-                   float* amax, int64_t* nonfinite) {
+/* elements off, off + stride, ..., off + (len - 1) stride */
+void or_unit_stats_strided(const void* x, int dtype, int64_t off, int64_t len, int64_t stride,
+                           float* mn, float* mx, float* amax, int64_t* nonfinite) {
   float m = INFINITY, M = -INFINITY, A = 0.0f;
   int64_t bad = 0;
   for (int64_t i = 0; i < len; ++i) {
-    float v = load_elem(x, dtype, off + i);
+    float v = load_elem(x, dtype, off + i * stride);
     if (!isfinite(v)) { bad++; continue; }
     if (less_total(v, m)) m = v;
     if (less_total(M, v)) M = v;
@@ -149,6 +151,11 @@ void or_unit_stats(const void* x, int dtype, int64_t off, int64_t len, float* mn
     if (a > A) A = a;
   }
   *mn = m; *mx = M; *amax = A; *nonfinite = bad;
+}
+
+void or_unit_stats(const void* x, int dtype, int64_t off, int64_t len, float* mn, float* mx,
+                   float* amax, int64_t* nonfinite) {
+  or_unit_stats_strided(x, dtype, off, len, 1, mn, mx, amax, nonfinite);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -338,19 +345,25 @@ static int fq_int(const void* x, int dtype, int64_t rows, int64_t cols, int bits
   if (st) return st;
   if (rows < 0 || cols < 0) return OR_ERR_INVALID;
   int64_t n = rows * cols;
-  int64_t L;
+  /* unit u holds L elements: start(u) + k * stride, k < L */
+  int64_t L, stride = 1, units;
   if (gran == OR_PER_TENSOR) L = n;
   else if (gran == OR_PER_ROW) L = cols;
   else if (gran == OR_PER_GROUP) {
     if (group <= 0 || cols % group != 0) return OR_ERR_INVALID;
     L = group;
+  } else if (gran == OR_PER_COLUMN) {
+    /* [QAT] per_channel_params / fake_quant_int_per_channel with axis 1:
+     * each column is a channel, calibrated from that column only */
+    L = rows;
+    stride = cols;
   } else return OR_ERR_INVALID;
   if (n == 0) return OR_OK;
   if (codes && bits == 4) memset(codes, 0, (size_t)((n + 1) / 2));
   if (mask) memset(mask, 0, (size_t)((n + 31) / 32) * 4);
-  int64_t units = n / L;
+  units = gran == OR_PER_COLUMN ? cols : n / L;
   for (int64_t u = 0; u < units; ++u) {
-    int64_t off = u * L;
+    int64_t off = gran == OR_PER_COLUMN ? u : u * L;
     float s;
     int32_t z;
     int flag = 0;
@@ -361,7 +374,7 @@ static int fq_int(const void* x, int dtype, int64_t rows, int64_t cols, int bits
     } else {
       float mn, mx, A;
       int64_t bad;
-      or_unit_stats(x, dtype, off, L, &mn, &mx, &A, &bad);
+      or_unit_stats_strided(x, dtype, off, L, stride, &mn, &mx, &A, &bad);
       if (scheme == OR_SYM) {
         z = 0;
         flag = or_params_from_absmax(A, qmax, &s);
@@ -373,7 +386,8 @@ static int fq_int(const void* x, int dtype, int64_t rows, int64_t cols, int bits
       if (zp) zp[u] = z;
     }
     if (flag && flags) *flags |= flag;
-    for (int64_t i = off; i < off + L; ++i) {
+    for (int64_t k = 0; k < L; ++k) {
+      int64_t i = off + k * stride;
       float v = load_elem(x, dtype, i);
       if (flag) {
         set_code(codes, bits, i, 0);
@@ -753,20 +767,24 @@ int or64_fake_quant_int(const void* x, int dtype, int64_t rows, int64_t cols, in
   int32_t qmin, qmax;
   int st = or_q_range(bits, scheme, &qmin, &qmax);
   if (st) return st;
-  int64_t n = rows * cols, L;
+  int64_t n = rows * cols, L, stride = 1;
   if (gran == OR_PER_TENSOR) L = n;
   else if (gran == OR_PER_ROW) L = cols;
-  else {
+  else if (gran == OR_PER_COLUMN) {
+    L = rows;
+    stride = cols;
+  } else {
     if (group <= 0 || cols % group) return OR_ERR_INVALID;
     L = group;
   }
   if (n == 0) return OR_OK;
-  for (int64_t u = 0; u < n / L; ++u) {
-    int64_t off = u * L;
+  const int64_t units = gran == OR_PER_COLUMN ? cols : n / L;
+  for (int64_t u = 0; u < units; ++u) {
+    int64_t off = gran == OR_PER_COLUMN ? u : u * L;
     double mn = INFINITY, mx = -INFINITY, A = 0.0;
     int bad = 0;
-    for (int64_t i = off; i < off + L; ++i) {
-      double v = load_elem(x, dtype, i);
+    for (int64_t k = 0; k < L; ++k) {
+      double v = load_elem(x, dtype, off + k * stride);
       if (!isfinite(v)) { bad = 1; continue; }
       if (v < mn) mn = v;
       if (v > mx) mx = v;
@@ -791,7 +809,8 @@ int or64_fake_quant_int(const void* x, int dtype, int64_t rows, int64_t cols, in
     }
     scale64[u] = s;
     zp64[u] = z;
-    for (int64_t i = off; i < off + L; ++i) {
+    for (int64_t k0 = 0; k0 < L; ++k0) {
+      const int64_t i = off + k0 * stride;
       if (dead) { y64[i] = 0.0; continue; }
       double v = load_elem(x, dtype, i);
       double k = rne64(v / s);
