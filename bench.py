@@ -329,7 +329,72 @@ def run_next_rows(args, suite, wb, peak):
     w1["l2"] = "256 MiB memset before every timed iteration"
     del flush
     return {"stochastic_rounding": out, "w1_int8_tensor_fwd_ste": w1,
-            "qat_optimizer_step": run_optimizer_rows(args, suite, peak)}
+            "qat_optimizer_step": run_optimizer_rows(args, suite, peak),
+            "per_column": run_column_rows(args, suite, peak)}
+
+
+def run_column_rows(args, suite, peak):
+    """Per-column (channel axis 1) calibrated fake quant: affine int8 and
+    symmetric int4 of the w2 weights fp32[4096, 4096] (the per-row calls'
+    shape, one scale per column instead of per row), the int8 affine call
+    with stochastic rounding, and symmetric int8 per channel of the w3
+    activations bf16[8192, 8192] (channels = the last dimension).  The
+    column statistics must see every row before the first element is mapped,
+    so x is read twice (statistics, then the map), as for per-tensor
+    calibration; algorithmic bytes count both reads.  A 256 MiB L2 flush
+    precedes every timed call (CUDA events on the launching stream)."""
+    fq, o, fl = suite.fq, suite.o, suite.flags
+    r2, c2 = suite.r2, suite.c2
+    dev = suite.x1.device
+    n2, n3 = r2 * c2, suite.n[2]
+    side3 = int(round(n3 ** 0.5))
+    m = lambda n: (n + 31) // 32 * 4  # noqa: E731
+    ws = torch.empty(max(fq.qat_workspace_bytes(r2, c2, 3, 0),
+                         fq.qat_workspace_bytes(side3, side3, 3, 0)), dtype=torch.uint8,
+                     device=dev)
+    c3 = torch.empty(n3, dtype=torch.int8, device=dev)
+    s3 = torch.empty(side3, dtype=torch.float32, device=dev)
+    sc = torch.empty(c2, dtype=torch.float32, device=dev)  # one scale / zero point per column
+    zc = torch.empty(c2, dtype=torch.int32, device=dev)
+    rows = [
+        ("w2_affine_int8_col", n2 * (4 + 4 + 4 + 1) + m(n2) + c2 * 8,
+         lambda: fq.qat_fake_quant_int(suite.w2, r2, c2, 8, 1, 3, 0, False, sc, zc,
+                                       o["y2a"], o["c2a"], o["m2a"], fl, ws)),
+        ("w2_sym_int4_col", n2 * (4 + 4 + 4) + (n2 + 1) // 2 + m(n2) + c2 * 4,
+         lambda: fq.qat_fake_quant_int(suite.w2, r2, c2, 4, 0, 3, 0, False, sc, None,
+                                       o["y2b"], o["c2b"], o["m2b"], fl, ws)),
+        ("w2_affine_int8_col_sr", n2 * (4 + 4 + 4 + 1) + m(n2) + c2 * 8,
+         lambda: fq.qat_fake_quant_int_sr(suite.w2, r2, c2, 8, 1, 3, 0, False, sc, zc, 0x5EED,
+                                          0, o["y2a"], o["c2a"], o["m2a"], fl, ws)),
+        ("w3_sym_int8_col_bf16", n3 * (2 + 2 + 2 + 1) + m(n3) + side3 * 4,
+         lambda: fq.qat_fake_quant_int(suite.a3, side3, side3, 8, 0, 3, 0, False, s3, None,
+                                       o["y3a"], c3, o["m3a"], fl, ws)),
+    ]
+    if side3 * side3 != n3:  # a reduced profiling workload that is not square
+        rows.pop()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 100))
+    out = {}
+    for name, b, call in rows:
+        for _ in range(3):
+            call()
+        t = []
+        for _ in range(steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            z = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            z.record(stream)
+            t.append((a, z))
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(z) for a, z in t) / len(t)
+        out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(b / (ms * 1e-3) / 1e9, 1),
+                     "frac_of_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peak, 4),
+                     "bytes": b, "launches": 3}
+    del flush
+    return out
 
 
 def run_optimizer_rows(args, suite, peak, n=1 << 26):

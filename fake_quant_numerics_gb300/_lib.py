@@ -27,7 +27,7 @@ FLAG_BAD_PARAMS = 4
 FLAG_NONFINITE_INPUT = 8
 F32, BF16 = 0, 1
 SYMMETRIC, AFFINE = 0, 1
-PER_TENSOR, PER_ROW, PER_GROUP = 0, 1, 2
+PER_TENSOR, PER_ROW, PER_GROUP, PER_COLUMN = 0, 1, 2, 3
 E4M3, E5M2 = 0, 1
 
 _lib = None

@@ -21,14 +21,16 @@ import torch
 
 from . import _lib
 from ._lib import (AFFINE, BF16, E4M3, E5M2, F32, FLAG_BAD_PARAMS, FLAG_DEGENERATE,
-                   FLAG_NONFINITE_CALIB, PER_GROUP, PER_ROW, PER_TENSOR, SYMMETRIC, QatError)
+                   FLAG_NONFINITE_CALIB, PER_COLUMN, PER_GROUP, PER_ROW, PER_TENSOR, SYMMETRIC,
+                   QatError)
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 _SCHEME = {"symmetric": SYMMETRIC, "sym": SYMMETRIC, "affine": AFFINE,
            SYMMETRIC: SYMMETRIC, AFFINE: AFFINE}
 _GRAN = {"tensor": PER_TENSOR, "per_tensor": PER_TENSOR, "row": PER_ROW, "per_row": PER_ROW,
-         "channel": PER_ROW, "group": PER_GROUP, "per_group": PER_GROUP,
-         PER_TENSOR: PER_TENSOR, PER_ROW: PER_ROW, PER_GROUP: PER_GROUP}
+         "channel": PER_ROW, "group": PER_GROUP, "per_group": PER_GROUP, "column": PER_COLUMN,
+         "per_column": PER_COLUMN, PER_TENSOR: PER_TENSOR, PER_ROW: PER_ROW, PER_GROUP: PER_GROUP,
+         PER_COLUMN: PER_COLUMN}
 _FMT = {"e4m3": E4M3, "E4M3": E4M3, "e5m2": E5M2, "E5M2": E5M2, E4M3: E4M3, E5M2: E5M2}
 ERROR_FLAGS = FLAG_NONFINITE_CALIB | FLAG_DEGENERATE | FLAG_BAD_PARAMS
 
@@ -178,6 +180,8 @@ def n_units(rows: int, cols: int, granularity, group: int = 0) -> int:
         return 1
     if g == PER_ROW:
         return rows
+    if g == PER_COLUMN:
+        return cols
     return rows * cols // group
 
 
@@ -233,7 +237,8 @@ def fake_quant_int(x: torch.Tensor, bits: int = 8, scheme="symmetric", granulari
                    want_mask: bool = True, check: bool = False, rounding: str = "nearest",
                    seed: int = 0, offset: int = 0) -> FakeQuantInt:
     """Integer fake quantization of x (float32 or bfloat16, CUDA), calibrated per
-    tensor / row / group, or with the given per-unit scale and zero point.
+    tensor / row / group / column (of the last dimension), or with the given
+    per-unit scale and zero point.
     rounding="stochastic" rounds with the counter-based draws of (seed, offset)."""
     x = _ready(x)
     rows, cols = _shape2d(x)

@@ -19,10 +19,10 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqat.so")
 
 SOURCES = ["qat_abi.cu", "kernels_tensor.cu", "kernels_fused.cu", "kernels_fp8.cu",
-           "kernels_misc.cu", "kernels_optim.cu", "qat_noalloc.cu"]
+           "kernels_misc.cu", "kernels_optim.cu", "kernels_cols.cu", "qat_noalloc.cu"]
 # sources compiled a second time with QAT_SR=1: their stochastic-rounding
 # kernels and *_sr launchers (object <name>_sr.o)
-SR_SOURCES = ["kernels_tensor.cu", "kernels_fused.cu", "kernels_fp8.cu"]
+SR_SOURCES = ["kernels_tensor.cu", "kernels_fused.cu", "kernels_fp8.cu", "kernels_cols.cu"]
 HEADERS = ["qat_device.cuh", "qat_launch.h", "qat_sr.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-fmad=false",

@@ -196,12 +196,14 @@ __global__ void __maxnreg__(SR ? 128 : 80) k_int_tensor(const void* __restrict__
 }
 
 // ---------------------------------------------------------------------------
-// integer fake quant with per-unit parameter arrays, unit = element / L
-// (given per-row / per-group parameters, and the calibrated fallback for unit
-// lengths the fused kernels do not cover)
+// integer fake quant with per-unit parameter arrays, unit = element / L, or
+// element % ucols for per-column units (ucols > 0): given per-row, per-group
+// and per-column parameters, and the calibrated fallback for unit shapes the
+// fused and column kernels do not cover
 // ---------------------------------------------------------------------------
 template <typename T, int BITS, bool AFFINE, bool GIVEN, bool SR>
 __global__ void __maxnreg__(SR ? 128 : 80) k_int_units(const void* __restrict__ x, int64_t n, int64_t L,
+                                                   int64_t ucols,
                                                    const float* __restrict__ scale,
                                                    const int32_t* __restrict__ zp,
                                                    const uint8_t* __restrict__ dead, SrCtx sr,
@@ -247,7 +249,7 @@ __global__ void __maxnreg__(SR ? 128 : 80) k_int_units(const void* __restrict__ 
         float yv = 0.0f;
         uint32_t m = 0u;
         if (e < cnt) {
-          int64_t u = (base + e) / L;
+          int64_t u = ucols > 0 ? (base + e) % ucols : (base + e) / L;
           if (u != cur) {
             cur = u;
             if (GIVEN) {
@@ -411,24 +413,26 @@ qat_status QAT_SR_NAME(launch_int_tensor)(qat_dtype dt, int bits, bool affine, b
 }
 
 template <typename T, int BITS, bool AFFINE>
-static void int_units_t(bool given, const void* x, int64_t n, int64_t L, const float* scale,
+static void int_units_t(bool given, const void* x, int64_t n, int64_t L, int64_t ucols,
+                        const float* scale,
                         const int32_t* zp, const uint8_t* dead, const SrCtx& sr, void* y,
                         void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
   const int grid = map_grid(n, 8);
   if (given)
     k_int_units<T, BITS, AFFINE, true, QAT_SR>
-        <<<grid, 256, 0, s>>>(x, n, L, scale, zp, dead, sr, y, codes, mask, flags);
+        <<<grid, 256, 0, s>>>(x, n, L, ucols, scale, zp, dead, sr, y, codes, mask, flags);
   else
     k_int_units<T, BITS, AFFINE, false, QAT_SR>
-        <<<grid, 256, 0, s>>>(x, n, L, scale, zp, dead, sr, y, codes, mask, flags);
+        <<<grid, 256, 0, s>>>(x, n, L, ucols, scale, zp, dead, sr, y, codes, mask, flags);
 }
 
 qat_status QAT_SR_NAME(launch_int_units)(qat_dtype dt, int bits, bool affine, bool given,
-                                         const void* x, int64_t n, int64_t L, const float* scale,
+                                         const void* x, int64_t n, int64_t L, int64_t ucols,
+                                         const float* scale,
                                          const int32_t* zp, const uint8_t* dead, const SrCtx& sr,
                                          void* y, void* codes, uint32_t* mask, int32_t* flags,
                                          cudaStream_t s) {
-#define QAT_IU(T, B, A) int_units_t<T, B, A>(given, x, n, L, scale, zp, dead, sr, y, codes, mask, flags, s)
+#define QAT_IU(T, B, A) int_units_t<T, B, A>(given, x, n, L, ucols, scale, zp, dead, sr, y, codes, mask, flags, s)
   if (dt == QAT_F32) {
     if (bits == 8) { if (affine) QAT_IU(F32, 8, true); else QAT_IU(F32, 8, false); }
     else { if (affine) QAT_IU(F32, 4, true); else QAT_IU(F32, 4, false); }

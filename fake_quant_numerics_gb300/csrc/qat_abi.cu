@@ -52,14 +52,29 @@ bool elems(int64_t rows, int64_t cols, int64_t* n) {
   return true;
 }
 
+// Longest row of a per-column call: the column kernels' grids take one
+// block per 128 (statistics, map) or 256 (set-up) columns in x.
+constexpr int64_t kMaxColumns = INT64_C(1) << 36;
+
 size_t ws_bytes_for(int64_t rows, int64_t cols, qat_granularity g, int64_t group) {
   if (g == QAT_PER_TENSOR) return (size_t)kMaxPartials * sizeof(uint4);
   int64_t n;
   if (!elems(rows, cols, &n)) return 0;
+  const auto r16 = [](int64_t b) { return (b + 15) / 16 * 16; };
+  if (g == QAT_PER_COLUMN) return (size_t)(cols * 16 + r16(cols) + r16(cols * 4));
   int64_t units = 0;
   if (g == QAT_PER_ROW) units = rows;
   else if (g == QAT_PER_GROUP && group > 0) units = n / group;
-  return (size_t)((units + 15) / 16 * 16);
+  return (size_t)(r16(units) + r16(units * 4));
+}
+
+// The fallback's per-unit arrays inside the workspace: the dead bytes, then
+// the zero points (used when the caller passes no zero-point array).
+static uint8_t* ws_dead(void* ws, int64_t rows, int64_t cols, qat_granularity g) {
+  return static_cast<uint8_t*>(ws) + (g == QAT_PER_COLUMN ? cols * 16 : 0);
+}
+static int32_t* ws_zp(void* ws, int64_t rows, int64_t cols, qat_granularity g, int64_t units) {
+  return reinterpret_cast<int32_t*>(ws_dead(ws, rows, cols, g) + (units + 15) / 16 * 16);
 }
 
 // Unit length and count of a granularity; false on an invalid combination.
@@ -80,6 +95,11 @@ bool unit_shape(int64_t rows, int64_t cols, qat_granularity g, int64_t group, in
     if (group <= 0 || cols % group != 0) return false;
     *L = group;
     *units = n / group;
+    return true;
+  }
+  if (g == QAT_PER_COLUMN) {
+    *L = rows;
+    *units = n > 0 ? cols : 0;
     return true;
   }
   return false;
@@ -129,6 +149,14 @@ qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t 
     if (st) return st;
     return launch_stats_finalize(ws, grid, absmax, minv, maxv, flags, s);
   }
+  if (g == QAT_PER_COLUMN) {
+    if (cols > kMaxColumns) return QAT_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
+    if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+    qat_status st = launch_col_stats(dtype, x, rows, cols, kMMKeys, ws, s);
+    if (st) return st;
+    return launch_col_finalize(ws, cols, absmax, minv, maxv, flags, s);
+  }
   if (fused_units_supported(dtype, L))
     return launch_int_fused(dtype, 8, false, true, x, units, L, nullptr, nullptr, absmax, minv, maxv,
                             SrCtx{}, nullptr, nullptr, nullptr, flags, s);
@@ -152,6 +180,7 @@ static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t ro
   if (!elems(rows, cols, &n)) return QAT_ERR_INVALID_ARGUMENT;
   if (!unit_shape(rows, cols, g, group, &L, &units)) return QAT_ERR_INVALID_ARGUMENT;
   if (n == 0) return QAT_OK;
+  if (g == QAT_PER_COLUMN && cols > kMaxColumns) return QAT_ERR_UNSUPPORTED;
   if (!x || !scale) return QAT_ERR_INVALID_ARGUMENT;
   if (params_given && affine && !zp) return QAT_ERR_INVALID_ARGUMENT;
   if (!aligned(x, kAlignVec) || (y && !aligned(y, kAlignVec)) ||
@@ -175,21 +204,38 @@ static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t ro
     return map_tensor(dtype, bits, affine, false, x, n, ws, grid, scale, zp, c, y, codes, mask,
                       flags, s);
   }
+  const bool col = g == QAT_PER_COLUMN;
+  const int64_t ucols = col ? cols : 0;
   if (params_given)
-    return map_units(dtype, bits, affine, true, x, n, L, scale, zp, nullptr, c, y, codes, mask,
-                     flags, s);
-  if (fused_units_supported(dtype, L))
+    return map_units(dtype, bits, affine, true, x, n, L, ucols, scale, zp, nullptr, c, y, codes,
+                     mask, flags, s);
+  if (!col && fused_units_supported(dtype, L))
     return map_fused(dtype, bits, affine, false, x, units, L, scale, zp, nullptr, nullptr, nullptr,
                      c, y, codes, mask, flags, s);
-  // fallback: calibrate every unit (warp per unit), then the flat map
   if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
   if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
-  uint8_t* dead = static_cast<uint8_t*>(ws);
-  qat_status st = launch_unit_generic(dtype, 1, bits, affine, x, units, L, nullptr, nullptr, nullptr,
-                                      scale, zp, dead, flags, s);
+  qat_status st;
+  if (col) {
+    // column statistics, then the strip map (whole mask words per warp row)
+    st = launch_col_stats(dtype, x, rows, cols, affine ? kMMKeys : kMMNone, ws, s);
+    if (st) return st;
+    if (cols % 32 == 0) {
+      auto map_cols = sr ? launch_int_cols_sr : launch_int_cols;
+      return map_cols(dtype, bits, affine, x, rows, cols, ws, scale, zp, c, y, codes, mask, flags,
+                      s);
+    }
+  }
+  // fallback: calibrate every unit, then the flat map with per-unit arrays
+  uint8_t* dead = ws_dead(ws, rows, cols, g);
+  int32_t* zpu = (affine && !zp) ? ws_zp(ws, rows, cols, g, units) : zp;
+  if (col)
+    st = launch_col_params(bits, affine, ws, cols, scale, zpu, dead, flags, s);
+  else
+    st = launch_unit_generic(dtype, 1, bits, affine, x, units, L, nullptr, nullptr, nullptr, scale,
+                             zpu, dead, flags, s);
   if (st) return st;
-  return map_units(dtype, bits, affine, false, x, n, L, scale, zp, dead, c, y, codes, mask, flags,
-                   s);
+  return map_units(dtype, bits, affine, false, x, n, L, ucols, scale, zpu, dead, c, y, codes, mask,
+                   flags, s);
 }
 
 qat_status qat_fake_quant_int(const void* x, qat_dtype dtype, int64_t rows, int64_t cols, int bits,

@@ -40,10 +40,11 @@ qat_status launch_stats_finalize(const void* ws, int nparts, float* absmax, floa
 QAT_DECL_INT_TENSOR(launch_int_tensor);
 QAT_DECL_INT_TENSOR(launch_int_tensor_sr);
 
-// integer fake quant with per-unit parameter arrays (unit = i / L)
+// integer fake quant with per-unit parameter arrays (unit = i / L, or
+// i % ucols for per-column units when ucols > 0)
 #define QAT_DECL_INT_UNITS(name)                                                                \
   qat_status name(qat_dtype dt, int bits, bool affine, bool given, const void* x, int64_t n,    \
-                  int64_t L, const float* scale, const int32_t* zp, const uint8_t* dead,        \
+                  int64_t L, int64_t ucols, const float* scale, const int32_t* zp, const uint8_t* dead,        \
                   const SrCtx& sr, void* y, void* codes, uint32_t* mask, int32_t* flags,        \
                   cudaStream_t s)
 QAT_DECL_INT_UNITS(launch_int_units);
@@ -67,6 +68,25 @@ bool fused_units_supported(qat_dtype dt, int64_t L);
                   uint32_t* mask, int32_t* flags, cudaStream_t s)
 QAT_DECL_INT_FUSED(launch_int_fused);
 QAT_DECL_INT_FUSED(launch_int_fused_sr);  // stats_only unsupported
+
+// per-column units of a row-major [rows, cols] tensor (workspace: one uint4
+// accumulator per column, then, for the unit-kernel fallback, one dead byte
+// per column).  launch_col_stats initialises and fills the accumulators
+// (mm: kMMNone or kMMKeys); launch_col_finalize writes absmax / min / max;
+// launch_col_params writes scale, zero point and the dead bytes.
+qat_status launch_col_stats(qat_dtype dt, const void* x, int64_t rows, int64_t cols, int mm,
+                            void* ws, cudaStream_t s);
+qat_status launch_col_finalize(const void* ws, int64_t cols, float* absmax, float* minv,
+                               float* maxv, int32_t* flags, cudaStream_t s);
+qat_status launch_col_params(int bits, bool affine, const void* ws, int64_t cols, float* scale,
+                             int32_t* zp, uint8_t* dead, int32_t* flags, cudaStream_t s);
+// the calibrated per-column map from the accumulators (cols % 32 == 0)
+#define QAT_DECL_INT_COLS(name)                                                                 \
+  qat_status name(qat_dtype dt, int bits, bool affine, const void* x, int64_t rows,             \
+                  int64_t cols, const void* ws, float* scale, int32_t* zp, const SrCtx& sr,     \
+                  void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s)
+QAT_DECL_INT_COLS(launch_int_cols);
+QAT_DECL_INT_COLS(launch_int_cols_sr);
 
 // FP8
 #define QAT_DECL_FP8_TENSOR(name)                                                               \

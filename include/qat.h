@@ -90,7 +90,20 @@ typedef enum {
 
 typedef enum { QAT_F32 = 0, QAT_BF16 = 1 } qat_dtype;
 typedef enum { QAT_SYMMETRIC = 0, QAT_AFFINE = 1 } qat_scheme;
-typedef enum { QAT_PER_TENSOR = 0, QAT_PER_ROW = 1, QAT_PER_GROUP = 2 } qat_granularity;
+/*
+ * Units of one parameter set in a row-major [rows, cols] tensor: the whole
+ * tensor; each row (cols elements, [QAT] per_channel_params with the channel
+ * axis first); consecutive groups of `group` elements inside a row; each
+ * column (rows elements at stride cols, [QAT] per_channel_params /
+ * fake_quant_int_per_channel with the channel axis 1; rows up to 2^36
+ * elements long, QAT_ERR_UNSUPPORTED beyond).
+ */
+typedef enum {
+  QAT_PER_TENSOR = 0,
+  QAT_PER_ROW = 1,
+  QAT_PER_GROUP = 2,
+  QAT_PER_COLUMN = 3
+} qat_granularity;
 typedef enum { QAT_E4M3 = 0, QAT_E5M2 = 1 } qat_fp8_format;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -98,11 +111,14 @@ const char* qat_status_string(qat_status status);
 
 /*
  * Bytes of device workspace a call may need: per tensor, the cross-block
- * partial statistics (16 KiB); per row / per group, one byte per unit
- * (rounded up to 16), used only by the fallback for unit lengths the fused
- * single-pass kernels do not cover.  The workspace is scratch: its contents on
- * entry do not matter and are overwritten.  Two calls that use the same
- * workspace must be ordered on one stream.
+ * partial statistics (16 KiB); per row / per group, five bytes per unit
+ * (a dead byte and a zero point, each array rounded up to 16 bytes), used
+ * only by the fallback for unit lengths the fused single-pass kernels do not
+ * cover; per column, 21 bytes per column (a 16-byte statistics accumulator,
+ * then the fallback's dead byte and zero point), used by every calibrated
+ * call.  The workspace is scratch: its contents on entry do not matter and
+ * are overwritten.  Two calls that use the same workspace must be ordered on
+ * one stream.
  */
 size_t qat_workspace_bytes(int64_t rows, int64_t cols, qat_granularity granularity, int64_t group);
 
@@ -113,7 +129,7 @@ size_t qat_workspace_bytes(int64_t rows, int64_t cols, qat_granularity granulari
  * without finite elements gives absmax 0, minv +inf, maxv -inf.  Outputs are
  * float[units], each nullable.  Any NaN/Inf sets QAT_FLAG_NONFINITE_INPUT.
  * workspace: qat_workspace_bytes(rows, cols, granularity, group) bytes
- * (per tensor only).
+ * (per tensor and per column only).
  */
 qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t cols,
                           qat_granularity granularity, int64_t group, float* absmax, float* minv,

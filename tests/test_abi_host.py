@@ -41,9 +41,14 @@ def test_status_strings(lib):
 
 def test_workspace_bytes(lib):
     assert lib.qat_workspace_bytes(1, 1 << 20, L.PER_TENSOR, 0) == 1024 * 16
-    assert lib.qat_workspace_bytes(4096, 4096, L.PER_ROW, 0) == 4096
-    assert lib.qat_workspace_bytes(14336, 4096, L.PER_GROUP, 128) == 14336 * 32
-    assert lib.qat_workspace_bytes(3, 5, L.PER_ROW, 0) == 16
+    # per unit of the fallback: a dead byte and a zero point, each array
+    # rounded up to 16 bytes
+    assert lib.qat_workspace_bytes(4096, 4096, L.PER_ROW, 0) == 4096 * 5
+    assert lib.qat_workspace_bytes(14336, 4096, L.PER_GROUP, 128) == 14336 * 32 * 5
+    assert lib.qat_workspace_bytes(3, 5, L.PER_ROW, 0) == 16 + 16
+    # per column: a 16-byte accumulator per column, then the fallback's arrays
+    assert lib.qat_workspace_bytes(4096, 4096, L.PER_COLUMN, 0) == 4096 * 21
+    assert lib.qat_workspace_bytes(7, 33, L.PER_COLUMN, 0) == 33 * 16 + 48 + 144
 
 
 def _int(lib, **kw):
@@ -75,6 +80,9 @@ def test_int_argument_errors(lib):
     assert _int(lib, ws=A, wsb=100) == L.QAT_ERR_WORKSPACE
     # a unit length the fused kernels do not cover needs the fallback workspace
     assert _int(lib, gran=L.PER_ROW, cols=40, ws=None) == L.QAT_ERR_WORKSPACE
+    # calibrated columns always take the column statistics workspace
+    assert _int(lib, gran=L.PER_COLUMN, ws=None) == L.QAT_ERR_WORKSPACE
+    assert _int(lib, gran=L.PER_COLUMN, ws=A, wsb=64 * 21 - 1) == L.QAT_ERR_WORKSPACE
     # empty tensors are a no-op even with NULL buffers
     assert _int(lib, rows=0, x=None, scale=None) == L.QAT_OK
     assert _int(lib, cols=0, x=None, scale=None) == L.QAT_OK
@@ -110,3 +118,4 @@ def test_stats_argument_errors(lib):
     assert f(None, L.F32, 4, 4, L.PER_ROW, 0, None, None, None, None, None, 0, None) == L.QAT_ERR_INVALID_ARGUMENT
     assert f(A, L.F32, 4, 6, L.PER_GROUP, 4, None, None, None, None, None, 0, None) == L.QAT_ERR_INVALID_ARGUMENT
     assert f(MIS, L.F32, 4, 4, L.PER_ROW, 0, None, None, None, None, None, 0, None) == L.QAT_ERR_MISALIGNED
+    assert f(A, L.F32, 4, 4, L.PER_COLUMN, 0, None, None, None, None, None, 0, None) == L.QAT_ERR_WORKSPACE
