@@ -25,6 +25,7 @@ FLAG_NONFINITE_CALIB = 1
 FLAG_DEGENERATE = 2
 FLAG_BAD_PARAMS = 4
 FLAG_NONFINITE_INPUT = 8
+FLAG_DEVICE_TIMEOUT = 16
 F32, BF16 = 0, 1
 SYMMETRIC, AFFINE = 0, 1
 PER_TENSOR, PER_ROW, PER_GROUP, PER_COLUMN = 0, 1, 2, 3

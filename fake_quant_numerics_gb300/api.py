@@ -21,7 +21,7 @@ import torch
 
 from . import _lib
 from ._lib import (AFFINE, BF16, E4M3, E5M2, F32, FLAG_BAD_PARAMS, FLAG_DEGENERATE,
-                   FLAG_NONFINITE_CALIB, PER_COLUMN, PER_GROUP, PER_ROW, PER_TENSOR, SYMMETRIC,
+                   FLAG_DEVICE_TIMEOUT, FLAG_NONFINITE_CALIB, PER_COLUMN, PER_GROUP, PER_ROW, PER_TENSOR, SYMMETRIC,
                    QatError)
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
@@ -186,8 +186,11 @@ def n_units(rows: int, cols: int, granularity, group: int = 0) -> int:
 
 
 def raise_on_flags(flags: torch.Tensor, what: str = "fake quant"):
-    """Synchronise on the flag word and raise QatDataError for error flags."""
+    """Synchronise on the flag word and raise QatDataError for error flags
+    (QatError for a device-side wait that ran out)."""
     f = int(flags.item())
+    if f & FLAG_DEVICE_TIMEOUT:
+        raise QatError(what, _lib.QAT_ERR_CUDA)
     if f & ERROR_FLAGS:
         parts = []
         if f & FLAG_NONFINITE_CALIB:

@@ -6,163 +6,219 @@
 // absmax (symmetric) or min / max (affine) exactly as a row is.
 //
 // A column's statistics need every row before its first element can be
-// mapped, so the calibrated path is two passes over x:
-//   k_col_init   the per-column accumulators (16 bytes per column)
-//   k_col_stats  a block takes a strip of 128 columns and a chunk of rows;
-//                each lane folds 4 consecutive columns down its rows, the
-//                block merges its 8 warps in shared memory and combines into
-//                the accumulators with integer atomics (the absmax bits and
-//                order keys are monotone as unsigned integers)
-//   k_int_cols   the same strips: the block calibrates its 128 columns into
-//                shared memory, each lane keeps the parameters of its 4
-//                columns in registers and maps its rows
-// The second read of x hits L2 when the tensor fits in it.  Shapes whose
-// row length is not a multiple of 32 (mask words would straddle rows) and
-// given parameters take the per-element unit kernel in column mode.
+// mapped, so the calibrated path is two passes over x.  In both kernels a
+// lane takes 16 bytes of a row (4 fp32 or 8 bf16 columns), a warp a strip of
+// 32 lanes, and the 8 warps of a block sit side by side (up to 8 strips, so
+// the block reads up to 4 KiB of each row) and walk the rows of their chunk,
+// each keeping loads of 4 rows in flight.
+//   k_col_init   zeroes the per-column accumulators and the strip counters
+//   k_col_stats  folds the chunk into per-column partials and combines the
+//                block's partial into the accumulators with integer atomics
+//                (absmax bits and order keys are monotone as unsigned
+//                integers); the last block of a strip to finish (a counter per
+//                strip) calibrates the strip's columns: scale, zero point,
+//                the dead flag and the 32-byte parameter record of each column
+//   k_int_cols   each lane loads the records of its columns into registers
+//                once and maps the rows of its chunk
+// Row lengths that are not a multiple of 32 (mask words would straddle rows)
+// and given parameters take the per-element unit kernel in column mode.
+#include <atomic>
+
 #include "qat_device.cuh"
 #include "qat_launch.h"
 
 namespace qat {
 
-constexpr int kColStrip = 128;  // columns per block strip (4 per lane)
-constexpr int kColWarps = 8;    // warps per block, one row each at a time
-
-// four consecutive elements of one row as fp32 bits; scalar loads when the
-// row length is not a multiple of 4 (unaligned rows) or at the row's end
+constexpr int kColWarps = 8;    // warps per block, interleaved along rows
+// columns per lane (16 bytes of a row) and per warp strip
 template <typename T>
-__device__ __forceinline__ void load4(const void* x, int64_t i, int have, bool vec,
-                                      uint32_t (&b)[4]) {
-  if (vec && have >= 4) {
-    if (T::BYTES == 4) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(x) + i));
-      b[0] = v.x;
-      b[1] = v.y;
-      b[2] = v.z;
-      b[3] = v.w;
-    } else {
-      const uint2 v = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(x) + i));
-      b[0] = v.x << 16;
-      b[1] = v.x & 0xffff0000u;
-      b[2] = v.y << 16;
-      b[3] = v.y & 0xffff0000u;
-    }
-    return;
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) b[j] = j < have ? load_elem_bits<T>(x, i + j) : 0u;
-}
+constexpr int kColLane = 16 / T::BYTES;
+template <typename T>
+constexpr int kColStrip = 32 * kColLane<T>;
 
-#if !QAT_SR
-__global__ void k_col_init(uint4* __restrict__ acc, int64_t cols) {
-  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (c < cols) acc[c] = make_uint4(0u, 0u, kKeyPosInf, kKeyNegInf);
-}
-
-// MM: kMMNone (absmax and the non-finite bit) or kMMKeys (also min / max)
-template <typename T, int MM>
-__global__ void __launch_bounds__(256) k_col_stats(const void* __restrict__ x, int64_t rows,
-                                                   int64_t cols, int64_t rchunk,
-                                                   uint4* __restrict__ acc) {
-  __shared__ uint4 red[kColWarps][kColStrip];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t c = (int64_t)blockIdx.x * kColStrip + lane * 4;
-  const bool vec = (cols & 3) == 0;
-  const int have = c < cols ? (cols - c >= 4 ? 4 : (int)(cols - c)) : 0;
-  Stats st[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) st[j].init<MM>();
-  const int64_t r0 = (int64_t)blockIdx.y * rchunk;
-  const int64_t r1 = min(rows, r0 + rchunk);
-  if (have > 0) {
-    // four rows per step, their loads issued before the folds
-    for (int64_t r = r0 + warp; r < r1; r += 4 * kColWarps) {
-      uint32_t b[4][4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int64_t rk = r + k * kColWarps;
-        if (rk < r1) load4<T>(x, rk * cols + c, have, vec, b[k]);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (r + k * kColWarps < r1) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (j < have) st[j].add<MM>(b[k][j]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) red[warp][lane * 4 + j] = st[j].pack();
-  __syncthreads();
-  if (threadIdx.x < kColStrip) {
-    const int64_t col = (int64_t)blockIdx.x * kColStrip + threadIdx.x;
-    if (col < cols) {
-      Stats s;
-      s.unpack(red[0][threadIdx.x]);
-#pragma unroll
-      for (int w = 1; w < kColWarps; ++w) {
-        Stats o;
-        o.unpack(red[w][threadIdx.x]);
-        s.merge<MM>(o);
-      }
-      uint32_t* a = reinterpret_cast<uint32_t*>(acc + col);
-      atomicMax(a + 0, s.amax);
-      if (s.nonfinite) atomicOr(a + 1, 1u);
-      if (MM == kMMKeys) {
-        atomicMin(a + 2, s.kmin);
-        atomicMax(a + 3, s.kmax);
-      }
-    }
-  }
-}
-
-// accumulators -> per-column absmax / min / max and the non-finite flag
-__global__ void k_col_finalize(const uint4* __restrict__ acc, int64_t cols, float* absmax,
-                               float* minv, float* maxv, int32_t* flags) {
-  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  int f = 0;
-  if (c < cols) {
-    Stats s;
-    s.unpack(acc[c]);
-    if (absmax) absmax[c] = s.absmax_f();
-    if (minv) minv[c] = s.min_f<kMMKeys>();
-    if (maxv) maxv[c] = s.max_f<kMMKeys>();
-    f = s.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0;
-  }
-  warp_flag_or(flags, f);
-}
-
-// accumulators -> scale, zero point and the dead byte of every column (the
-// unit-kernel fallback)
-template <int BITS, bool AFFINE>
-__global__ void k_col_params(const uint4* __restrict__ acc, int64_t cols, float* scale,
-                             int32_t* zp, uint8_t* dead, int32_t* flags) {
-  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  int f = 0;
-  if (c < cols) {
-    Stats s;
-    s.unpack(acc[c]);
-    IntParams p;
-    f = calibrate<BITS, AFFINE, kMMKeys>(s, p);
-    scale[c] = p.s;
-    if (zp) zp[c] = p.zp;
-    dead[c] = (uint8_t)p.dead;
-  }
-  warp_flag_or(flags, f);
-}
-#endif  // !QAT_SR
-
-// ---------------------------------------------------------------------------
-// the calibrated per-column map
-// ---------------------------------------------------------------------------
-// The parameters of one column as the map keeps them (32 bytes in shared
-// memory): wlo is stored as -0 when it is zero (the window test below).
+// The parameters of one column as the map keeps them (a 32-byte record in
+// the workspace): wlo is stored as -0 when it is zero (the window test).
 struct ColP {
   float s, rcp, wlo, whi, klof, khif;
   int zp;
   int st;  // bit 0 dead, bit 1 fast (scale in the reciprocal's safe range)
 };
+static_assert(sizeof(ColP) == kColRecordBytes, "column record size");
+
+// Grid of both column kernels: `wc` warp strips side by side in a block (a
+// power of two up to 8; the other 8 / wc warps interleave along rows), so a
+// block covers wc * ws columns of every row it reads; strips of that width
+// along x, chunks of `rchunk` rows along y (a multiple of `mult` chunks,
+// trailing ones empty).
+struct ColShape {
+  int wc;
+  int64_t strips, chunks, rchunk;
+};
+
+static ColShape col_shape(int64_t rows, int64_t cols, int64_t ws, int per_sm, int64_t min_rows,
+                          int64_t mult) {
+  ColShape g;
+  const int64_t warps = (cols + ws - 1) / ws;
+  g.wc = 1;
+  while (g.wc < kColWarps && g.wc < warps) g.wc <<= 1;
+  const int64_t sw = ws * g.wc;
+  g.strips = (cols + sw - 1) / sw;
+  const int64_t want = ((int64_t)device_info().sms * per_sm + g.strips - 1) / g.strips;
+  const int64_t most = (rows + min_rows - 1) / min_rows;
+  int64_t chunks = want < most ? want : most;
+  if (chunks < 1) chunks = 1;
+  if (chunks > 65535 - mult) chunks = 65535 - mult;
+  g.rchunk = (rows + chunks - 1) / chunks;
+  chunks = (rows + g.rchunk - 1) / g.rchunk;
+  g.chunks = (chunks + mult - 1) / mult * mult;
+  return g;
+}
+
+// 16 bytes of one row as loaded: four fp32 or eight bf16 values
+struct Raw16 {
+  uint32_t w[4];
+};
+__device__ __forceinline__ Raw16 load_raw16(const void* p) {
+  const uint4 v = __ldg(static_cast<const uint4*>(p));
+  return Raw16{{v.x, v.y, v.z, v.w}};
+}
+// element j of a lane's columns as fp32
+template <typename T>
+__device__ __forceinline__ float raw_elem(const Raw16& r, int j) {
+  if (T::BYTES == 4) return __uint_as_float(r.w[j]);
+  const uint32_t w = r.w[j >> 1];
+  return __uint_as_float((j & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+// the lane's columns of row element offset i: one 16-byte load when the row
+// is 16-byte aligned (vec) and all `have` columns exist, else element loads
+// (absent ones read +0)
+template <typename T>
+__device__ __forceinline__ Raw16 load_lane(const void* x, int64_t i, int have, bool vec) {
+  constexpr int NC = kColLane<T>;
+  if (vec && have >= NC) return load_raw16(static_cast<const char*>(x) + i * T::BYTES);
+  Raw16 r = {{0u, 0u, 0u, 0u}};
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    if (j < have) {
+      const uint32_t b = load_elem_bits<T>(x, i + j);
+      if (T::BYTES == 4)
+        r.w[j] = b;
+      else
+        r.w[j >> 1] |= (j & 1) ? (b & 0xffff0000u) : (b >> 16);
+    }
+  }
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// staged row tiles: a block walks its chunk in tiles of `tr` rows of its
+// strip, copied into shared memory by bulk copies (cp.async.bulk, one per
+// row segment, or one per tile when the strip is the whole row) that complete
+// on a per-stage mbarrier; kColStages tiles are in flight.  Every wait is
+// bounded: when one runs out the block records QAT_FLAG_DEVICE_TIMEOUT,
+// waits (bounded) for the copies it issued and leaves.
+// ---------------------------------------------------------------------------
+constexpr int kColStageBytes = 32768;
+constexpr int kColStages = 3;
+constexpr uint32_t kColWaitLimit = 1u << 24;  // try_wait polls before giving up
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(b))
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+  for (uint32_t i = 0; i < kColWaitLimit; ++i)
+    if (mbar_try_wait(b, parity)) return true;
+  return false;
+}
+
+// The tiles of one block: rows [r0, r1) of the strip starting at column cs,
+// `segc` columns wide (whole rows when contig), `tr` rows per tile.
+struct ColTiles {
+  const char* x;
+  int64_t cols, cs, r0, r1;
+  int segc, tr, tiles, bytes_per_elem;
+  bool contig;
+  __device__ __forceinline__ uint32_t seg_bytes() const { return (uint32_t)segc * bytes_per_elem; }
+  __device__ __forceinline__ int rows_of(int t) const {
+    const int64_t left = r1 - r0 - (int64_t)t * tr;
+    return left < tr ? (int)left : tr;
+  }
+  // thread 0: the copies of tile t into stage buffer `dst`, completing on `bar`
+  __device__ __forceinline__ void issue(int t, char* dst, uint64_t* bar) const {
+    const int nr = rows_of(t);
+    const uint32_t sb = seg_bytes();
+    const int64_t rs = r0 + (int64_t)t * tr;
+    mbar_expect_tx(bar, (uint32_t)nr * sb);
+    if (contig) {
+      bulk_g2s(dst, x + rs * cols * bytes_per_elem, (uint32_t)nr * sb, bar);
+    } else {
+      for (int i = 0; i < nr; ++i)
+        bulk_g2s(dst + (size_t)i * sb, x + ((rs + i) * cols + cs) * bytes_per_elem, sb, bar);
+    }
+  }
+};
+
+// The staged walk: calls body(tile_base, tile, rows_in_tile) for every tile of the
+// block, with all threads; returns false (flag set, copies drained) when a
+// wait ran out.  The caller provides kColStages * kColStageBytes bytes of
+// dynamic shared memory at `stage` and kColStages mbarriers at `bars`.
+template <typename Body>
+__device__ __forceinline__ bool col_staged(const ColTiles& tl, char* stage, uint64_t* bars,
+                                           int32_t* flags, Body&& body) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kColStages; ++s) mbar_init(bars + s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (int s = 0; s < kColStages && s < tl.tiles; ++s)
+      tl.issue(s, stage + s * kColStageBytes, bars + s);
+  for (int t = 0; t < tl.tiles; ++t) {
+    const int s = t % kColStages;
+    const uint32_t par = (uint32_t)(t / kColStages) & 1u;
+    const bool ok = mbar_wait(bars + s, par);
+    if (ok) body(stage + s * kColStageBytes, t, tl.rows_of(t));
+    // every thread is done with stage s (or a wait ran out somewhere)
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        // drain the copies still in flight, then report
+        for (int u = t; u < tl.tiles && u < t + kColStages; ++u)
+          mbar_wait(bars + u % kColStages, (uint32_t)(u / kColStages) & 1u);
+        if (flags) atomicOr(flags, QAT_FLAG_DEVICE_TIMEOUT);
+      }
+      return false;
+    }
+    if (threadIdx.x == 0 && t + kColStages < tl.tiles) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tl.issue(t + kColStages, stage + s * kColStageBytes, bars + s);
+    }
+  }
+  return true;
+}
 
 template <int BITS, bool AFFINE>
 __device__ __forceinline__ ColP col_params(const IntParams& p) {
@@ -178,13 +234,241 @@ __device__ __forceinline__ ColP col_params(const IntParams& p) {
   return q;
 }
 
+#if !QAT_SR
+// One element into a column's statistics.  With order keys the absmax is
+// left to the finalisation (max(|min|, |max|)), so only min, max and the
+// non-finite bit are folded.
+template <int MM>
+__device__ __forceinline__ void col_add(Stats& st, uint32_t u) {
+  if (MM != kMMKeys) {
+    st.add<MM>(u);
+    return;
+  }
+  const bool fin = (u & 0x7fffffffu) < 0x7f800000u;
+  const uint32_t k = order_key(u);
+  st.nonfinite |= fin ? 0u : 1u;
+  st.kmin = min(st.kmin, fin ? k : kKeyPosInf);
+  st.kmax = max(st.kmax, fin ? k : kKeyNegInf);
+}
+
+__global__ void k_col_init(uint4* __restrict__ acc, int64_t cols, uint32_t* __restrict__ cnt,
+                           int64_t strips) {
+  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (c < cols) acc[c] = make_uint4(0u, 0u, kKeyPosInf, kKeyNegInf);
+  if (c < strips) cnt[c] = 0u;
+}
+
+// Column statistics, MODE 0: per-column absmax / min / max (finite values)
+// and the non-finite input flag.  MODE 1: integer calibration (BITS, AFFINE)
+// -> scale, zero point, dead byte and record of every column.  Symmetric
+// calibration tracks the absmax alone; otherwise the order keys of min and
+// max, from which the finite absmax is max(|min|, |max|).
+//
+// After the fold: merge the warps that share a strip (red: the block's
+// kColWarps x WW partials in shared memory), combine the block's partial of
+// each column into the accumulators, and let the last block of the strip
+// finalise its columns.
+template <typename T, int MODE, int BITS, bool AFFINE>
+__device__ __forceinline__ void col_stats_finish(const Stats (&st)[kColLane<T>], uint4* red,
+                                                 int wc, int64_t cols, uint4* __restrict__ acc,
+                                                 uint32_t* __restrict__ cnt, float* out0,
+                                                 float* out1, float* out2, int32_t* zp,
+                                                 uint8_t* dead, ColP* table, int32_t* flags,
+                                                 int* last) {
+  constexpr int MM = (MODE == 0 || AFFINE) ? kMMKeys : kMMNone;
+  constexpr int NC = kColLane<T>, WW = kColStrip<T>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nrw = kColWarps / wc;
+  const int sw = WW * wc;
+#pragma unroll
+  for (int j = 0; j < NC; ++j) red[warp * WW + lane * NC + j] = st[j].pack();
+  __syncthreads();
+  if (nrw > 1) {
+    for (int t = threadIdx.x; t < sw; t += blockDim.x) {
+      const int ts = t / WW, tl = t % WW;
+      Stats s;
+      s.unpack(red[ts * WW + tl]);
+      for (int w = 1; w < nrw; ++w) {
+        Stats o;
+        o.unpack(red[(w * wc + ts) * WW + tl]);
+        s.merge<MM>(o);
+      }
+      red[ts * WW + tl] = s.pack();
+    }
+  }
+  __syncthreads();
+  // combine the block's partial of each column into the accumulators
+  for (int t = threadIdx.x; t < sw; t += blockDim.x) {
+    const int64_t col = (int64_t)blockIdx.x * sw + t;
+    if (col < cols) {
+      Stats s;
+      s.unpack(red[t]);
+      uint32_t* a = reinterpret_cast<uint32_t*>(acc + col);
+      if (MM == kMMKeys) {
+        if (s.kmin != kKeyPosInf) atomicMin(a + 2, s.kmin);
+        if (s.kmax != kKeyNegInf) atomicMax(a + 3, s.kmax);
+      } else if (s.amax) {
+        atomicMax(a + 0, s.amax);
+      }
+      if (s.nonfinite) atomicOr(a + 1, 1u);
+    }
+  }
+  // the last block of the strip to get here finalises its columns
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) *last = atomicAdd(cnt + blockIdx.x, 1u) == gridDim.y - 1;
+  __syncthreads();
+  if (!*last) return;
+  __threadfence();
+  int f = 0;
+  for (int t = threadIdx.x; t < sw; t += blockDim.x) {
+    const int64_t col = (int64_t)blockIdx.x * sw + t;
+    if (col >= cols) break;
+    Stats s;
+    s.unpack(__ldcg(acc + col));
+    if (MM == kMMKeys) {
+      // finite absmax from the finite min and max (0 when there is none)
+      const uint32_t am = max(key_to_bits(s.kmin) & 0x7fffffffu, key_to_bits(s.kmax) & 0x7fffffffu);
+      s.amax = s.kmin <= s.kmax ? am : 0u;
+    }
+    if (MODE == 0) {
+      if (out0) out0[col] = s.absmax_f();
+      if (out1) out1[col] = s.min_f<kMMKeys>();
+      if (out2) out2[col] = s.max_f<kMMKeys>();
+      f |= s.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0;
+    } else {
+      IntParams p;
+      f |= calibrate<BITS, AFFINE, MM>(s, p);
+      out0[col] = p.s;
+      if (zp) zp[col] = p.zp;
+      dead[col] = (uint8_t)p.dead;
+      table[col] = col_params<BITS, AFFINE>(p);
+    }
+  }
+  warp_flag_or(flags, f);
+}
+
+// The statistics for any row length (element loads where a row is not
+// 16-byte aligned), the rows through registers: kColDepth loads in flight per
+// warp.
+constexpr int kColDepth = 4;
+
+template <typename T, int MODE, int BITS, bool AFFINE>
+__global__ void __launch_bounds__(256, 3)
+    k_col_stats(const void* __restrict__ x, int64_t rows, int64_t cols, int wc, int64_t rchunk,
+                uint4* __restrict__ acc, uint32_t* __restrict__ cnt, float* out0, float* out1,
+                float* out2, int32_t* zp, uint8_t* dead, ColP* table, int32_t* flags) {
+  constexpr int MM = (MODE == 0 || AFFINE) ? kMMKeys : kMMNone;
+  constexpr int NC = kColLane<T>, WW = kColStrip<T>, D = kColDepth;
+  // per warp slot and column of its strip; after the merge of the warps that
+  // share a strip, red[0 .. wc - 1] is the block's partial of its wc * WW
+  // columns, in column order
+  __shared__ uint4 red[kColWarps * WW];
+  __shared__ int last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = warp & (wc - 1), rw = warp / wc, nrw = kColWarps / wc;
+  const int sw = WW * wc;
+  const int64_t c = (int64_t)blockIdx.x * sw + sub * WW + lane * NC;
+  const bool vec = cols % NC == 0;
+  const int have = c < cols ? (cols - c >= NC ? NC : (int)(cols - c)) : 0;
+  Stats st[NC];
+#pragma unroll
+  for (int j = 0; j < NC; ++j) st[j].template init<MM>();
+  const int64_t r0 = (int64_t)blockIdx.y * rchunk + rw;
+  const int64_t r1 = min(rows, (int64_t)blockIdx.y * rchunk + rchunk);
+  const int64_t step = nrw;
+  if (have > 0) {
+    // rows r0, r0 + step, ...: D loads in flight, each row's load issued D
+    // rows ahead of its fold
+    Raw16 b[D];
+#pragma unroll
+    for (int k = 0; k < D; ++k) {
+      const int64_t rk = r0 + k * step;
+      if (rk < r1) b[k] = load_lane<T>(x, rk * cols + c, have, vec);
+    }
+    for (int64_t r = r0; r < r1; r += D * step) {
+#pragma unroll
+      for (int k = 0; k < D; ++k) {
+        const int64_t rk = r + k * step;
+        if (rk >= r1) break;
+        const Raw16 cur = b[k];
+        const int64_t rn = rk + D * step;
+        if (rn < r1) b[k] = load_lane<T>(x, rn * cols + c, have, vec);
+#pragma unroll
+        for (int j = 0; j < NC; ++j)
+          if (j < have) col_add<MM>(st[j], __float_as_uint(raw_elem<T>(cur, j)));
+      }
+    }
+  }
+  col_stats_finish<T, MODE, BITS, AFFINE>(st, red, wc, cols, acc, cnt, out0, out1, out2, zp, dead,
+                                          table, flags, &last);
+}
+
+// The same statistics for row lengths that are a multiple of 32: the rows of
+// the block's strip come in through the staged tiles (shared memory), so the
+// loads in flight do not occupy registers.
+template <typename T, int MODE, int BITS, bool AFFINE>
+__global__ void __launch_bounds__(256, 2)
+    k_col_stats_staged(const void* __restrict__ x, int64_t rows, int64_t cols, int wc,
+                       int64_t rchunk, int tr, uint4* __restrict__ acc, uint32_t* __restrict__ cnt,
+                       float* out0, float* out1, float* out2, int32_t* zp, uint8_t* dead,
+                       ColP* table, int32_t* flags) {
+  constexpr int MM = (MODE == 0 || AFFINE) ? kMMKeys : kMMNone;
+  constexpr int NC = kColLane<T>, WW = kColStrip<T>;
+  extern __shared__ __align__(128) char col_stage[];
+  __shared__ __align__(8) uint64_t bars[kColStages];
+  __shared__ int last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = warp & (wc - 1), rw = warp / wc, nrw = kColWarps / wc;
+  const int sw = WW * wc;
+  ColTiles tl;
+  tl.x = static_cast<const char*>(x);
+  tl.cols = cols;
+  tl.cs = (int64_t)blockIdx.x * sw;
+  tl.segc = (int)(cols - tl.cs < sw ? cols - tl.cs : sw);
+  tl.contig = tl.segc == cols;
+  tl.bytes_per_elem = T::BYTES;
+  tl.r0 = (int64_t)blockIdx.y * rchunk;
+  tl.r1 = min(rows, tl.r0 + rchunk);
+  tl.tr = tr;
+  tl.tiles = tl.r1 > tl.r0 ? (int)((tl.r1 - tl.r0 + tr - 1) / tr) : 0;
+  const int cl = sub * WW + lane * NC;  // the lane's first column in the strip
+  const bool active = cl < tl.segc;
+  const uint32_t sb = tl.seg_bytes();
+  Stats st[NC];
+#pragma unroll
+  for (int j = 0; j < NC; ++j) st[j].template init<MM>();
+  const bool ok = col_staged(tl, col_stage, bars, flags, [&](const char* tile, int, int nr) {
+    if (!active) return;
+    for (int r = rw; r < nr; r += nrw) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + (size_t)r * sb + cl * T::BYTES);
+      const Raw16 cur = {{v.x, v.y, v.z, v.w}};
+#pragma unroll
+      for (int j = 0; j < NC; ++j) col_add<MM>(st[j], __float_as_uint(raw_elem<T>(cur, j)));
+    }
+  });
+  if (!ok) return;
+  col_stats_finish<T, MODE, BITS, AFFINE>(st, reinterpret_cast<uint4*>(col_stage), wc, cols, acc,
+                                          cnt, out0, out1, out2, zp, dead, table, flags, &last);
+}
+#endif  // !QAT_SR
+
+// ---------------------------------------------------------------------------
+// the calibrated per-column map
+// ---------------------------------------------------------------------------
+// the fields of a record the fast path reads, held in registers per column
+struct ColR {
+  float s, rcp, wlo, whi, klof, khif;
+  int zp;
+};
+
 // The IEEE-division path of one element of a calibrated column that is dead
 // or has a scale outside the reciprocal's safe range.
 template <int BITS, bool AFFINE, bool SR>
-__device__ __forceinline__ void col_slow_elem(float x, float u, const ColP& c, float& y, int& q,
-                                              uint32_t& m) {
+__device__ __forceinline__ void col_slow_elem(float x, float u, const ColR& c, bool dead, float& y,
+                                              int& q, uint32_t& m) {
   constexpr int qmin = QRange<BITS, AFFINE>::qmin, qmax = QRange<BITS, AFFINE>::qmax;
-  if (c.st & 1) {
+  if (dead) {
     y = 0.0f;
     q = 0;
     m = 0u;
@@ -210,7 +494,7 @@ __device__ __forceinline__ void col_slow_elem(float x, float u, const ColP& c, f
 // stochastic rounding), y = k s, the code from the bits of k + M, and the
 // out-of-window sign bits (whi - |x| symmetric; whi - x, x - wlo affine).
 template <bool AFFINE, bool SR>
-__device__ __forceinline__ void col_pair(float xa, float xb, const ColP& a, const ColP& b,
+__device__ __forceinline__ void col_pair(float xa, float xb, const ColR& a, const ColR& b,
                                          float ua, float ub, float& ya, float& yb, int& qa,
                                          int& qb, uint32_t& oa, uint32_t& ob) {
   float fa, fb, ra, rb, ta, tb;
@@ -248,201 +532,242 @@ __device__ __forceinline__ void col_pair(float xa, float xb, const ColP& a, cons
   }
 }
 
-// One row of a lane's four columns: map, store y and the codes, return the
-// four mask bits (bit j = column j).
-template <typename T, int BITS, bool AFFINE, bool SR>
-__device__ __forceinline__ uint32_t col_row(const uint32_t (&b)[4], const ColP (&P)[4], bool slow,
-                                            const SrCtx& sr, int64_t i, void* y, void* codes) {
-  float u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  if (SR) sr_draws4(sr, i / 4, u);
-  float yv[4];
-  int q[4];
-  uint32_t o[4];
-#pragma unroll
-  for (int j = 0; j < 4; j += 2)
-    col_pair<AFFINE, SR>(__uint_as_float(b[j]), __uint_as_float(b[j + 1]), P[j], P[j + 1], u[j],
-                         u[j + 1], yv[j], yv[j + 1], q[j], q[j + 1], o[j], o[j + 1]);
+// One row of a lane's NC columns at element i: map, store y and the codes
+// (packed as each pair is done), return the NC mask bits (bit j = column j).
+// SLOW: columns whose bit is set in `slowm` take the IEEE path (dead ones,
+// bit set in `deadm`, give zeros).
+template <typename T, int BITS, bool AFFINE, bool SR, bool SLOW>
+__device__ __forceinline__ uint32_t col_row(const Raw16& b, const ColR (&P)[kColLane<T>],
+                                            uint32_t slowm, uint32_t deadm, const SrCtx& sr,
+                                            int64_t i, void* y, void* codes) {
+  constexpr int NC = kColLane<T>;
+  uint32_t yw[4];         // the y row as stored: 4 fp32, or 8 bf16 in pairs
+  uint32_t cw[NC / 4];    // the codes as stored
   uint32_t mb = 0u;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) mb |= (o[j] ^ 1u) << j;
-  if (slow) {
+  for (int k = 0; k < NC / 4; ++k) cw[k] = 0u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (!(P[j].st & 2)) {
-        uint32_t m;
-        col_slow_elem<BITS, AFFINE, SR>(__uint_as_float(b[j]), u[j], P[j], yv[j], q[j], m);
-        mb = (mb & ~(1u << j)) | (m << j);
+  for (int g = 0; g < NC / 4; ++g) {
+    float u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (SR) sr_draws4(sr, i / 4 + g, u);
+#pragma unroll
+    for (int h = 0; h < 4; h += 2) {
+      const int j = 4 * g + h;
+      const float xa = raw_elem<T>(b, j), xb = raw_elem<T>(b, j + 1);
+      float ya, yb;
+      int qa, qb;
+      uint32_t oa, ob;
+      col_pair<AFFINE, SR>(xa, xb, P[j], P[j + 1], u[h], u[h + 1], ya, yb, qa, qb, oa, ob);
+      uint32_t ma = oa ^ 1u, mbb = ob ^ 1u;
+      if (SLOW) {
+        if ((slowm >> j) & 1u)
+          col_slow_elem<BITS, AFFINE, SR>(xa, u[h], P[j], (deadm >> j) & 1u, ya, qa, ma);
+        if ((slowm >> (j + 1)) & 1u)
+          col_slow_elem<BITS, AFFINE, SR>(xb, u[h + 1], P[j + 1], (deadm >> (j + 1)) & 1u, yb, qb,
+                                          mbb);
       }
+      mb |= (ma << j) | (mbb << (j + 1));
+      if (T::BYTES == 4) {
+        yw[j] = __float_as_uint(ya);
+        yw[j + 1] = __float_as_uint(yb);
+      } else {
+        yw[j >> 1] = pack_bf16x2(ya, yb);
+      }
+      // int8: byte j = code j; int4: element 2m in the high nibble of byte m
+      if (BITS == 8)
+        cw[j >> 2] |= ((uint32_t)(qa & 0xff) << (8 * (j & 3))) |
+                      ((uint32_t)(qb & 0xff) << (8 * ((j + 1) & 3)));
+      else
+        cw[j >> 3] |= (((uint32_t)(qa & 0xf) << 4) | (uint32_t)(qb & 0xf)) << (8 * ((j >> 1) & 3));
     }
   }
-  if (y) {
-    if (T::BYTES == 4)
-      *reinterpret_cast<uint4*>(static_cast<float*>(y) + i) =
-          make_uint4(__float_as_uint(yv[0]), __float_as_uint(yv[1]), __float_as_uint(yv[2]),
-                     __float_as_uint(yv[3]));
-    else
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + i) =
-          make_uint2(pack_bf16x2(yv[0], yv[1]), pack_bf16x2(yv[2], yv[3]));
-  }
+  if (y) *reinterpret_cast<uint4*>(static_cast<char*>(y) + i * T::BYTES) =
+      make_uint4(yw[0], yw[1], yw[2], yw[3]);
   if (codes) {
-    if (BITS == 8)
-      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(codes) + i) =
-          (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) |
-          ((uint32_t)(q[2] & 0xff) << 16) | ((uint32_t)(q[3] & 0xff) << 24);
-    else  // element 2j in the high nibble of byte j
-      *reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(codes) + i / 2) =
-          (uint16_t)(((q[0] & 0xf) << 4) | (q[1] & 0xf) | ((q[2] & 0xf) << 12) |
-                     ((q[3] & 0xf) << 8));
+    uint8_t* p = static_cast<uint8_t*>(codes) + (BITS == 8 ? i : i / 2);
+    if (BITS == 8 && NC == 8)
+      *reinterpret_cast<uint2*>(p) = make_uint2(cw[0], cw[1]);
+    else if (BITS == 8 || NC == 8)
+      *reinterpret_cast<uint32_t*>(p) = cw[0];
+    else
+      *reinterpret_cast<uint16_t*>(p) = (uint16_t)cw[0];
   }
   return mb;
 }
 
-// Requires cols % 32 == 0: every lane's four columns are in the row and a
-// warp's 128 columns make four whole mask words.
+// The rows rw, rw + nrw, ... of one staged tile (the tile's first row is rs):
+// map, store, and assemble the mask words with shuffles (the loop is
+// warp-uniform).  Requires cols % 32 == 0: every lane's columns are in the row
+// and a warp's strip makes whole mask words.
+template <typename T, int BITS, bool AFFINE, bool SR, bool SLOW>
+__device__ __forceinline__ void col_map_tile(const char* tile, int nr, uint32_t sb, int cl, int rw,
+                                             int nrw, int64_t rs, int64_t cols, int64_t c,
+                                             bool active, const ColR (&P)[kColLane<T>],
+                                             uint32_t slowm, uint32_t deadm, const SrCtx& sr,
+                                             void* y, void* codes, uint32_t* mask, int lane) {
+  constexpr int NC = kColLane<T>, LPW = 32 / NC;  // LPW: lanes per mask word
+  for (int r = rw; r < nr; r += nrw) {
+    const int64_t i = (rs + r) * cols + c;
+    uint32_t mb = 0u;
+    if (active) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + (size_t)r * sb + cl * T::BYTES);
+      const Raw16 cur = {{v.x, v.y, v.z, v.w}};
+      mb = col_row<T, BITS, AFFINE, SR, SLOW>(cur, P, slowm, deadm, sr, i, y, codes);
+    }
+    uint32_t w = mb << (NC * (lane & (LPW - 1)));
+#pragma unroll
+    for (int o = 1; o < LPW; o <<= 1) w |= __shfl_xor_sync(kFull, w, o);
+    if (mask && active && (lane & (LPW - 1)) == 0) mask[i / 32] = w;
+  }
+}
+
+// The calibrated per-column map (cols % 32 == 0): each lane keeps the
+// records of its columns in registers; the rows of the block's strip come in
+// through the staged tiles.
 template <typename T, int BITS, bool AFFINE, bool SR>
-__global__ void __launch_bounds__(256) k_int_cols(const void* __restrict__ x, int64_t rows,
-                                                  int64_t cols, int64_t rchunk,
-                                                  const uint4* __restrict__ acc, float* scale,
-                                                  int32_t* zp, SrCtx sr, void* y, void* codes,
-                                                  uint32_t* mask, int32_t* flags) {
-  __shared__ ColP sp[kColStrip];
+__global__ void __launch_bounds__(256, 2)
+    k_int_cols(const void* __restrict__ x, int64_t rows, int64_t cols, int wc, int64_t rchunk,
+               int tr, const ColP* __restrict__ table, SrCtx sr, void* y, void* codes,
+               uint32_t* mask, int32_t* flags) {
+  constexpr int NC = kColLane<T>, WW = kColStrip<T>;
+  extern __shared__ __align__(128) char col_stage[];
+  __shared__ __align__(8) uint64_t bars[kColStages];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t cb = (int64_t)blockIdx.x * kColStrip;
-  int f = 0;
-  if (threadIdx.x < kColStrip) {
-    const int64_t col = cb + threadIdx.x;
-    IntParams p;
-    p.s = 1.0f;
-    p.zp = 0;
-    p.dead = 1;
-    p.fast = 0;
-    p.rcp = 0.0f;
-    if (col < cols) {
-      Stats s;
-      s.unpack(acc[col]);
-      f = calibrate<BITS, AFFINE, kMMKeys>(s, p);
-      if (blockIdx.y == 0) {
-        scale[col] = p.s;
-        if (zp) zp[col] = p.zp;
-      } else {
-        f = 0;
-      }
+  const int sub = warp & (wc - 1), rw = warp / wc, nrw = kColWarps / wc;
+  const int sw = WW * wc;
+  ColTiles tl;
+  tl.x = static_cast<const char*>(x);
+  tl.cols = cols;
+  tl.cs = (int64_t)blockIdx.x * sw;
+  tl.segc = (int)(cols - tl.cs < sw ? cols - tl.cs : sw);
+  tl.contig = tl.segc == cols;
+  tl.bytes_per_elem = T::BYTES;
+  tl.r0 = (int64_t)blockIdx.y * rchunk;
+  tl.r1 = min(rows, tl.r0 + rchunk);
+  tl.tr = tr;
+  tl.tiles = tl.r1 > tl.r0 ? (int)((tl.r1 - tl.r0 + tr - 1) / tr) : 0;
+  const int cl = sub * WW + lane * NC;
+  const bool active = cl < tl.segc;
+  const int64_t c = tl.cs + cl;
+  const uint32_t sb = tl.seg_bytes();
+  ColR P[NC];
+  uint32_t slowm = 0u, deadm = 0u;
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    ColP q;
+    if (active) {
+      q = table[c + j];
     } else {
-      finish_params(p, QRange<BITS, AFFINE>::qmin, QRange<BITS, AFFINE>::qmax);
+      q.s = q.rcp = q.wlo = q.whi = q.klof = q.khif = 0.0f;
+      q.zp = 0;
+      q.st = 2;
     }
-    sp[threadIdx.x] = col_params<BITS, AFFINE>(p);
+    P[j] = ColR{q.s, q.rcp, q.wlo, q.whi, q.klof, q.khif, q.zp};
+    slowm |= (q.st & 2) ? 0u : (1u << j);
+    deadm |= (q.st & 1) ? (1u << j) : 0u;
   }
-  warp_flag_or(flags, f);
-  __syncthreads();
-  const int64_t c = cb + lane * 4;
-  const bool active = c < cols;
-  ColP P[4];
-  bool slow = false;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    P[j] = sp[lane * 4 + j];
-    slow |= !(P[j].st & 2);
-  }
-  const int64_t r0 = (int64_t)blockIdx.y * rchunk;
-  const int64_t r1 = min(rows, r0 + rchunk);
-  // two rows per step, both loads issued first; the row loop is warp-uniform
-  // (the mask words are assembled with shuffles)
-  for (int64_t r = r0 + warp; r < r1; r += 2 * kColWarps) {
-    const int64_t rb = r + kColWarps;
-    const bool hb = rb < r1;
-    uint32_t b0[4], b1[4];
-    if (active) {
-      load4<T>(x, r * cols + c, 4, true, b0);
-      if (hb) load4<T>(x, rb * cols + c, 4, true, b1);
-    }
-    uint32_t m0 = 0u, m1 = 0u;
-    if (active) {
-      m0 = col_row<T, BITS, AFFINE, SR>(b0, P, slow, sr, r * cols + c, y, codes);
-      if (hb) m1 = col_row<T, BITS, AFFINE, SR>(b1, P, slow, sr, rb * cols + c, y, codes);
-    }
-    // mask word k of the warp's 128 columns: lanes 8k .. 8k + 7, 4 bits each
-    uint32_t w0 = m0 << (4 * (lane & 7)), w1 = m1 << (4 * (lane & 7));
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      w0 |= __shfl_xor_sync(kFull, w0, o);
-      w1 |= __shfl_xor_sync(kFull, w1, o);
-    }
-    if (mask && active && (lane & 7) == 0) {
-      mask[(r * cols + c) / 32] = w0;
-      if (hb) mask[(rb * cols + c) / 32] = w1;
-    }
-  }
+  // a warp with a dead column or a scale outside the reciprocal's safe range
+  // also runs the IEEE path for those columns
+  const bool slow = __any_sync(kFull, slowm != 0u);
+  col_staged(tl, col_stage, bars, flags, [&](const char* tile, int t, int nr) {
+    const int64_t rs = tl.r0 + (int64_t)t * tr;
+    if (slow)
+      col_map_tile<T, BITS, AFFINE, SR, true>(tile, nr, sb, cl, rw, nrw, rs, cols, c, active, P,
+                                              slowm, deadm, sr, y, codes, mask, lane);
+    else
+      col_map_tile<T, BITS, AFFINE, SR, false>(tile, nr, sb, cl, rw, nrw, rs, cols, c, active, P,
+                                               0u, 0u, sr, y, codes, mask, lane);
+  });
 }
 
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-// Row chunks per column strip: about `per_sm` blocks per SM in all, each
-// chunk at least `min_rows` rows.
-static int64_t col_chunk(int64_t rows, int64_t cols, int per_sm, int64_t min_rows) {
-  const int64_t strips = (cols + kColStrip - 1) / kColStrip;
-  int64_t want = ((int64_t)device_info().sms * per_sm + strips - 1) / strips;
-  int64_t most = (rows + min_rows - 1) / min_rows;
-  int64_t chunks = want < most ? want : most;
-  if (chunks < 1) chunks = 1;
-  if (chunks > 65535) chunks = 65535;
-  return (rows + chunks - 1) / chunks;
+constexpr int kColStagedBytes = kColStages * kColStageBytes;
+
+// rows per staged tile of a strip of `sw` columns
+static int col_tile_rows(int64_t sw, int bytes) {
+  const int64_t tr = kColStageBytes / (sw * bytes);
+  return (int)(tr < 1 ? 1 : tr);
+}
+
+// The dynamic shared memory of a staged kernel, raised once per kernel and
+// device (a failure shows as a launch error).
+template <auto Kernel>
+static void col_staged_smem() {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 63;
+  const uint64_t bit = uint64_t{1} << dev;
+  if (done.load(std::memory_order_acquire) & bit) return;
+  if (cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kColStagedBytes) == cudaSuccess)
+    done.fetch_or(bit, std::memory_order_acq_rel);
 }
 
 #if !QAT_SR
-qat_status launch_col_stats(qat_dtype dt, const void* x, int64_t rows, int64_t cols, int mm,
-                            void* ws, cudaStream_t s) {
-  uint4* acc = static_cast<uint4*>(ws);
-  k_col_init<<<(unsigned)((cols + 255) / 256), 256, 0, s>>>(acc, cols);
-  const int64_t rchunk = col_chunk(rows, cols, 8, 32);
-  const dim3 grid((unsigned)((cols + kColStrip - 1) / kColStrip),
-                  (unsigned)((rows + rchunk - 1) / rchunk));
-#define QAT_CS(T, M) k_col_stats<T, M><<<grid, 256, 0, s>>>(x, rows, cols, rchunk, acc)
-  if (dt == QAT_F32) {
-    if (mm == kMMKeys) QAT_CS(F32, kMMKeys); else QAT_CS(F32, kMMNone);
-  } else {
-    if (mm == kMMKeys) QAT_CS(BF16, kMMKeys); else QAT_CS(BF16, kMMNone);
-  }
+template <typename T>
+static void col_stats_t(int mode, int bits, bool affine, const void* x, int64_t rows, int64_t cols,
+                        const ColWs& w, float* out0, float* out1, float* out2, int32_t* zp,
+                        int32_t* flags, cudaStream_t s) {
+  const bool staged = cols % 32 == 0;
+  // one wave: 2 staged blocks per SM (shared memory), else 3 (registers)
+  const ColShape g = col_shape(rows, cols, kColStrip<T>, staged ? 2 : 3, 8, 1);
+  const int tr = col_tile_rows((int64_t)kColStrip<T> * g.wc, T::BYTES);
+  const int64_t ninit = cols > g.strips ? cols : g.strips;
+  k_col_init<<<(unsigned)((ninit + 255) / 256), 256, 0, s>>>(w.acc, cols, w.cnt, g.strips);
+  const dim3 grid((unsigned)g.strips, (unsigned)g.chunks);
+  ColP* table = static_cast<ColP*>(w.table);
+#define QAT_CS(M, B, A)                                                                        \
+  do {                                                                                         \
+    if (staged) {                                                                              \
+      col_staged_smem<k_col_stats_staged<T, M, B, A>>();                                       \
+      k_col_stats_staged<T, M, B, A><<<grid, 256, kColStagedBytes, s>>>(                       \
+          x, rows, cols, g.wc, g.rchunk, tr, w.acc, w.cnt, out0, out1, out2, zp, w.dead, table, \
+          flags);                                                                              \
+    } else {                                                                                   \
+      k_col_stats<T, M, B, A><<<grid, 256, 0, s>>>(x, rows, cols, g.wc, g.rchunk, w.acc, w.cnt, \
+                                                   out0, out1, out2, zp, w.dead, table, flags); \
+    }                                                                                          \
+  } while (0)
+  if (mode == 0) QAT_CS(0, 8, false);
+  else if (bits == 8) { if (affine) QAT_CS(1, 8, true); else QAT_CS(1, 8, false); }
+  else { if (affine) QAT_CS(1, 4, true); else QAT_CS(1, 4, false); }
 #undef QAT_CS
+}
+
+qat_status launch_col_stats(qat_dtype dt, int mode, int bits, bool affine, const void* x,
+                            int64_t rows, int64_t cols, void* ws, float* out0, float* out1,
+                            float* out2, int32_t* zp, int32_t* flags, cudaStream_t s) {
+  const ColWs w = col_ws(ws, cols);
+  if (dt == QAT_F32)
+    col_stats_t<F32>(mode, bits, affine, x, rows, cols, w, out0, out1, out2, zp, flags, s);
+  else
+    col_stats_t<BF16>(mode, bits, affine, x, rows, cols, w, out0, out1, out2, zp, flags, s);
   count_launch(2);
-  return launch_status();
-}
-
-qat_status launch_col_finalize(const void* ws, int64_t cols, float* absmax, float* minv,
-                               float* maxv, int32_t* flags, cudaStream_t s) {
-  k_col_finalize<<<(unsigned)((cols + 255) / 256), 256, 0, s>>>(static_cast<const uint4*>(ws), cols,
-                                                                absmax, minv, maxv, flags);
-  count_launch(1);
-  return launch_status();
-}
-
-qat_status launch_col_params(int bits, bool affine, const void* ws, int64_t cols, float* scale,
-                             int32_t* zp, uint8_t* dead, int32_t* flags, cudaStream_t s) {
-  const uint4* acc = static_cast<const uint4*>(ws);
-  const unsigned g = (unsigned)((cols + 255) / 256);
-  if (bits == 8) {
-    if (affine) k_col_params<8, true><<<g, 256, 0, s>>>(acc, cols, scale, zp, dead, flags);
-    else k_col_params<8, false><<<g, 256, 0, s>>>(acc, cols, scale, zp, dead, flags);
-  } else {
-    if (affine) k_col_params<4, true><<<g, 256, 0, s>>>(acc, cols, scale, zp, dead, flags);
-    else k_col_params<4, false><<<g, 256, 0, s>>>(acc, cols, scale, zp, dead, flags);
-  }
-  count_launch(1);
   return launch_status();
 }
 #endif  // !QAT_SR
 
+template <typename T, int BITS, bool AFFINE>
+static void int_cols_t(const void* x, int64_t rows, int64_t cols, const ColWs& w, const SrCtx& sr,
+                       void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
+  // one wave of 2 blocks per SM (their staged tiles fill the shared memory)
+  const ColShape g = col_shape(rows, cols, kColStrip<T>, 2, 8, 1);
+  const int tr = col_tile_rows((int64_t)kColStrip<T> * g.wc, T::BYTES);
+  const dim3 grid((unsigned)g.strips, (unsigned)g.chunks);
+  col_staged_smem<k_int_cols<T, BITS, AFFINE, QAT_SR>>();
+  k_int_cols<T, BITS, AFFINE, QAT_SR><<<grid, 256, kColStagedBytes, s>>>(
+      x, rows, cols, g.wc, g.rchunk, tr, static_cast<const ColP*>(w.table), sr, y, codes, mask,
+      flags);
+}
+
 qat_status QAT_SR_NAME(launch_int_cols)(qat_dtype dt, int bits, bool affine, const void* x,
-                                        int64_t rows, int64_t cols, const void* ws, float* scale,
-                                        int32_t* zp, const SrCtx& sr, void* y, void* codes,
-                                        uint32_t* mask, int32_t* flags, cudaStream_t s) {
-  const uint4* acc = static_cast<const uint4*>(ws);
-  const int64_t rchunk = col_chunk(rows, cols, 6, 64);
-  const dim3 grid((unsigned)((cols + kColStrip - 1) / kColStrip),
-                  (unsigned)((rows + rchunk - 1) / rchunk));
-#define QAT_IC(T, B, A)                                                                       \
-  k_int_cols<T, B, A, QAT_SR><<<grid, 256, 0, s>>>(x, rows, cols, rchunk, acc, scale, zp, sr, y, \
-                                                   codes, mask, flags)
+                                        int64_t rows, int64_t cols, const void* ws,
+                                        const SrCtx& sr, void* y, void* codes, uint32_t* mask,
+                                        int32_t* flags, cudaStream_t s) {
+  const ColWs w = col_ws(const_cast<void*>(ws), cols);
+#define QAT_IC(T, B, A) int_cols_t<T, B, A>(x, rows, cols, w, sr, y, codes, mask, flags, s)
   if (dt == QAT_F32) {
     if (bits == 8) { if (affine) QAT_IC(F32, 8, true); else QAT_IC(F32, 8, false); }
     else { if (affine) QAT_IC(F32, 4, true); else QAT_IC(F32, 4, false); }

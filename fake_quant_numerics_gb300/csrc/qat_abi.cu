@@ -61,7 +61,7 @@ size_t ws_bytes_for(int64_t rows, int64_t cols, qat_granularity g, int64_t group
   int64_t n;
   if (!elems(rows, cols, &n)) return 0;
   const auto r16 = [](int64_t b) { return (b + 15) / 16 * 16; };
-  if (g == QAT_PER_COLUMN) return (size_t)(cols * 16 + r16(cols) + r16(cols * 4));
+  if (g == QAT_PER_COLUMN) return col_ws_bytes(cols);
   int64_t units = 0;
   if (g == QAT_PER_ROW) units = rows;
   else if (g == QAT_PER_GROUP && group > 0) units = n / group;
@@ -70,11 +70,13 @@ size_t ws_bytes_for(int64_t rows, int64_t cols, qat_granularity g, int64_t group
 
 // The fallback's per-unit arrays inside the workspace: the dead bytes, then
 // the zero points (used when the caller passes no zero-point array).
-static uint8_t* ws_dead(void* ws, int64_t rows, int64_t cols, qat_granularity g) {
-  return static_cast<uint8_t*>(ws) + (g == QAT_PER_COLUMN ? cols * 16 : 0);
+static uint8_t* ws_dead(void* ws, int64_t cols, qat_granularity g) {
+  return g == QAT_PER_COLUMN ? col_ws(ws, cols).dead : static_cast<uint8_t*>(ws);
 }
-static int32_t* ws_zp(void* ws, int64_t rows, int64_t cols, qat_granularity g, int64_t units) {
-  return reinterpret_cast<int32_t*>(ws_dead(ws, rows, cols, g) + (units + 15) / 16 * 16);
+static int32_t* ws_zp(void* ws, int64_t cols, qat_granularity g, int64_t units) {
+  return g == QAT_PER_COLUMN ? col_ws(ws, cols).zp
+                             : reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) +
+                                                          (units + 15) / 16 * 16);
 }
 
 // Unit length and count of a granularity; false on an invalid combination.
@@ -153,9 +155,8 @@ qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t 
     if (cols > kMaxColumns) return QAT_ERR_UNSUPPORTED;
     if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
     if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
-    qat_status st = launch_col_stats(dtype, x, rows, cols, kMMKeys, ws, s);
-    if (st) return st;
-    return launch_col_finalize(ws, cols, absmax, minv, maxv, flags, s);
+    return launch_col_stats(dtype, 0, 8, false, x, rows, cols, ws, absmax, minv, maxv, nullptr,
+                            flags, s);
   }
   if (fused_units_supported(dtype, L))
     return launch_int_fused(dtype, 8, false, true, x, units, L, nullptr, nullptr, absmax, minv, maxv,
@@ -214,26 +215,25 @@ static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t ro
                      c, y, codes, mask, flags, s);
   if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
   if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+  uint8_t* dead = ws_dead(ws, cols, g);
+  int32_t* zpu = (affine && !zp) ? ws_zp(ws, cols, g, units) : zp;
   qat_status st;
   if (col) {
-    // column statistics, then the strip map (whole mask words per warp row)
-    st = launch_col_stats(dtype, x, rows, cols, affine ? kMMKeys : kMMNone, ws, s);
+    // column statistics and calibration, then the strip map (whole mask
+    // words per warp row) or the unit kernel
+    st = launch_col_stats(dtype, 1, bits, affine, x, rows, cols, ws, scale, nullptr, nullptr, zpu,
+                          flags, s);
     if (st) return st;
     if (cols % 32 == 0) {
       auto map_cols = sr ? launch_int_cols_sr : launch_int_cols;
-      return map_cols(dtype, bits, affine, x, rows, cols, ws, scale, zp, c, y, codes, mask, flags,
-                      s);
+      return map_cols(dtype, bits, affine, x, rows, cols, ws, c, y, codes, mask, flags, s);
     }
-  }
-  // fallback: calibrate every unit, then the flat map with per-unit arrays
-  uint8_t* dead = ws_dead(ws, rows, cols, g);
-  int32_t* zpu = (affine && !zp) ? ws_zp(ws, rows, cols, g, units) : zp;
-  if (col)
-    st = launch_col_params(bits, affine, ws, cols, scale, zpu, dead, flags, s);
-  else
+  } else {
+    // fallback: calibrate every unit, then the flat map with per-unit arrays
     st = launch_unit_generic(dtype, 1, bits, affine, x, units, L, nullptr, nullptr, nullptr, scale,
                              zpu, dead, flags, s);
-  if (st) return st;
+    if (st) return st;
+  }
   return map_units(dtype, bits, affine, false, x, n, L, ucols, scale, zpu, dead, c, y, codes, mask,
                    flags, s);
 }

@@ -87,6 +87,9 @@ typedef enum {
 #define QAT_FLAG_BAD_PARAMS 4      /* given scale not finite and > 0 (int) or not finite and >= 0
                                       (fp8), or given zero point outside [qmin, qmax] */
 #define QAT_FLAG_NONFINITE_INPUT 8 /* NaN/Inf seen by an FP8 amax or by qat_amax_stats; informational */
+#define QAT_FLAG_DEVICE_TIMEOUT 16 /* a kernel's bounded wait for its own staged copies ran out (an
+                                      internal fault, not a data error); the call's outputs are
+                                      invalid */
 
 typedef enum { QAT_F32 = 0, QAT_BF16 = 1 } qat_dtype;
 typedef enum { QAT_SYMMETRIC = 0, QAT_AFFINE = 1 } qat_scheme;
@@ -114,9 +117,10 @@ const char* qat_status_string(qat_status status);
  * partial statistics (16 KiB); per row / per group, five bytes per unit
  * (a dead byte and a zero point, each array rounded up to 16 bytes), used
  * only by the fallback for unit lengths the fused single-pass kernels do not
- * cover; per column, 21 bytes per column (a 16-byte statistics accumulator,
- * then the fallback's dead byte and zero point), used by every calibrated
- * call.  The workspace is scratch: its contents on entry do not matter and
+ * cover; per column, 53 bytes per column and 4 per 128 columns (a 16-byte
+ * statistics accumulator and a 32-byte parameter record per column, a
+ * counter per 128 columns, then the fallback's dead byte and zero point, each
+ * array rounded up to 16 bytes), used by every calibrated call.  The workspace is scratch: its contents on entry do not matter and
  * are overwritten.  Two calls that use the same workspace must be ordered on
  * one stream.
  */

@@ -46,9 +46,10 @@ def test_workspace_bytes(lib):
     assert lib.qat_workspace_bytes(4096, 4096, L.PER_ROW, 0) == 4096 * 5
     assert lib.qat_workspace_bytes(14336, 4096, L.PER_GROUP, 128) == 14336 * 32 * 5
     assert lib.qat_workspace_bytes(3, 5, L.PER_ROW, 0) == 16 + 16
-    # per column: a 16-byte accumulator per column, then the fallback's arrays
-    assert lib.qat_workspace_bytes(4096, 4096, L.PER_COLUMN, 0) == 4096 * 21
-    assert lib.qat_workspace_bytes(7, 33, L.PER_COLUMN, 0) == 33 * 16 + 48 + 144
+    # per column: a 16-byte accumulator and a 32-byte record per column, a
+    # counter per 128 columns, then the fallback's arrays
+    assert lib.qat_workspace_bytes(4096, 4096, L.PER_COLUMN, 0) == 4096 * 48 + 128 + 4096 + 16384
+    assert lib.qat_workspace_bytes(7, 33, L.PER_COLUMN, 0) == 33 * 48 + 16 + 48 + 144
 
 
 def _int(lib, **kw):
@@ -82,7 +83,8 @@ def test_int_argument_errors(lib):
     assert _int(lib, gran=L.PER_ROW, cols=40, ws=None) == L.QAT_ERR_WORKSPACE
     # calibrated columns always take the column statistics workspace
     assert _int(lib, gran=L.PER_COLUMN, ws=None) == L.QAT_ERR_WORKSPACE
-    assert _int(lib, gran=L.PER_COLUMN, ws=A, wsb=64 * 21 - 1) == L.QAT_ERR_WORKSPACE
+    need = lib.qat_workspace_bytes(4, 64, L.PER_COLUMN, 0)
+    assert _int(lib, gran=L.PER_COLUMN, ws=A, wsb=need - 1) == L.QAT_ERR_WORKSPACE
     # empty tensors are a no-op even with NULL buffers
     assert _int(lib, rows=0, x=None, scale=None) == L.QAT_OK
     assert _int(lib, cols=0, x=None, scale=None) == L.QAT_OK
