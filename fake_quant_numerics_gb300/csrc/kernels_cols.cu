@@ -9,17 +9,19 @@
 // mapped, so the calibrated path is two passes over x.  In both kernels a
 // lane takes 16 bytes of a row (4 fp32 or 8 bf16 columns), a warp a strip of
 // 32 lanes, and the 8 warps of a block sit side by side (up to 8 strips, so
-// the block reads up to 4 KiB of each row) and walk the rows of their chunk,
-// each keeping loads of 4 rows in flight.
-//   k_col_init   zeroes the per-column accumulators and the strip counters
-//   k_col_stats  folds the chunk into per-column partials and combines the
-//                block's partial into the accumulators with integer atomics
-//                (absmax bits and order keys are monotone as unsigned
-//                integers); the last block of a strip to finish (a counter per
-//                strip) calibrates the strip's columns: scale, zero point,
-//                the dead flag and the 32-byte parameter record of each column
-//   k_int_cols   each lane loads the records of its columns into registers
-//                once and maps the rows of its chunk
+// the block reads up to 4 KiB of each row) and walk the rows of their chunk.
+// When the row length is a multiple of 32 the rows come in through shared
+// memory (bulk copies, several tiles in flight); otherwise through registers.
+//   k_col_init      resets the per-column accumulators
+//   k_col_stats*    fold the chunk into per-column partials and combine each
+//                   block's partial into the accumulators with integer
+//                   atomics (absmax bits and order keys are monotone as
+//                   unsigned integers)
+//   k_int_cols      calibrates its columns from the accumulators while its
+//                   first tiles are in flight, keeps their parameters in
+//                   registers and maps the rows of its chunk
+//   k_col_finalize  the accumulators -> statistics outputs, or scale, zero
+//                   point and dead byte for the unit-kernel fallback
 // Row lengths that are not a multiple of 32 (mask words would straddle rows)
 // and given parameters take the per-element unit kernel in column mode.
 #include <atomic>
@@ -36,14 +38,13 @@ constexpr int kColLane = 16 / T::BYTES;
 template <typename T>
 constexpr int kColStrip = 32 * kColLane<T>;
 
-// The parameters of one column as the map keeps them (a 32-byte record in
-// the workspace): wlo is stored as -0 when it is zero (the window test).
+// The parameters of one column as the map uses them: wlo is stored as -0
+// when it is zero (the window test).
 struct ColP {
   float s, rcp, wlo, whi, klof, khif;
   int zp;
   int st;  // bit 0 dead, bit 1 fast (scale in the reciprocal's safe range)
 };
-static_assert(sizeof(ColP) == kColRecordBytes, "column record size");
 
 // Grid of both column kernels: `wc` warp strips side by side in a block (a
 // power of two up to 8; the other 8 / wc warps interleave along rows), so a
@@ -182,13 +183,13 @@ struct ColTiles {
   }
 };
 
-// The staged walk: calls body(tile_base, tile, rows_in_tile) for every tile of the
-// block, with all threads; returns false (flag set, copies drained) when a
-// wait ran out.  The caller provides kColStages * kColStageBytes bytes of
+// The staged walk: issues the first tiles, runs prologue(), then calls
+// body(tile_base, tile, rows_in_tile) for every tile of the block, with all
+// threads; returns false (flag set, copies drained) when a wait ran out.  The caller provides kColStages * kColStageBytes bytes of
 // dynamic shared memory at `stage` and kColStages mbarriers at `bars`.
-template <typename Body>
+template <typename Pro, typename Body>
 __device__ __forceinline__ bool col_staged(const ColTiles& tl, char* stage, uint64_t* bars,
-                                           int32_t* flags, Body&& body) {
+                                           int32_t* flags, Pro&& prologue, Body&& body) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < kColStages; ++s) mbar_init(bars + s, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -197,6 +198,7 @@ __device__ __forceinline__ bool col_staged(const ColTiles& tl, char* stage, uint
   if (threadIdx.x == 0)
     for (int s = 0; s < kColStages && s < tl.tiles; ++s)
       tl.issue(s, stage + s * kColStageBytes, bars + s);
+  prologue();  // runs while the first tiles are in flight
   for (int t = 0; t < tl.tiles; ++t) {
     const int s = t % kColStages;
     const uint32_t par = (uint32_t)(t / kColStages) & 1u;
@@ -251,31 +253,17 @@ __device__ __forceinline__ void col_add(Stats& st, uint32_t u) {
   st.kmax = max(st.kmax, fin ? k : kKeyNegInf);
 }
 
-__global__ void k_col_init(uint4* __restrict__ acc, int64_t cols, uint32_t* __restrict__ cnt,
-                           int64_t strips) {
+__global__ void k_col_init(uint4* __restrict__ acc, int64_t cols) {
   const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (c < cols) acc[c] = make_uint4(0u, 0u, kKeyPosInf, kKeyNegInf);
-  if (c < strips) cnt[c] = 0u;
 }
 
-// Column statistics, MODE 0: per-column absmax / min / max (finite values)
-// and the non-finite input flag.  MODE 1: integer calibration (BITS, AFFINE)
-// -> scale, zero point, dead byte and record of every column.  Symmetric
-// calibration tracks the absmax alone; otherwise the order keys of min and
-// max, from which the finite absmax is max(|min|, |max|).
-//
 // After the fold: merge the warps that share a strip (red: the block's
-// kColWarps x WW partials in shared memory), combine the block's partial of
-// each column into the accumulators, and let the last block of the strip
-// finalise its columns.
-template <typename T, int MODE, int BITS, bool AFFINE>
-__device__ __forceinline__ void col_stats_finish(const Stats (&st)[kColLane<T>], uint4* red,
-                                                 int wc, int64_t cols, uint4* __restrict__ acc,
-                                                 uint32_t* __restrict__ cnt, float* out0,
-                                                 float* out1, float* out2, int32_t* zp,
-                                                 uint8_t* dead, ColP* table, int32_t* flags,
-                                                 int* last) {
-  constexpr int MM = (MODE == 0 || AFFINE) ? kMMKeys : kMMNone;
+// kColWarps x WW partials in shared memory) and combine the block's partial
+// of each column into the accumulators.
+template <typename T, int MM>
+__device__ __forceinline__ void col_stats_combine(const Stats (&st)[kColLane<T>], uint4* red,
+                                                  int wc, int64_t cols, uint4* __restrict__ acc) {
   constexpr int NC = kColLane<T>, WW = kColStrip<T>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nrw = kColWarps / wc;
@@ -295,9 +283,8 @@ __device__ __forceinline__ void col_stats_finish(const Stats (&st)[kColLane<T>],
       }
       red[ts * WW + tl] = s.pack();
     }
+    __syncthreads();
   }
-  __syncthreads();
-  // combine the block's partial of each column into the accumulators
   for (int t = threadIdx.x; t < sw; t += blockDim.x) {
     const int64_t col = (int64_t)blockIdx.x * sw + t;
     if (col < cols) {
@@ -313,58 +300,63 @@ __device__ __forceinline__ void col_stats_finish(const Stats (&st)[kColLane<T>],
       if (s.nonfinite) atomicOr(a + 1, 1u);
     }
   }
-  // the last block of the strip to get here finalises its columns
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) *last = atomicAdd(cnt + blockIdx.x, 1u) == gridDim.y - 1;
-  __syncthreads();
-  if (!*last) return;
-  __threadfence();
+}
+#endif  // !QAT_SR
+
+// A column's statistics from its accumulator; with order keys the finite
+// absmax is max(|min|, |max|) (0 when the column has no finite value).
+template <int MM>
+__device__ __forceinline__ Stats col_acc_stats(const uint4& a) {
+  Stats s;
+  s.unpack(a);
+  if (MM == kMMKeys) {
+    const uint32_t am = max(key_to_bits(s.kmin) & 0x7fffffffu, key_to_bits(s.kmax) & 0x7fffffffu);
+    s.amax = s.kmin <= s.kmax ? am : 0u;
+  }
+  return s;
+}
+
+#if !QAT_SR
+// The accumulators of every column (one thread each).  MODE 0: absmax / min /
+// max (finite values) and QAT_FLAG_NONFINITE_INPUT.  MODE 1: the integer
+// calibration -> scale, zero point and dead byte (the unit-kernel fallback),
+// and the calibration flags.
+template <int MODE, int BITS, bool AFFINE>
+__global__ void k_col_finalize(const uint4* __restrict__ acc, int64_t cols, float* out0,
+                               float* out1, float* out2, int32_t* zp, uint8_t* dead,
+                               int32_t* flags) {
+  constexpr int MM = (MODE == 0 || AFFINE) ? kMMKeys : kMMNone;
+  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   int f = 0;
-  for (int t = threadIdx.x; t < sw; t += blockDim.x) {
-    const int64_t col = (int64_t)blockIdx.x * sw + t;
-    if (col >= cols) break;
-    Stats s;
-    s.unpack(__ldcg(acc + col));
-    if (MM == kMMKeys) {
-      // finite absmax from the finite min and max (0 when there is none)
-      const uint32_t am = max(key_to_bits(s.kmin) & 0x7fffffffu, key_to_bits(s.kmax) & 0x7fffffffu);
-      s.amax = s.kmin <= s.kmax ? am : 0u;
-    }
+  if (c < cols) {
+    const Stats s = col_acc_stats<MM>(acc[c]);
     if (MODE == 0) {
-      if (out0) out0[col] = s.absmax_f();
-      if (out1) out1[col] = s.min_f<kMMKeys>();
-      if (out2) out2[col] = s.max_f<kMMKeys>();
-      f |= s.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0;
+      if (out0) out0[c] = s.absmax_f();
+      if (out1) out1[c] = s.min_f<kMMKeys>();
+      if (out2) out2[c] = s.max_f<kMMKeys>();
+      f = s.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0;
     } else {
       IntParams p;
-      f |= calibrate<BITS, AFFINE, MM>(s, p);
-      out0[col] = p.s;
-      if (zp) zp[col] = p.zp;
-      dead[col] = (uint8_t)p.dead;
-      table[col] = col_params<BITS, AFFINE>(p);
+      f = calibrate<BITS, AFFINE, MM>(s, p);
+      out0[c] = p.s;
+      if (zp) zp[c] = p.zp;
+      dead[c] = (uint8_t)p.dead;
     }
   }
   warp_flag_or(flags, f);
 }
 
-// The statistics for any row length (element loads where a row is not
-// 16-byte aligned), the rows through registers: kColDepth loads in flight per
-// warp.
+// Column statistics (MM: kMMNone for the symmetric calibration, otherwise
+// kMMKeys) for any row length (element loads where a row is not 16-byte
+// aligned), the rows through registers: kColDepth loads in flight per warp.
 constexpr int kColDepth = 4;
 
-template <typename T, int MODE, int BITS, bool AFFINE>
+template <typename T, int MM>
 __global__ void __launch_bounds__(256, 3)
     k_col_stats(const void* __restrict__ x, int64_t rows, int64_t cols, int wc, int64_t rchunk,
-                uint4* __restrict__ acc, uint32_t* __restrict__ cnt, float* out0, float* out1,
-                float* out2, int32_t* zp, uint8_t* dead, ColP* table, int32_t* flags) {
-  constexpr int MM = (MODE == 0 || AFFINE) ? kMMKeys : kMMNone;
+                uint4* __restrict__ acc) {
   constexpr int NC = kColLane<T>, WW = kColStrip<T>, D = kColDepth;
-  // per warp slot and column of its strip; after the merge of the warps that
-  // share a strip, red[0 .. wc - 1] is the block's partial of its wc * WW
-  // columns, in column order
   __shared__ uint4 red[kColWarps * WW];
-  __shared__ int last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = warp & (wc - 1), rw = warp / wc, nrw = kColWarps / wc;
   const int sw = WW * wc;
@@ -400,24 +392,19 @@ __global__ void __launch_bounds__(256, 3)
       }
     }
   }
-  col_stats_finish<T, MODE, BITS, AFFINE>(st, red, wc, cols, acc, cnt, out0, out1, out2, zp, dead,
-                                          table, flags, &last);
+  col_stats_combine<T, MM>(st, red, wc, cols, acc);
 }
 
 // The same statistics for row lengths that are a multiple of 32: the rows of
 // the block's strip come in through the staged tiles (shared memory), so the
 // loads in flight do not occupy registers.
-template <typename T, int MODE, int BITS, bool AFFINE>
+template <typename T, int MM>
 __global__ void __launch_bounds__(256, 2)
     k_col_stats_staged(const void* __restrict__ x, int64_t rows, int64_t cols, int wc,
-                       int64_t rchunk, int tr, uint4* __restrict__ acc, uint32_t* __restrict__ cnt,
-                       float* out0, float* out1, float* out2, int32_t* zp, uint8_t* dead,
-                       ColP* table, int32_t* flags) {
-  constexpr int MM = (MODE == 0 || AFFINE) ? kMMKeys : kMMNone;
+                       int64_t rchunk, int tr, uint4* __restrict__ acc, int32_t* flags) {
   constexpr int NC = kColLane<T>, WW = kColStrip<T>;
   extern __shared__ __align__(128) char col_stage[];
   __shared__ __align__(8) uint64_t bars[kColStages];
-  __shared__ int last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = warp & (wc - 1), rw = warp / wc, nrw = kColWarps / wc;
   const int sw = WW * wc;
@@ -434,22 +421,98 @@ __global__ void __launch_bounds__(256, 2)
   tl.tiles = tl.r1 > tl.r0 ? (int)((tl.r1 - tl.r0 + tr - 1) / tr) : 0;
   const int cl = sub * WW + lane * NC;  // the lane's first column in the strip
   const bool active = cl < tl.segc;
+  const int64_t c = tl.cs + cl;
   const uint32_t sb = tl.seg_bytes();
-  Stats st[NC];
+  // Raw folds over every value, non-finite ones included: the absmax bits
+  // (symmetric) or the order keys of min and max, per column (fp32) or per
+  // pair of columns in 16-bit halves (bf16).  A non-finite value pushes the
+  // raw result past the finite range, and only then is the column folded
+  // again, exactly, from global memory.
+  constexpr int NW = T::BYTES == 4 ? NC : NC / 2;  // accumulator words
+  uint32_t lo[NW], hi[NW];
 #pragma unroll
-  for (int j = 0; j < NC; ++j) st[j].template init<MM>();
-  const bool ok = col_staged(tl, col_stage, bars, flags, [&](const char* tile, int, int nr) {
+  for (int k = 0; k < NW; ++k) {
+    lo[k] = 0xffffffffu;  // min of keys
+    hi[k] = 0u;           // max of keys, or of absmax bits
+  }
+  const bool ok = col_staged(tl, col_stage, bars, flags, [] {}, [&](const char* tile, int, int nr) {
     if (!active) return;
     for (int r = rw; r < nr; r += nrw) {
       const uint4 v = *reinterpret_cast<const uint4*>(tile + (size_t)r * sb + cl * T::BYTES);
-      const Raw16 cur = {{v.x, v.y, v.z, v.w}};
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int j = 0; j < NC; ++j) col_add<MM>(st[j], __float_as_uint(raw_elem<T>(cur, j)));
+      for (int k = 0; k < 4; ++k) {
+        if (T::BYTES == 4) {
+          if (MM == kMMKeys) {
+            const uint32_t key = order_key(w[k]);
+            lo[k] = min(lo[k], key);
+            hi[k] = max(hi[k], key);
+          } else {
+            hi[k] = max(hi[k], w[k] & 0x7fffffffu);
+          }
+        } else if (MM == kMMKeys) {
+          // 16-bit order keys of both halves: h ^ 0xffff when negative, h ^ 0x8000 otherwise
+          const uint32_t key2 = w[k] ^ (((w[k] >> 15) & 0x00010001u) * 0x7fffu) ^ 0x80008000u;
+          asm("min.u16x2 %0, %0, %1;" : "+r"(lo[k]) : "r"(key2));
+          asm("max.u16x2 %0, %0, %1;" : "+r"(hi[k]) : "r"(key2));
+        } else {
+          asm("max.u16x2 %0, %0, %1;" : "+r"(hi[k]) : "r"(w[k] & 0x7fff7fffu));
+        }
+      }
     }
   });
   if (!ok) return;
-  col_stats_finish<T, MODE, BITS, AFFINE>(st, reinterpret_cast<uint4*>(col_stage), wc, cols, acc,
-                                          cnt, out0, out1, out2, zp, dead, table, flags, &last);
+  Stats st[NC];
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    Stats& sj = st[j];
+    sj.init<MM>();
+    if (!active) continue;
+    if (T::BYTES == 4) {
+      if (MM == kMMKeys) {
+        bad |= lo[j] <= kKeyNegInf || hi[j] >= kKeyPosInf;
+        sj.kmin = lo[j];
+        sj.kmax = hi[j];
+      } else {
+        bad |= hi[j] >= 0x7f800000u;
+        sj.amax = hi[j];
+      }
+    } else {
+      const int sh = (j & 1) ? 16 : 0;
+      if (MM == kMMKeys) {
+        // the fp32 key of a bf16 key: key << 16, low bits all ones when negative
+        const uint32_t kl = (lo[j >> 1] >> sh) & 0xffffu, kh = (hi[j >> 1] >> sh) & 0xffffu;
+        bad |= kl <= 0x007fu || kh >= 0xff80u;
+        sj.kmin = (kl << 16) | (kl < 0x8000u ? 0xffffu : 0u);
+        sj.kmax = (kh << 16) | (kh < 0x8000u ? 0xffffu : 0u);
+      } else {
+        const uint32_t a = (hi[j >> 1] >> sh) & 0xffffu;
+        bad |= a >= 0x7f80u;
+        sj.amax = a << 16;
+      }
+    }
+  }
+  if (bad) {
+    // a non-finite value in one of the lane's columns: their exact statistics
+    // over the lane's rows of the chunk, one 16-byte load per row, 4 in flight
+#pragma unroll
+    for (int j = 0; j < NC; ++j) st[j].template init<MM>();
+    const int64_t step = nrw;
+    for (int64_t r = tl.r0 + rw; r < tl.r1; r += 4 * step) {
+      Raw16 b[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (r + k * step < tl.r1) b[k] = load_lane<T>(x, (r + k * step) * cols + c, NC, true);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (r + k * step >= tl.r1) break;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) st[j].template add<MM>(__float_as_uint(raw_elem<T>(b[k], j)));
+      }
+    }
+  }
+  col_stats_combine<T, MM>(st, reinterpret_cast<uint4*>(col_stage), wc, cols, acc);
 }
 #endif  // !QAT_SR
 
@@ -621,15 +684,18 @@ __device__ __forceinline__ void col_map_tile(const char* tile, int nr, uint32_t 
   }
 }
 
-// The calibrated per-column map (cols % 32 == 0): each lane keeps the
-// records of its columns in registers; the rows of the block's strip come in
-// through the staged tiles.
+// The calibrated per-column map (cols % 32 == 0): while its first tiles are
+// in flight, each lane calibrates its columns from the accumulators and keeps
+// their parameters in registers (blocks of the first row chunk write scale,
+// zero point and the calibration flags); the rows of the block's strip come
+// in through the staged tiles.
 template <typename T, int BITS, bool AFFINE, bool SR>
 __global__ void __launch_bounds__(256, 2)
     k_int_cols(const void* __restrict__ x, int64_t rows, int64_t cols, int wc, int64_t rchunk,
-               int tr, const ColP* __restrict__ table, SrCtx sr, void* y, void* codes,
-               uint32_t* mask, int32_t* flags) {
+               int tr, const uint4* __restrict__ acc, float* scale, int32_t* zp, SrCtx sr,
+               void* y, void* codes, uint32_t* mask, int32_t* flags) {
   constexpr int NC = kColLane<T>, WW = kColStrip<T>;
+  constexpr int MM = AFFINE ? kMMKeys : kMMNone;
   extern __shared__ __align__(128) char col_stage[];
   __shared__ __align__(8) uint64_t bars[kColStages];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -652,24 +718,39 @@ __global__ void __launch_bounds__(256, 2)
   const uint32_t sb = tl.seg_bytes();
   ColR P[NC];
   uint32_t slowm = 0u, deadm = 0u;
+  bool slow = false;
+  const auto calibrate_columns = [&] {
+    int f = 0;
 #pragma unroll
-  for (int j = 0; j < NC; ++j) {
-    ColP q;
-    if (active) {
-      q = table[c + j];
-    } else {
-      q.s = q.rcp = q.wlo = q.whi = q.klof = q.khif = 0.0f;
-      q.zp = 0;
-      q.st = 2;
+    for (int j = 0; j < NC; ++j) {
+      IntParams p;
+      p.s = 1.0f;
+      p.zp = 0;
+      p.dead = 1;
+      p.fast = 0;
+      p.rcp = 0.0f;
+      if (active) {
+        f |= calibrate<BITS, AFFINE, MM>(col_acc_stats<MM>(acc[c + j]), p);
+        // one writer per column (the warps of other row phases share it)
+        if (blockIdx.y == 0 && rw == 0) {
+          scale[c + j] = p.s;
+          if (zp) zp[c + j] = p.zp;
+        }
+      } else {
+        finish_params(p, QRange<BITS, AFFINE>::qmin, QRange<BITS, AFFINE>::qmax);
+      }
+      const ColP q = col_params<BITS, AFFINE>(p);
+      P[j] = ColR{q.s, q.rcp, q.wlo, q.whi, q.klof, q.khif, q.zp};
+      slowm |= (q.st & 2) ? 0u : (1u << j);
+      deadm |= (q.st & 1) ? (1u << j) : 0u;
     }
-    P[j] = ColR{q.s, q.rcp, q.wlo, q.whi, q.klof, q.khif, q.zp};
-    slowm |= (q.st & 2) ? 0u : (1u << j);
-    deadm |= (q.st & 1) ? (1u << j) : 0u;
-  }
-  // a warp with a dead column or a scale outside the reciprocal's safe range
-  // also runs the IEEE path for those columns
-  const bool slow = __any_sync(kFull, slowm != 0u);
-  col_staged(tl, col_stage, bars, flags, [&](const char* tile, int t, int nr) {
+    if (!active) slowm = deadm = 0u;
+    warp_flag_or(flags, (blockIdx.y == 0 && rw == 0) ? f : 0);
+    // a warp with a dead column or a scale outside the reciprocal's safe
+    // range also runs the IEEE path for those columns
+    slow = __any_sync(kFull, slowm != 0u);
+  };
+  col_staged(tl, col_stage, bars, flags, calibrate_columns, [&](const char* tile, int t, int nr) {
     const int64_t rs = tl.r0 + (int64_t)t * tr;
     if (slow)
       col_map_tile<T, BITS, AFFINE, SR, true>(tile, nr, sb, cl, rw, nrw, rs, cols, c, active, P,
@@ -707,67 +788,76 @@ static void col_staged_smem() {
 
 #if !QAT_SR
 template <typename T>
-static void col_stats_t(int mode, int bits, bool affine, const void* x, int64_t rows, int64_t cols,
-                        const ColWs& w, float* out0, float* out1, float* out2, int32_t* zp,
+static void col_stats_t(bool keys, const void* x, int64_t rows, int64_t cols, uint4* acc,
                         int32_t* flags, cudaStream_t s) {
   const bool staged = cols % 32 == 0;
   // one wave: 2 staged blocks per SM (shared memory), else 3 (registers)
   const ColShape g = col_shape(rows, cols, kColStrip<T>, staged ? 2 : 3, 8, 1);
   const int tr = col_tile_rows((int64_t)kColStrip<T> * g.wc, T::BYTES);
-  const int64_t ninit = cols > g.strips ? cols : g.strips;
-  k_col_init<<<(unsigned)((ninit + 255) / 256), 256, 0, s>>>(w.acc, cols, w.cnt, g.strips);
+  k_col_init<<<(unsigned)((cols + 255) / 256), 256, 0, s>>>(acc, cols);
   const dim3 grid((unsigned)g.strips, (unsigned)g.chunks);
-  ColP* table = static_cast<ColP*>(w.table);
-#define QAT_CS(M, B, A)                                                                        \
-  do {                                                                                         \
-    if (staged) {                                                                              \
-      col_staged_smem<k_col_stats_staged<T, M, B, A>>();                                       \
-      k_col_stats_staged<T, M, B, A><<<grid, 256, kColStagedBytes, s>>>(                       \
-          x, rows, cols, g.wc, g.rchunk, tr, w.acc, w.cnt, out0, out1, out2, zp, w.dead, table, \
-          flags);                                                                              \
-    } else {                                                                                   \
-      k_col_stats<T, M, B, A><<<grid, 256, 0, s>>>(x, rows, cols, g.wc, g.rchunk, w.acc, w.cnt, \
-                                                   out0, out1, out2, zp, w.dead, table, flags); \
-    }                                                                                          \
+#define QAT_CS(M)                                                                               \
+  do {                                                                                          \
+    if (staged) {                                                                               \
+      col_staged_smem<k_col_stats_staged<T, M>>();                                              \
+      k_col_stats_staged<T, M><<<grid, 256, kColStagedBytes, s>>>(x, rows, cols, g.wc, g.rchunk, \
+                                                                  tr, acc, flags);              \
+    } else {                                                                                    \
+      k_col_stats<T, M><<<grid, 256, 0, s>>>(x, rows, cols, g.wc, g.rchunk, acc);                \
+    }                                                                                           \
   } while (0)
-  if (mode == 0) QAT_CS(0, 8, false);
-  else if (bits == 8) { if (affine) QAT_CS(1, 8, true); else QAT_CS(1, 8, false); }
-  else { if (affine) QAT_CS(1, 4, true); else QAT_CS(1, 4, false); }
+  if (keys) QAT_CS(kMMKeys);
+  else QAT_CS(kMMNone);
 #undef QAT_CS
 }
 
-qat_status launch_col_stats(qat_dtype dt, int mode, int bits, bool affine, const void* x,
-                            int64_t rows, int64_t cols, void* ws, float* out0, float* out1,
-                            float* out2, int32_t* zp, int32_t* flags, cudaStream_t s) {
-  const ColWs w = col_ws(ws, cols);
+qat_status launch_col_stats(qat_dtype dt, bool keys, const void* x, int64_t rows, int64_t cols,
+                            void* ws, int32_t* flags, cudaStream_t s) {
+  uint4* acc = col_ws(ws, cols).acc;
   if (dt == QAT_F32)
-    col_stats_t<F32>(mode, bits, affine, x, rows, cols, w, out0, out1, out2, zp, flags, s);
+    col_stats_t<F32>(keys, x, rows, cols, acc, flags, s);
   else
-    col_stats_t<BF16>(mode, bits, affine, x, rows, cols, w, out0, out1, out2, zp, flags, s);
+    col_stats_t<BF16>(keys, x, rows, cols, acc, flags, s);
   count_launch(2);
+  return launch_status();
+}
+
+qat_status launch_col_finalize(int mode, int bits, bool affine, void* ws, int64_t cols, float* out0,
+                               float* out1, float* out2, int32_t* zp, int32_t* flags,
+                               cudaStream_t s) {
+  const ColWs w = col_ws(ws, cols);
+  const unsigned g = (unsigned)((cols + 255) / 256);
+#define QAT_CF(M, B, A) \
+  k_col_finalize<M, B, A><<<g, 256, 0, s>>>(w.acc, cols, out0, out1, out2, zp, w.dead, flags)
+  if (mode == 0) QAT_CF(0, 8, false);
+  else if (bits == 8) { if (affine) QAT_CF(1, 8, true); else QAT_CF(1, 8, false); }
+  else { if (affine) QAT_CF(1, 4, true); else QAT_CF(1, 4, false); }
+#undef QAT_CF
+  count_launch(1);
   return launch_status();
 }
 #endif  // !QAT_SR
 
 template <typename T, int BITS, bool AFFINE>
-static void int_cols_t(const void* x, int64_t rows, int64_t cols, const ColWs& w, const SrCtx& sr,
-                       void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
+static void int_cols_t(const void* x, int64_t rows, int64_t cols, const uint4* acc, float* scale,
+                       int32_t* zp, const SrCtx& sr, void* y, void* codes, uint32_t* mask,
+                       int32_t* flags, cudaStream_t s) {
   // one wave of 2 blocks per SM (their staged tiles fill the shared memory)
   const ColShape g = col_shape(rows, cols, kColStrip<T>, 2, 8, 1);
   const int tr = col_tile_rows((int64_t)kColStrip<T> * g.wc, T::BYTES);
   const dim3 grid((unsigned)g.strips, (unsigned)g.chunks);
   col_staged_smem<k_int_cols<T, BITS, AFFINE, QAT_SR>>();
   k_int_cols<T, BITS, AFFINE, QAT_SR><<<grid, 256, kColStagedBytes, s>>>(
-      x, rows, cols, g.wc, g.rchunk, tr, static_cast<const ColP*>(w.table), sr, y, codes, mask,
-      flags);
+      x, rows, cols, g.wc, g.rchunk, tr, acc, scale, zp, sr, y, codes, mask, flags);
 }
 
 qat_status QAT_SR_NAME(launch_int_cols)(qat_dtype dt, int bits, bool affine, const void* x,
-                                        int64_t rows, int64_t cols, const void* ws,
-                                        const SrCtx& sr, void* y, void* codes, uint32_t* mask,
-                                        int32_t* flags, cudaStream_t s) {
-  const ColWs w = col_ws(const_cast<void*>(ws), cols);
-#define QAT_IC(T, B, A) int_cols_t<T, B, A>(x, rows, cols, w, sr, y, codes, mask, flags, s)
+                                        int64_t rows, int64_t cols, const void* ws, float* scale,
+                                        int32_t* zp, const SrCtx& sr, void* y, void* codes,
+                                        uint32_t* mask, int32_t* flags, cudaStream_t s) {
+  const uint4* acc = col_ws(const_cast<void*>(ws), cols).acc;
+#define QAT_IC(T, B, A) \
+  int_cols_t<T, B, A>(x, rows, cols, acc, scale, zp, sr, y, codes, mask, flags, s)
   if (dt == QAT_F32) {
     if (bits == 8) { if (affine) QAT_IC(F32, 8, true); else QAT_IC(F32, 8, false); }
     else { if (affine) QAT_IC(F32, 4, true); else QAT_IC(F32, 4, false); }

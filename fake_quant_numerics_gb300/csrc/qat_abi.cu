@@ -155,8 +155,9 @@ qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t 
     if (cols > kMaxColumns) return QAT_ERR_UNSUPPORTED;
     if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
     if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
-    return launch_col_stats(dtype, 0, 8, false, x, rows, cols, ws, absmax, minv, maxv, nullptr,
-                            flags, s);
+    qat_status st = launch_col_stats(dtype, true, x, rows, cols, ws, flags, s);
+    if (st) return st;
+    return launch_col_finalize(0, 8, false, ws, cols, absmax, minv, maxv, nullptr, flags, s);
   }
   if (fused_units_supported(dtype, L))
     return launch_int_fused(dtype, 8, false, true, x, units, L, nullptr, nullptr, absmax, minv, maxv,
@@ -219,15 +220,17 @@ static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t ro
   int32_t* zpu = (affine && !zp) ? ws_zp(ws, cols, g, units) : zp;
   qat_status st;
   if (col) {
-    // column statistics and calibration, then the strip map (whole mask
-    // words per warp row) or the unit kernel
-    st = launch_col_stats(dtype, 1, bits, affine, x, rows, cols, ws, scale, nullptr, nullptr, zpu,
-                          flags, s);
+    // column statistics, then the strip map that calibrates its columns
+    // (whole mask words per warp row), or the calibration and the unit kernel
+    st = launch_col_stats(dtype, affine, x, rows, cols, ws, flags, s);
     if (st) return st;
     if (cols % 32 == 0) {
       auto map_cols = sr ? launch_int_cols_sr : launch_int_cols;
-      return map_cols(dtype, bits, affine, x, rows, cols, ws, c, y, codes, mask, flags, s);
+      return map_cols(dtype, bits, affine, x, rows, cols, ws, scale, zp, c, y, codes, mask, flags,
+                      s);
     }
+    st = launch_col_finalize(1, bits, affine, ws, cols, scale, nullptr, nullptr, zpu, flags, s);
+    if (st) return st;
   } else {
     // fallback: calibrate every unit, then the flat map with per-unit arrays
     st = launch_unit_generic(dtype, 1, bits, affine, x, units, L, nullptr, nullptr, nullptr, scale,

@@ -70,50 +70,45 @@ QAT_DECL_INT_FUSED(launch_int_fused);
 QAT_DECL_INT_FUSED(launch_int_fused_sr);  // stats_only unsupported
 
 // per-column units of a row-major [rows, cols] tensor.  Workspace layout:
-// one 16-byte statistics accumulator per column, one 32-byte parameter
-// record per column, a counter per strip of 128 columns, then the unit-kernel
+// one 16-byte statistics accumulator per column, then the unit-kernel
 // fallback's dead bytes and zero points (each array rounded up to 16 bytes).
-constexpr int kColRecordBytes = 32;
 struct ColWs {
   uint4* acc;
-  void* table;
-  uint32_t* cnt;
   uint8_t* dead;
   int32_t* zp;
 };
 inline int64_t col_r16(int64_t b) { return (b + 15) / 16 * 16; }
 inline size_t col_ws_bytes(int64_t cols) {
-  return (size_t)(cols * (16 + kColRecordBytes) + col_r16((cols + 127) / 128 * 4) + col_r16(cols) +
-                  col_r16(cols * 4));
+  return (size_t)(cols * 16 + col_r16(cols) + col_r16(cols * 4));
 }
 inline ColWs col_ws(void* ws, int64_t cols) {
   char* p = static_cast<char*>(ws);
   ColWs w;
   w.acc = reinterpret_cast<uint4*>(p);
   p += cols * 16;
-  w.table = p;
-  p += cols * kColRecordBytes;
-  w.cnt = reinterpret_cast<uint32_t*>(p);
-  p += col_r16((cols + 127) / 128 * 4);
   w.dead = reinterpret_cast<uint8_t*>(p);
   p += col_r16(cols);
   w.zp = reinterpret_cast<int32_t*>(p);
   return w;
 }
-// Column statistics (two launches).  mode 0: absmax / min / max into out0 /
-// out1 / out2 (each nullable) and QAT_FLAG_NONFINITE_INPUT; mode 1: the
-// calibration of the int grid (bits, affine): scale into out0, zero points
-// into zp (nullable), the dead bytes and records into the workspace, the
-// calibration flags.
-qat_status launch_col_stats(qat_dtype dt, int mode, int bits, bool affine, const void* x,
-                            int64_t rows, int64_t cols, void* ws, float* out0, float* out1,
-                            float* out2, int32_t* zp, int32_t* flags, cudaStream_t s);
-// the calibrated per-column map from the records (cols % 32 == 0); flags
-// receives QAT_FLAG_DEVICE_TIMEOUT if a staged copy wait runs out
+// Column statistics into the accumulators (two launches; keys: min / max
+// order keys, else the absmax alone).  flags receives
+// QAT_FLAG_DEVICE_TIMEOUT if a staged copy wait runs out.
+qat_status launch_col_stats(qat_dtype dt, bool keys, const void* x, int64_t rows, int64_t cols,
+                            void* ws, int32_t* flags, cudaStream_t s);
+// Accumulators -> mode 0: absmax / min / max into out0 / out1 / out2 (each
+// nullable) and QAT_FLAG_NONFINITE_INPUT; mode 1: the calibration of the int
+// grid (bits, affine): scale into out0, zero points into zp (nullable), the
+// dead bytes into the workspace, the calibration flags.
+qat_status launch_col_finalize(int mode, int bits, bool affine, void* ws, int64_t cols, float* out0,
+                               float* out1, float* out2, int32_t* zp, int32_t* flags,
+                               cudaStream_t s);
+// The calibrated per-column map (cols % 32 == 0) from the accumulators: it
+// calibrates every column itself and writes scale and zero point (nullable)
 #define QAT_DECL_INT_COLS(name)                                                                 \
   qat_status name(qat_dtype dt, int bits, bool affine, const void* x, int64_t rows,             \
-                  int64_t cols, const void* ws, const SrCtx& sr, void* y, void* codes,          \
-                  uint32_t* mask, int32_t* flags, cudaStream_t s)
+                  int64_t cols, const void* ws, float* scale, int32_t* zp, const SrCtx& sr,     \
+                  void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s)
 QAT_DECL_INT_COLS(launch_int_cols);
 QAT_DECL_INT_COLS(launch_int_cols_sr);
 

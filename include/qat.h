@@ -117,10 +117,9 @@ const char* qat_status_string(qat_status status);
  * partial statistics (16 KiB); per row / per group, five bytes per unit
  * (a dead byte and a zero point, each array rounded up to 16 bytes), used
  * only by the fallback for unit lengths the fused single-pass kernels do not
- * cover; per column, 53 bytes per column and 4 per 128 columns (a 16-byte
- * statistics accumulator and a 32-byte parameter record per column, a
- * counter per 128 columns, then the fallback's dead byte and zero point, each
- * array rounded up to 16 bytes), used by every calibrated call.  The workspace is scratch: its contents on entry do not matter and
+ * cover; per column, 21 bytes per column (a 16-byte statistics accumulator,
+ * then the fallback's dead byte and zero point, each array rounded up to 16
+ * bytes), used by every calibrated call.  The workspace is scratch: its contents on entry do not matter and
  * are overwritten.  Two calls that use the same workspace must be ordered on
  * one stream.
  */

@@ -46,10 +46,9 @@ def test_workspace_bytes(lib):
     assert lib.qat_workspace_bytes(4096, 4096, L.PER_ROW, 0) == 4096 * 5
     assert lib.qat_workspace_bytes(14336, 4096, L.PER_GROUP, 128) == 14336 * 32 * 5
     assert lib.qat_workspace_bytes(3, 5, L.PER_ROW, 0) == 16 + 16
-    # per column: a 16-byte accumulator and a 32-byte record per column, a
-    # counter per 128 columns, then the fallback's arrays
-    assert lib.qat_workspace_bytes(4096, 4096, L.PER_COLUMN, 0) == 4096 * 48 + 128 + 4096 + 16384
-    assert lib.qat_workspace_bytes(7, 33, L.PER_COLUMN, 0) == 33 * 48 + 16 + 48 + 144
+    # per column: a 16-byte accumulator per column, then the fallback's arrays
+    assert lib.qat_workspace_bytes(4096, 4096, L.PER_COLUMN, 0) == 4096 * 16 + 4096 + 16384
+    assert lib.qat_workspace_bytes(7, 33, L.PER_COLUMN, 0) == 33 * 16 + 48 + 144
 
 
 def _int(lib, **kw):
