@@ -95,6 +95,14 @@ def lib():
         L.or_adam_update.argtypes = [vp, vp, vp, vp, i64, f32, f32, f32, f32, f32, f32, f32]
         L.or_qat_optimizer_step.argtypes = [vp, vp, vp, vp, i64, f32, f32, f32, f32, f32, f32, f32,
                                             i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, vp, vp]
+        L.or_round_fp16.argtypes = [f32]
+        L.or_round_fp16.restype = f32
+        L.or_fake_quant_int_opts.argtypes = [vp, i32, i64, i64, i32, i32, i32, i64, f32, i32, i32,
+                                             u64, u64, vp, vp, vp, vp, vp, vp]
+        f64 = ctypes.c_double
+        L.or_percentile_minmax.argtypes = [vp, i32, i64, f64, vp, vp, vp]
+        L.or_fake_quant_int_percentile.argtypes = [vp, i32, i64, i32, i32, f64, i32, u64, u64, vp,
+                                                   vp, vp, vp, vp, vp]
     return _lib
 
 
@@ -254,6 +262,67 @@ def fake_quant_int_sr(x: np.ndarray, rows: int, cols: int, bits: int, scheme: in
     if st:
         raise ValueError(f"oracle fake_quant_int_sr status {st}")
     return dict(y=y, codes=codes, mask=mask, scale=sc[:u], zero_point=zp[:u], flags=flags.value)
+
+
+def round_fp16(x) -> np.ndarray:
+    """IEEE binary16 rounding (nearest, ties to even) of binary32 values, as binary32."""
+    a = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    return np.array([lib().or_round_fp16(float(v)) for v in a], np.float32).reshape(np.shape(x))
+
+
+def fake_quant_int_opts(x: np.ndarray, rows: int, cols: int, bits: int, scheme: int,
+                        granularity: int, group: int = 0, clip: float = 1.0, fp16: bool = False,
+                        stochastic: bool = False, seed: int = 0, offset: int = 0):
+    """Calibrated fake_quant_int with the range options (clip factor in (0, 1],
+    binary16 scales); returns dict(y, codes, mask, scale, zero_point, flags)."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    dt = _dtype_code(x)
+    n = rows * cols
+    u = n_units(rows, cols, granularity, group) if (granularity != PER_GROUP or group > 0) else 0
+    sc = np.zeros(max(u, 1), np.float32)
+    zp = np.zeros(max(u, 1), np.int32)
+    y = np.empty(n, dtype=x.dtype)
+    codes = np.empty(n, np.int8) if bits == 8 else np.empty((n + 1) // 2, np.uint8)
+    mask = np.empty((n + 31) // 32, np.uint32)
+    flags = ctypes.c_int32(0)
+    st = lib().or_fake_quant_int_opts(_p(x), dt, rows, cols, bits, scheme, granularity, group,
+                                      float(np.float32(clip)), int(fp16), int(stochastic), seed,
+                                      offset, _p(sc), _p(zp), _p(y), _p(codes), _p(mask),
+                                      ctypes.byref(flags))
+    if st:
+        raise ValueError(f"oracle fake_quant_int_opts status {st}")
+    return dict(y=y, codes=codes, mask=mask, scale=sc[:u], zero_point=zp[:u], flags=flags.value)
+
+
+def percentile_minmax(x: np.ndarray, clip_fraction: float):
+    """(lo, hi, flags): the nearest-rank quantiles of per_tensor_percentile."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    lo, hi, fl = ctypes.c_float(), ctypes.c_float(), ctypes.c_int32(0)
+    st = lib().or_percentile_minmax(_p(x), _dtype_code(x), x.size, float(clip_fraction),
+                                    ctypes.byref(lo), ctypes.byref(hi), ctypes.byref(fl))
+    if st:
+        raise ValueError(f"oracle percentile_minmax status {st}")
+    return np.float32(lo.value), np.float32(hi.value), fl.value
+
+
+def fake_quant_int_percentile(x: np.ndarray, bits: int, scheme: int, clip_fraction: float,
+                              stochastic: bool = False, seed: int = 0, offset: int = 0):
+    """Per-tensor fake quant calibrated by per_tensor_percentile; returns
+    dict(y, codes, mask, scale, zero_point, flags)."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    n = x.size
+    s, z, fl = ctypes.c_float(), ctypes.c_int32(), ctypes.c_int32(0)
+    y = np.empty(n, dtype=x.dtype)
+    codes = np.empty(n, np.int8) if bits == 8 else np.empty((n + 1) // 2, np.uint8)
+    mask = np.empty((n + 31) // 32, np.uint32)
+    st = lib().or_fake_quant_int_percentile(_p(x), _dtype_code(x), n, bits, scheme,
+                                            float(clip_fraction), int(stochastic), seed, offset,
+                                            ctypes.byref(s), ctypes.byref(z), _p(y), _p(codes),
+                                            _p(mask), ctypes.byref(fl))
+    if st:
+        raise ValueError(f"oracle fake_quant_int_percentile status {st}")
+    return dict(y=y, codes=codes, mask=mask, scale=np.array([s.value], np.float32),
+                zero_point=np.array([z.value], np.int32), flags=fl.value)
 
 
 def fake_quant_fp8_sr(x: np.ndarray, fmt: int, seed: int = 0, offset: int = 0, scale=None,

@@ -34,6 +34,10 @@
  *          and the Weyl key schedule as published)
  *   [QAT]  QatConfig, QatOptimizer::{step, requantize} (Adam/AdamW update of
  *          the master weights, then the fake-quant view)
+ *   [QAT]  QuantParams::per_tensor_percentile (nearest-rank quantiles, then
+ *          from_minmax); per_channel_params with axis 1 (per-column units)
+ *   [EDU]  demo 2 (the range c * max|x|: clip factor), demo 3 (one FP16
+ *          scale per group); IEEE 754 binary16 (round to nearest, ties to even)
  *
  * Every place where the sources are silent and a reading was taken is marked
  * "reading:" below.
@@ -163,6 +167,27 @@ void or_unit_stats(const void* x, int dtype, int64_t off, int64_t len, float* mn
 /* Returns 0 on success, OR_FLAG_DEGENERATE when absmax <= 0 or the scale is  */
 /* not a positive finite number.                                              */
 /* ------------------------------------------------------------------------- */
+/* ------------------------------------------------------------------------- */
+/* IEEE binary16 rounding of a binary32 value (round to nearest, ties to     */
+/* even): the grid step is 2^(e-10) for a normal binary16 exponent e in      */
+/* [-14, 15] and 2^-24 below 2^-14 (subnormals); a magnitude that rounds past */
+/* the largest finite value 65504 (i.e. >= 65520) becomes infinity.  x / step */
+/* and k * step are exact power-of-two scalings in binary32.  Used for fp16   */
+/* group scales ([EDU] demo 3: one FP16 scale per group).                     */
+/* ------------------------------------------------------------------------- */
+float or_round_fp16(float x) {
+  if (isnan(x) || isinf(x) || x == 0.0f) return x;
+  float a = fabsf(x);
+  if (a >= 65520.0f) return copysignf(INFINITY, x);
+  int e;
+  frexpf(a, &e); /* a = f * 2^e, f in [0.5, 1): the binary exponent is e - 1 */
+  int ex = e - 1;
+  if (ex < -14) ex = -14; /* subnormal binary16: step 2^-24 */
+  float step = ldexpf(1.0f, ex - 10);
+  float k = rintf(a / step);
+  return copysignf(k * step, x);
+}
+
 int or_params_from_absmax(float absmax, int32_t qmax, float* scale) {
   if (!(absmax > 0.0f) || isinf(absmax)) { *scale = absmax / (float)qmax; return OR_FLAG_DEGENERATE; }
   float s = absmax / (float)qmax;
@@ -336,10 +361,50 @@ static void set_mask(uint32_t* mask, int64_t i, int bit) {
 /* A unit that fails calibration (flag set) or has invalid given params gets  */
 /* codes 0, y = +0, mask 0.  reading: the module returns an error there.      */
 /* ------------------------------------------------------------------------- */
+/* Calibration with the range options: the observed absmax (symmetric) or
+ * min and max (affine) times the clip factor c, one binary32 product each
+ * ([EDU] demo 2: the range c * max|x|, values beyond it clip; reading: for
+ * the affine scheme the same factor scales both ends, so 0 stays inside);
+ * with fp16 set the scale is rounded to binary16 and that value is the
+ * unit's scale (reading of the FP16 group scales of [EDU] demo 3), the zero
+ * point derived from it.  c = 1 and fp16 = 0 are the module's calibration. */
+static int calib_opts(int scheme, float mn, float mx, float A, int32_t qmin, int32_t qmax, float c,
+                      int fp16, float* s, int32_t* z) {
+  int flag;
+  if (scheme == OR_SYM) {
+    *z = 0;
+    float Ac = (c == 1.0f) ? A : c * A;
+    if (!fp16) return or_params_from_absmax(Ac, qmax, s);
+    flag = or_params_from_absmax(Ac, qmax, s);
+    *s = or_round_fp16(*s);
+    if (!flag && (!(*s > 0.0f) || isinf(*s))) flag = OR_FLAG_DEGENERATE;
+    return flag;
+  }
+  if (c != 1.0f) {
+    mn = c * mn;
+    mx = c * mx;
+  }
+  if (!fp16) return or_params_affine(mn, mx, qmin, qmax, s, z);
+  /* from_minmax with the binary16 scale */
+  float rmin = (mn < 0.0f) ? mn : 0.0f;
+  float rmax = (mx > 0.0f) ? mx : 0.0f;
+  float range = rmax - rmin;
+  *s = or_round_fp16(range / (float)(qmax - qmin));
+  *z = 0;
+  if (!(range > 0.0f)) return OR_FLAG_DEGENERATE;
+  if (!(*s > 0.0f) || isinf(*s)) return OR_FLAG_DEGENERATE;
+  float t = (float)qmin - rmin / *s;
+  float zz = rintf(t);
+  if (zz < (float)qmin) zz = (float)qmin;
+  if (zz > (float)qmax) zz = (float)qmax;
+  *z = (int32_t)zz;
+  return 0;
+}
+
 static int fq_int(const void* x, int dtype, int64_t rows, int64_t cols, int bits, int scheme,
                   int gran, int64_t group, int params_given, float* scale, int32_t* zp, void* y,
                   void* codes, uint32_t* mask, int32_t* flags, int doc_form, int stochastic,
-                  uint64_t seed, uint64_t offset) {
+                  uint64_t seed, uint64_t offset, float clip, int fp16) {
   int32_t qmin, qmax;
   int st = or_q_range(bits, scheme, &qmin, &qmax);
   if (st) return st;
@@ -375,12 +440,7 @@ static int fq_int(const void* x, int dtype, int64_t rows, int64_t cols, int bits
       float mn, mx, A;
       int64_t bad;
       or_unit_stats_strided(x, dtype, off, L, stride, &mn, &mx, &A, &bad);
-      if (scheme == OR_SYM) {
-        z = 0;
-        flag = or_params_from_absmax(A, qmax, &s);
-      } else {
-        flag = or_params_affine(mn, mx, qmin, qmax, &s, &z);
-      }
+      flag = calib_opts(scheme, mn, mx, A, qmin, qmax, clip, fp16, &s, &z);
       if (bad) flag = OR_FLAG_NONFINITE;
       scale[u] = s;
       if (zp) zp[u] = z;
@@ -410,7 +470,7 @@ int or_fake_quant_int(const void* x, int dtype, int64_t rows, int64_t cols, int 
                       int gran, int64_t group, int params_given, float* scale, int32_t* zp,
                       void* y, void* codes, uint32_t* mask, int32_t* flags, int doc_form) {
   return fq_int(x, dtype, rows, cols, bits, scheme, gran, group, params_given, scale, zp, y, codes,
-                mask, flags, doc_form, 0, 0, 0);
+                mask, flags, doc_form, 0, 0, 0, 1.0f, 0);
 }
 
 /* The same with stochastic rounding: element i rounds with the draw
@@ -421,7 +481,113 @@ int or_fake_quant_int_sr(const void* x, int dtype, int64_t rows, int64_t cols, i
                          int32_t* zp, uint64_t seed, uint64_t offset, void* y, void* codes,
                          uint32_t* mask, int32_t* flags) {
   return fq_int(x, dtype, rows, cols, bits, scheme, gran, group, params_given, scale, zp, y, codes,
-                mask, flags, 1, 1, seed, offset);
+                mask, flags, 1, 1, seed, offset, 1.0f, 0);
+}
+
+/* Calibrated integer fake quant with the range options (clip factor c in
+ * (0, 1], binary16 scales), nearest or stochastic rounding. */
+int or_fake_quant_int_opts(const void* x, int dtype, int64_t rows, int64_t cols, int bits,
+                           int scheme, int gran, int64_t group, float clip, int fp16,
+                           int stochastic, uint64_t seed, uint64_t offset, float* scale,
+                           int32_t* zp, void* y, void* codes, uint32_t* mask, int32_t* flags) {
+  if (!(clip > 0.0f) || !(clip <= 1.0f)) return OR_ERR_INVALID;
+  return fq_int(x, dtype, rows, cols, bits, scheme, gran, group, 0, scale, zp, y, codes, mask,
+                flags, 1, stochastic, seed, offset, clip, fp16);
+}
+
+/* ------------------------------------------------------------------------- */
+/* [QAT] QuantParams::per_tensor_percentile: the values sorted in the total   */
+/* order (-0 before +0), last = n - 1, the nearest-rank quantiles             */
+/* lo = sorted[floor(c * last)] and hi = sorted[min(ceil((1 - c) * last),     */
+/* last)] with the index products in binary64 as printed, then from_minmax:   */
+/* symmetric from_absmax(max(|lo|, |hi|)), affine the min/max calibration.    */
+/* c outside [0, 0.5) is an error; a non-finite value anywhere is the         */
+/* module's calibration error, reported as OR_FLAG_NONFINITE (the tensor is   */
+/* then a failed unit: codes 0, y = +0, mask 0).                              */
+/* ------------------------------------------------------------------------- */
+static int cmp_total(const void* a, const void* b) {
+  float x = *(const float*)a, y = *(const float*)b;
+  if (x < y) return -1;
+  if (x > y) return 1;
+  /* equal values: only the zeros differ, -0 first */
+  return (int)(signbit(y) != 0) - (int)(signbit(x) != 0);
+}
+
+int or_percentile_minmax(const void* x, int dtype, int64_t n, double clip_fraction, float* lo,
+                         float* hi, int32_t* flags) {
+  if (!(clip_fraction >= 0.0 && clip_fraction < 0.5)) return OR_ERR_INVALID;
+  if (n <= 0) return OR_ERR_INVALID;
+  float* v = (float*)malloc((size_t)n * sizeof(float));
+  if (!v) return OR_ERR_INVALID;
+  int bad = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    v[i] = load_elem(x, dtype, i);
+    if (!isfinite(v[i])) bad = 1;
+  }
+  if (bad) {
+    free(v);
+    *lo = *hi = 0.0f;
+    if (flags) *flags |= OR_FLAG_NONFINITE;
+    return OR_OK;
+  }
+  qsort(v, (size_t)n, sizeof(float), cmp_total);
+  int64_t last = n - 1;
+  int64_t lo_idx = (int64_t)floor(clip_fraction * (double)last);
+  int64_t hi_idx = (int64_t)ceil((1.0 - clip_fraction) * (double)last);
+  if (lo_idx > last) lo_idx = last;
+  if (hi_idx > last) hi_idx = last;
+  *lo = v[lo_idx];
+  *hi = v[hi_idx];
+  free(v);
+  return OR_OK;
+}
+
+/* Per-tensor fake quant of x[n] calibrated by per_tensor_percentile, nearest
+ * or stochastic rounding (elements beyond the quantiles clamp to the code
+ * range). */
+int or_fake_quant_int_percentile(const void* x, int dtype, int64_t n, int bits, int scheme,
+                                 double clip_fraction, int stochastic, uint64_t seed,
+                                 uint64_t offset, float* scale, int32_t* zp, void* y, void* codes,
+                                 uint32_t* mask, int32_t* flags) {
+  int32_t qmin, qmax;
+  int st = or_q_range(bits, scheme, &qmin, &qmax);
+  if (st) return st;
+  if (!(clip_fraction >= 0.0 && clip_fraction < 0.5) || n < 0) return OR_ERR_INVALID;
+  if (n == 0) return OR_OK;
+  float lo, hi;
+  int32_t f = 0;
+  st = or_percentile_minmax(x, dtype, n, clip_fraction, &lo, &hi, &f);
+  if (st) return st;
+  float s;
+  int32_t z = 0;
+  int flag;
+  if (f) {
+    flag = OR_FLAG_NONFINITE;
+    s = 0.0f;
+  } else if (scheme == OR_SYM) {
+    flag = or_params_from_absmax(fmaxf(fabsf(lo), fabsf(hi)), qmax, &s);
+  } else {
+    flag = or_params_affine(lo, hi, qmin, qmax, &s, &z);
+  }
+  *scale = s;
+  if (zp) *zp = z;
+  if (flags) *flags |= flag;
+  if (codes && bits == 4) memset(codes, 0, (size_t)((n + 1) / 2));
+  if (mask) memset(mask, 0, (size_t)((n + 31) / 32) * 4);
+  for (int64_t i = 0; i < n; ++i) {
+    float v = load_elem(x, dtype, i);
+    if (flag) {
+      set_code(codes, bits, i, 0);
+      if (y) store_elem(y, dtype, i, 0.0f);
+      continue;
+    }
+    int32_t q = stochastic ? or_quantize_sr(v, s, z, qmin, qmax, or_sr_uniform(seed, offset, i))
+                           : or_quantize(v, s, z, qmin, qmax, 1);
+    set_code(codes, bits, i, q);
+    if (y) store_elem(y, dtype, i, or_dequantize(q, s, z));
+    set_mask(mask, i, in_window(v, s, z, qmin, qmax));
+  }
+  return OR_OK;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -622,7 +788,7 @@ int or_qat_optimizer_step(float* w, const float* g, float* m, float* v, int64_t 
   if (n == 0) return OR_OK;
   if (bits == 8 || bits == 4)
     return fq_int(w, OR_F32, 1, n, bits, scheme, OR_PER_TENSOR, 0, 0, scale, zp, view, codes, mask,
-                  flags, 1, stochastic, seed, offset);
+                  flags, 1, stochastic, seed, offset, 1.0f, 0);
   if (bits != 0) return OR_ERR_UNSUPPORTED;
   *scale = 1.0f;
   return fq_fp8(w, OR_F32, n, fmt, 1, scale, view, (uint8_t*)codes, mask, flags, stochastic, seed,
