@@ -45,6 +45,11 @@ class AdamHparams(ctypes.Structure):
                 ("bias_correction1", ctypes.c_float), ("bias_correction2", ctypes.c_float)]
 
 
+class CalibOptions(ctypes.Structure):
+    """qat_calib_options (include/qat.h)."""
+    _fields_ = [("clip", ctypes.c_float), ("scale_fp16", ctypes.c_int)]
+
+
 PROTOTYPES = {
     "qat_status_string": ([_int], ctypes.c_char_p),
     "qat_workspace_bytes": ([_i64, _i64, _int, _i64], _sz),
@@ -53,6 +58,8 @@ PROTOTYPES = {
                             _vp, _vp, _vp, _sz, _vp], _int),
     "qat_fake_quant_fp8": ([_vp, _int, _i64, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _int),
     "qat_fake_quant_fp8_noalloc": ([_vp, _int, _i64, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp], _int),
+    "qat_fake_quant_int_opts": ([_vp, _int, _i64, _i64, _int, _int, _int, _i64, _vp, _int, _u64, _u64,
+                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _int),
     "qat_fake_quant_int_sr": ([_vp, _int, _i64, _i64, _int, _int, _int, _i64, _int, _vp, _vp, _u64,
                                _u64, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _int),
     "qat_optimizer_step": ([_vp, _vp, _vp, _vp, _i64, ctypes.POINTER(AdamHparams), _int, _int, _int,

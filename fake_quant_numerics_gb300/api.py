@@ -107,6 +107,23 @@ def qat_fake_quant_int_sr(x, rows, cols, bits, scheme, granularity, group, param
     _lib.check("qat_fake_quant_int_sr", st)
 
 
+def calib_options(clip: float = 1.0, scale_fp16: bool = False) -> "_lib.CalibOptions":
+    """qat_calib_options: the calibrated range times clip (in (0, 1]), binary16 scales."""
+    return _lib.CalibOptions(float(clip), int(bool(scale_fp16)))
+
+
+def qat_fake_quant_int_opts(x, rows, cols, bits, scheme, granularity, group, options, stochastic,
+                            seed, offset, scale, zero_point, y, codes, mask, dev_flags, workspace,
+                            stream=None):
+    opt = ctypes.byref(options) if options is not None else None
+    st = _lib.lib().qat_fake_quant_int_opts(_p(x), _dt(x), rows, cols, bits, _SCHEME[scheme],
+                                            _GRAN[granularity], group, opt, int(bool(stochastic)),
+                                            int(seed), int(offset), _p(scale), _p(zero_point),
+                                            _p(y), _p(codes), _p(mask), _p(dev_flags),
+                                            _p(workspace), _nbytes(workspace), _s(stream))
+    _lib.check("qat_fake_quant_int_opts", st)
+
+
 def qat_fake_quant_fp8_sr(x, n, fmt, scale_given, scale, seed, offset, y, codes, mask, dev_flags,
                           workspace, stream=None):
     st = _lib.lib().qat_fake_quant_fp8_sr(_p(x), _dt(x), n, _FMT[fmt], int(scale_given), _p(scale),
@@ -238,11 +255,14 @@ def fake_quant_int(x: torch.Tensor, bits: int = 8, scheme="symmetric", granulari
                    group: int = 0, scale: Optional[torch.Tensor] = None,
                    zero_point: Optional[torch.Tensor] = None, want_codes: bool = True,
                    want_mask: bool = True, check: bool = False, rounding: str = "nearest",
-                   seed: int = 0, offset: int = 0) -> FakeQuantInt:
+                   seed: int = 0, offset: int = 0, clip: float = 1.0,
+                   scale_fp16: bool = False) -> FakeQuantInt:
     """Integer fake quantization of x (float32 or bfloat16, CUDA), calibrated per
     tensor / row / group / column (of the last dimension), or with the given
     per-unit scale and zero point.
-    rounding="stochastic" rounds with the counter-based draws of (seed, offset)."""
+    rounding="stochastic" rounds with the counter-based draws of (seed, offset).
+    clip (in (0, 1]) shrinks the calibrated range; scale_fp16 rounds the
+    calibrated scales to binary16 (calibrated calls only)."""
     x = _ready(x)
     rows, cols = _shape2d(x)
     n = x.numel()
@@ -273,7 +293,15 @@ def fake_quant_int(x: torch.Tensor, bits: int = 8, scheme="symmetric", granulari
     flags = torch.zeros(1, dtype=torch.int32, device=dev)
     wsb = qat_workspace_bytes(rows, cols, gran, group)
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
-    if rounding == "stochastic":
+    if rounding not in ("nearest", "stochastic"):
+        raise ValueError(f"rounding must be 'nearest' or 'stochastic', not {rounding!r}")
+    if clip != 1.0 or scale_fp16:
+        if given:
+            raise ValueError("clip and scale_fp16 apply to calibrated calls only")
+        qat_fake_quant_int_opts(x, rows, cols, bits, sch, gran, group,
+                                calib_options(clip, scale_fp16), rounding == "stochastic", seed,
+                                offset, scale, zero_point, y, codes, mask, flags, ws)
+    elif rounding == "stochastic":
         qat_fake_quant_int_sr(x, rows, cols, bits, sch, gran, group, given, scale, zero_point, seed,
                               offset, y, codes, mask, flags, ws)
     elif rounding == "nearest":
@@ -290,7 +318,9 @@ def fake_quant_fp8(x: torch.Tensor, fmt="e4m3", scale: Optional[float] = None,
                    want_codes: bool = False, want_mask: bool = True, rounding: str = "nearest",
                    seed: int = 0, offset: int = 0) -> FakeQuantFp8:
     """Per-tensor amax-scaled (or given-scale) saturating FP8 fake quantization;
-    rounding="stochastic" rounds with the counter-based draws of (seed, offset)."""
+    rounding="stochastic" rounds with the counter-based draws of (seed, offset).
+    clip (in (0, 1]) shrinks the calibrated range; scale_fp16 rounds the
+    calibrated scales to binary16 (calibrated calls only)."""
     x = _ready(x)
     n = x.numel()
     dev = x.device

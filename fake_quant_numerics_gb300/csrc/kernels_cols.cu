@@ -323,7 +323,7 @@ __device__ __forceinline__ Stats col_acc_stats(const uint4& a) {
 // and the calibration flags.
 template <int MODE, int BITS, bool AFFINE>
 __global__ void k_col_finalize(const uint4* __restrict__ acc, int64_t cols, float* out0,
-                               float* out1, float* out2, int32_t* zp, uint8_t* dead,
+                               float* out1, float* out2, int32_t* zp, uint8_t* dead, CalOpts co,
                                int32_t* flags) {
   constexpr int MM = (MODE == 0 || AFFINE) ? kMMKeys : kMMNone;
   const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -337,7 +337,7 @@ __global__ void k_col_finalize(const uint4* __restrict__ acc, int64_t cols, floa
       f = s.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0;
     } else {
       IntParams p;
-      f = calibrate<BITS, AFFINE, MM>(s, p);
+      f = calibrate<BITS, AFFINE, MM>(s, p, co);
       out0[c] = p.s;
       if (zp) zp[c] = p.zp;
       dead[c] = (uint8_t)p.dead;
@@ -553,13 +553,13 @@ __device__ __forceinline__ void col_slow_elem(float x, float u, const ColR& c, b
 // Two elements of two fast calibrated columns a, b (finite values): the
 // exact quotient RN(x / s) (the Markstein step of quotient_rn2 with a
 // reciprocal and a scale per element), rint by the magic constant (nearest)
-// or the stochastic rounding with draws ua, ub, the clamp (affine, and every
-// stochastic rounding), y = k s, the code from the bits of k + M, and the
+// or the stochastic rounding with draws ua, ub, the clamp (affine, clampsym,
+// and every stochastic rounding), y = k s, the code from the bits of k + M, and the
 // out-of-window sign bits (whi - |x| symmetric; whi - x, x - wlo affine).
 template <bool AFFINE, bool SR>
 __device__ __forceinline__ void col_pair(float xa, float xb, const ColR& a, const ColR& b,
-                                         float ua, float ub, float& ya, float& yb, int& qa,
-                                         int& qb, uint32_t& oa, uint32_t& ob) {
+                                         float ua, float ub, bool clampsym, float& ya, float& yb,
+                                         int& qa, int& qb, uint32_t& oa, uint32_t& ob) {
   float fa, fb, ra, rb, ta, tb;
   const float nsa = -a.s, nsb = -b.s;
   mul2(xa, xb, a.rcp, b.rcp, fa, fb);
@@ -574,7 +574,7 @@ __device__ __forceinline__ void col_pair(float xa, float xb, const ColR& a, cons
   } else {
     add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
     sub2(ta, tb, kRintMagic, kRintMagic, fa, fb);
-    if (AFFINE) {
+    if (AFFINE || clampsym) {
       fa = fminf(fmaxf(fa, a.klof), a.khif);
       fb = fminf(fmaxf(fb, b.klof), b.khif);
       add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
@@ -601,8 +601,8 @@ __device__ __forceinline__ void col_pair(float xa, float xb, const ColR& a, cons
 // bit set in `deadm`, give zeros).
 template <typename T, int BITS, bool AFFINE, bool SR, bool SLOW>
 __device__ __forceinline__ uint32_t col_row(const Raw16& b, const ColR (&P)[kColLane<T>],
-                                            uint32_t slowm, uint32_t deadm, const SrCtx& sr,
-                                            int64_t i, void* y, void* codes) {
+                                            uint32_t slowm, uint32_t deadm, bool clampsym,
+                                            const SrCtx& sr, int64_t i, void* y, void* codes) {
   constexpr int NC = kColLane<T>;
   uint32_t yw[4];         // the y row as stored: 4 fp32, or 8 bf16 in pairs
   uint32_t cw[NC / 4];    // the codes as stored
@@ -620,7 +620,8 @@ __device__ __forceinline__ uint32_t col_row(const Raw16& b, const ColR (&P)[kCol
       float ya, yb;
       int qa, qb;
       uint32_t oa, ob;
-      col_pair<AFFINE, SR>(xa, xb, P[j], P[j + 1], u[h], u[h + 1], ya, yb, qa, qb, oa, ob);
+      col_pair<AFFINE, SR>(xa, xb, P[j], P[j + 1], u[h], u[h + 1], clampsym, ya, yb, qa, qb, oa,
+                           ob);
       uint32_t ma = oa ^ 1u, mbb = ob ^ 1u;
       if (SLOW) {
         if ((slowm >> j) & 1u)
@@ -666,8 +667,9 @@ template <typename T, int BITS, bool AFFINE, bool SR, bool SLOW>
 __device__ __forceinline__ void col_map_tile(const char* tile, int nr, uint32_t sb, int cl, int rw,
                                              int nrw, int64_t rs, int64_t cols, int64_t c,
                                              bool active, const ColR (&P)[kColLane<T>],
-                                             uint32_t slowm, uint32_t deadm, const SrCtx& sr,
-                                             void* y, void* codes, uint32_t* mask, int lane) {
+                                             uint32_t slowm, uint32_t deadm, bool clampsym,
+                                             const SrCtx& sr, void* y, void* codes,
+                                             uint32_t* mask, int lane) {
   constexpr int NC = kColLane<T>, LPW = 32 / NC;  // LPW: lanes per mask word
   for (int r = rw; r < nr; r += nrw) {
     const int64_t i = (rs + r) * cols + c;
@@ -675,7 +677,7 @@ __device__ __forceinline__ void col_map_tile(const char* tile, int nr, uint32_t 
     if (active) {
       const uint4 v = *reinterpret_cast<const uint4*>(tile + (size_t)r * sb + cl * T::BYTES);
       const Raw16 cur = {{v.x, v.y, v.z, v.w}};
-      mb = col_row<T, BITS, AFFINE, SR, SLOW>(cur, P, slowm, deadm, sr, i, y, codes);
+      mb = col_row<T, BITS, AFFINE, SR, SLOW>(cur, P, slowm, deadm, clampsym, sr, i, y, codes);
     }
     uint32_t w = mb << (NC * (lane & (LPW - 1)));
 #pragma unroll
@@ -693,7 +695,7 @@ template <typename T, int BITS, bool AFFINE, bool SR>
 __global__ void __launch_bounds__(256, 2)
     k_int_cols(const void* __restrict__ x, int64_t rows, int64_t cols, int wc, int64_t rchunk,
                int tr, const uint4* __restrict__ acc, float* scale, int32_t* zp, SrCtx sr,
-               void* y, void* codes, uint32_t* mask, int32_t* flags) {
+               CalOpts co, void* y, void* codes, uint32_t* mask, int32_t* flags) {
   constexpr int NC = kColLane<T>, WW = kColStrip<T>;
   constexpr int MM = AFFINE ? kMMKeys : kMMNone;
   extern __shared__ __align__(128) char col_stage[];
@@ -730,7 +732,7 @@ __global__ void __launch_bounds__(256, 2)
       p.fast = 0;
       p.rcp = 0.0f;
       if (active) {
-        f |= calibrate<BITS, AFFINE, MM>(col_acc_stats<MM>(acc[c + j]), p);
+        f |= calibrate<BITS, AFFINE, MM>(col_acc_stats<MM>(acc[c + j]), p, co);
         // one writer per column (the warps of other row phases share it)
         if (blockIdx.y == 0 && rw == 0) {
           scale[c + j] = p.s;
@@ -750,14 +752,15 @@ __global__ void __launch_bounds__(256, 2)
     // range also runs the IEEE path for those columns
     slow = __any_sync(kFull, slowm != 0u);
   };
+  const bool clampsym = co.clamp || co.clip != 1.0f || co.fp16;
   col_staged(tl, col_stage, bars, flags, calibrate_columns, [&](const char* tile, int t, int nr) {
     const int64_t rs = tl.r0 + (int64_t)t * tr;
     if (slow)
       col_map_tile<T, BITS, AFFINE, SR, true>(tile, nr, sb, cl, rw, nrw, rs, cols, c, active, P,
-                                              slowm, deadm, sr, y, codes, mask, lane);
+                                              slowm, deadm, clampsym, sr, y, codes, mask, lane);
     else
       col_map_tile<T, BITS, AFFINE, SR, false>(tile, nr, sb, cl, rw, nrw, rs, cols, c, active, P,
-                                               0u, 0u, sr, y, codes, mask, lane);
+                                               0u, 0u, clampsym, sr, y, codes, mask, lane);
   });
 }
 
@@ -823,12 +826,12 @@ qat_status launch_col_stats(qat_dtype dt, bool keys, const void* x, int64_t rows
 }
 
 qat_status launch_col_finalize(int mode, int bits, bool affine, void* ws, int64_t cols, float* out0,
-                               float* out1, float* out2, int32_t* zp, int32_t* flags,
-                               cudaStream_t s) {
+                               float* out1, float* out2, int32_t* zp, const CalOpts& co,
+                               int32_t* flags, cudaStream_t s) {
   const ColWs w = col_ws(ws, cols);
   const unsigned g = (unsigned)((cols + 255) / 256);
 #define QAT_CF(M, B, A) \
-  k_col_finalize<M, B, A><<<g, 256, 0, s>>>(w.acc, cols, out0, out1, out2, zp, w.dead, flags)
+  k_col_finalize<M, B, A><<<g, 256, 0, s>>>(w.acc, cols, out0, out1, out2, zp, w.dead, co, flags)
   if (mode == 0) QAT_CF(0, 8, false);
   else if (bits == 8) { if (affine) QAT_CF(1, 8, true); else QAT_CF(1, 8, false); }
   else { if (affine) QAT_CF(1, 4, true); else QAT_CF(1, 4, false); }
@@ -840,24 +843,25 @@ qat_status launch_col_finalize(int mode, int bits, bool affine, void* ws, int64_
 
 template <typename T, int BITS, bool AFFINE>
 static void int_cols_t(const void* x, int64_t rows, int64_t cols, const uint4* acc, float* scale,
-                       int32_t* zp, const SrCtx& sr, void* y, void* codes, uint32_t* mask,
-                       int32_t* flags, cudaStream_t s) {
+                       int32_t* zp, const SrCtx& sr, const CalOpts& co, void* y, void* codes,
+                       uint32_t* mask, int32_t* flags, cudaStream_t s) {
   // one wave of 2 blocks per SM (their staged tiles fill the shared memory)
   const ColShape g = col_shape(rows, cols, kColStrip<T>, 2, 8, 1);
   const int tr = col_tile_rows((int64_t)kColStrip<T> * g.wc, T::BYTES);
   const dim3 grid((unsigned)g.strips, (unsigned)g.chunks);
   col_staged_smem<k_int_cols<T, BITS, AFFINE, QAT_SR>>();
   k_int_cols<T, BITS, AFFINE, QAT_SR><<<grid, 256, kColStagedBytes, s>>>(
-      x, rows, cols, g.wc, g.rchunk, tr, acc, scale, zp, sr, y, codes, mask, flags);
+      x, rows, cols, g.wc, g.rchunk, tr, acc, scale, zp, sr, co, y, codes, mask, flags);
 }
 
 qat_status QAT_SR_NAME(launch_int_cols)(qat_dtype dt, int bits, bool affine, const void* x,
                                         int64_t rows, int64_t cols, const void* ws, float* scale,
-                                        int32_t* zp, const SrCtx& sr, void* y, void* codes,
-                                        uint32_t* mask, int32_t* flags, cudaStream_t s) {
+                                        int32_t* zp, const SrCtx& sr, const CalOpts& co, void* y,
+                                        void* codes, uint32_t* mask, int32_t* flags,
+                                        cudaStream_t s) {
   const uint4* acc = col_ws(const_cast<void*>(ws), cols).acc;
 #define QAT_IC(T, B, A) \
-  int_cols_t<T, B, A>(x, rows, cols, acc, scale, zp, sr, y, codes, mask, flags, s)
+  int_cols_t<T, B, A>(x, rows, cols, acc, scale, zp, sr, co, y, codes, mask, flags, s)
   if (dt == QAT_F32) {
     if (bits == 8) { if (affine) QAT_IC(F32, 8, true); else QAT_IC(F32, 8, false); }
     else { if (affine) QAT_IC(F32, 4, true); else QAT_IC(F32, 4, false); }

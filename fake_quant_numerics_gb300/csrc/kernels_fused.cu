@@ -20,12 +20,15 @@
 
 namespace qat {
 
-template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY, bool FULL, bool SR>
+// OPT: the calibration options apply (else the plain calibration, so that the
+// plain kernel keeps the registers the options would take)
+template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY, bool FULL, bool SR, bool OPT>
 __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n, int64_t tile,
                                            V32 (&v)[kTile / (32 * T::VEC)], bool have,
                                            int64_t next, float* scale, int32_t* zp, float* absmax,
                                            float* minv, float* maxv, const SrCtx& sr,
-                                           void* __restrict__ y, void* __restrict__ codes,
+                                           const CalOpts& co, void* __restrict__ y,
+                                           void* __restrict__ codes,
                                            uint32_t* __restrict__ mask, int lane, int& fl) {
   constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
   constexpr int L = VEC * LPG;
@@ -75,7 +78,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
       if (lane / G == j) g = t;
     }
     IntParams q;
-    const int f = calibrate<BITS, AFFINE, MM>(g, q);
+    const int f = calibrate<BITS, AFFINE, MM>(g, q, OPT ? co : CalOpts{1.0f, 0, 0});
     const int64_t ug = tb / L + lane;
     if (lane < NG && ug * L < n) {
       scale[ug] = q.s;
@@ -89,7 +92,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
       OutVec<T> ov;
       CodeVec<BITS, VEC> cv;
       uint32_t mb;
-      int_map_vec<T, BITS, AFFINE, SR>(v[j], p, ov, cv, mb, sr, base);
+      int_map_vec<T, BITS, AFFINE, SR, OPT>(v[j], p, ov, cv, mb, sr, base);
       slot_prefetch<T>(x, next, j, v[j], lane);
       if (!present[j]) mb = 0u;
       if (present[j]) {
@@ -122,7 +125,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
         continue;
       }
       IntParams p;
-      int f = calibrate<BITS, AFFINE, MM>(st, p);
+      int f = calibrate<BITS, AFFINE, MM>(st, p, OPT ? co : CalOpts{1.0f, 0, 0});
       if (leader) {
         scale[u] = p.s;
         if (zp) zp[u] = p.zp;
@@ -131,7 +134,7 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
       OutVec<T> ov;
       CodeVec<BITS, VEC> cv;
       uint32_t mb;
-      int_map_vec<T, BITS, AFFINE, SR>(v[j], p, ov, cv, mb, sr, base);
+      int_map_vec<T, BITS, AFFINE, SR, OPT>(v[j], p, ov, cv, mb, sr, base);
       slot_prefetch<T>(x, next, j, v[j], lane);
       if (!present[j]) mb = 0u;
       if (present[j]) {
@@ -148,11 +151,11 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
   }
 }
 
-template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY, bool SR>
+template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY, bool SR, bool OPT>
 __global__ void __maxnreg__(SR ? 128 : (T::BYTES == 4 ? 96 : 80))
     k_int_groups(const void* __restrict__ x, int64_t n, float* scale, int32_t* zp, float* absmax,
-                 float* minv, float* maxv, SrCtx sr, void* y, void* codes, uint32_t* mask,
-                 int32_t* flags) {
+                 float* minv, float* maxv, SrCtx sr, CalOpts co, void* y, void* codes,
+                 uint32_t* mask, int32_t* flags) {
   const int lane = threadIdx.x & 31;
   const int64_t ntiles = (n + kTile - 1) / kTile;
   const int64_t nfull = n / kTile;
@@ -167,12 +170,12 @@ __global__ void __maxnreg__(SR ? 128 : (T::BYTES == 4 ? 96 : 80))
     // whose draws need the registers)
     const int64_t next = (!SR && nt < nfull) ? nt : -1;
     if (t < nfull)
-      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, true, SR>(x, n, t, v, have, next, scale, zp,
-                                                             absmax, minv, maxv, sr, y, codes, mask,
-                                                             lane, fl);
+      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, true, SR, OPT>(x, n, t, v, have, next, scale, zp,
+                                                             absmax, minv, maxv, sr, co, y, codes,
+                                                             mask, lane, fl);
     else
-      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, false, SR>(x, n, t, v, have, next, scale, zp,
-                                                              absmax, minv, maxv, sr, y, codes,
+      group_tile<T, BITS, AFFINE, LPG, STATS_ONLY, false, SR, OPT>(x, n, t, v, have, next, scale, zp,
+                                                              absmax, minv, maxv, sr, co, y, codes,
                                                               mask, lane, fl);
     have = next >= 0;
   }
@@ -185,7 +188,7 @@ __global__ void __maxnreg__(SR ? 128 : (T::BYTES == 4 ? 96 : 80))
 template <typename T, int BITS, bool AFFINE, int NV, bool STATS_ONLY, bool SR>
 __global__ void __launch_bounds__(256, NV <= 2 ? 3 : 1)
     k_int_rows(const void* __restrict__ x, int64_t units, int64_t L, float* scale, int32_t* zp,
-               float* absmax, float* minv, float* maxv, SrCtx sr, void* y, void* codes,
+               float* absmax, float* minv, float* maxv, SrCtx sr, CalOpts co, void* y, void* codes,
                uint32_t* mask, int32_t* flags) {
   constexpr int VEC = T::VEC, NT = 256;
   constexpr int LPW = 32 / VEC;
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(256, NV <= 2 ? 3 : 1)
           flag_or(flags, b.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
         } else {
           IntParams q;
-          const int f = calibrate<BITS, AFFINE, MM>(b, q);
+          const int f = calibrate<BITS, AFFINE, MM>(b, q, co);
           sp = q;
           scale[u] = q.s;
           if (zp) zp[u] = q.zp;
@@ -306,16 +309,25 @@ bool fused_units_supported(qat_dtype dt, int64_t L) { return lpg_of(dt, L) || nv
 
 template <typename T, int BITS, bool AFFINE, bool SO>
 static qat_status groups_t(int lpg, const void* x, int64_t n, float* scale, int32_t* zp,
-                           float* absmax, float* minv, float* maxv, const SrCtx& sr, void* y,
-                           void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
+                           float* absmax, float* minv, float* maxv, const SrCtx& sr,
+                           const CalOpts& co, void* y, void* codes, uint32_t* mask, int32_t* flags,
+                           cudaStream_t s) {
   const int64_t ntiles = (n + kTile - 1) / kTile;
   int64_t g = (ntiles + 7) / 8;
   int64_t cap = (int64_t)device_info().sms * 8;
   int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
-#define QAT_G(LP)                                                                         \
-  k_int_groups<T, BITS, AFFINE, LP, SO, QAT_SR><<<grid, 256, 0, s>>>(x, n, scale, zp, absmax, \
-                                                                     minv, maxv, sr, y, codes, \
-                                                                     mask, flags)
+  // the options as a compile-time switch of the nearest-rounding build (the
+  // stochastic build has the registers and always takes them at run time)
+  const bool opt = QAT_SR || co.clip != 1.0f || co.fp16 || co.clamp;
+#define QAT_G(LP)                                                                              \
+  do {                                                                                         \
+    if (opt)                                                                                   \
+      k_int_groups<T, BITS, AFFINE, LP, SO, QAT_SR, true><<<grid, 256, 0, s>>>(                \
+          x, n, scale, zp, absmax, minv, maxv, sr, co, y, codes, mask, flags);                 \
+    else /* the stochastic build never gets here (opt is set): same instantiation */      \
+      k_int_groups<T, BITS, AFFINE, LP, SO, QAT_SR, (QAT_SR != 0)><<<grid, 256, 0, s>>>(       \
+          x, n, scale, zp, absmax, minv, maxv, sr, co, y, codes, mask, flags);                 \
+  } while (0)
   switch (lpg) {
     case 2: QAT_G(2); break;
     case 4: QAT_G(4); break;
@@ -329,14 +341,14 @@ static qat_status groups_t(int lpg, const void* x, int64_t n, float* scale, int3
 
 template <typename T, int BITS, bool AFFINE, bool SO>
 static void rows_t(int nv, const void* x, int64_t units, int64_t L, float* scale, int32_t* zp,
-                   float* absmax, float* minv, float* maxv, const SrCtx& sr, void* y, void* codes,
-                   uint32_t* mask, int32_t* flags, cudaStream_t s) {
+                   float* absmax, float* minv, float* maxv, const SrCtx& sr, const CalOpts& co,
+                   void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
   int64_t cap = (int64_t)device_info().sms * 8;
   int grid = (int)(units > cap ? cap : (units < 1 ? 1 : units));
 #define QAT_R(NV)                                                                         \
   k_int_rows<T, BITS, AFFINE, NV, SO, QAT_SR><<<grid, 256, 0, s>>>(x, units, L, scale, zp,     \
-                                                                   absmax, minv, maxv, sr, y,  \
-                                                                   codes, mask, flags)
+                                                                   absmax, minv, maxv, sr, co, \
+                                                                   y, codes, mask, flags)
   switch (nv) {
     case 1: QAT_R(1); break;
     case 2: QAT_R(2); break;
@@ -348,14 +360,15 @@ static void rows_t(int nv, const void* x, int64_t units, int64_t L, float* scale
 
 template <typename T, int BITS, bool AFFINE, bool SO>
 static qat_status fused_t(const void* x, int64_t units, int64_t L, float* scale, int32_t* zp,
-                          float* absmax, float* minv, float* maxv, const SrCtx& sr, void* y,
-                          void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
+                          float* absmax, float* minv, float* maxv, const SrCtx& sr,
+                          const CalOpts& co, void* y, void* codes, uint32_t* mask,
+                          int32_t* flags, cudaStream_t s) {
   const qat_dtype dt = T::kDtype;
   int lpg = lpg_of(dt, L);
   if (lpg)
-    return groups_t<T, BITS, AFFINE, SO>(lpg, x, units * L, scale, zp, absmax, minv, maxv, sr, y,
-                                         codes, mask, flags, s);
-  rows_t<T, BITS, AFFINE, SO>(nv_of(dt, L), x, units, L, scale, zp, absmax, minv, maxv, sr, y,
+    return groups_t<T, BITS, AFFINE, SO>(lpg, x, units * L, scale, zp, absmax, minv, maxv, sr, co,
+                                         y, codes, mask, flags, s);
+  rows_t<T, BITS, AFFINE, SO>(nv_of(dt, L), x, units, L, scale, zp, absmax, minv, maxv, sr, co, y,
                               codes, mask, flags, s);
   return launch_status();
 }
@@ -364,7 +377,7 @@ QAT_DECL_INT_FUSED(QAT_SR_NAME(launch_int_fused)) {
   if (!(lpg_of(dt, L) || nv_of(dt, L))) return QAT_ERR_UNSUPPORTED;
   qat_status st;
 #define QAT_F(T, B, A, SO) \
-  st = fused_t<T, B, A, SO>(x, units, L, scale, zp, absmax, minv, maxv, sr, y, codes, mask, flags, s)
+  st = fused_t<T, B, A, SO>(x, units, L, scale, zp, absmax, minv, maxv, sr, co, y, codes, mask, flags, s)
   if (stats_only) {
 #if QAT_SR
     return QAT_ERR_UNSUPPORTED;

@@ -104,6 +104,8 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
     if (!GIVEN && p.fast) {
       if (SR)
         int_vec_cal_sr<T, BITS, AFFINE, FULL>(v[j], p, cnt[j], sr, base, ov, cv, mb);
+      else if (!AFFINE && p.fast == 2)
+        int_vec_cal<T, BITS, AFFINE, FULL, true>(v[j], p, cnt[j], ov, cv, mb);
       else
         int_vec_cal<T, BITS, AFFINE, FULL>(v[j], p, cnt[j], ov, cv, mb);
     } else if (!p.dead) {
@@ -148,8 +150,9 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
 template <typename T, int BITS, bool AFFINE, bool GIVEN, bool SR>
 __global__ void __maxnreg__(SR ? 128 : 80) k_int_tensor(const void* __restrict__ x, int64_t n,
                                                     const uint4* __restrict__ part, int nparts,
-                                                    float* scale, int32_t* zp, SrCtx sr, void* y,
-                                                    void* codes, uint32_t* mask, int32_t* flags) {
+                                                    float* scale, int32_t* zp, SrCtx sr,
+                                                    CalOpts co, void* y, void* codes,
+                                                    uint32_t* mask, int32_t* flags) {
   __shared__ __align__(16) uint32_t red[4 * 8];
   __shared__ IntParams sp;
   if (GIVEN) {
@@ -161,7 +164,7 @@ __global__ void __maxnreg__(SR ? 128 : 80) k_int_tensor(const void* __restrict__
     constexpr int MM = AFFINE ? kMMFloat : kMMNone;
     Stats st = reduce_partials<MM>(part, nparts, red);
     if (threadIdx.x == 0) {
-      int f = calibrate<BITS, AFFINE, MM>(st, sp);
+      int f = calibrate<BITS, AFFINE, MM>(st, sp, co);
       if (blockIdx.x == 0) {
         scale[0] = sp.s;
         if (zp) zp[0] = sp.zp;
@@ -297,7 +300,7 @@ template <typename T, int MODE, int BITS, bool AFFINE>
 __global__ void __launch_bounds__(256) k_unit_generic(const void* __restrict__ x, int64_t units,
                                                       int64_t L, float* absmax, float* minv,
                                                       float* maxv, float* scale, int32_t* zp,
-                                                      uint8_t* dead, int32_t* flags) {
+                                                      uint8_t* dead, CalOpts co, int32_t* flags) {
   const int lane = threadIdx.x & 31;
   const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units;
@@ -315,7 +318,7 @@ __global__ void __launch_bounds__(256) k_unit_generic(const void* __restrict__ x
         flag_or(flags, st.has_nonfinite() ? QAT_FLAG_NONFINITE_INPUT : 0);
       } else {
         IntParams p;
-        int f = calibrate<BITS, AFFINE, kMMKeys>(st, p);
+        int f = calibrate<BITS, AFFINE, kMMKeys>(st, p, co);
         scale[u] = p.s;
         if (zp) zp[u] = p.zp;
         dead[u] = (uint8_t)p.dead;
@@ -382,24 +385,24 @@ qat_status launch_stats_finalize(const void* ws, int nparts, float* absmax, floa
 
 template <typename T, int BITS, bool AFFINE>
 static void int_tensor_t(bool given, const void* x, int64_t n, const void* ws, int nparts,
-                         float* scale, int32_t* zp, const SrCtx& sr, void* y, void* codes,
-                         uint32_t* mask, int32_t* flags, cudaStream_t s) {
+                         float* scale, int32_t* zp, const SrCtx& sr, const CalOpts& co, void* y,
+                         void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
   const int grid = map_grid(n, 8);
   const uint4* part = static_cast<const uint4*>(ws);
   if (given)
     k_int_tensor<T, BITS, AFFINE, true, QAT_SR>
-        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, y, codes, mask, flags);
+        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, co, y, codes, mask, flags);
   else
     k_int_tensor<T, BITS, AFFINE, false, QAT_SR>
-        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, y, codes, mask, flags);
+        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, co, y, codes, mask, flags);
 }
 
 qat_status QAT_SR_NAME(launch_int_tensor)(qat_dtype dt, int bits, bool affine, bool given,
                                           const void* x, int64_t n, const void* ws, int nparts,
-                                          float* scale, int32_t* zp, const SrCtx& sr, void* y,
-                                          void* codes, uint32_t* mask, int32_t* flags,
-                                          cudaStream_t s) {
-#define QAT_IT(T, B, A) int_tensor_t<T, B, A>(given, x, n, ws, nparts, scale, zp, sr, y, codes, mask, flags, s)
+                                          float* scale, int32_t* zp, const SrCtx& sr,
+                                          const CalOpts& co, void* y, void* codes, uint32_t* mask,
+                                          int32_t* flags, cudaStream_t s) {
+#define QAT_IT(T, B, A) int_tensor_t<T, B, A>(given, x, n, ws, nparts, scale, zp, sr, co, y, codes, mask, flags, s)
   if (dt == QAT_F32) {
     if (bits == 8) { if (affine) QAT_IT(F32, 8, true); else QAT_IT(F32, 8, false); }
     else { if (affine) QAT_IT(F32, 4, true); else QAT_IT(F32, 4, false); }
@@ -449,12 +452,12 @@ qat_status QAT_SR_NAME(launch_int_units)(qat_dtype dt, int bits, bool affine, bo
 template <typename T>
 static void unit_generic_t(int mode, int bits, bool affine, const void* x, int64_t units, int64_t L,
                            float* absmax, float* minv, float* maxv, float* scale, int32_t* zp,
-                           uint8_t* dead, int32_t* flags, cudaStream_t s) {
+                           uint8_t* dead, const CalOpts& co, int32_t* flags, cudaStream_t s) {
   int64_t g = (units + 7) / 8;
   int64_t cap = (int64_t)device_info().sms * 8;
   int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
 #define QAT_UG(M, B, A) \
-  k_unit_generic<T, M, B, A><<<grid, 256, 0, s>>>(x, units, L, absmax, minv, maxv, scale, zp, dead, flags)
+  k_unit_generic<T, M, B, A><<<grid, 256, 0, s>>>(x, units, L, absmax, minv, maxv, scale, zp, dead, co, flags)
   if (mode == 0) QAT_UG(0, 8, false);
   else if (bits == 8) { if (affine) QAT_UG(1, 8, true); else QAT_UG(1, 8, false); }
   else { if (affine) QAT_UG(1, 4, true); else QAT_UG(1, 4, false); }
@@ -463,12 +466,14 @@ static void unit_generic_t(int mode, int bits, bool affine, const void* x, int64
 
 qat_status launch_unit_generic(qat_dtype dt, int mode, int bits, bool affine, const void* x,
                                int64_t units, int64_t L, float* absmax, float* minv, float* maxv,
-                               float* scale, int32_t* zp, uint8_t* dead, int32_t* flags,
-                               cudaStream_t s) {
+                               float* scale, int32_t* zp, uint8_t* dead, const CalOpts& co,
+                               int32_t* flags, cudaStream_t s) {
   if (dt == QAT_F32)
-    unit_generic_t<F32>(mode, bits, affine, x, units, L, absmax, minv, maxv, scale, zp, dead, flags, s);
+    unit_generic_t<F32>(mode, bits, affine, x, units, L, absmax, minv, maxv, scale, zp, dead, co,
+                        flags, s);
   else
-    unit_generic_t<BF16>(mode, bits, affine, x, units, L, absmax, minv, maxv, scale, zp, dead, flags, s);
+    unit_generic_t<BF16>(mode, bits, affine, x, units, L, absmax, minv, maxv, scale, zp, dead, co,
+                         flags, s);
   count_launch(1);
   return launch_status();
 }

@@ -157,13 +157,14 @@ qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t 
     if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
     qat_status st = launch_col_stats(dtype, true, x, rows, cols, ws, flags, s);
     if (st) return st;
-    return launch_col_finalize(0, 8, false, ws, cols, absmax, minv, maxv, nullptr, flags, s);
+    return launch_col_finalize(0, 8, false, ws, cols, absmax, minv, maxv, nullptr, kCalPlain, flags,
+                               s);
   }
   if (fused_units_supported(dtype, L))
     return launch_int_fused(dtype, 8, false, true, x, units, L, nullptr, nullptr, absmax, minv, maxv,
-                            SrCtx{}, nullptr, nullptr, nullptr, flags, s);
+                            SrCtx{}, kCalPlain, nullptr, nullptr, nullptr, flags, s);
   return launch_unit_generic(dtype, 0, 8, false, x, units, L, absmax, minv, maxv, nullptr, nullptr,
-                             nullptr, flags, s);
+                             nullptr, kCalPlain, flags, s);
 }
 
 // The integer and FP8 entry points share one body; sr == nullptr rounds to
@@ -171,8 +172,8 @@ qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t 
 static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t rows, int64_t cols,
                                       int bits, qat_scheme scheme, qat_granularity g,
                                       int64_t group, int params_given, float* scale, int32_t* zp,
-                                      const SrCtx* sr, void* y, void* codes, uint32_t* mask,
-                                      int32_t* flags, void* ws, size_t ws_bytes,
+                                      const SrCtx* sr, const CalOpts& co, void* y, void* codes,
+                                      uint32_t* mask, int32_t* flags, void* ws, size_t ws_bytes,
                                       qat_stream_t stream) {
   if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
   if (bits != 8 && bits != 4) return QAT_ERR_UNSUPPORTED;
@@ -196,14 +197,14 @@ static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t ro
   auto map_fused = sr ? launch_int_fused_sr : launch_int_fused;
   if (g == QAT_PER_TENSOR) {
     if (params_given)
-      return map_tensor(dtype, bits, affine, true, x, n, nullptr, 0, scale, zp, c, y, codes, mask,
+      return map_tensor(dtype, bits, affine, true, x, n, nullptr, 0, scale, zp, c, co, y, codes, mask,
                         flags, s);
     if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
     if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
     int grid = stats_grid(n);
     qat_status st = launch_stats_tensor(dtype, x, n, affine ? kMMFloat : kMMNone, ws, grid, s);
     if (st) return st;
-    return map_tensor(dtype, bits, affine, false, x, n, ws, grid, scale, zp, c, y, codes, mask,
+    return map_tensor(dtype, bits, affine, false, x, n, ws, grid, scale, zp, c, co, y, codes, mask,
                       flags, s);
   }
   const bool col = g == QAT_PER_COLUMN;
@@ -213,7 +214,7 @@ static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t ro
                      mask, flags, s);
   if (!col && fused_units_supported(dtype, L))
     return map_fused(dtype, bits, affine, false, x, units, L, scale, zp, nullptr, nullptr, nullptr,
-                     c, y, codes, mask, flags, s);
+                     c, co, y, codes, mask, flags, s);
   if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
   if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
   uint8_t* dead = ws_dead(ws, cols, g);
@@ -226,15 +227,15 @@ static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t ro
     if (st) return st;
     if (cols % 32 == 0) {
       auto map_cols = sr ? launch_int_cols_sr : launch_int_cols;
-      return map_cols(dtype, bits, affine, x, rows, cols, ws, scale, zp, c, y, codes, mask, flags,
-                      s);
+      return map_cols(dtype, bits, affine, x, rows, cols, ws, scale, zp, c, co, y, codes, mask,
+                      flags, s);
     }
-    st = launch_col_finalize(1, bits, affine, ws, cols, scale, nullptr, nullptr, zpu, flags, s);
+    st = launch_col_finalize(1, bits, affine, ws, cols, scale, nullptr, nullptr, zpu, co, flags, s);
     if (st) return st;
   } else {
     // fallback: calibrate every unit, then the flat map with per-unit arrays
     st = launch_unit_generic(dtype, 1, bits, affine, x, units, L, nullptr, nullptr, nullptr, scale,
-                             zpu, dead, flags, s);
+                             zpu, dead, co, flags, s);
     if (st) return st;
   }
   return map_units(dtype, bits, affine, false, x, n, L, ucols, scale, zpu, dead, c, y, codes, mask,
@@ -246,7 +247,7 @@ qat_status qat_fake_quant_int(const void* x, qat_dtype dtype, int64_t rows, int6
                               float* scale, int32_t* zp, void* y, void* codes, uint32_t* mask,
                               int32_t* flags, void* ws, size_t ws_bytes, qat_stream_t stream) {
   return fake_quant_int_impl(x, dtype, rows, cols, bits, scheme, g, group, params_given, scale, zp,
-                             nullptr, y, codes, mask, flags, ws, ws_bytes, stream);
+                             nullptr, kCalPlain, y, codes, mask, flags, ws, ws_bytes, stream);
 }
 
 static SrCtx sr_ctx(uint64_t seed, uint64_t offset) {
@@ -264,7 +265,25 @@ qat_status qat_fake_quant_int_sr(const void* x, qat_dtype dtype, int64_t rows, i
                                  int32_t* flags, void* ws, size_t ws_bytes, qat_stream_t stream) {
   const SrCtx c = sr_ctx(seed, offset);
   return fake_quant_int_impl(x, dtype, rows, cols, bits, scheme, g, group, params_given, scale, zp,
-                             &c, y, codes, mask, flags, ws, ws_bytes, stream);
+                             &c, kCalPlain, y, codes, mask, flags, ws, ws_bytes, stream);
+}
+
+qat_status qat_fake_quant_int_opts(const void* x, qat_dtype dtype, int64_t rows, int64_t cols,
+                                   int bits, qat_scheme scheme, qat_granularity g, int64_t group,
+                                   const qat_calib_options* options, int stochastic, uint64_t seed,
+                                   uint64_t offset, float* scale, int32_t* zp, void* y, void* codes,
+                                   uint32_t* mask, int32_t* flags, void* ws, size_t ws_bytes,
+                                   qat_stream_t stream) {
+  CalOpts co = kCalPlain;
+  if (options) {
+    if (!(options->clip > 0.0f && options->clip <= 1.0f)) return QAT_ERR_INVALID_ARGUMENT;
+    co.clip = options->clip;
+    co.fp16 = options->scale_fp16 ? 1 : 0;
+  }
+  const SrCtx c = sr_ctx(seed, offset);
+  return fake_quant_int_impl(x, dtype, rows, cols, bits, scheme, g, group, 0, scale, zp,
+                             stochastic ? &c : nullptr, co, y, codes, mask, flags, ws, ws_bytes,
+                             stream);
 }
 
 static qat_status fake_quant_fp8_impl(const void* x, qat_dtype dtype, int64_t n,
@@ -357,8 +376,8 @@ qat_status qat_optimizer_step(float* master, const float* grad, float* exp_avg, 
   const SrCtx c = sr_ctx(seed, offset);
   if (int_view) {
     auto map = stochastic ? launch_int_tensor_sr : launch_int_tensor;
-    return map(QAT_F32, bits, affine, false, master, n, ws, grid, scale, zp, c, view, codes, mask,
-               flags, s);
+    return map(QAT_F32, bits, affine, false, master, n, ws, grid, scale, zp, c, kCalPlain, view,
+               codes, mask, flags, s);
   }
   auto map = stochastic ? launch_fp8_tensor_sr : launch_fp8_tensor;
   return map(QAT_F32, format, true, master, n, nullptr, 0, scale, c, view,

@@ -12,6 +12,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "qat.h"
@@ -566,7 +567,9 @@ struct IntParams {
   int klo, khi;    // clamp range of k = q - zp
   int zp;
   int dead;        // unit outputs are codes 0, y +0, mask 0
-  int fast;        // calibrated unit with a scale in the safe range (quot_scale_ok)
+  int fast;        // calibrated unit with a scale in the safe range (quot_scale_ok):
+                   // 1, or 2 when a symmetric unit's codes need the clamp too
+                   // (calibration options can leave values beyond the range)
 };
 
 template <int BITS, bool AFFINE>
@@ -586,21 +589,32 @@ __device__ __forceinline__ void finish_params(IntParams& p, int qmin, int qmax) 
 
 // Calibration (QuantParams::from_absmax / from_minmax).  Returns the flag bit
 // (0, QAT_FLAG_NONFINITE_CALIB or QAT_FLAG_DEGENERATE).
+// With options (CalOpts): the range times co.clip before the formulas, the
+// scale rounded to binary16 after them (the zero point follows the rounded
+// scale).
 template <int BITS, bool AFFINE, int MM>
-__device__ __forceinline__ int calibrate(const Stats& st, IntParams& p) {
+__device__ __forceinline__ int calibrate(const Stats& st, IntParams& p,
+                                         const CalOpts& co = CalOpts{1.0f, 0, 0}) {
   constexpr int qmin = QRange<BITS, AFFINE>::qmin, qmax = QRange<BITS, AFFINE>::qmax;
   int degenerate = 0;
   p.zp = 0;
   if (!AFFINE) {
     float A = st.absmax_f();
+    if (co.clip != 1.0f) A = __fmul_rn(co.clip, A);
     p.s = __fdiv_rn(A, (float)qmax);
+    if (co.fp16) p.s = __half2float(__float2half_rn(p.s));
     degenerate = !(A > 0.0f) || !(p.s > 0.0f) || isinf(p.s);
   } else {
     float mn = st.min_f<MM>(), mx = st.max_f<MM>();
+    if (co.clip != 1.0f) {
+      mn = __fmul_rn(co.clip, mn);
+      mx = __fmul_rn(co.clip, mx);
+    }
     float rmin = (mn < 0.0f) ? mn : 0.0f;
     float rmax = (mx > 0.0f) ? mx : 0.0f;
     float range = __fsub_rn(rmax, rmin);
     p.s = __fdiv_rn(range, (float)(qmax - qmin));
+    if (co.fp16) p.s = __half2float(__float2half_rn(p.s));
     degenerate = !(range > 0.0f) || !(p.s > 0.0f) || isinf(p.s);
     if (!degenerate) {
       float t = __fsub_rn((float)qmin, __fdiv_rn(rmin, p.s));
@@ -611,7 +625,9 @@ __device__ __forceinline__ int calibrate(const Stats& st, IntParams& p) {
   }
   int flag = st.has_nonfinite() ? QAT_FLAG_NONFINITE_CALIB : (degenerate ? QAT_FLAG_DEGENERATE : 0);
   p.dead = flag != 0;
-  p.fast = !p.dead && quot_scale_ok(p.s);
+  p.fast = (!p.dead && quot_scale_ok(p.s))
+               ? ((!AFFINE && (co.clamp || co.clip != 1.0f || co.fp16)) ? 2 : 1)
+               : 0;
   p.rcp = p.fast ? __frcp_rn(p.s) : 0.0f;
   finish_params(p, qmin, qmax);
   return flag;
@@ -628,11 +644,11 @@ __device__ __forceinline__ IntParams shfl_params(const IntParams& q, int src) {
   p.rcp = __shfl_sync(kFull, q.rcp, src);
   p.whi = __shfl_sync(kFull, q.whi, src);
   const int bitsw =
-      __shfl_sync(kFull, q.dead | (q.fast << 1) | (AFFINE ? ((q.zp & 0xff) << 2) : 0), src);
+      __shfl_sync(kFull, q.dead | (q.fast << 1) | (AFFINE ? ((q.zp & 0xff) << 3) : 0), src);
   p.dead = bitsw & 1;
-  p.fast = (bitsw >> 1) & 1;
+  p.fast = (bitsw >> 1) & 3;
   if (AFFINE) {
-    p.zp = (int)(int8_t)(uint8_t)((bitsw >> 2) & 0xff);
+    p.zp = (int)(int8_t)(uint8_t)((bitsw >> 3) & 0xff);
     p.wlo = __shfl_sync(kFull, q.wlo, src);
   } else {
     p.zp = 0;
@@ -685,7 +701,8 @@ constexpr uint32_t kRintMagicBits = 0x4b400000u;
 // p.fast holds only finite values (a NaN or Inf makes it dead), which the
 // window test below relies on.
 //   quotient: q = RN(x/s) by quotient_rn2, f = rint(q) by the magic constant;
-//   k = clamp(f) (affine), y = k * s, code k + zp from the bits of k + M;
+//   k = clamp(f) (affine, or CLAMP: p.fast == 2), y = k * s, code k + zp from the
+//   bits of k + M;
 //   STE window: whi - |x| >= 0 (symmetric), whi - x >= 0 and x - wlo >= 0
 //     (affine); RN never changes the sign of a difference and an exact zero
 //     difference is +0, except (-0) - (+0) = -0: a lower bound of +0 is used
@@ -694,7 +711,7 @@ constexpr uint32_t kRintMagicBits = 0x4b400000u;
 //     are the window test; they are shifted into the mask with funnel
 //     shifts, highest element first.
 // FULL == false: elements e >= cnt are absent (read as +0) and get code 0.
-template <typename T, int BITS, bool AFFINE, bool FULL>
+template <typename T, int BITS, bool AFFINE, bool FULL, bool CLAMP = false>
 __device__ __forceinline__ void int_vec_cal(const V32& v, const IntParams& p, int cnt,
                                             OutVec<T>& ov, CodeVec<BITS, T::VEC>& cv,
                                             uint32_t& mb) {
@@ -710,7 +727,7 @@ __device__ __forceinline__ void int_vec_cal(const V32& v, const IntParams& p, in
     quotient_rn2(xa, xb, p.rcp, ns, fa, fb);
     add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
     sub2(ta, tb, kRintMagic, kRintMagic, fa, fb);
-    if (AFFINE) {
+    if (AFFINE || CLAMP) {
       fa = fminf(fmaxf(fa, p.klof), p.khif);
       fb = fminf(fmaxf(fb, p.klof), p.khif);
       add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
@@ -863,7 +880,8 @@ __device__ __forceinline__ void int_elem_sr(float x, float u, const IntParams& p
 // Element map of one full vector with calibrated or given parameters: the
 // reciprocal path when p.fast, the IEEE path otherwise, zeros for a dead unit.
 // SR: stochastic rounding with the draws of elements base .. base + VEC - 1.
-template <typename T, int BITS, bool AFFINE, bool SR = false>
+// OPT = false: the unit comes from the plain calibration (p.fast is never 2).
+template <typename T, int BITS, bool AFFINE, bool SR = false, bool OPT = true>
 __device__ __forceinline__ void int_map_vec(const V32& v, const IntParams& p, OutVec<T>& ov,
                                             CodeVec<BITS, T::VEC>& cv, uint32_t& mb,
                                             const SrCtx& sr = SrCtx{}, int64_t base = 0) {
@@ -873,6 +891,8 @@ __device__ __forceinline__ void int_map_vec(const V32& v, const IntParams& p, Ou
   if (p.fast) {
     if (SR)
       int_vec_cal_sr<T, BITS, AFFINE, true>(v, p, VEC, sr, base, ov, cv, mb);
+    else if (OPT && !AFFINE && p.fast == 2)
+      int_vec_cal<T, BITS, AFFINE, true, true>(v, p, VEC, ov, cv, mb);
     else
       int_vec_cal<T, BITS, AFFINE, true>(v, p, VEC, ov, cv, mb);
   } else if (!p.dead) {

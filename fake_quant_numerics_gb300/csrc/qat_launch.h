@@ -36,7 +36,8 @@ qat_status launch_stats_finalize(const void* ws, int nparts, float* absmax, floa
 #define QAT_DECL_INT_TENSOR(name)                                                               \
   qat_status name(qat_dtype dt, int bits, bool affine, bool given, const void* x, int64_t n,    \
                   const void* ws, int nparts, float* scale, int32_t* zp, const SrCtx& sr,       \
-                  void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s)
+                  const CalOpts& co, void* y, void* codes, uint32_t* mask, int32_t* flags,      \
+                  cudaStream_t s)
 QAT_DECL_INT_TENSOR(launch_int_tensor);
 QAT_DECL_INT_TENSOR(launch_int_tensor_sr);
 
@@ -54,8 +55,8 @@ QAT_DECL_INT_UNITS(launch_int_units_sr);
 // mode 0: absmax/minv/maxv outputs; mode 1: int params -> scale, zp, dead
 qat_status launch_unit_generic(qat_dtype dt, int mode, int bits, bool affine, const void* x,
                                int64_t units, int64_t L, float* absmax, float* minv, float* maxv,
-                               float* scale, int32_t* zp, uint8_t* dead, int32_t* flags,
-                               cudaStream_t s);
+                               float* scale, int32_t* zp, uint8_t* dead, const CalOpts& co,
+                               int32_t* flags, cudaStream_t s);
 
 // fused single-pass per-unit calibration + fake quant (or statistics only)
 // for units of L elements.  Returns QAT_ERR_UNSUPPORTED when L does not fit
@@ -64,8 +65,8 @@ bool fused_units_supported(qat_dtype dt, int64_t L);
 #define QAT_DECL_INT_FUSED(name)                                                                \
   qat_status name(qat_dtype dt, int bits, bool affine, bool stats_only, const void* x,          \
                   int64_t units, int64_t L, float* scale, int32_t* zp, float* absmax,           \
-                  float* minv, float* maxv, const SrCtx& sr, void* y, void* codes,              \
-                  uint32_t* mask, int32_t* flags, cudaStream_t s)
+                  float* minv, float* maxv, const SrCtx& sr, const CalOpts& co, void* y,        \
+                  void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s)
 QAT_DECL_INT_FUSED(launch_int_fused);
 QAT_DECL_INT_FUSED(launch_int_fused_sr);  // stats_only unsupported
 
@@ -101,14 +102,15 @@ qat_status launch_col_stats(qat_dtype dt, bool keys, const void* x, int64_t rows
 // grid (bits, affine): scale into out0, zero points into zp (nullable), the
 // dead bytes into the workspace, the calibration flags.
 qat_status launch_col_finalize(int mode, int bits, bool affine, void* ws, int64_t cols, float* out0,
-                               float* out1, float* out2, int32_t* zp, int32_t* flags,
-                               cudaStream_t s);
+                               float* out1, float* out2, int32_t* zp, const CalOpts& co,
+                               int32_t* flags, cudaStream_t s);
 // The calibrated per-column map (cols % 32 == 0) from the accumulators: it
 // calibrates every column itself and writes scale and zero point (nullable)
 #define QAT_DECL_INT_COLS(name)                                                                 \
   qat_status name(qat_dtype dt, int bits, bool affine, const void* x, int64_t rows,             \
                   int64_t cols, const void* ws, float* scale, int32_t* zp, const SrCtx& sr,     \
-                  void* y, void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s)
+                  const CalOpts& co, void* y, void* codes, uint32_t* mask, int32_t* flags,      \
+                  cudaStream_t s)
 QAT_DECL_INT_COLS(launch_int_cols);
 QAT_DECL_INT_COLS(launch_int_cols_sr);
 

@@ -13,6 +13,20 @@ struct SrCtx {
   uint64_t offset;  // counter base
 };
 
+// Calibration options of a call (the module's calibration is {1, 0, 0}):
+// the observed absmax (symmetric) or min and max (affine) times `clip` (one
+// binary32 product, clip in (0, 1]); with `fp16` the scale is rounded to
+// binary16 and that value is the unit's scale; `clamp` makes the symmetric
+// fast path clamp its codes, which every option that can leave values beyond
+// the calibrated range needs (a clip below 1, a rounded scale, percentile
+// bounds).
+struct CalOpts {
+  float clip;
+  int fp16;
+  int clamp;
+};
+constexpr CalOpts kCalPlain{1.0f, 0, 0};
+
 }  // namespace qat
 
 // Each kernel source is compiled twice: with QAT_SR 0 (nearest rounding, the

@@ -168,6 +168,39 @@ qat_status qat_fake_quant_int(const void* x, qat_dtype dtype, int64_t rows, int6
                               size_t workspace_bytes, qat_stream_t stream);
 
 /*
+ * Calibration options for qat_fake_quant_int_opts.
+ *   clip: the calibrated range times clip, in (0, 1] ([EDU] demo 2: the
+ *     range c * max|x|, values beyond it clip to the end codes): the absmax
+ *     (symmetric), or the min and the max (affine; 0 stays inside), times
+ *     clip in one binary32 product, before the usual formulas.  1 is the
+ *     plain calibration.
+ *   scale_fp16: nonzero rounds every calibrated scale to binary16 (round to
+ *     nearest, ties to even) and uses that value ([EDU] demo 3: one FP16
+ *     scale per group); the zero point is derived from it; the scale array
+ *     still holds fp32 (each value exactly representable in binary16).  A
+ *     scale that rounds to 0 or to infinity is QAT_FLAG_DEGENERATE.
+ */
+typedef struct {
+  float clip;
+  int scale_fp16;
+} qat_calib_options;
+
+/*
+ * Calibrated integer fake quantization (as qat_fake_quant_int with
+ * params_given = 0) with calibration options (NULL: the plain calibration),
+ * nearest (stochastic = 0) or stochastic rounding (the draws of
+ * qat_fake_quant_int_sr).  Every granularity.  QAT_ERR_INVALID_ARGUMENT for
+ * a clip outside (0, 1].
+ */
+qat_status qat_fake_quant_int_opts(const void* x, qat_dtype dtype, int64_t rows, int64_t cols,
+                                   int bits, qat_scheme scheme, qat_granularity granularity,
+                                   int64_t group, const qat_calib_options* options,
+                                   int stochastic, uint64_t seed, uint64_t offset, float* scale,
+                                   int32_t* zero_point, void* y, void* codes, uint32_t* mask,
+                                   int32_t* dev_flags, void* workspace, size_t workspace_bytes,
+                                   qat_stream_t stream);
+
+/*
  * Per-tensor amax-scaled FP8 fake quantization ([QAT] fake_quant_fp8 /
  * fp8_quantize_magnitude; scale as in [MAR]).
  *   scale_given == 0: s = (max |x| over finite x) / fmt_max, written to *scale
