@@ -344,7 +344,72 @@ def run_next_rows(args, suite, wb, peak):
     del flush
     return {"stochastic_rounding": out, "w1_int8_tensor_fwd_ste": w1,
             "qat_optimizer_step": run_optimizer_rows(args, suite, peak),
-            "per_column": run_column_rows(args, suite, peak)}
+            "per_column": run_column_rows(args, suite, peak),
+            "calibration_options": run_calib_option_rows(args, suite, wb, peak)}
+
+
+def run_calib_option_rows(args, suite, wb, peak):
+    """Calibration options and percentile calibration, timed like the
+    per-column rows (an L2 flush before every call):
+    - w4 weights bf16[14336, 4096], symmetric int4 per group of 128 with the
+      scales rounded to binary16 (same bytes as the w4 call);
+    - w2 weights fp32[4096, 4096], symmetric int4 per row with the range
+      clipped to 0.7 * absmax (same bytes as the w2 int4 call);
+    - w2 weights, symmetric int8 per tensor calibrated by the nearest-rank
+      quantiles at 0.001 / 0.999 (per_tensor_percentile); algorithmic bytes
+      count x read twice (the selection, then the map), y, codes and mask
+      written; the radix select reads x three times (five launches: a reset,
+      three passes, the map)."""
+    fq, o, fl = suite.fq, suite.o, suite.flags
+    n1, n2, n3, n4, n5 = suite.n
+    r2, c2, r4, c4 = suite.r2, suite.c2, suite.r4, suite.c4
+    dev = suite.x1.device
+    m = lambda n: (n + 31) // 32 * 4  # noqa: E731
+    wsg = torch.empty(max(fq.qat_workspace_bytes(r4, c4, 2, 128), 16), dtype=torch.uint8,
+                      device=dev)
+    wsr = torch.empty(max(fq.qat_workspace_bytes(r2, c2, 1, 0), 16), dtype=torch.uint8, device=dev)
+    wsp = torch.empty(fq.qat_percentile_workspace_bytes(), dtype=torch.uint8, device=dev)
+    s1 = torch.empty(1, dtype=torch.float32, device=dev)
+    c8 = torch.empty(n2, dtype=torch.int8, device=dev)
+    bytes_of = {name: b for name, _, b, _ in wb}
+    rows = [
+        ("w4_int4_group_fp16_scales", bytes_of["w4_int4_group_fwd"],
+         lambda: fq.qat_fake_quant_int_opts(suite.w4, r4, c4, 4, 0, 2, 128,
+                                            fq.calib_options(1.0, True), False, 0, 0, o["s4"],
+                                            None, o["y4"], o["c4"], o["m4"], fl, wsg)),
+        ("w2_sym_int4_row_clip0.7", bytes_of["w2_sym_int4_row"],
+         lambda: fq.qat_fake_quant_int_opts(suite.w2, r2, c2, 4, 0, 1, 0, fq.calib_options(0.7),
+                                            False, 0, 0, o["s2b"], None, o["y2b"], o["c2b"],
+                                            o["m2b"], fl, wsr)),
+        ("w2_sym_int8_tensor_percentile", n2 * (4 + 4 + 4 + 1) + m(n2) + 4,
+         lambda: fq.qat_fake_quant_int_percentile(suite.w2, n2, 8, 0, 0.001, False, 0, 0, s1,
+                                                  None, o["y2a"], c8, o["m2a"], fl, wsp)),
+    ]
+    launches = {"w4_int4_group_fp16_scales": 1, "w2_sym_int4_row_clip0.7": 1,
+                "w2_sym_int8_tensor_percentile": 5}
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 100))
+    out = {}
+    for name, b, call in rows:
+        for _ in range(3):
+            call()
+        t = []
+        for _ in range(steps):
+            flush()
+            a = torch.cuda.Event(enable_timing=True)
+            z = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            z.record(stream)
+            t.append((a, z))
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(z) for a, z in t) / len(t)
+        out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(b / (ms * 1e-3) / 1e9, 1),
+                     "frac_of_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peak, 4),
+                     "bytes": b, "launches": launches[name]}
+    del flush
+    return out
 
 
 def run_column_rows(args, suite, peak):

@@ -11,7 +11,9 @@ from .api import (DoubleQuantized4Bit, FakeQuantFp8, FakeQuantInt, FakeQuantSTE,
                   OptimizerStep, QatDataError, adam_hparams, amax_stats, calib_options,
                   dequantize_4bit_double,
                   fake_quant_backward, optimizer_step, qat_optimizer_step,
-                  fake_quant_fp8, fake_quant_int, qat_amax_stats, qat_dequant4_double,
+                  fake_quant_fp8, fake_quant_int, fake_quant_int_percentile, qat_amax_stats,
+                  qat_dequant4_double, qat_fake_quant_int_percentile,
+                  qat_percentile_workspace_bytes,
                   qat_fake_quant_fp8, qat_fake_quant_fp8_sr, qat_fake_quant_int,
                   qat_fake_quant_int_opts, qat_fake_quant_int_sr, qat_kernel_launch_count,
                   qat_quant4_double, qat_ste_backward, qat_workspace_bytes, quantize_4bit_double,

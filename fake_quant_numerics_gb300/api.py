@@ -124,6 +124,53 @@ def qat_fake_quant_int_opts(x, rows, cols, bits, scheme, granularity, group, opt
     _lib.check("qat_fake_quant_int_opts", st)
 
 
+def qat_percentile_workspace_bytes() -> int:
+    return int(_lib.lib().qat_percentile_workspace_bytes())
+
+
+def qat_fake_quant_int_percentile(x, n, bits, scheme, clip_fraction, stochastic, seed, offset,
+                                  scale, zero_point, y, codes, mask, dev_flags, workspace,
+                                  stream=None):
+    st = _lib.lib().qat_fake_quant_int_percentile(_p(x), _dt(x), n, bits, _SCHEME[scheme],
+                                                  float(clip_fraction), int(bool(stochastic)),
+                                                  int(seed), int(offset), _p(scale),
+                                                  _p(zero_point), _p(y), _p(codes), _p(mask),
+                                                  _p(dev_flags), _p(workspace),
+                                                  _nbytes(workspace), _s(stream))
+    _lib.check("qat_fake_quant_int_percentile", st)
+
+
+def fake_quant_int_percentile(x: torch.Tensor, bits: int = 8, scheme="symmetric",
+                              clip_fraction: float = 0.0, want_codes: bool = True,
+                              want_mask: bool = True, check: bool = False,
+                              rounding: str = "nearest", seed: int = 0,
+                              offset: int = 0) -> FakeQuantInt:
+    """Per-tensor integer fake quantization calibrated by the nearest-rank
+    quantiles at clip_fraction and 1 - clip_fraction (the module's
+    per_tensor_percentile)."""
+    x = _ready(x)
+    n = x.numel()
+    sch = _SCHEME[scheme]
+    dev = x.device
+    scale = torch.empty(1, dtype=torch.float32, device=dev)
+    zero_point = torch.empty(1, dtype=torch.int32, device=dev) if sch == AFFINE else None
+    y = torch.empty_like(x)
+    codes = None
+    if want_codes:
+        codes = (torch.empty(n, dtype=torch.int8, device=dev) if bits == 8
+                 else torch.empty((n + 1) // 2, dtype=torch.uint8, device=dev))
+    mask = torch.empty((n + 31) // 32, dtype=torch.int32, device=dev) if want_mask else None
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(qat_percentile_workspace_bytes(), dtype=torch.uint8, device=dev)
+    if rounding not in ("nearest", "stochastic"):
+        raise ValueError(f"rounding must be 'nearest' or 'stochastic', not {rounding!r}")
+    qat_fake_quant_int_percentile(x, n, bits, sch, clip_fraction, rounding == "stochastic", seed,
+                                  offset, scale, zero_point, y, codes, mask, flags, ws)
+    if check:
+        raise_on_flags(flags, "fake_quant_int_percentile")
+    return FakeQuantInt(y, codes, mask, scale, zero_point, flags)
+
+
 def qat_fake_quant_fp8_sr(x, n, fmt, scale_given, scale, seed, offset, y, codes, mask, dev_flags,
                           workspace, stream=None):
     st = _lib.lib().qat_fake_quant_fp8_sr(_p(x), _dt(x), n, _FMT[fmt], int(scale_given), _p(scale),

@@ -4,6 +4,8 @@
 #include <cstdint>
 
 #include "qat_device.cuh"
+#include <cmath>
+
 #include "qat_launch.h"
 
 namespace qat {
@@ -284,6 +286,45 @@ qat_status qat_fake_quant_int_opts(const void* x, qat_dtype dtype, int64_t rows,
   return fake_quant_int_impl(x, dtype, rows, cols, bits, scheme, g, group, 0, scale, zp,
                              stochastic ? &c : nullptr, co, y, codes, mask, flags, ws, ws_bytes,
                              stream);
+}
+
+size_t qat_percentile_workspace_bytes(void) { return pct_ws_bytes(); }
+
+qat_status qat_fake_quant_int_percentile(const void* x, qat_dtype dtype, int64_t n, int bits,
+                                         qat_scheme scheme, double clip_fraction, int stochastic,
+                                         uint64_t seed, uint64_t offset, float* scale, int32_t* zp,
+                                         void* y, void* codes, uint32_t* mask, int32_t* flags,
+                                         void* ws, size_t ws_bytes, qat_stream_t stream) {
+  if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
+  if (bits != 8 && bits != 4) return QAT_ERR_UNSUPPORTED;
+  if (scheme != QAT_SYMMETRIC && scheme != QAT_AFFINE) return QAT_ERR_UNSUPPORTED;
+  if (!(clip_fraction >= 0.0 && clip_fraction < 0.5)) return QAT_ERR_INVALID_ARGUMENT;
+  if (n < 0 || n > (INT64_C(1) << 40)) return QAT_ERR_INVALID_ARGUMENT;
+  if (n == 0) return QAT_OK;
+  if (!x || !scale) return QAT_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, kAlignVec) || (y && !aligned(y, kAlignVec)) ||
+      (codes && !aligned(codes, kAlignBuf)) || (mask && !aligned(mask, kAlignBuf)) ||
+      !aligned(scale, 4) || (zp && !aligned(zp, 4)))
+    return QAT_ERR_MISALIGNED;
+  if (!ws || ws_bytes < pct_ws_bytes()) return QAT_ERR_WORKSPACE;
+  if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+  // QuantParams::per_tensor_percentile: the index products in binary64
+  const int64_t last = n - 1;
+  int64_t lo = (int64_t)floor(clip_fraction * (double)last);
+  int64_t hi = (int64_t)ceil((1.0 - clip_fraction) * (double)last);
+  if (lo > last) lo = last;
+  if (hi > last) hi = last;
+  const bool affine = scheme == QAT_AFFINE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  qat_status st = launch_percentile(dtype, x, n, affine, (unsigned long long)lo,
+                                    (unsigned long long)hi, ws, s);
+  if (st) return st;
+  // the per-tensor map from the one partial; values beyond the quantiles
+  // clamp to the end codes
+  const CalOpts co{1.0f, 0, 1};
+  const SrCtx c = sr_ctx(seed, offset);
+  auto map = stochastic ? launch_int_tensor_sr : launch_int_tensor;
+  return map(dtype, bits, affine, false, x, n, ws, 1, scale, zp, c, co, y, codes, mask, flags, s);
 }
 
 static qat_status fake_quant_fp8_impl(const void* x, qat_dtype dtype, int64_t n,

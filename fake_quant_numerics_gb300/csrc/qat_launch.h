@@ -114,6 +114,15 @@ qat_status launch_col_finalize(int mode, int bits, bool affine, void* ws, int64_
 QAT_DECL_INT_COLS(launch_int_cols);
 QAT_DECL_INT_COLS(launch_int_cols_sr);
 
+// Percentile calibration of a whole tensor (radix select of the two
+// nearest-rank quantiles): leaves at offset 0 of the workspace the one
+// statistics partial the per-tensor map calibrates from (absmax, or min and
+// max, of the quantiles; the non-finite bit).  pct_ws_bytes: its workspace.
+size_t pct_ws_bytes();
+qat_status launch_percentile(qat_dtype dt, const void* x, int64_t n, bool affine,
+                             unsigned long long rank_lo, unsigned long long rank_hi, void* ws,
+                             cudaStream_t s);
+
 // FP8
 #define QAT_DECL_FP8_TENSOR(name)                                                               \
   qat_status name(qat_dtype dt, qat_fp8_format fmt, bool given, const void* x, int64_t n,       \

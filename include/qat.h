@@ -201,6 +201,30 @@ qat_status qat_fake_quant_int_opts(const void* x, qat_dtype dtype, int64_t rows,
                                    qat_stream_t stream);
 
 /*
+ * Per-tensor integer fake quantization calibrated by percentiles ([QAT]
+ * QuantParams::per_tensor_percentile): the n values in the total order (-0
+ * before +0), last = n - 1, the nearest-rank quantiles lo = sorted[floor(c *
+ * last)] and hi = sorted[min(ceil((1 - c) * last), last)] (the index products
+ * in binary64), then from_minmax: symmetric scale = max(|lo|, |hi|) / qmax,
+ * affine the min/max calibration of [lo, hi].  Values beyond the quantiles
+ * clamp to the end codes.  Outputs as qat_fake_quant_int (scale[0],
+ * zero_point[0]), nearest (stochastic = 0) or stochastic rounding (the draws
+ * of qat_fake_quant_int_sr).  A NaN or Inf anywhere is the module's
+ * calibration error: QAT_FLAG_NONFINITE_CALIB, scale 0, codes 0, y = +0,
+ * mask 0.  clip_fraction c outside [0, 0.5): QAT_ERR_INVALID_ARGUMENT; n up
+ * to 2^40.  workspace: qat_percentile_workspace_bytes() bytes (the radix
+ * select's histograms).  Five kernel launches: a reset, three radix-select
+ * passes over x, then the map.
+ */
+size_t qat_percentile_workspace_bytes(void);
+qat_status qat_fake_quant_int_percentile(const void* x, qat_dtype dtype, int64_t n, int bits,
+                                         qat_scheme scheme, double clip_fraction, int stochastic,
+                                         uint64_t seed, uint64_t offset, float* scale,
+                                         int32_t* zero_point, void* y, void* codes,
+                                         uint32_t* mask, int32_t* dev_flags, void* workspace,
+                                         size_t workspace_bytes, qat_stream_t stream);
+
+/*
  * Per-tensor amax-scaled FP8 fake quantization ([QAT] fake_quant_fp8 /
  * fp8_quantize_magnitude; scale as in [MAR]).
  *   scale_given == 0: s = (max |x| over finite x) / fmt_max, written to *scale
