@@ -95,6 +95,13 @@ def lib():
         L.or_adam_update.argtypes = [vp, vp, vp, vp, i64, f32, f32, f32, f32, f32, f32, f32]
         L.or_qat_optimizer_step.argtypes = [vp, vp, vp, vp, i64, f32, f32, f32, f32, f32, f32, f32,
                                             i32, i32, i32, i32, u64, u64, vp, vp, vp, vp, vp, vp]
+        L.or_elem_round.argtypes = [f32, i32]
+        L.or_elem_round.restype = f32
+        L.or_elem_encode.argtypes = [f32, i32]
+        L.or_elem_encode.restype = ctypes.c_uint8
+        L.or_elem_decode.argtypes = [ctypes.c_uint8, i32]
+        L.or_elem_decode.restype = f32
+        L.or_fake_quant_block.argtypes = [vp, i32, i64, i32, i64, i32, vp, vp, vp, vp, vp, vp]
         L.or_round_fp16.argtypes = [f32]
         L.or_round_fp16.restype = f32
         L.or_fake_quant_int_opts.argtypes = [vp, i32, i64, i64, i32, i32, i32, i64, f32, i32, i32,
@@ -292,6 +299,47 @@ def fake_quant_int_opts(x: np.ndarray, rows: int, cols: int, bits: int, scheme: 
     if st:
         raise ValueError(f"oracle fake_quant_int_opts status {st}")
     return dict(y=y, codes=codes, mask=mask, scale=sc[:u], zero_point=zp[:u], flags=flags.value)
+
+
+ELEM_E4M3, ELEM_E5M2, ELEM_E2M3, ELEM_E3M2, ELEM_E2M1 = 0, 1, 2, 3, 4
+ELEM_MAX = {0: 448.0, 1: 57344.0, 2: 7.5, 3: 28.0, 4: 6.0}
+ELEM_BITS = {0: 8, 1: 8, 2: 6, 3: 6, 4: 4}
+SCALE_E8M0, SCALE_E4M3, SCALE_FP32 = 0, 1, 2
+
+
+def elem_round(v, fmt: int) -> np.ndarray:
+    """Round-to-nearest-even with saturation on an element format's grid."""
+    a = np.ascontiguousarray(v, dtype=np.float32).reshape(-1)
+    return np.array([lib().or_elem_round(float(t), fmt) for t in a], np.float32).reshape(np.shape(v))
+
+
+def elem_encode(v, fmt: int) -> np.ndarray:
+    a = np.ascontiguousarray(v, dtype=np.float32).reshape(-1)
+    return np.array([lib().or_elem_encode(float(t), fmt) for t in a], np.uint8).reshape(np.shape(v))
+
+
+def elem_decode(codes, fmt: int) -> np.ndarray:
+    a = np.asarray(codes, dtype=np.uint8).reshape(-1)
+    return np.array([lib().or_elem_decode(int(c), fmt) for c in a], np.float32).reshape(np.shape(codes))
+
+
+def fake_quant_block(x: np.ndarray, fmt: int, block: int, kind: int):
+    """Block-scaled fake quant (the teaching script's block_scaled); returns
+    dict(y, codes, bscales, tensor_scale, mask, flags)."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    n = x.size
+    y = np.empty(n, dtype=x.dtype)
+    codes = np.empty(n, np.uint8)
+    nb = n // block if block > 0 else 0
+    bs = np.empty(max(nb, 1), np.float32 if kind == SCALE_FP32 else np.uint8)
+    mask = np.empty((n + 31) // 32, np.uint32)
+    g, fl = ctypes.c_float(1.0), ctypes.c_int32(0)
+    st = lib().or_fake_quant_block(_p(x), _dtype_code(x), n, fmt, block, kind, ctypes.byref(g),
+                                   _p(y), _p(codes), _p(bs), _p(mask), ctypes.byref(fl))
+    if st:
+        raise ValueError(f"oracle fake_quant_block status {st}")
+    return dict(y=y, codes=codes, bscales=bs[:nb], tensor_scale=np.float32(g.value), mask=mask,
+                flags=fl.value)
 
 
 def percentile_minmax(x: np.ndarray, clip_fraction: float):

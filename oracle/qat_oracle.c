@@ -38,6 +38,10 @@
  *          from_minmax); per_channel_params with axis 1 (per-column units)
  *   [EDU]  demo 2 (the range c * max|x|: clip factor), demo 3 (one FP16
  *          scale per group); IEEE 754 binary16 (round to nearest, ties to even)
+ *   [EDU]  demo 4, block_scaled (E8M0 / E4M3 + FP32 / exact block scales)
+ *   [MX]   OCP Microscaling Formats (MX) Specification v1.0 (the FP8 / FP6 /
+ *          FP4 element encodings, E8M0 scales); NVIDIA NVFP4 (E2M1 elements,
+ *          16-element blocks, E4M3 block scales under an FP32 tensor scale)
  *
  * Every place where the sources are silent and a reading was taken is marked
  * "reading:" below.
@@ -587,6 +591,147 @@ int or_fake_quant_int_percentile(const void* x, int dtype, int64_t n, int bits, 
     if (y) store_elem(y, dtype, i, or_dequantize(q, s, z));
     set_mask(mask, i, in_window(v, s, z, qmin, qmax));
   }
+  return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Block-scaled floating-point formats ([EDU] demo 4, block_scaled).          */
+/*                                                                            */
+/* Element formats (the module's numfmt definitions are not on the pages;    */
+/* written from the OCP Microscaling (MX) v1.0 and NVIDIA NVFP4 public        */
+/* definitions): sign, `ebits` exponent bits with bias, `mbits` mantissa      */
+/* bits, subnormals, largest finite value maxv; FP6 / FP4 have no Inf or NaN. */
+/*   E4M3 (bias 7, max 448), E5M2 (15, 57344), E2M3 (1, 7.5), E3M2 (3, 28),   */
+/*   E2M1 (1, 6); emax = floor(log2 maxv).                                    */
+/* The page's steps, per block of `block` consecutive elements:               */
+/*   amax = max |x| over the block;                                           */
+/*   scale X:  E8M0 -- 2^(floor(log2 amax) - emax) (amax = 0: 2^-emax, the    */
+/*               page's frexp(1.0) branch);                                   */
+/*             E4M3 -- g = max|x| over the tensor / (maxv * 448),             */
+/*               X = E4M3_round_sat(amax / maxv / g) * g (NVFP4);             */
+/*             FP32 -- X = amax / maxv;                                       */
+/*             X <= 0 or NaN -> 1;                                            */
+/*   y = x / X; out = round_sat(y) * X (round to nearest even on the element  */
+/*   grid, magnitudes past maxv saturate).                                    */
+/* reading: binary32 throughout with one rounding per printed operation (the  */
+/* page computes in binary64); amax and the tensor max over finite values; a  */
+/* NaN element stays NaN (code 0x7F for FP8 elements, 0 for FP6 / FP4), an   */
+/* Inf saturates; the E8M0 exponent is held to [-127, 127]; the STE mask bit  */
+/* is |y| <= maxv.                                                            */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  int ebits, mbits, bias, emax;
+  float maxv;
+} or_elemfmt;
+
+static const or_elemfmt OR_ELEM[5] = {
+    {4, 3, 7, 8, 448.0f},     /* E4M3 */
+    {5, 2, 15, 15, 57344.0f}, /* E5M2 */
+    {2, 3, 1, 2, 7.5f},       /* E2M3 */
+    {3, 2, 3, 4, 28.0f},      /* E3M2 */
+    {2, 1, 1, 2, 6.0f},       /* E2M1 */
+};
+
+/* round to nearest even on the element grid, saturating; sign kept */
+float or_elem_round(float y, int fmt) {
+  const or_elemfmt f = OR_ELEM[fmt];
+  if (isnan(y)) return y;
+  float a = fabsf(y);
+  if (isinf(a)) return copysignf(f.maxv, y);
+  if (a == 0.0f) return y;
+  int emin = 1 - f.bias;
+  int e = (int)((f2u(a) >> 23) & 0xFF) - 127; /* floor(log2 a); -127 for binary32 subnormals */
+  int se = (e > emin ? e : emin) - f.mbits;
+  float step = ldexpf(1.0f, se);
+  float mag = rintf(a / step) * step;
+  if (mag > f.maxv) mag = f.maxv;
+  return copysignf(mag, y);
+}
+
+/* the element code of a grid value: sign, biased exponent, mantissa */
+uint8_t or_elem_encode(float c, int fmt) {
+  const or_elemfmt f = OR_ELEM[fmt];
+  if (isnan(c)) return fmt <= 1 ? 0x7F : 0x00;
+  uint8_t sign = signbit(c) ? (uint8_t)(1u << (f.ebits + f.mbits)) : 0;
+  float a = fabsf(c);
+  if (a == 0.0f) return sign;
+  int emin = 1 - f.bias;
+  int ex;
+  (void)frexpf(a, &ex);
+  int e = ex - 1;
+  if (e < emin) return (uint8_t)(sign | (int)(a / ldexpf(1.0f, emin - f.mbits)));
+  int man = (int)((a / ldexpf(1.0f, e) - 1.0f) * ldexpf(1.0f, f.mbits));
+  return (uint8_t)(sign | ((e + f.bias) << f.mbits) | man);
+}
+
+/* The value of an element code (inverse of or_elem_encode on the grid). */
+float or_elem_decode(uint8_t code, int fmt) {
+  const or_elemfmt f = OR_ELEM[fmt];
+  int nb = f.ebits + f.mbits;
+  int sign = (code >> nb) & 1;
+  int E = (code >> f.mbits) & ((1 << f.ebits) - 1);
+  int M = code & ((1 << f.mbits) - 1);
+  float mag = E == 0 ? ldexpf((float)M, 1 - f.bias - f.mbits)
+                     : ldexpf(1.0f + ldexpf((float)M, -f.mbits), E - f.bias);
+  return sign ? -mag : mag;
+}
+
+int or_fake_quant_block(const void* x, int dtype, int64_t n, int fmt, int64_t block, int kind,
+                        float* tensor_scale, void* y, uint8_t* codes, void* bscales,
+                        uint32_t* mask, int32_t* flags) {
+  if (fmt < 0 || fmt > 4 || kind < 0 || kind > 2) return OR_ERR_UNSUPPORTED;
+  if (block <= 0 || n < 0 || n % block != 0) return OR_ERR_INVALID;
+  const or_elemfmt f = OR_ELEM[fmt];
+  int nonfinite = 0;
+  float A = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    float v = load_elem(x, dtype, i);
+    if (!isfinite(v)) nonfinite = 1;
+    else if (fabsf(v) > A) A = fabsf(v);
+  }
+  float g = 1.0f;
+  if (kind == 1) g = A / (f.maxv * 448.0f);
+  if (tensor_scale) *tensor_scale = g;
+  if (mask) memset(mask, 0, (size_t)((n + 31) / 32) * 4);
+  for (int64_t b = 0; b < n / block; ++b) {
+    float amax = 0.0f;
+    for (int64_t k = 0; k < block; ++k) {
+      float v = load_elem(x, dtype, b * block + k);
+      if (isfinite(v) && fabsf(v) > amax) amax = fabsf(v);
+    }
+    float X;
+    if (kind == 0) {
+      int e = amax > 0.0f ? (int)((f2u(amax) >> 23) & 0xFF) - 127 : 0;
+      if (amax > 0.0f && e == -127) { /* binary32 subnormal: its own exponent */
+        int ex;
+        (void)frexpf(amax, &ex);
+        e = ex - 1;
+      }
+      int es = e - f.emax;
+      if (es < -127) es = -127;
+      if (es > 127) es = 127;
+      X = ldexpf(1.0f, es);
+      if (bscales) ((uint8_t*)bscales)[b] = (uint8_t)(es + 127);
+    } else if (kind == 1) {
+      float c = or_elem_round((amax / f.maxv) / g, 0);
+      X = c * g;
+      if (bscales) ((uint8_t*)bscales)[b] = or_elem_encode(c, 0);
+    } else {
+      X = amax / f.maxv;
+    }
+    if (!(X > 0.0f)) X = 1.0f;
+    if (kind == 2 && bscales) ((float*)bscales)[b] = X;
+    for (int64_t k = 0; k < block; ++k) {
+      int64_t i = b * block + k;
+      float v = load_elem(x, dtype, i);
+      float t = v / X;
+      float q = or_elem_round(t, fmt);
+      if (y) store_elem(y, dtype, i, q * X);
+      if (codes) codes[i] = or_elem_encode(q, fmt);
+      set_mask(mask, i, fabsf(t) <= f.maxv);
+    }
+  }
+  if (flags && nonfinite) *flags |= OR_FLAG_NONFINITE_INPUT;
   return OR_OK;
 }
 
