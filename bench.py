@@ -345,7 +345,58 @@ def run_next_rows(args, suite, wb, peak):
     return {"stochastic_rounding": out, "w1_int8_tensor_fwd_ste": w1,
             "qat_optimizer_step": run_optimizer_rows(args, suite, peak),
             "per_column": run_column_rows(args, suite, peak),
-            "calibration_options": run_calib_option_rows(args, suite, wb, peak)}
+            "calibration_options": run_calib_option_rows(args, suite, wb, peak),
+            "block_formats": run_block_rows(args, suite, peak)}
+
+
+def run_block_rows(args, suite, peak):
+    """Block-scaled floating-point fake quant of the w4 weights bf16[14336,
+    4096] (an L2 flush before every call): NVFP4 (E2M1 elements, blocks of 16,
+    E4M3 scales under the FP32 tensor scale: a statistics pass, then the map),
+    MXFP4 (E2M1, 32, E8M0) and MXFP8 (E4M3, 32, E8M0).  Algorithmic bytes per
+    element: x read (2; twice for NVFP4), y written (2), the element code (1/2
+    or 1), the block scale (1/16 or 1/32), the mask (1/8)."""
+    fq, fl = suite.fq, suite.flags
+    r4, c4 = suite.r4, suite.c4
+    n = r4 * c4
+    dev = suite.x1.device
+    o = suite.o
+    m = (n + 31) // 32 * 4
+    ws = torch.empty(fq.qat_workspace_bytes(1, n, 0, 0), dtype=torch.uint8, device=dev)
+    codes = torch.empty(n, dtype=torch.uint8, device=dev)
+    bs = torch.empty(n // 16, dtype=torch.uint8, device=dev)
+    g = torch.empty(1, dtype=torch.float32, device=dev)
+    rows = [
+        ("w4_nvfp4", n * (2 + 2 + 2) + n // 2 + n // 16 + m, 2, (4, 16, 1)),
+        ("w4_mxfp4", n * (2 + 2) + n // 2 + n // 32 + m, 1, (4, 32, 0)),
+        ("w4_mxfp8_e4m3", n * (2 + 2) + n + n // 32 + m, 1, (0, 32, 0)),
+    ]
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 100))
+    out = {}
+    for name, b, launches, (fmt, block, kind) in rows:
+        def call():
+            fq.qat_fake_quant_block(suite.w4, n, fmt, block, kind, g, o["y4"], codes, bs,
+                                    o["m4"], fl, ws)
+        for _ in range(3):
+            call()
+        t = []
+        for _ in range(steps):
+            flush()
+            a = torch.cuda.Event(enable_timing=True)
+            z = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            z.record(stream)
+            t.append((a, z))
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(z) for a, z in t) / len(t)
+        out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(b / (ms * 1e-3) / 1e9, 1),
+                     "frac_of_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peak, 4),
+                     "bytes": b, "launches": launches}
+    del flush
+    return out
 
 
 def run_calib_option_rows(args, suite, wb, peak):

@@ -4,10 +4,12 @@ straight-through-estimator backward, and the QLoRA two-level 4-bit block
 format, as CUDA kernels for sm_103a behind a C ABI (include/qat.h); the
 integer and FP8 maps also round stochastically with counter-based draws;
 units may also be columns, and calibration takes a clip factor and binary16
-scales.
+scales; block-scaled floating-point formats (MX with E8M0 scales, NVFP4
+with E4M3 scales under an FP32 tensor scale).
 """
 from ._lib import QatError, load  # noqa: F401
-from .api import (DoubleQuantized4Bit, FakeQuantFp8, FakeQuantInt, FakeQuantSTE,  # noqa: F401
+from .api import (DoubleQuantized4Bit, FakeQuantBlock, FakeQuantFp8, FakeQuantInt,  # noqa: F401
+                  FakeQuantSTE, fake_quant_block, qat_fake_quant_block,
                   OptimizerStep, QatDataError, adam_hparams, amax_stats, calib_options,
                   dequantize_4bit_double,
                   fake_quant_backward, optimizer_step, qat_optimizer_step,

@@ -60,6 +60,8 @@ PROTOTYPES = {
     "qat_fake_quant_fp8_noalloc": ([_vp, _int, _i64, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp], _int),
     "qat_fake_quant_int_opts": ([_vp, _int, _i64, _i64, _int, _int, _int, _i64, _vp, _int, _u64, _u64,
                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _int),
+    "qat_fake_quant_block": ([_vp, _int, _i64, _int, _i64, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                              _sz, _vp], _int),
     "qat_percentile_workspace_bytes": ([], _sz),
     "qat_fake_quant_int_percentile": ([_vp, _int, _i64, _int, _int, ctypes.c_double, _int, _u64,
                                        _u64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _int),

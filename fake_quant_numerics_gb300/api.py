@@ -124,6 +124,56 @@ def qat_fake_quant_int_opts(x, rows, cols, bits, scheme, granularity, group, opt
     _lib.check("qat_fake_quant_int_opts", st)
 
 
+_ELEM = {"e4m3": 0, "e5m2": 1, "e2m3": 2, "e3m2": 3, "e2m1": 4, 0: 0, 1: 1, 2: 2, 3: 3, 4: 4}
+_BSCALE = {"e8m0": 0, "e4m3": 1, "fp32": 2, 0: 0, 1: 1, 2: 2}
+_ELEM_BITS = {0: 8, 1: 8, 2: 6, 3: 6, 4: 4}
+
+
+def qat_fake_quant_block(x, n, elem, block, scale_kind, tensor_scale, y, codes, block_scales,
+                         mask, dev_flags, workspace, stream=None):
+    st = _lib.lib().qat_fake_quant_block(_p(x), _dt(x), n, _ELEM[elem], block, _BSCALE[scale_kind],
+                                         _p(tensor_scale), _p(y), _p(codes), _p(block_scales),
+                                         _p(mask), _p(dev_flags), _p(workspace),
+                                         _nbytes(workspace), _s(stream))
+    _lib.check("qat_fake_quant_block", st)
+
+
+class FakeQuantBlock(NamedTuple):
+    y: torch.Tensor
+    codes: Optional[torch.Tensor]
+    block_scales: torch.Tensor
+    tensor_scale: torch.Tensor
+    mask: Optional[torch.Tensor]
+    flags: torch.Tensor
+
+
+def fake_quant_block(x: torch.Tensor, elem="e2m1", block: int = 16, scale="e4m3",
+                     want_codes: bool = True, want_mask: bool = True) -> FakeQuantBlock:
+    """Block-scaled floating-point fake quantization of x (float32 or bfloat16,
+    CUDA; blocks of 16 or 32 consecutive elements).  NVFP4 is elem="e2m1",
+    block=16, scale="e4m3"; MXFP4 / MXFP6 / MXFP8 are block=32, scale="e8m0"
+    with elem "e2m1" / "e2m3" or "e3m2" / "e4m3" or "e5m2"."""
+    x = _ready(x)
+    n = x.numel()
+    dev = x.device
+    e, k = _ELEM[elem], _BSCALE[scale]
+    if n % block:
+        raise ValueError(f"{n} elements are not a whole number of blocks of {block}")
+    nb = n // block
+    y = torch.empty_like(x)
+    codes = None
+    if want_codes:
+        codes = torch.empty(n // 2 if _ELEM_BITS[e] == 4 else n, dtype=torch.uint8, device=dev)
+    bs = torch.empty(nb, dtype=torch.float32 if k == 2 else torch.uint8, device=dev)
+    g = torch.empty(1, dtype=torch.float32, device=dev)
+    mask = torch.empty((n + 31) // 32, dtype=torch.int32, device=dev) if want_mask else None
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(max(qat_workspace_bytes(1, n, PER_TENSOR, 0), 16), dtype=torch.uint8,
+                     device=dev)
+    qat_fake_quant_block(x, n, e, block, k, g, y, codes, bs, mask, flags, ws)
+    return FakeQuantBlock(y, codes, bs, g, mask, flags)
+
+
 def qat_percentile_workspace_bytes() -> int:
     return int(_lib.lib().qat_percentile_workspace_bytes())
 

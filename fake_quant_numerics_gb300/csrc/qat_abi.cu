@@ -327,6 +327,34 @@ qat_status qat_fake_quant_int_percentile(const void* x, qat_dtype dtype, int64_t
   return map(dtype, bits, affine, false, x, n, ws, 1, scale, zp, c, co, y, codes, mask, flags, s);
 }
 
+qat_status qat_fake_quant_block(const void* x, qat_dtype dtype, int64_t n, qat_elem_format elem,
+                                int64_t block, qat_block_scale kind, float* tensor_scale, void* y,
+                                uint8_t* codes, void* bscales, uint32_t* mask, int32_t* flags,
+                                void* ws, size_t ws_bytes, qat_stream_t stream) {
+  if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
+  if (elem < QAT_ELEM_E4M3 || elem > QAT_ELEM_E2M1) return QAT_ERR_UNSUPPORTED;
+  if (kind < QAT_BLOCK_SCALE_E8M0 || kind > QAT_BLOCK_SCALE_FP32) return QAT_ERR_UNSUPPORTED;
+  if (block != 16 && block != 32) return QAT_ERR_UNSUPPORTED;
+  if (n < 0 || n > (INT64_C(1) << 50) || n % block != 0) return QAT_ERR_INVALID_ARGUMENT;
+  if (n == 0) return QAT_OK;
+  if (!x) return QAT_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, kAlignVec) || (y && !aligned(y, kAlignVec)) ||
+      (codes && !aligned(codes, kAlignBuf)) || (mask && !aligned(mask, kAlignBuf)) ||
+      (bscales && !aligned(bscales, 4)) || (tensor_scale && !aligned(tensor_scale, 4)))
+    return QAT_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int grid = 0;
+  if (kind == QAT_BLOCK_SCALE_E4M3) {
+    if (!ws || ws_bytes < ws_bytes_for(1, n, QAT_PER_TENSOR, 0)) return QAT_ERR_WORKSPACE;
+    if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+    grid = stats_grid(n);
+    qat_status st = launch_stats_tensor(dtype, x, n, kMMNone, ws, grid, s);
+    if (st) return st;
+  }
+  return launch_block_fq(dtype, elem, kind, block, x, n, ws, grid, tensor_scale, y, codes,
+                         bscales, mask, flags, s);
+}
+
 static qat_status fake_quant_fp8_impl(const void* x, qat_dtype dtype, int64_t n,
                                       qat_fp8_format fmt, int scale_given, float* scale,
                                       const SrCtx* sr, void* y, uint8_t* codes, uint32_t* mask,

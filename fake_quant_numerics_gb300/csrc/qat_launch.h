@@ -123,6 +123,13 @@ qat_status launch_percentile(qat_dtype dt, const void* x, int64_t n, bool affine
                              unsigned long long rank_lo, unsigned long long rank_hi, void* ws,
                              cudaStream_t s);
 
+// block-scaled floating point (fmt: qat_elem_format, kind: qat_block_scale,
+// block 16 or 32); ws / nparts: the tensor statistics partials (E4M3 kind)
+qat_status launch_block_fq(qat_dtype dt, int fmt, int kind, int64_t block, const void* x,
+                           int64_t n, const void* ws, int nparts, float* tensor_scale, void* y,
+                           uint8_t* codes, void* bscales, uint32_t* mask, int32_t* flags,
+                           cudaStream_t s);
+
 // FP8
 #define QAT_DECL_FP8_TENSOR(name)                                                               \
   qat_status name(qat_dtype dt, qat_fp8_format fmt, bool given, const void* x, int64_t n,       \

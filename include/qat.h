@@ -225,6 +225,51 @@ qat_status qat_fake_quant_int_percentile(const void* x, qat_dtype dtype, int64_t
                                          size_t workspace_bytes, qat_stream_t stream);
 
 /*
+ * Block-scaled floating-point fake quantization ([EDU] demo 4, block_scaled;
+ * OCP MX formats and NVFP4).  One scale per block of `block` consecutive
+ * elements (16 or 32; n a multiple of it), from the block's absmax over
+ * finite values:
+ *   QAT_BLOCK_SCALE_E8M0  X = 2^(floor(log2 amax) - emax) (amax 0: 2^-emax;
+ *     the exponent held to [-127, 127]); block_scales: uint8 E8M0 codes
+ *     (exponent + 127)  [MX];
+ *   QAT_BLOCK_SCALE_E4M3  g = max|x| / (elem_max * 448) over the tensor
+ *     (written to *tensor_scale), X = E4M3(amax / elem_max / g) * g with the
+ *     saturating round to nearest even; block_scales: uint8 E4M3 codes
+ *     [NVFP4: E2M1 elements, blocks of 16];
+ *   QAT_BLOCK_SCALE_FP32  X = amax / elem_max; block_scales: float.
+ *   A scale that is 0 or NaN becomes 1.
+ * Elements: y = E(x / X) * X with E the saturating round to nearest even on
+ * the element grid: E4M3 (max 448), E5M2 (57344), E2M3 (7.5), E3M2 (28),
+ * E2M1 (6).  binary32 arithmetic, one rounding per operation in that order.
+ * codes (nullable): one byte per element for FP8 / FP6 elements (the FP6 code
+ * in the low 6 bits), two per byte for E2M1 (element 2j in the high nibble).
+ * NaN elements: y NaN, code 0x7F (FP8) or 0 (FP6 / FP4); Inf saturates.
+ * mask (nullable): bit set where |x / X| <= elem_max.  NaN or Inf in x sets
+ * QAT_FLAG_NONFINITE_INPUT (informational).  *tensor_scale (nullable) is 1
+ * for the E8M0 and FP32 kinds.  workspace: qat_workspace_bytes(1, n,
+ * QAT_PER_TENSOR, 0) bytes for the E4M3 kind (its tensor statistics pass),
+ * none otherwise.  One launch (two for E4M3).
+ */
+typedef enum {
+  QAT_ELEM_E4M3 = 0,
+  QAT_ELEM_E5M2 = 1,
+  QAT_ELEM_E2M3 = 2,
+  QAT_ELEM_E3M2 = 3,
+  QAT_ELEM_E2M1 = 4
+} qat_elem_format;
+typedef enum {
+  QAT_BLOCK_SCALE_E8M0 = 0,
+  QAT_BLOCK_SCALE_E4M3 = 1,
+  QAT_BLOCK_SCALE_FP32 = 2
+} qat_block_scale;
+
+qat_status qat_fake_quant_block(const void* x, qat_dtype dtype, int64_t n, qat_elem_format elem,
+                                int64_t block, qat_block_scale scale_kind, float* tensor_scale,
+                                void* y, uint8_t* codes, void* block_scales, uint32_t* mask,
+                                int32_t* dev_flags, void* workspace, size_t workspace_bytes,
+                                qat_stream_t stream);
+
+/*
  * Per-tensor amax-scaled FP8 fake quantization ([QAT] fake_quant_fp8 /
  * fp8_quantize_magnitude; scale as in [MAR]).
  *   scale_given == 0: s = (max |x| over finite x) / fmt_max, written to *scale
