@@ -193,10 +193,37 @@ __global__ void __launch_bounds__(256) k_block_fq(const void* __restrict__ x, in
       OutVec<T> ov;
       uint32_t mb = 0u;
       uint32_t cw[VEC / 4] = {};  // the vector's codes: a byte per element (FP4: a nibble)
+      // The quotient t = RN(x / X) without a division: for a power-of-two
+      // scale the product with its exact reciprocal; otherwise, for a finite
+      // vector and a scale in the reciprocal's safe range, the exact quotient
+      // of the residual steps (a quotient small enough to underflow rounds to
+      // 0 in every element format either way); else the IEEE division.
+      const bool fin = st.nonfinite == 0u;
+      const bool quot = KIND != QAT_BLOCK_SCALE_E8M0 && fin && quot_scale_ok(X);
+      float inv = 0.0f;
+      if (KIND == QAT_BLOCK_SCALE_E8M0) {
+        const int ei = 127 - (int)(__float_as_uint(X) >> 23);  // -es (X normal)
+        inv = __float_as_uint(X) >= 0x00800000u
+                  ? __uint_as_float((uint32_t)(ei + 127) << 23)
+                  : __uint_as_float(0x7f000000u);  // X = 2^-127: 1 / X = 2^127
+      } else if (quot) {
+        inv = __frcp_rn(X);
+      }
 #pragma unroll
       for (int e = 0; e < VEC; e += 2) {
         const float xa = elem<T>(v, e), xb = elem<T>(v, e + 1);
-        const float ta = __fdiv_rn(xa, X), tb = __fdiv_rn(xb, X);
+        float ta, tb;
+        if (KIND == QAT_BLOCK_SCALE_E8M0) {
+          mul2(xa, xb, inv, inv, ta, tb);
+        } else if (quot) {
+          quotient_rn2(xa, xb, inv, -X, ta, tb);
+          // the residual steps turn -0 into +0; X > 0, so t has the sign of x
+          ta = copysignf(ta, xa);
+          tb = copysignf(tb, xb);
+        } else {
+          ta = __fdiv_rn(xa, X);
+          tb = __fdiv_rn(xb, X);
+        }
         const bool na = isnan(ta), nb = isnan(tb);
         const bool nan_code = FMT == QAT_ELEM_E4M3 || FMT == QAT_ELEM_E5M2;
         const uint32_t c2 =
