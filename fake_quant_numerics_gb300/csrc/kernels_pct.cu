@@ -78,30 +78,47 @@ __device__ __forceinline__ unsigned long long block_scan256(unsigned long long v
   return v + before;
 }
 
+// A target's prefix on the raw bits: after the first pass the known bits hold
+// the sign, which fixes the key's flip (order_key: ~u for a negative value,
+// u with the sign bit set for a positive one), so (order_key(u) & km) == pf
+// exactly when (u & km) == pct_raw_target(pf, km).
+__device__ __forceinline__ uint32_t pct_raw_target(uint32_t pf, uint32_t km) {
+  return (pf ^ ((pf & 0x80000000u) ? 0x80000000u : 0xffffffffu)) & km;
+}
+
 // One vector's elements into the block histograms.  PASS 0 counts every
 // element in h0 (both targets share the empty prefix); later passes count the
-// elements that match a target's prefix, a warp vote first so that a warp
-// with no match skips the atomics.  cnt: the vector's elements present.
-template <typename T, int PASS, bool SHARED>
-__device__ __forceinline__ void pct_fold(const V32& v, int cnt, uint32_t pf0, uint32_t km0,
-                                         uint32_t pf1, uint32_t km1, uint32_t* h0, uint32_t* h1) {
+// elements that match a target's prefix (raw-bit targets rp0 / rp1), one warp
+// vote per vector first, so that the usual vector, with no match in the warp,
+// costs a masked compare per element.  cnt: the vector's elements present
+// (FULL: all of them).
+template <typename T, int PASS, bool SHARED, bool FULL>
+__device__ __forceinline__ void pct_fold(const V32& v, int cnt, uint32_t rp0, uint32_t km0,
+                                         uint32_t rp1, uint32_t km1, uint32_t* h0, uint32_t* h1) {
   constexpr int SHIFT = pct_shift(PASS);
   constexpr uint32_t DMASK = (1u << pct_bits(PASS)) - 1u;
+  if (PASS == 0) {
+#pragma unroll
+    for (int e = 0; e < T::VEC; ++e) {
+      const uint32_t bin = (order_key(elem_bits<T>(v, e)) >> SHIFT) & DMASK;
+      if (FULL || e < cnt) atomicAdd(h0 + bin, 1u);
+    }
+    return;
+  }
+  bool any = false;
 #pragma unroll
   for (int e = 0; e < T::VEC; ++e) {
-    const uint32_t key = order_key(elem_bits<T>(v, e));
-    const uint32_t bin = (key >> SHIFT) & DMASK;
-    const bool valid = e < cnt;
-    if (PASS == 0) {
-      if (valid) atomicAdd(h0 + bin, 1u);
-    } else {
-      const bool m0 = valid && (key & km0) == pf0;
-      if (__any_sync(kFull, m0) && m0) atomicAdd(h0 + bin, 1u);
-      if (!SHARED) {
-        const bool m1 = valid && (key & km1) == pf1;
-        if (__any_sync(kFull, m1) && m1) atomicAdd(h1 + bin, 1u);
-      }
-    }
+    const uint32_t u = elem_bits<T>(v, e);
+    const bool m = (u & km0) == rp0 || (!SHARED && (u & km1) == rp1);
+    any |= m && (FULL || e < cnt);
+  }
+  if (!__any_sync(kFull, any)) return;
+#pragma unroll
+  for (int e = 0; e < T::VEC; ++e) {
+    const uint32_t u = elem_bits<T>(v, e);
+    const uint32_t bin = (order_key(u) >> SHIFT) & DMASK;
+    if ((FULL || e < cnt) && (u & km0) == rp0) atomicAdd(h0 + bin, 1u);
+    if (!SHARED && (FULL || e < cnt) && (u & km1) == rp1) atomicAdd(h1 + bin, 1u);
   }
 }
 
@@ -109,10 +126,10 @@ __device__ __forceinline__ void pct_fold(const V32& v, int cnt, uint32_t pf0, ui
 // rounds on every lane of a warp, for the votes), the next U vectors loaded
 // before the current ones are counted.
 template <typename T, int PASS, bool SHARED>
-__device__ __forceinline__ void pct_walk(const void* __restrict__ x, int64_t n, uint32_t pf0,
-                                         uint32_t km0, uint32_t pf1, uint32_t km1, uint32_t* h0,
+__device__ __forceinline__ void pct_walk(const void* __restrict__ x, int64_t n, uint32_t rp0,
+                                         uint32_t km0, uint32_t rp1, uint32_t km1, uint32_t* h0,
                                          uint32_t* h1, uint32_t& bad) {
-  constexpr int VEC = T::VEC, U = 2;
+  constexpr int VEC = T::VEC, U = 1;
   const int64_t nvec = (n + VEC - 1) / VEC;
   const int64_t nfull = n / VEC;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -145,7 +162,10 @@ __device__ __forceinline__ void pct_walk(const void* __restrict__ x, int64_t n, 
         Stats probe;
         if (probe.vec_absmax_nan<T>(cur[k]) >= 0x7f800000u) bad = 1u;
       }
-      pct_fold<T, PASS, SHARED>(cur[k], cnt, pf0, km0, pf1, km1, h0, h1);
+      if (cnt == VEC)
+        pct_fold<T, PASS, SHARED, true>(cur[k], cnt, rp0, km0, rp1, km1, h0, h1);
+      else
+        pct_fold<T, PASS, SHARED, false>(cur[k], cnt, rp0, km0, rp1, km1, h0, h1);
     }
 #pragma unroll
     for (int k = 0; k < U; ++k) cur[k] = nxt[k];
@@ -156,7 +176,7 @@ __device__ __forceinline__ void pct_walk(const void* __restrict__ x, int64_t n, 
 // (a counter per pass) picks each target's bin, extends its prefix, clears the
 // histograms and, after the last pass, writes the map's partial.
 template <typename T, bool AFFINE, int PASS>
-__global__ void __launch_bounds__(256) k_pct_pass(const void* __restrict__ x, int64_t n,
+__global__ void __launch_bounds__(256, 5) k_pct_pass(const void* __restrict__ x, int64_t n,
                                                   PctState* st, unsigned long long* hist,
                                                   uint4* part) {
   constexpr int PER = kPctBins / 256;  // bins per thread in the pick
@@ -171,14 +191,15 @@ __global__ void __launch_bounds__(256) k_pct_pass(const void* __restrict__ x, in
   const int lane = threadIdx.x & 31;
   const int shift = pct_shift(pass);
   const uint32_t dmask = (1u << pct_bits(pass)) - 1u;
-  const uint32_t pf0 = st->prefix[0], pf1 = st->prefix[1];
   const uint32_t km0 = st->known[0], km1 = st->known[1];
+  const uint32_t rp0 = pct_raw_target(st->prefix[0], km0);
+  const uint32_t rp1 = pct_raw_target(st->prefix[1], km1);
   const bool shared = st->shared != 0u;
   uint32_t bad = 0u;
   if (PASS == 0 || shared)
-    pct_walk<T, PASS, true>(x, n, pf0, km0, pf1, km1, h[0], h[1], bad);
+    pct_walk<T, PASS, true>(x, n, rp0, km0, rp1, km1, h[0], h[1], bad);
   else
-    pct_walk<T, PASS, false>(x, n, pf0, km0, pf1, km1, h[0], h[1], bad);
+    pct_walk<T, PASS, false>(x, n, rp0, km0, rp1, km1, h[0], h[1], bad);
   if (pass == 0 && __reduce_or_sync(kFull, bad) && lane == 0) atomicOr(&st->nonfinite, 1u);
   __syncthreads();
   for (int i = threadIdx.x; i < 2 * kPctBins; i += blockDim.x) {
@@ -249,7 +270,8 @@ qat_status launch_percentile(qat_dtype dt, const void* x, int64_t n, bool affine
   k_pct_init<<<1, 1024, 0, s>>>(w.st, w.hist, rank_lo, rank_hi);
   const int64_t nvec = (n + 7) / 8;
   int64_t g = (nvec + 511) / 512;
-  // the resident blocks: 5 per SM (48 registers, 16 KiB of shared memory)
+  // the resident blocks: 5 per SM (48 registers, 16 KiB of shared memory);
+  // one vector requested ahead per thread (measured faster than two)
   const int64_t cap = (int64_t)device_info().sms * 5;
   const int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
 #define QAT_PP(T, A, P) k_pct_pass<T, A, P><<<grid, 256, 0, s>>>(x, n, w.st, w.hist, w.part)

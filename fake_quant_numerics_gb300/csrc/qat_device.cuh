@@ -324,6 +324,17 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
+// three-input forms (sm_100 and later): one instruction for two steps of a fold
+__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float fmin3_nan(float a, float b, float c) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -390,10 +401,11 @@ struct Stats {
       for (int k = 0; k < 8; ++k) m2 = bf16x2_max_nan(m2, v.w[k] & 0x7fff7fffu);
       return __float_as_uint(fmax_nan(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u)));
     }
-    float m = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) m = fmax_nan(m, fabsf(__uint_as_float(v.w[k])));
-    return __float_as_uint(m);
+    auto a = [&](int k) { return fabsf(__uint_as_float(v.w[k])); };
+    float m = fmax3_nan(a(0), a(1), a(2));
+    m = fmax3_nan(m, a(3), a(4));
+    m = fmax3_nan(m, a(5), a(6));
+    return __float_as_uint(fmax_nan(m, a(7)));
   }
   // absmax of one 32-byte vector (absent tail elements read +0): one max.NaN
   // per element (per two for bf16); only a vector holding NaN or Inf takes
@@ -408,18 +420,21 @@ struct Stats {
       for (int e = 0; e < T::VEC; ++e) add<kMMNone>(elem_bits<T>(v, e));
     }
   }
-  // finite min / max as floats of one full 32-byte vector (kMMFloat): plain
-  // fminf / fmaxf unless the vector holds NaN or Inf
+  // finite min / max as floats of one full 32-byte vector (kMMFloat): the
+  // running min and max folded with the elements by three-input min.NaN /
+  // max.NaN, kept when both results are finite (then every element was: a
+  // NaN makes both NaN, an Inf shows as the min or the max); a vector with a
+  // NaN or Inf takes the filtered per-element fold instead
   template <typename T>
   __device__ __forceinline__ void add_minmax_float(const V32& v) {
-    if (vec_absmax_nan<T>(v) < 0x7f800000u) {
-      float mn = __uint_as_float(kmin), mx = __uint_as_float(kmax);
+    auto x = [&](int e) { return __uint_as_float(elem_bits<T>(v, e)); };
+    float mn = __uint_as_float(kmin), mx = __uint_as_float(kmax);
 #pragma unroll
-      for (int e = 0; e < T::VEC; ++e) {
-        const float x = __uint_as_float(elem_bits<T>(v, e));
-        mn = fminf(mn, x);
-        mx = fmaxf(mx, x);
-      }
+    for (int e = 0; e < T::VEC; e += 2) {
+      mn = fmin3_nan(mn, x(e), x(e + 1));
+      mx = fmax3_nan(mx, x(e), x(e + 1));
+    }
+    if (fabsf(mn) < __int_as_float(0x7f800000) && fabsf(mx) < __int_as_float(0x7f800000)) {
       kmin = __float_as_uint(mn);
       kmax = __float_as_uint(mx);
     } else {
@@ -708,8 +723,9 @@ constexpr uint32_t kRintMagicBits = 0x4b400000u;
 //     difference is +0, except (-0) - (+0) = -0: a lower bound of +0 is used
 //     as -0 (x - (-0) is +0 for both zeros), and the whi side never meets
 //     that case (whi >= +0, and whi - |x| has |x| >= +0).  So the sign bits
-//     are the window test; they are shifted into the mask with funnel
-//     shifts, highest element first.
+//     are the window test (affine: the sign of the product of the two
+//     differences); they are shifted into the mask with funnel shifts,
+//     highest element first.
 // FULL == false: elements e >= cnt are absent (read as +0) and get code 0.
 template <typename T, int BITS, bool AFFINE, bool FULL, bool CLAMP = false>
 __device__ __forceinline__ void int_vec_cal(const V32& v, const IntParams& p, int cnt,
@@ -718,6 +734,7 @@ __device__ __forceinline__ void int_vec_cal(const V32& v, const IntParams& p, in
   constexpr int VEC = T::VEC;
   const float ns = -p.s;
   const float wlo = p.wlo == 0.0f ? -0.0f : p.wlo;
+  const float kloM = __fadd_rn(p.klof, kRintMagic), khiM = __fadd_rn(p.khif, kRintMagic);
   cv.clear();
   uint32_t out = 0u;  // out-of-window bits
 #pragma unroll
@@ -726,12 +743,12 @@ __device__ __forceinline__ void int_vec_cal(const V32& v, const IntParams& p, in
     float fa, fb, ta, tb, ya, yb;
     quotient_rn2(xa, xb, p.rcp, ns, fa, fb);
     add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
-    sub2(ta, tb, kRintMagic, kRintMagic, fa, fb);
     if (AFFINE || CLAMP) {
-      fa = fminf(fmaxf(fa, p.klof), p.khif);
-      fb = fminf(fmaxf(fb, p.klof), p.khif);
-      add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
+      // M + clamp(f) = clamp(M + f) to [M + klo, M + khi], all exact integers
+      ta = fminf(fmaxf(ta, kloM), khiM);
+      tb = fminf(fmaxf(tb, kloM), khiM);
     }
+    sub2(ta, tb, kRintMagic, kRintMagic, fa, fb);
     mul2(fa, fb, p.s, p.s, ya, yb);
     ov.set2(e, ya, yb);
     int qa = (int)(__float_as_uint(ta) - kRintMagicBits) + (AFFINE ? p.zp : 0);
@@ -743,11 +760,15 @@ __device__ __forceinline__ void int_vec_cal(const V32& v, const IntParams& p, in
     cv.set2(e, qa, qb);
     uint32_t oa, ob;
     if (AFFINE) {
-      float ha, hb, la, lb;
+      // out of the window when one difference is negative (both cannot be:
+      // wlo <= whi); a product keeps the sign of the pair even when it rounds
+      // to zero or overflows, so its sign bit is the test
+      float ha, hb, la, lb, pa, pb;
       sub2(p.whi, p.whi, xa, xb, ha, hb);
       sub2(xa, xb, wlo, wlo, la, lb);
-      oa = __float_as_uint(ha) | __float_as_uint(la);
-      ob = __float_as_uint(hb) | __float_as_uint(lb);
+      mul2(ha, hb, la, lb, pa, pb);
+      oa = __float_as_uint(pa);
+      ob = __float_as_uint(pb);
     } else {
       oa = __float_as_uint(__fsub_rn(p.whi, fabsf(xa)));
       ob = __float_as_uint(__fsub_rn(p.whi, fabsf(xb)));
@@ -845,11 +866,15 @@ __device__ __forceinline__ void int_vec_cal_sr(const V32& v, const IntParams& p,
       cv.set2(e, qa_, qb_);
       uint32_t oa, ob;
       if (AFFINE) {
-        float ha, hb, la, lb;
+        // out of the window when one difference is negative (both cannot be:
+        // wlo <= whi); a product keeps the sign of the pair even when it rounds
+        // to zero or overflows, so its sign bit is the test
+        float ha, hb, la, lb, pa, pb;
         sub2(p.whi, p.whi, xa, xb, ha, hb);
         sub2(xa, xb, wlo, wlo, la, lb);
-        oa = __float_as_uint(ha) | __float_as_uint(la);
-        ob = __float_as_uint(hb) | __float_as_uint(lb);
+        mul2(ha, hb, la, lb, pa, pb);
+        oa = __float_as_uint(pa);
+        ob = __float_as_uint(pb);
       } else {
         oa = __float_as_uint(__fsub_rn(p.whi, fabsf(xa)));
         ob = __float_as_uint(__fsub_rn(p.whi, fabsf(xb)));
