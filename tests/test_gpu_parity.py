@@ -121,6 +121,45 @@ def test_int_per_group(qat, orc, dt, bits_, scheme):
         run_int(qat, orc, x, r, c, bits_, SCHEMES[scheme], 2, g)
 
 
+def plant_nonfinite(x, L):
+    """Units of L elements with infinities placed where the statistics fold
+    meets them in different ways: a lone +Inf or -Inf first, mid-vector or
+    last; both signs; a whole unit of +Inf; a NaN beside an Inf; finite units
+    between them (the fold keeps its running min / max across vectors)."""
+    a = x.float().numpy().reshape(-1).copy()
+    units = a.size // L
+    plan = [(1, [(0, np.inf)]), (2, [(L // 2 + 3, -np.inf)]), (4, [(L - 1, np.inf)]),
+            (5, [(5, np.inf), (L - 9, -np.inf)]), (7, "all"), (8, [(1, np.nan), (L - 2, np.inf)]),
+            (10, [(L // 3, -np.inf)])]
+    for u, spots in plan:
+        if u >= units:
+            continue
+        if spots == "all":
+            a[u * L:(u + 1) * L] = np.inf
+        else:
+            for off, v in spots:
+                a[u * L + off] = v
+    t = torch.from_numpy(a.reshape(x.shape))
+    return t.to(x.dtype) if x.dtype != torch.float32 else t
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("scheme", ["sym", "affine"])
+def test_int_infinities_in_units(qat, orc, dt, scheme):
+    """Per-row and per-group calibration with infinities in some units: those
+    units are flagged and their outputs zero, the others unchanged."""
+    for gran, shapes in ((1, [(12, 256), (11, 4096), (12, 1000)]),
+                         (2, [(3, 1536, 128), (2, 1408, 64), (12, 96, 32)])):
+        for i, shp in enumerate(shapes):
+            r, c = shp[0], shp[1]
+            g = shp[2] if gran == 2 else 0
+            L = g if gran == 2 else c
+            x = plant_nonfinite(make_input(r, c, DT[dt], seed=900 + 10 * gran + i), L)
+            for bits_ in (8, 4):
+                o = run_int(qat, orc, x, r, c, bits_, SCHEMES[scheme], gran, g)
+                assert o["flags"] & orc.FLAG_NONFINITE
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("bits_", [8, 4])
 def test_int_affine_zero_window_ends(qat, orc, dt, bits_):
