@@ -253,6 +253,33 @@ class L2Flush:
         self.r.sum()
 
 
+def isolated_call_ms(calls, stream, iters=30, warm=3):
+    """Each call of the step alone: an L2 flush (L2Flush) before every timed
+    iteration, CUDA events around the call on its stream; the mean in ms.
+    Back to back, a call also pays for writing back the dirty L2 lines that
+    the call before it left (w2 follows the 1 GiB written by w5's dequant);
+    alone, it pays only for its own traffic."""
+    flush = L2Flush(torch.device("cuda", torch.cuda.current_device()))
+    out = []
+    for c in calls:
+        for _ in range(warm):
+            flush()
+            c()
+        ev = []
+        for _ in range(iters):
+            flush()
+            a = torch.cuda.Event(enable_timing=True)
+            z = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            c()
+            z.record(stream)
+            ev.append((a, z))
+        torch.cuda.synchronize()
+        out.append(sum(a.elapsed_time(z) for a, z in ev) / iters)
+    del flush
+    return out
+
+
 def run_next_rows(args, suite, wb, peak):
     """Rows past the headline path, timed like it (CUDA events per call on the
     launching stream, after warm-up) but reported outside `value`:
@@ -705,12 +732,17 @@ def run_ours(args, rank, world, local):
     next_rows = None
     if not args.only and args.fraction >= 1.0 and not args.no_next:
         next_rows = run_next_rows(args, suite, wb, peak)
+    iso_ms = isolated_call_ms(calls, stream) if not args.no_isolated else None
     per_wl = {}
-    for (name, elems, b, nl), ms in zip(wb, mean_ms):
+    for i, ((name, elems, b, nl), ms) in enumerate(zip(wb, mean_ms)):
         per_wl[name] = {"ms": round(float(ms), 5), "GB_s": round(b / (ms * 1e-3) / 1e9, 1),
                         "Gelem_s": round(elems / (ms * 1e-3) / 1e9, 2),
                         "frac_of_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peak, 4),
                         "launches": nl, "bytes": b}
+        if iso_ms is not None:
+            per_wl[name]["isolated_ms"] = round(float(iso_ms[i]), 5)
+            per_wl[name]["isolated_frac_of_measured_hbm"] = round(
+                b / (iso_ms[i] * 1e-3) / 1e9 / peak, 4)
     # dominant kernel: the single-launch call with the largest time (a subset
     # run of multi-launch calls only reports its longest call)
     single = [i for i, w in enumerate(wb) if w[3] == 1] or list(range(len(wb)))
@@ -892,6 +924,8 @@ def main(argv=None):
     ap.add_argument("--ref-fraction", type=float, default=0.0,
                     help="per-step sample of the reference arm (0: sized to ~2 min in total)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-isolated", action="store_true",
+                    help="skip the per-call timings with an L2 flush before each call")
     ap.add_argument("--no-next", action="store_true",
                     help="skip the stochastic-rounding and CUDA-graph timings (next_rows)")
     ap.add_argument("--only", default="",
