@@ -79,3 +79,27 @@ def test_reference_arm_non_zero_rank_prints_nothing():
                         "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
                        timeout=300, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_recorded_traffic_follows_the_source_key(tmp_path, monkeypatch):
+    """The DRAM traffic recorded for a kernel is reported only while its
+    source and the shared device header hash to the recorded key; an edit to
+    either makes it null."""
+    import bench
+
+    csrc = tmp_path / "fake_quant_numerics_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "kernels_misc.cu").write_text("// kernel source\n")
+    (csrc / "qat_device.cuh").write_text("// device header\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    key = bench.source_key("kernels_misc.cu")
+    assert len(key) == 16
+    (tmp_path / "profiles" / "traffic.txt").write_text(
+        "# kernel key bytes\n"
+        f"k_q4_quant     {key}  1204138496   # read write algorithmic\n"
+        "k_q4_dequant   0000000000000000  1148113664\n")
+    assert bench.recorded_traffic("k_q4_quant", "kernels_misc.cu") == 1204138496.0
+    assert bench.recorded_traffic("k_q4_dequant", "kernels_misc.cu") is None
+    (csrc / "qat_device.cuh").write_text("// device header, edited\n")
+    assert bench.recorded_traffic("k_q4_quant", "kernels_misc.cu") is None
