@@ -186,7 +186,7 @@ __global__ void __maxnreg__(SR ? 128 : (T::BYTES == 4 ? 96 : 80))
 // one thread block (256 threads) per unit of L elements, NV vectors / thread
 // ---------------------------------------------------------------------------
 template <typename T, int BITS, bool AFFINE, int NV, bool STATS_ONLY, bool SR>
-__global__ void __launch_bounds__(256, NV <= 2 ? 3 : 1)
+__global__ void __launch_bounds__(256, NV <= 2 ? 4 : 1)
     k_int_rows(const void* __restrict__ x, int64_t units, int64_t L, float* scale, int32_t* zp,
                float* absmax, float* minv, float* maxv, SrCtx sr, CalOpts co, void* y, void* codes,
                uint32_t* mask, int32_t* flags) {
