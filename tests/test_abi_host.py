@@ -120,3 +120,93 @@ def test_stats_argument_errors(lib):
     assert f(A, L.F32, 4, 6, L.PER_GROUP, 4, None, None, None, None, None, 0, None) == L.QAT_ERR_INVALID_ARGUMENT
     assert f(MIS, L.F32, 4, 4, L.PER_ROW, 0, None, None, None, None, None, 0, None) == L.QAT_ERR_MISALIGNED
     assert f(A, L.F32, 4, 4, L.PER_COLUMN, 0, None, None, None, None, None, 0, None) == L.QAT_ERR_WORKSPACE
+
+
+def _opts(lib, options, **kw):
+    a = dict(x=A, dt=L.F32, rows=4, cols=64, bits=8, scheme=L.SYMMETRIC, gran=L.PER_TENSOR, group=0,
+             sr=0, scale=A, zp=A, y=A, codes=A, mask=A, flags=None, ws=None, wsb=0)
+    a.update(kw)
+    return lib.qat_fake_quant_int_opts(a["x"], a["dt"], a["rows"], a["cols"], a["bits"],
+                                       a["scheme"], a["gran"], a["group"], options, a["sr"], 1, 0,
+                                       a["scale"], a["zp"], a["y"], a["codes"], a["mask"],
+                                       a["flags"], a["ws"], a["wsb"], None)
+
+
+def test_calibration_options_argument_errors(lib):
+    for clip in (0.0, -0.5, 1.5, float("nan"), float("inf")):
+        o = L.CalibOptions(clip, 0)
+        assert _opts(lib, ctypes.addressof(o)) == L.QAT_ERR_INVALID_ARGUMENT, clip
+    ok = L.CalibOptions(0.7, 1)
+    # valid options, then the integer path's own checks
+    assert _opts(lib, ctypes.addressof(ok), bits=3) == L.QAT_ERR_UNSUPPORTED
+    assert _opts(lib, ctypes.addressof(ok), x=MIS) == L.QAT_ERR_MISALIGNED
+    assert _opts(lib, ctypes.addressof(ok)) == L.QAT_ERR_WORKSPACE        # per tensor, no workspace
+    assert _opts(lib, None, sr=1) == L.QAT_ERR_WORKSPACE                  # NULL options: plain
+    assert _opts(lib, ctypes.addressof(ok), rows=0, x=None, scale=None) == L.QAT_OK
+    f = lib.qat_fake_quant_int_sr
+    assert f(A, L.F32, 4, 64, 5, 0, 0, 0, 0, A, A, 1, 0, A, A, A, None, None, 0, None) \
+        == L.QAT_ERR_UNSUPPORTED
+    assert f(A, L.F32, 4, 64, 8, 0, 0, 0, 0, A, A, 1, 0, A, A, A, None, None, 0, None) \
+        == L.QAT_ERR_WORKSPACE
+
+
+def _pct(lib, **kw):
+    a = dict(x=A, dt=L.F32, n=1000, bits=8, scheme=L.SYMMETRIC, c=0.01, scale=A, zp=A, y=A, codes=A,
+             mask=A, ws=A, wsb=lib.qat_percentile_workspace_bytes())
+    a.update(kw)
+    return lib.qat_fake_quant_int_percentile(a["x"], a["dt"], a["n"], a["bits"], a["scheme"],
+                                             a["c"], 0, 0, 0, a["scale"], a["zp"], a["y"],
+                                             a["codes"], a["mask"], None, a["ws"], a["wsb"], None)
+
+
+def test_percentile_argument_errors(lib):
+    assert lib.qat_percentile_workspace_bytes() >= 1024
+    assert _pct(lib, bits=6) == L.QAT_ERR_UNSUPPORTED
+    assert _pct(lib, dt=4) == L.QAT_ERR_UNSUPPORTED
+    assert _pct(lib, scheme=2) == L.QAT_ERR_UNSUPPORTED
+    # QuantParams::per_tensor_percentile takes a clip fraction in [0, 0.5)
+    for c in (-0.01, 0.5, 0.75, float("nan")):
+        assert _pct(lib, c=c) == L.QAT_ERR_INVALID_ARGUMENT, c
+    assert _pct(lib, n=-1) == L.QAT_ERR_INVALID_ARGUMENT
+    assert _pct(lib, n=(1 << 40) + 1) == L.QAT_ERR_INVALID_ARGUMENT
+    assert _pct(lib, n=0, x=None, scale=None, ws=None) == L.QAT_OK
+    assert _pct(lib, x=None) == L.QAT_ERR_INVALID_ARGUMENT
+    assert _pct(lib, scale=None) == L.QAT_ERR_INVALID_ARGUMENT
+    assert _pct(lib, x=MIS) == L.QAT_ERR_MISALIGNED
+    assert _pct(lib, y=MIS) == L.QAT_ERR_MISALIGNED
+    assert _pct(lib, codes=ctypes.c_void_p(0x10001)) == L.QAT_ERR_MISALIGNED
+    assert _pct(lib, scale=ctypes.c_void_p(0x10002)) == L.QAT_ERR_MISALIGNED
+    assert _pct(lib, ws=None) == L.QAT_ERR_WORKSPACE
+    assert _pct(lib, wsb=lib.qat_percentile_workspace_bytes() - 1) == L.QAT_ERR_WORKSPACE
+    assert _pct(lib, ws=MIS) == L.QAT_ERR_MISALIGNED
+
+
+def _blk(lib, **kw):
+    a = dict(x=A, dt=L.BF16, n=4096, elem=4, block=16, kind=1, ts=A, y=A, codes=A, bs=A, mask=A,
+             ws=None, wsb=0)
+    a.update(kw)
+    return lib.qat_fake_quant_block(a["x"], a["dt"], a["n"], a["elem"], a["block"], a["kind"],
+                                    a["ts"], a["y"], a["codes"], a["bs"], a["mask"], None, a["ws"],
+                                    a["wsb"], None)
+
+
+def test_block_scaled_argument_errors(lib):
+    # element formats E4M3 .. E2M1 (0 .. 4), scales E8M0 / E4M3 / FP32 (0 .. 2)
+    assert _blk(lib, dt=5) == L.QAT_ERR_UNSUPPORTED
+    assert _blk(lib, elem=5) == L.QAT_ERR_UNSUPPORTED
+    assert _blk(lib, elem=-1) == L.QAT_ERR_UNSUPPORTED
+    assert _blk(lib, kind=3) == L.QAT_ERR_UNSUPPORTED
+    for b in (8, 24, 64):
+        assert _blk(lib, block=b) == L.QAT_ERR_UNSUPPORTED, b
+    assert _blk(lib, n=-16) == L.QAT_ERR_INVALID_ARGUMENT
+    assert _blk(lib, n=100) == L.QAT_ERR_INVALID_ARGUMENT          # not whole blocks of 16
+    assert _blk(lib, n=48, block=32) == L.QAT_ERR_INVALID_ARGUMENT
+    assert _blk(lib, n=0, x=None) == L.QAT_OK
+    assert _blk(lib, x=None) == L.QAT_ERR_INVALID_ARGUMENT
+    assert _blk(lib, x=MIS) == L.QAT_ERR_MISALIGNED
+    assert _blk(lib, bs=ctypes.c_void_p(0x10002)) == L.QAT_ERR_MISALIGNED
+    assert _blk(lib, ts=ctypes.c_void_p(0x10002)) == L.QAT_ERR_MISALIGNED
+    # the E4M3 scale (NVFP4) needs the tensor statistics workspace
+    assert _blk(lib, ws=None) == L.QAT_ERR_WORKSPACE
+    assert _blk(lib, ws=A, wsb=15) == L.QAT_ERR_WORKSPACE
+    assert _blk(lib, ws=MIS, wsb=1 << 20) == L.QAT_ERR_MISALIGNED
