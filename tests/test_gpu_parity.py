@@ -474,3 +474,26 @@ def test_named_ops_and_launch_count(qat, orc):
     with pytest.raises(qat.QatDataError):
         qat.fake_quant_int(torch.zeros(64, device="cuda"), check=True)
     _ = r
+
+
+def test_binding_dimension_mismatch(qat):
+    """The binding's DIMENSION_MISMATCH (raised before any launch): a given
+    parameter array whose length is not the unit count, an affine call given
+    scales without zero points, and an STE mask of the wrong length."""
+    from fake_quant_numerics_gb300 import _lib as L
+
+    x = torch.randn(4, 64, device="cuda")
+    c0 = qat.qat_kernel_launch_count()
+    for kw in (dict(granularity="row", scale=torch.ones(3, device="cuda")),
+               dict(granularity="group", group=32, scale=torch.ones(4, device="cuda")),
+               dict(granularity="row", scheme="affine", scale=torch.ones(4, device="cuda")),
+               dict(granularity="row", scheme="affine", scale=torch.ones(4, device="cuda"),
+                    zero_point=torch.zeros(5, dtype=torch.int32, device="cuda"))):
+        with pytest.raises(qat.QatError) as e:
+            qat.fake_quant_int(x, 8, **kw)
+        assert e.value.status == L.QAT_ERR_DIMENSION_MISMATCH, kw
+    with pytest.raises(qat.QatError) as e:
+        qat.fake_quant_backward(torch.randn(256, device="cuda"),
+                                torch.zeros(7, dtype=torch.int32, device="cuda"))
+    assert e.value.status == L.QAT_ERR_DIMENSION_MISMATCH
+    assert qat.qat_kernel_launch_count() == c0
