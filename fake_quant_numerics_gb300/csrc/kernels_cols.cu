@@ -232,7 +232,8 @@ __device__ __forceinline__ ColP col_params(const IntParams& p) {
   q.klof = p.klof;
   q.khif = p.khif;
   q.zp = p.zp;
-  q.st = (p.dead ? 1 : 0) | (p.fast ? 2 : 0);
+  // a unit whose quotients may overflow (fast == 3) takes the division path
+  q.st = (p.dead ? 1 : 0) | ((p.fast == 1 || p.fast == 2) ? 2 : 0);
   return q;
 }
 

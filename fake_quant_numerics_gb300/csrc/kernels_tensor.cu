@@ -83,7 +83,9 @@ __global__ void __launch_bounds__(256) k_stats_finalize(const uint4* __restrict_
 // ---------------------------------------------------------------------------
 // integer fake quant, one parameter set (calibrated from partials or given)
 // ---------------------------------------------------------------------------
-template <typename T, int BITS, bool AFFINE, bool GIVEN, bool FULL, bool SR>
+// OPT: the unit may come from a calibration with options (p.fast 2 or 3);
+// without, only the plain reciprocal path is built, which keeps its registers.
+template <typename T, int BITS, bool AFFINE, bool GIVEN, bool FULL, bool SR, bool OPT>
 __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, int64_t tile,
                                          V32 (&v)[kTile / (32 * T::VEC)], bool have, int64_t next,
                                          const IntParams& p, const SrCtx& sr,
@@ -102,12 +104,18 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
     cv.clear();
     uint32_t mb = 0u;
     if (!GIVEN && p.fast) {
-      if (SR)
-        int_vec_cal_sr<T, BITS, AFFINE, FULL>(v[j], p, cnt[j], sr, base, ov, cv, mb);
-      else if (!AFFINE && p.fast == 2)
-        int_vec_cal<T, BITS, AFFINE, FULL, true>(v[j], p, cnt[j], ov, cv, mb);
-      else
+      if (SR) {
+        if (OPT && p.fast == 3)
+          int_vec_cal_sr<T, BITS, AFFINE, FULL, true>(v[j], p, cnt[j], sr, base, ov, cv, mb);
+        else
+          int_vec_cal_sr<T, BITS, AFFINE, FULL>(v[j], p, cnt[j], sr, base, ov, cv, mb);
+      } else if (OPT && p.fast == 3) {
+        int_vec_cal<T, BITS, AFFINE, FULL, 2>(v[j], p, cnt[j], ov, cv, mb);
+      } else if (OPT && !AFFINE && p.fast == 2) {
+        int_vec_cal<T, BITS, AFFINE, FULL, 1>(v[j], p, cnt[j], ov, cv, mb);
+      } else {
         int_vec_cal<T, BITS, AFFINE, FULL>(v[j], p, cnt[j], ov, cv, mb);
+      }
     } else if (!p.dead) {
 #pragma unroll
       for (int g = 0; g < VEC / 4; ++g) {
@@ -147,7 +155,7 @@ __device__ __forceinline__ void int_tile(const void* __restrict__ x, int64_t n, 
   }
 }
 
-template <typename T, int BITS, bool AFFINE, bool GIVEN, bool SR>
+template <typename T, int BITS, bool AFFINE, bool GIVEN, bool SR, bool OPT>
 __global__ void __maxnreg__(SR ? 128 : 80) k_int_tensor(const void* __restrict__ x, int64_t n,
                                                     const uint4* __restrict__ part, int nparts,
                                                     float* scale, int32_t* zp, SrCtx sr,
@@ -164,7 +172,7 @@ __global__ void __maxnreg__(SR ? 128 : 80) k_int_tensor(const void* __restrict__
     constexpr int MM = AFFINE ? kMMFloat : kMMNone;
     Stats st = reduce_partials<MM>(part, nparts, red);
     if (threadIdx.x == 0) {
-      int f = calibrate<BITS, AFFINE, MM>(st, sp, co);
+      int f = calibrate<BITS, AFFINE, MM>(st, sp, OPT ? co : CalOpts{1.0f, 0, 0});
       if (blockIdx.x == 0) {
         scale[0] = sp.s;
         if (zp) zp[0] = sp.zp;
@@ -189,11 +197,11 @@ __global__ void __maxnreg__(SR ? 128 : 80) k_int_tensor(const void* __restrict__
     const int64_t ntile = GIVEN ? nt : ntiles - 1 - nt;
     const int64_t next = (nt < ntiles && ntile < nfull) ? ntile : -1;
     if (tile < nfull)
-      int_tile<T, BITS, AFFINE, GIVEN, true, SR>(x, n, tile, v, have, next, p, sr, y, codes, mask,
-                                                 lane);
+      int_tile<T, BITS, AFFINE, GIVEN, true, SR, OPT>(x, n, tile, v, have, next, p, sr, y, codes,
+                                                      mask, lane);
     else
-      int_tile<T, BITS, AFFINE, GIVEN, false, SR>(x, n, tile, v, have, next, p, sr, y, codes, mask,
-                                                  lane);
+      int_tile<T, BITS, AFFINE, GIVEN, false, SR, OPT>(x, n, tile, v, have, next, p, sr, y, codes,
+                                                       mask, lane);
     have = next >= 0;
   }
 }
@@ -389,11 +397,16 @@ static void int_tensor_t(bool given, const void* x, int64_t n, const void* ws, i
                          void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
   const int grid = map_grid(n, 8);
   const uint4* part = static_cast<const uint4*>(ws);
+  // calibration options as a compile-time switch (the plain build keeps its registers)
+  const bool opt = co.clip != 1.0f || co.fp16 || co.clamp;
   if (given)
-    k_int_tensor<T, BITS, AFFINE, true, QAT_SR>
+    k_int_tensor<T, BITS, AFFINE, true, QAT_SR, false>
+        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, co, y, codes, mask, flags);
+  else if (opt)
+    k_int_tensor<T, BITS, AFFINE, false, QAT_SR, true>
         <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, co, y, codes, mask, flags);
   else
-    k_int_tensor<T, BITS, AFFINE, false, QAT_SR>
+    k_int_tensor<T, BITS, AFFINE, false, QAT_SR, false>
         <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, co, y, codes, mask, flags);
 }
 

@@ -584,8 +584,16 @@ struct IntParams {
   int dead;        // unit outputs are codes 0, y +0, mask 0
   int fast;        // calibrated unit with a scale in the safe range (quot_scale_ok):
                    // 1, or 2 when a symmetric unit's codes need the clamp too
-                   // (calibration options can leave values beyond the range)
+                   // (calibration options can leave values beyond the range),
+                   // or 3 when, besides, a quotient x * RN(1/s) may overflow
+                   // binary32 (kQuotGuard): the per-tensor map then clamps x
+                   // to +-2^24 s before the quotient, the other maps take the
+                   // division path for the unit
 };
+
+// A calibrated unit whose largest magnitude times RN(1/s) stays at or below
+// this bound keeps every product and remainder of quotient_rn finite.
+constexpr float kQuotGuard = 0x1p64f;
 
 template <int BITS, bool AFFINE>
 struct QRange {
@@ -640,10 +648,23 @@ __device__ __forceinline__ int calibrate(const Stats& st, IntParams& p,
   }
   int flag = st.has_nonfinite() ? QAT_FLAG_NONFINITE_CALIB : (degenerate ? QAT_FLAG_DEGENERATE : 0);
   p.dead = flag != 0;
-  p.fast = (!p.dead && quot_scale_ok(p.s))
-               ? ((!AFFINE && (co.clamp || co.clip != 1.0f || co.fp16)) ? 2 : 1)
-               : 0;
-  p.rcp = p.fast ? __frcp_rn(p.s) : 0.0f;
+  p.fast = 0;
+  p.rcp = 0.0f;
+  if (!p.dead && quot_scale_ok(p.s)) {
+    p.rcp = __frcp_rn(p.s);
+    const bool opts = co.clamp || co.clip != 1.0f || co.fp16;
+    p.fast = (!AFFINE && opts) ? 2 : 1;
+    // With options a value can lie far beyond the range; its quotient by s
+    // must stay finite on the reciprocal path (QuantParams::quantize clamps
+    // the real quotient, so such a value takes an end code).  The statistics
+    // of a percentile calibration (clamp) are the quantiles, not the unit's
+    // extremes, so it always takes the guard.
+    if (opts) {
+      const float ext =
+          AFFINE ? fmaxf(fabsf(st.min_f<MM>()), fabsf(st.max_f<MM>())) : st.absmax_f();
+      if (co.clamp || !(__fmul_rn(ext, p.rcp) <= kQuotGuard)) p.fast = 3;
+    }
+  }
   finish_params(p, qmin, qmax);
   return flag;
 }
@@ -716,8 +737,12 @@ constexpr uint32_t kRintMagicBits = 0x4b400000u;
 // p.fast holds only finite values (a NaN or Inf makes it dead), which the
 // window test below relies on.
 //   quotient: q = RN(x/s) by quotient_rn2, f = rint(q) by the magic constant;
-//   k = clamp(f) (affine, or CLAMP: p.fast == 2), y = k * s, code k + zp from the
-//   bits of k + M;
+//   k = clamp(f) (affine, or CL >= 1: p.fast == 2), y = k * s, code k + zp from
+//   the bits of k + M;
+//   CL == 2 (p.fast == 3): the quotient is taken of x clamped to
+//     [-2^24 s, 2^24 s] (2^24 s is exact: s <= 2^100), so it stays finite; an
+//     element beyond that bound has |x / s| > 2^24, far past every code, and
+//     both forms give it the end code of its sign (the window test keeps x);
 //   STE window: whi - |x| >= 0 (symmetric), whi - x >= 0 and x - wlo >= 0
 //     (affine); RN never changes the sign of a difference and an exact zero
 //     difference is +0, except (-0) - (+0) = -0: a lower bound of +0 is used
@@ -727,7 +752,7 @@ constexpr uint32_t kRintMagicBits = 0x4b400000u;
 //     differences); they are shifted into the mask with funnel shifts,
 //     highest element first.
 // FULL == false: elements e >= cnt are absent (read as +0) and get code 0.
-template <typename T, int BITS, bool AFFINE, bool FULL, bool CLAMP = false>
+template <typename T, int BITS, bool AFFINE, bool FULL, int CL = 0>
 __device__ __forceinline__ void int_vec_cal(const V32& v, const IntParams& p, int cnt,
                                             OutVec<T>& ov, CodeVec<BITS, T::VEC>& cv,
                                             uint32_t& mb) {
@@ -735,15 +760,20 @@ __device__ __forceinline__ void int_vec_cal(const V32& v, const IntParams& p, in
   const float ns = -p.s;
   const float wlo = p.wlo == 0.0f ? -0.0f : p.wlo;
   const float kloM = __fadd_rn(p.klof, kRintMagic), khiM = __fadd_rn(p.khif, kRintMagic);
+  const float xlim = CL == 2 ? __fmul_rn(p.s, 0x1p24f) : 0.0f;
   cv.clear();
   uint32_t out = 0u;  // out-of-window bits
 #pragma unroll
   for (int e = VEC - 2; e >= 0; e -= 2) {
     const float xa = elem<T>(v, e), xb = elem<T>(v, e + 1);
     float fa, fb, ta, tb, ya, yb;
-    quotient_rn2(xa, xb, p.rcp, ns, fa, fb);
+    if (CL == 2)
+      quotient_rn2(fminf(fmaxf(xa, -xlim), xlim), fminf(fmaxf(xb, -xlim), xlim), p.rcp, ns, fa,
+                   fb);
+    else
+      quotient_rn2(xa, xb, p.rcp, ns, fa, fb);
     add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
-    if (AFFINE || CLAMP) {
+    if (AFFINE || CL >= 1) {
       // M + clamp(f) = clamp(M + f) to [M + klo, M + khi], all exact integers
       ta = fminf(fmaxf(ta, kloM), khiM);
       tb = fminf(fmaxf(tb, kloM), khiM);
@@ -832,14 +862,16 @@ __device__ __forceinline__ float sr_round(float r, float u) {
 // quotient is the exact RN(x/s) (quotient_rn2), k = sr_round(q, u) clamped to
 // the code range (a value just above qmax - zp can round up past it), y = k s,
 // the window as in int_vec_cal.  base: element index of element 0 (a
-// multiple of 4).
-template <typename T, int BITS, bool AFFINE, bool FULL>
+// multiple of 4).  GUARD (p.fast == 3): the quotient of x clamped to
+// [-2^24 s, 2^24 s], as int_vec_cal with CL == 2.
+template <typename T, int BITS, bool AFFINE, bool FULL, bool GUARD = false>
 __device__ __forceinline__ void int_vec_cal_sr(const V32& v, const IntParams& p, int cnt,
                                                const SrCtx& sr, int64_t base, OutVec<T>& ov,
                                                CodeVec<BITS, T::VEC>& cv, uint32_t& mb) {
   constexpr int VEC = T::VEC;
   const float ns = -p.s;
   const float wlo = p.wlo == 0.0f ? -0.0f : p.wlo;
+  const float xlim = GUARD ? __fmul_rn(p.s, 0x1p24f) : 0.0f;
   cv.clear();
   uint32_t out = 0u;
 #pragma unroll
@@ -851,7 +883,11 @@ __device__ __forceinline__ void int_vec_cal_sr(const V32& v, const IntParams& p,
       const int e = 4 * g + 2 * h;
       const float xa = elem<T>(v, e), xb = elem<T>(v, e + 1);
       float qa, qb, ta, tb, ya, yb;
-      quotient_rn2(xa, xb, p.rcp, ns, qa, qb);
+      if (GUARD)
+        quotient_rn2(fminf(fmaxf(xa, -xlim), xlim), fminf(fmaxf(xb, -xlim), xlim), p.rcp, ns, qa,
+                     qb);
+      else
+        quotient_rn2(xa, xb, p.rcp, ns, qa, qb);
       float fa = fminf(fmaxf(sr_round(qa, u[2 * h]), p.klof), p.khif);
       float fb = fminf(fmaxf(sr_round(qb, u[2 * h + 1]), p.klof), p.khif);
       add2(fa, fb, kRintMagic, kRintMagic, ta, tb);
@@ -903,9 +939,11 @@ __device__ __forceinline__ void int_elem_sr(float x, float u, const IntParams& p
 }
 
 // Element map of one full vector with calibrated or given parameters: the
-// reciprocal path when p.fast, the IEEE path otherwise, zeros for a dead unit.
+// reciprocal path when p.fast is 1 or 2, the IEEE path otherwise (a unit whose
+// quotients may overflow, p.fast == 3, is rare: an extreme outlier against a
+// clipped range), zeros for a dead unit.
 // SR: stochastic rounding with the draws of elements base .. base + VEC - 1.
-// OPT = false: the unit comes from the plain calibration (p.fast is never 2).
+// OPT = false: the unit comes from the plain calibration (p.fast is 0 or 1).
 template <typename T, int BITS, bool AFFINE, bool SR = false, bool OPT = true>
 __device__ __forceinline__ void int_map_vec(const V32& v, const IntParams& p, OutVec<T>& ov,
                                             CodeVec<BITS, T::VEC>& cv, uint32_t& mb,
@@ -913,11 +951,11 @@ __device__ __forceinline__ void int_map_vec(const V32& v, const IntParams& p, Ou
   constexpr int VEC = T::VEC;
   cv.clear();
   mb = 0u;
-  if (p.fast) {
+  if (p.fast && (!OPT || p.fast != 3)) {
     if (SR)
       int_vec_cal_sr<T, BITS, AFFINE, true>(v, p, VEC, sr, base, ov, cv, mb);
     else if (OPT && !AFFINE && p.fast == 2)
-      int_vec_cal<T, BITS, AFFINE, true, true>(v, p, VEC, ov, cv, mb);
+      int_vec_cal<T, BITS, AFFINE, true, 1>(v, p, VEC, ov, cv, mb);
     else
       int_vec_cal<T, BITS, AFFINE, true>(v, p, VEC, ov, cv, mb);
   } else if (!p.dead) {

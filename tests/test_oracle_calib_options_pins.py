@@ -187,3 +187,26 @@ def test_percentile_map_and_errors(orc):
     for c in (-0.1, 0.5, 0.7, float("nan")):
         with pytest.raises(ValueError):
             orc.fake_quant_int_percentile(x, 8, 0, c)
+
+
+@pytest.mark.parametrize("scheme", [0, 1])
+def test_overflowing_quotient_takes_the_end_code(orc, scheme):
+    """QuantParams::quantize clamps the rounded quotient to [qmin, qmax], so an
+    element far beyond a clipped range takes the end code of its sign, even
+    when x / scale overflows binary32 (1e30 against a scale near 8e-10), with
+    mask 0; the values inside the range keep their own codes."""
+    x = np.array([1e30, -1e30, 3e29, -2e20, 0.0, 1e-10, -5e-10], F32)
+    r = orc.fake_quant_int_opts(x, 1, x.size, 8, scheme, 0, clip=1e-37)
+    s = r["scale"][0]
+    if scheme == 0:
+        assert s == F32(F32(F32(1e-37) * F32(1e30)) / F32(127))
+    codes = r["codes"].view(np.int8).astype(np.int32)
+    zp = int(r["zero_point"][0]) if scheme else 0
+    qmin, qmax = (-127, 127) if scheme == 0 else (-128, 127)
+    assert list(codes[:4]) == [qmax, qmin, qmax, qmin]
+    assert r["mask"][0] & 0b1111 == 0
+    # elements inside the window round to nearest: |y - x| <= scale / 2
+    for i in (4, 5, 6):
+        assert codes[i] - zp == int(np.rint(np.float64(x[i]) / np.float64(s)))
+    y = r["y"]
+    assert y[0] == F32(qmax - zp) * s and y[1] == F32(qmin - zp) * s
