@@ -103,3 +103,49 @@ def test_recorded_traffic_follows_the_source_key(tmp_path, monkeypatch):
     assert bench.recorded_traffic("k_q4_dequant", "kernels_misc.cu") is None
     (csrc / "qat_device.cuh").write_text("// device header, edited\n")
     assert bench.recorded_traffic("k_q4_quant", "kernels_misc.cu") is None
+
+
+def test_all_cores_oracle_driver_reproduces_the_serial_oracle():
+    """The all-cores CPU baseline runs the oracle's own functions on pieces of
+    each call (per-tensor: parallel statistics, the scale, then the map with
+    that scale given); its outputs must equal the serial oracle's bit for bit,
+    so the two CPU rows time the same computation."""
+    import concurrent.futures as cf
+
+    import numpy as np
+
+    import oracle
+    from fake_quant_numerics_gb300 import workloads as W
+
+    inputs = bench.oracle_sample(1 / 512)
+    x1, g1, w2, a3, w4, g4, x5 = inputs
+    keep = {}
+    with cf.ThreadPoolExecutor(max_workers=4) as pool:
+        bench.oracle_step_parallel(inputs, pool, 7, keep=keep)  # 7 pieces: ragged spans
+    y1, m1, s1, dx1 = keep["w1"]
+    o1 = oracle.fake_quant_int(x1.numpy(), 1, x1.numel(), 8, 0, 0, want_codes=False)
+    assert np.array_equal(y1.view(np.uint32), o1["y"].view(np.uint32))
+    assert np.array_equal(m1, o1["mask"]) and s1 == o1["scale"][0]
+    assert np.array_equal(dx1.view(np.uint32),
+                          oracle.ste_backward(g1.numpy(), o1["mask"]).view(np.uint32))
+    r2, c2 = w2.shape
+    r4, c4 = w4.shape
+    serial_rows = [oracle.fake_quant_int(w2.numpy(), r2, c2, 8, 1, 1),
+                   oracle.fake_quant_int(w2.numpy(), r2, c2, 4, 0, 1),
+                   oracle.fake_quant_int(W.bf16_bits(w4), r4, c4, 4, 0, 2, 128)]
+    for (y, codes, mask, sc, zp), o in zip(keep["rows"], serial_rows):
+        assert np.array_equal(y.view(np.uint8), o["y"].view(np.uint8))
+        assert np.array_equal(codes.view(np.uint8), o["codes"].view(np.uint8))
+        assert np.array_equal(mask, o["mask"])
+        assert np.array_equal(sc, o["scale"])
+    o4 = serial_rows[2]
+    assert np.array_equal(keep["dx4"], oracle.ste_backward(W.bf16_bits(g4), o4["mask"]))
+    for (y3, m3, s3), fmt in zip(keep["fp8"], (oracle.E4M3, oracle.E5M2)):
+        o3 = oracle.fake_quant_fp8(W.bf16_bits(a3), fmt, want_codes=False)
+        assert np.array_equal(y3, o3["y"]) and np.array_equal(m3, o3["mask"])
+        assert np.float32(s3) == o3["scale"]
+    d5, q5, u5, y5 = keep["w5"]
+    o5 = oracle.quant4_double(x5.numpy(), roundtrip=True)
+    assert np.array_equal(d5, o5["data"]) and np.array_equal(q5, o5["qscales"])
+    assert np.array_equal(u5, o5["super_scales"])
+    assert np.array_equal(y5.view(np.uint32), o5["y"].view(np.uint32))
