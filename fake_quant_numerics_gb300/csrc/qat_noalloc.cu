@@ -10,46 +10,42 @@
 // file-scope device array instead, so the caller passes only inputs and
 // outputs and nothing is allocated.
 //
-// The array holds kNoAllocSlots partials of 16 bytes (16 KiB).  Every GPU that
-// loads the library reserves it until the process exits.  All calls share it:
-// two calls whose kernels overlap on the GPU (different streams, or different
-// host threads on the same device) race on it and must be ordered by the
-// caller.  Every slot a call reads is first written by the same call, so the
-// contents left by the previous call never matter and nothing is cleared.
+// The array holds kNoAllocSlots partials of 16 bytes (16 KiB), as many as the
+// statistics pass can ever use (its grid is capped at kMaxPartials blocks).
+// Every GPU that loads the library reserves it until the process exits.  All
+// calls share it: two calls whose kernels overlap on the GPU (different
+// streams, or different host threads on the same device) race on it and must
+// be ordered by the caller.  Every slot a call reads is first written by the
+// same call, so the contents left by the previous call never matter and
+// nothing is cleared.
 //
-// In host code the array's name is only a host-side stand-in; the device
-// address comes from cudaGetSymbolAddress, looked up once per device (with
-// that device current) on the first call on that device and cached.  That
-// first call should therefore be made before any stream capture begins.
-#include <mutex>
-
+// In host code the array's name is only a host-side stand-in.  Each call looks
+// up the array's device address with cudaGetSymbolAddress in the context that
+// is current at the call (the address belongs to a context: another context
+// on the same device, or the primary context created again after
+// cudaDeviceReset, holds its own copy), checks the result and passes it to
+// the kernels.  After the first call in a context the lookup is a host-side
+// table search; the first call may also load the library's device code into
+// the context, so it should be made before any stream capture begins.
 #include "qat_device.cuh"
 #include "qat_launch.h"
 
 namespace {
 
 constexpr int kNoAllocSlots = qat::kMaxPartials;  // 1024 x 16 B = 16 KiB
-constexpr int kMaxDevices = 64;
+static_assert(kNoAllocSlots >= qat::kMaxPartials,
+              "the scratch must hold every partial the statistics pass can write");
 
 static __device__ __align__(256) uint4 g_noalloc_partials[kNoAllocSlots];
 
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once).
-qat_status scratch_of_current_device(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QAT_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();  // clear it, so a later launch check does not report it again
-      return QAT_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = p;
+// Device address of the scratch array in the current context.
+qat_status scratch_of_current_context(void** out) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();  // clear it, so a later launch check does not report it again
+    return QAT_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return QAT_OK;
 }
 
@@ -73,10 +69,9 @@ extern "C" qat_status qat_fake_quant_fp8_noalloc(const void* x, qat_dtype dtype,
   if (scale_given)
     return qat::launch_fp8_tensor(dtype, fmt, true, x, n, nullptr, 0, scale, qat::SrCtx{}, y, codes,
                                   mask, flags, s);
-  const int grid = qat::stats_grid(n);
-  if (grid > kNoAllocSlots) return QAT_ERR_WORKSPACE;  // more partials than the fixed scratch holds
+  const int grid = qat::stats_grid(n);  // at most kMaxPartials = kNoAllocSlots
   void* ws = nullptr;
-  qat_status st = scratch_of_current_device(&ws);
+  qat_status st = scratch_of_current_context(&ws);
   if (st) return st;
   st = qat::launch_stats_tensor(dtype, x, n, qat::kMMNone, ws, grid, s);
   if (st) return st;

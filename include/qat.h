@@ -407,16 +407,18 @@ qat_status qat_dequant4_double(const uint8_t* data, const uint8_t* qscales,
  *
  * The amax pass keeps its cross-block partials in a fixed file-scope device
  * array of 1024 slots x 16 bytes (16 KiB), reserved on every GPU that loads the
- * library until the process exits.  The statistics pass never needs more than
- * 2 x (number of SMs) slots; a device that would need more than 1024 gets
- * QAT_ERR_WORKSPACE.  Nothing is allocated and nothing needs clearing: every
- * slot a call reads is written earlier in the same call.  All calls share the
- * array, so calls whose kernels overlap on the GPU (other streams, other host
- * threads on the same device) race and must be ordered by the caller.  The
- * first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
- * capture begins.  Arguments and errors as qat_fake_quant_fp8, minus the
- * workspace.
+ * library until the process exits.  The statistics pass uses one slot per
+ * block and its grid is capped at 1024 blocks (2 x the SM count on current
+ * devices), so every n up to the library's limit of 2^50 elements fits; a
+ * larger n is QAT_ERR_INVALID_ARGUMENT.  Nothing is allocated and nothing
+ * needs clearing: every slot a call reads is written earlier in the same call.
+ * All calls share the array, so calls whose kernels overlap on the GPU (other
+ * streams, other host threads on the same device) race and must be ordered by
+ * the caller.  Each call looks up the array's device address in the context
+ * current at the call (the address belongs to that context); the first call
+ * in a context may load the library's device code into it, so make that first
+ * call before any stream capture begins.  A failed lookup is QAT_ERR_CUDA.
+ * Arguments and errors as qat_fake_quant_fp8, minus the workspace.
  */
 qat_status qat_fake_quant_fp8_noalloc(const void* x, qat_dtype dtype, int64_t n,
                                       qat_fp8_format format, int scale_given, float* scale,
