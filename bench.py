@@ -11,8 +11,8 @@ workload at full size (all resident in HBM):
   w5  two-level 4-bit quantize + dequantize round trip, fp32 [268,435,456]
 
 The metric is algorithmic bytes moved per second (each input read once per
-dependent pass, each output written once; per-tensor calibration needs two
-reads of x), i.e. GB/s, with Gelem/s and the fraction of the measured HBM
+dependent pass, each output written once; per-tensor calibration of a tensor
+larger than on-chip storage needs two reads of x), i.e. GB/s, with Gelem/s and the fraction of the measured HBM
 copy bandwidth beside it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -56,8 +56,10 @@ def workload_bytes(n1=1 << 20, r2=4096, c2=4096, n3=8192 * 8192, r4=14336, c4=40
                    n5=268_435_456):
     """(name, elements, algorithmic bytes, launches) of every call of one step.
 
-    Per element: per-tensor calibration reads x twice (statistics, then the
-    map); y has the dtype of x; masks are 1 bit; int8 codes 1 byte, int4 codes
+    Per element: per-tensor calibration of a tensor larger than on-chip
+    storage reads x twice (statistics, then the map: w3); a tensor that fits
+    in the registers of the resident blocks (w1, 4 MiB) is read once, its
+    statistics and map in one launch; y has the dtype of x; masks are 1 bit; int8 codes 1 byte, int4 codes
     half a byte; per-unit scales (and zero points) 4 bytes each; the 4-bit
     format stores half a byte per element, one byte per 64-element block and
     4 bytes per 256 blocks."""
@@ -66,7 +68,7 @@ def workload_bytes(n1=1 << 20, r2=4096, c2=4096, n3=8192 * 8192, r4=14336, c4=40
     ns5 = (nb5 + 255) // 256
     m = lambda n: (n + 31) // 32 * 4  # noqa: E731
     return [
-        ("w1_int8_tensor_fwd", n1, n1 * (4 + 4 + 4) + m(n1) + 4, 2),
+        ("w1_int8_tensor_fwd", n1, n1 * (4 + 4) + m(n1) + 4, 1),
         ("w1_ste_bwd", n1, n1 * (4 + 4) + m(n1), 1),
         ("w2_affine_int8_row", n2, n2 * (4 + 1 + 4) + m(n2) + r2 * 8, 1),
         ("w2_sym_int4_row", n2, n2 * 4 + (n2 + 1) // 2 + n2 * 4 + m(n2) + r2 * 4, 1),

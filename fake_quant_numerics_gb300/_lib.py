@@ -75,6 +75,7 @@ PROTOTYPES = {
     "qat_quant4_double": ([_vp, _i64, _vp, _vp, _vp, _vp, _vp], _int),
     "qat_dequant4_double": ([_vp, _vp, _vp, _i64, _vp, _vp], _int),
     "qat_kernel_launch_count": ([], ctypes.c_uint64),
+    "qat_debug_set_wait_limit": ([_i64], None),
 }
 
 

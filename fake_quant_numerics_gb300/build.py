@@ -19,7 +19,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqat.so")
 
 SOURCES = ["qat_abi.cu", "kernels_tensor.cu", "kernels_fused.cu", "kernels_fp8.cu",
-           "kernels_misc.cu", "kernels_optim.cu", "kernels_cols.cu", "kernels_pct.cu", "kernels_block.cu", "qat_noalloc.cu"]
+           "kernels_misc.cu", "kernels_optim.cu", "kernels_cols.cu", "kernels_pct.cu", "kernels_block.cu", "kernels_onchip.cu",
+           "qat_noalloc.cu"]
 # sources compiled a second time with QAT_SR=1: their stochastic-rounding
 # kernels and *_sr launchers (object <name>_sr.o)
 SR_SOURCES = ["kernels_tensor.cu", "kernels_fused.cu", "kernels_fp8.cu", "kernels_cols.cu"]

@@ -121,7 +121,7 @@ __device__ __forceinline__ Raw16 load_lane(const void* x, int64_t i, int have, b
 // ---------------------------------------------------------------------------
 constexpr int kColStageBytes = 32768;
 constexpr int kColStages = 3;
-constexpr uint32_t kColWaitLimit = 1u << 24;  // try_wait polls before giving up
+constexpr uint32_t kColWaitLimit = 1u << 24;  // try_wait polls of the drain before giving up
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -150,8 +150,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0u;
 }
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
-  for (uint32_t i = 0; i < kColWaitLimit; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(b, parity)) return true;
   return false;
 }
@@ -163,6 +163,7 @@ struct ColTiles {
   int64_t cols, cs, r0, r1;
   int segc, tr, tiles, bytes_per_elem;
   bool contig;
+  uint32_t wait_limit;  // polls of a tile wait (the drain always takes kColWaitLimit)
   __device__ __forceinline__ uint32_t seg_bytes() const { return (uint32_t)segc * bytes_per_elem; }
   __device__ __forceinline__ int rows_of(int t) const {
     const int64_t left = r1 - r0 - (int64_t)t * tr;
@@ -202,14 +203,14 @@ __device__ __forceinline__ bool col_staged(const ColTiles& tl, char* stage, uint
   for (int t = 0; t < tl.tiles; ++t) {
     const int s = t % kColStages;
     const uint32_t par = (uint32_t)(t / kColStages) & 1u;
-    const bool ok = mbar_wait(bars + s, par);
+    const bool ok = mbar_wait(bars + s, par, tl.wait_limit);
     if (ok) body(stage + s * kColStageBytes, t, tl.rows_of(t));
     // every thread is done with stage s (or a wait ran out somewhere)
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) {
         // drain the copies still in flight, then report
         for (int u = t; u < tl.tiles && u < t + kColStages; ++u)
-          mbar_wait(bars + u % kColStages, (uint32_t)(u / kColStages) & 1u);
+          mbar_wait(bars + u % kColStages, (uint32_t)(u / kColStages) & 1u, kColWaitLimit);
         if (flags) atomicOr(flags, QAT_FLAG_DEVICE_TIMEOUT);
       }
       return false;
@@ -402,7 +403,8 @@ __global__ void __launch_bounds__(256, 3)
 template <typename T, int MM>
 __global__ void __launch_bounds__(256, 2)
     k_col_stats_staged(const void* __restrict__ x, int64_t rows, int64_t cols, int wc,
-                       int64_t rchunk, int tr, uint4* __restrict__ acc, int32_t* flags) {
+                       int64_t rchunk, int tr, uint32_t wait_limit, uint4* __restrict__ acc,
+                       int32_t* flags) {
   constexpr int NC = kColLane<T>, WW = kColStrip<T>;
   extern __shared__ __align__(128) char col_stage[];
   __shared__ __align__(8) uint64_t bars[kColStages];
@@ -419,6 +421,7 @@ __global__ void __launch_bounds__(256, 2)
   tl.r0 = (int64_t)blockIdx.y * rchunk;
   tl.r1 = min(rows, tl.r0 + rchunk);
   tl.tr = tr;
+  tl.wait_limit = wait_limit;
   tl.tiles = tl.r1 > tl.r0 ? (int)((tl.r1 - tl.r0 + tr - 1) / tr) : 0;
   const int cl = sub * WW + lane * NC;  // the lane's first column in the strip
   const bool active = cl < tl.segc;
@@ -695,8 +698,9 @@ __device__ __forceinline__ void col_map_tile(const char* tile, int nr, uint32_t 
 template <typename T, int BITS, bool AFFINE, bool SR>
 __global__ void __launch_bounds__(256, 2)
     k_int_cols(const void* __restrict__ x, int64_t rows, int64_t cols, int wc, int64_t rchunk,
-               int tr, const uint4* __restrict__ acc, float* scale, int32_t* zp, SrCtx sr,
-               CalOpts co, void* y, void* codes, uint32_t* mask, int32_t* flags) {
+               int tr, uint32_t wait_limit, const uint4* __restrict__ acc, float* scale,
+               int32_t* zp, SrCtx sr, CalOpts co, void* y, void* codes, uint32_t* mask,
+               int32_t* flags) {
   constexpr int NC = kColLane<T>, WW = kColStrip<T>;
   constexpr int MM = AFFINE ? kMMKeys : kMMNone;
   extern __shared__ __align__(128) char col_stage[];
@@ -714,6 +718,7 @@ __global__ void __launch_bounds__(256, 2)
   tl.r0 = (int64_t)blockIdx.y * rchunk;
   tl.r1 = min(rows, tl.r0 + rchunk);
   tl.tr = tr;
+  tl.wait_limit = wait_limit;
   tl.tiles = tl.r1 > tl.r0 ? (int)((tl.r1 - tl.r0 + tr - 1) / tr) : 0;
   const int cl = sub * WW + lane * NC;
   const bool active = cl < tl.segc;
@@ -798,6 +803,7 @@ static void col_stats_t(bool keys, const void* x, int64_t rows, int64_t cols, ui
   // one wave: 2 staged blocks per SM (shared memory), else 3 (registers)
   const ColShape g = col_shape(rows, cols, kColStrip<T>, staged ? 2 : 3, 8, 1);
   const int tr = col_tile_rows((int64_t)kColStrip<T> * g.wc, T::BYTES);
+  const uint32_t limit = device_wait_limit();
   k_col_init<<<(unsigned)((cols + 255) / 256), 256, 0, s>>>(acc, cols);
   const dim3 grid((unsigned)g.strips, (unsigned)g.chunks);
 #define QAT_CS(M)                                                                               \
@@ -805,7 +811,7 @@ static void col_stats_t(bool keys, const void* x, int64_t rows, int64_t cols, ui
     if (staged) {                                                                               \
       col_staged_smem<k_col_stats_staged<T, M>>();                                              \
       k_col_stats_staged<T, M><<<grid, 256, kColStagedBytes, s>>>(x, rows, cols, g.wc, g.rchunk, \
-                                                                  tr, acc, flags);              \
+                                                                  tr, limit, acc, flags);       \
     } else {                                                                                    \
       k_col_stats<T, M><<<grid, 256, 0, s>>>(x, rows, cols, g.wc, g.rchunk, acc);                \
     }                                                                                           \
@@ -852,7 +858,8 @@ static void int_cols_t(const void* x, int64_t rows, int64_t cols, const uint4* a
   const dim3 grid((unsigned)g.strips, (unsigned)g.chunks);
   col_staged_smem<k_int_cols<T, BITS, AFFINE, QAT_SR>>();
   k_int_cols<T, BITS, AFFINE, QAT_SR><<<grid, 256, kColStagedBytes, s>>>(
-      x, rows, cols, g.wc, g.rchunk, tr, acc, scale, zp, sr, co, y, codes, mask, flags);
+      x, rows, cols, g.wc, g.rchunk, tr, device_wait_limit(), acc, scale, zp, sr, co, y, codes,
+      mask, flags);
 }
 
 qat_status QAT_SR_NAME(launch_int_cols)(qat_dtype dt, int bits, bool affine, const void* x,

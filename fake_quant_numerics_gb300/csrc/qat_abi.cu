@@ -15,6 +15,15 @@ void count_launch(int k) { g_launches.fetch_add((uint64_t)k, std::memory_order_r
 
 qat_status launch_status() { return cudaGetLastError() == cudaSuccess ? QAT_OK : QAT_ERR_CUDA; }
 
+// bounded device waits: polls before giving up (negative: the default)
+constexpr uint32_t kDefaultWaitLimit = 1u << 24;
+static std::atomic<int64_t> g_wait_limit{-1};
+uint32_t device_wait_limit() {
+  const int64_t v = g_wait_limit.load(std::memory_order_relaxed);
+  if (v < 0) return kDefaultWaitLimit;
+  return v > INT64_C(0xffffffff) ? 0xffffffffu : (uint32_t)v;
+}
+
 Dev device_info() {
   constexpr int kMaxDev = 64;
   static std::atomic<int> cache[kMaxDev];  // 0 = unknown
@@ -128,6 +137,10 @@ const char* qat_status_string(qat_status s) {
 
 uint64_t qat_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+void qat_debug_set_wait_limit(int64_t polls) {
+  g_wait_limit.store(polls, std::memory_order_relaxed);
+}
+
 size_t qat_workspace_bytes(int64_t rows, int64_t cols, qat_granularity g, int64_t group) {
   return ws_bytes_for(rows, cols, g, group);
 }
@@ -203,6 +216,14 @@ static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t ro
                         flags, s);
     if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
     if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+    const bool plain = co.clip == 1.0f && !co.fp16 && !co.clamp;
+    if (!sr && plain) {
+      // a tensor that fits on chip: statistics and map in one launch
+      bool done = false;
+      qat_status st = launch_int_tensor_onchip(dtype, bits, affine, x, n, ws, scale, zp, y, codes,
+                                               mask, flags, s, &done);
+      if (st || done) return st;
+    }
     int grid = stats_grid(n);
     qat_status st = launch_stats_tensor(dtype, x, n, affine ? kMMFloat : kMMNone, ws, grid, s);
     if (st) return st;

@@ -20,6 +20,18 @@ qat_status launch_status();  // QAT_OK or QAT_ERR_CUDA after a <<<>>> launch
 // Grid for a per-tensor statistics pass (<= kMaxPartials blocks).
 int stats_grid(int64_t n);
 
+// Polls a bounded device wait makes before it gives up (QAT_FLAG_DEVICE_TIMEOUT);
+// the default, or the value set by qat_debug_set_wait_limit.
+uint32_t device_wait_limit();
+
+// Calibrated per-tensor integer fake quant (nearest rounding, plain
+// calibration) of a tensor that fits in the registers of the resident blocks,
+// in one cooperative launch; *done = false (nothing launched) when it does not
+// fit.  ws: the per-tensor workspace.
+qat_status launch_int_tensor_onchip(qat_dtype dt, int bits, bool affine, const void* x, int64_t n,
+                                    void* ws, float* scale, int32_t* zp, void* y, void* codes,
+                                    uint32_t* mask, int32_t* flags, cudaStream_t s, bool* done);
+
 // per-tensor statistics -> workspace partials (uint4 per block); mm is the
 // min / max mode of Stats (kMMNone, kMMFloat, kMMKeys)
 qat_status launch_stats_tensor(qat_dtype dt, const void* x, int64_t n, int mm, void* ws,

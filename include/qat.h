@@ -428,6 +428,19 @@ qat_status qat_fake_quant_fp8_noalloc(const void* x, qat_dtype dtype, int64_t n,
 /* Number of kernels this library has launched in this process (diagnostic). */
 uint64_t qat_kernel_launch_count(void);
 
+/*
+ * Testing hook, no counterpart on the source pages: the number of polls a
+ * bounded device wait makes before it gives up, for the calls launched after
+ * this one in the process (a process-wide setting).  The waits are the grid
+ * barrier of the single-launch per-tensor path and the staged-copy waits of the
+ * per-column kernels; a wait that runs out sets QAT_FLAG_DEVICE_TIMEOUT in the
+ * call's dev_flags and its block returns early, leaving the call's outputs
+ * undefined (a block always drains the copies it has issued before it
+ * returns, with the default limit).  polls < 0 restores the default (2^24
+ * polls, a fraction of a second); 0 makes every such wait give up at once.
+ */
+void qat_debug_set_wait_limit(int64_t polls);
+
 #ifdef __cplusplus
 }
 #endif

@@ -210,3 +210,25 @@ def test_block_scaled_argument_errors(lib):
     assert _blk(lib, ws=None) == L.QAT_ERR_WORKSPACE
     assert _blk(lib, ws=A, wsb=15) == L.QAT_ERR_WORKSPACE
     assert _blk(lib, ws=MIS, wsb=1 << 20) == L.QAT_ERR_MISALIGNED
+
+
+def test_a_failed_launch_is_reported_as_a_cuda_error(lib):
+    """Failure detection on the host: on a machine without a usable CUDA
+    device every launching call fails inside the CUDA runtime, and the library
+    must return QAT_ERR_CUDA (after clearing the runtime's error) rather than
+    crash or report success.  Skipped where a device exists, since the fake
+    pointers would then reach a real launch."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("needs a host without a CUDA device")
+    assert lib.qat_ste_backward(A, L.F32, 1024, A, A, None) == L.QAT_ERR_CUDA
+    assert _int(lib, ws=A, wsb=16384) == L.QAT_ERR_CUDA
+    assert lib.qat_fake_quant_fp8(A, L.F32, 1024, L.E4M3, 0, A, A, None, A, None, A, 16384,
+                                  None) == L.QAT_ERR_CUDA
+    assert lib.qat_quant4_double(A, 1024, A, A, A, None, None) == L.QAT_ERR_CUDA
+    assert lib.qat_dequant4_double(A, A, A, 1024, A, None) == L.QAT_ERR_CUDA
+    assert lib.qat_fake_quant_fp8_noalloc(A, L.F32, 1024, L.E4M3, 0, A, A, None, A, None,
+                                          None) == L.QAT_ERR_CUDA
+    # the status survives: the same call fails the same way again
+    assert lib.qat_ste_backward(A, L.F32, 1024, A, A, None) == L.QAT_ERR_CUDA

@@ -17,13 +17,13 @@ import bench  # noqa: E402
 def test_workload_bytes_match_the_per_element_accounting():
     wb = {name: (e, b, nl) for name, e, b, nl in bench.workload_bytes()}
     n1 = 1 << 20
-    assert wb["w1_int8_tensor_fwd"][1] == n1 * 12 + n1 // 8 + 4     # two reads of x, y, mask
+    assert wb["w1_int8_tensor_fwd"][1] == n1 * 8 + n1 // 8 + 4      # one read of x (on chip), y, mask
     assert wb["w1_ste_bwd"][1] == n1 * 8 + n1 // 8
     n5 = 268_435_456
     assert wb["w5_quant4_double"][1] == n5 * 4 + n5 // 2 + n5 // 64 + 4 * (n5 // 16384)
     total = sum(b for _, b, _ in wb.values())
     assert 4.0e9 < total < 4.2e9
-    assert sum(nl for _, _, nl in wb.values()) == 13
+    assert sum(nl for _, _, nl in wb.values()) == 12
 
 
 def _free_port():
