@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libqat.so")
 
 SOURCES = ["qat_abi.cu", "kernels_tensor.cu", "kernels_fused.cu", "kernels_fp8.cu",
            "kernels_misc.cu", "kernels_optim.cu", "kernels_cols.cu", "kernels_pct.cu", "kernels_block.cu", "kernels_onchip.cu",
-           "qat_noalloc.cu"]
+           "kernels_unaligned.cu", "qat_noalloc.cu"]
 # sources compiled a second time with QAT_SR=1: their stochastic-rounding
 # kernels and *_sr launchers (object <name>_sr.o)
 SR_SOURCES = ["kernels_tensor.cu", "kernels_fused.cu", "kernels_fp8.cu", "kernels_cols.cu"]

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kOnchipThreads)
         ok = 1;
         break;
       }
-      __nanosleep(32);
+      __nanosleep(8);
     }
     timed_out = !ok;
     if (!ok && flags) atomicOr(flags, QAT_FLAG_DEVICE_TIMEOUT);
@@ -183,16 +183,19 @@ static int onchip_occupancy() {
   return occ;
 }
 
+// Launches with NV vectors per thread when the tensor then takes at most
+// `per_sm` blocks per SM (0: as many as are resident).
 template <typename T, int BITS, bool AFFINE, int NV>
 static qat_status onchip_launch(const void* x, int64_t n, void* ws, float* scale, int32_t* zp,
                                 void* y, void* codes, uint32_t* mask, int32_t* flags,
-                                cudaStream_t s, bool* done) {
+                                cudaStream_t s, int per_sm, bool* done) {
   constexpr auto K = k_int_tensor_onchip<T, BITS, AFFINE, NV>;
   const int occ = onchip_occupancy<K>();
   if (occ <= 0) return QAT_OK;
   const int64_t per_block = (int64_t)kOnchipThreads * NV * T::VEC;
   const int64_t blocks = (n + per_block - 1) / per_block;
-  if (blocks > (int64_t)occ * device_info().sms || blocks > kOnchipMaxBlocks) return QAT_OK;
+  const int64_t cap = (int64_t)(per_sm > 0 && per_sm < occ ? per_sm : occ) * device_info().sms;
+  if (blocks > cap || blocks > kOnchipMaxBlocks) return QAT_OK;
   uint4* part = static_cast<uint4*>(ws);
   uint32_t* arrive = reinterpret_cast<uint32_t*>(part + kOnchipBarrierSlot);
   if (cudaMemsetAsync(arrive, 0, sizeof(uint4), s) != cudaSuccess) return QAT_ERR_CUDA;
@@ -220,13 +223,15 @@ template <typename T, int BITS, bool AFFINE>
 static qat_status onchip_t(const void* x, int64_t n, void* ws, float* scale, int32_t* zp, void* y,
                            void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s,
                            bool* done) {
-  // the fewest vectors per thread that cover the tensor with resident blocks
+  // the fewest vectors per thread with at most one block per SM (the barrier
+  // waits for the slowest block, and a second block on an SM is one), else
+  // four vectors per thread with every resident block
   qat_status st = onchip_launch<T, BITS, AFFINE, 1>(x, n, ws, scale, zp, y, codes, mask, flags, s,
-                                                    done);
+                                                    1, done);
   if (st || *done) return st;
-  st = onchip_launch<T, BITS, AFFINE, 2>(x, n, ws, scale, zp, y, codes, mask, flags, s, done);
+  st = onchip_launch<T, BITS, AFFINE, 2>(x, n, ws, scale, zp, y, codes, mask, flags, s, 1, done);
   if (st || *done) return st;
-  return onchip_launch<T, BITS, AFFINE, 4>(x, n, ws, scale, zp, y, codes, mask, flags, s, done);
+  return onchip_launch<T, BITS, AFFINE, 4>(x, n, ws, scale, zp, y, codes, mask, flags, s, 0, done);
 }
 
 qat_status launch_int_tensor_onchip(qat_dtype dt, int bits, bool affine, const void* x, int64_t n,

@@ -9,7 +9,8 @@
 //
 // The two order statistics come from a radix select on the order keys of the
 // values (monotone unsigned integers, -0 below +0), most significant digit
-// first: three passes of 11, 11 and 10 bits.  Each pass reads x, histograms
+// first: three passes of 11, 11 and 10 bits.  Each pass reads x (a warp loads
+// a whole 1024-element tile at once, as the statistics pass does), histograms
 // the digit of the elements whose higher bits match a target's prefix so far
 // (one block-wide histogram in shared memory per target, a shared atomic per
 // counted element), and the last block of the pass to finish scans the
@@ -122,53 +123,40 @@ __device__ __forceinline__ void pct_fold(const V32& v, int cnt, uint32_t rp0, ui
   }
 }
 
-// The block's share of x: vectors vi, vi + stride, ... (the same number of
-// rounds on every lane of a warp, for the votes), the next U vectors loaded
-// before the current ones are counted.
+// The block's share of x: warp w takes the 1024-element tiles w, w + W, ...
+// (W warps in the grid), each lane loading its SLOTS vectors of a tile at
+// once, so a warp has a whole tile in flight (the loop is warp-uniform, for
+// the votes).
 template <typename T, int PASS, bool SHARED>
 __device__ __forceinline__ void pct_walk(const void* __restrict__ x, int64_t n, uint32_t rp0,
                                          uint32_t km0, uint32_t rp1, uint32_t km1, uint32_t* h0,
                                          uint32_t* h1, uint32_t& bad) {
-  constexpr int VEC = T::VEC, U = 1;
-  const int64_t nvec = (n + VEC - 1) / VEC;
-  const int64_t nfull = n / VEC;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t rounds = (nvec + U * stride - 1) / (U * stride);
-  int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  V32 cur[U];
+  constexpr int VEC = T::VEC, SLOTS = kTile / (32 * VEC);
+  const int lane = threadIdx.x & 31;
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  const int64_t nfull = n / kTile;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  V32 v[SLOTS];
+  int cnt[SLOTS];
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < ntiles;
+       t += wstride) {
+    const bool full = t < nfull;
+    if (full)
+      tile_load<T, true>(x, n, t, v, cnt, false, lane);
+    else
+      tile_load<T, false>(x, n, t, v, cnt, false, lane);
 #pragma unroll
-  for (int k = 0; k < U; ++k) {
-    const int64_t j = vi + k * stride;
-    if (j < nfull) cur[k] = ld_v32(static_cast<const char*>(x) + j * VEC * T::BYTES);
-  }
-  for (int64_t rd = 0; rd < rounds; ++rd, vi += U * stride) {
-    V32 nxt[U];
-#pragma unroll
-    for (int k = 0; k < U; ++k) {
-      const int64_t j = vi + (U + k) * stride;
-      if (j < nfull) nxt[k] = ld_v32(static_cast<const char*>(x) + j * VEC * T::BYTES);
-    }
-#pragma unroll
-    for (int k = 0; k < U; ++k) {
-      const int64_t j = vi + k * stride;
-      int cnt = VEC;
-      if (j >= nfull) {  // the ragged last vector (element loads) or none
-        const int64_t c = n - j * VEC;
-        cnt = c > 0 ? (int)c : 0;
-        cur[k] = load_vec<T>(x, cnt > 0 ? j * VEC : 0, cnt);
-      }
+    for (int j = 0; j < SLOTS; ++j) {
       if (PASS == 0) {
         // a NaN or Inf in the vector (absent elements read +0)
         Stats probe;
-        if (probe.vec_absmax_nan<T>(cur[k]) >= 0x7f800000u) bad = 1u;
+        if (probe.vec_absmax_nan<T>(v[j]) >= 0x7f800000u) bad = 1u;
       }
-      if (cnt == VEC)
-        pct_fold<T, PASS, SHARED, true>(cur[k], cnt, rp0, km0, rp1, km1, h0, h1);
+      if (full)
+        pct_fold<T, PASS, SHARED, true>(v[j], VEC, rp0, km0, rp1, km1, h0, h1);
       else
-        pct_fold<T, PASS, SHARED, false>(cur[k], cnt, rp0, km0, rp1, km1, h0, h1);
+        pct_fold<T, PASS, SHARED, false>(v[j], cnt[j], rp0, km0, rp1, km1, h0, h1);
     }
-#pragma unroll
-    for (int k = 0; k < U; ++k) cur[k] = nxt[k];
   }
 }
 
@@ -176,7 +164,7 @@ __device__ __forceinline__ void pct_walk(const void* __restrict__ x, int64_t n, 
 // (a counter per pass) picks each target's bin, extends its prefix, clears the
 // histograms and, after the last pass, writes the map's partial.
 template <typename T, bool AFFINE, int PASS>
-__global__ void __launch_bounds__(256, 5) k_pct_pass(const void* __restrict__ x, int64_t n,
+__global__ void __launch_bounds__(256, 4) k_pct_pass(const void* __restrict__ x, int64_t n,
                                                   PctState* st, unsigned long long* hist,
                                                   uint4* part) {
   constexpr int PER = kPctBins / 256;  // bins per thread in the pick
@@ -268,11 +256,11 @@ qat_status launch_percentile(qat_dtype dt, const void* x, int64_t n, bool affine
                              cudaStream_t s) {
   const PctWs w = pct_ws(ws);
   k_pct_init<<<1, 1024, 0, s>>>(w.st, w.hist, rank_lo, rank_hi);
-  const int64_t nvec = (n + 7) / 8;
-  int64_t g = (nvec + 511) / 512;
-  // the resident blocks: 5 per SM (48 registers, 16 KiB of shared memory);
-  // one vector requested ahead per thread (measured faster than two)
-  const int64_t cap = (int64_t)device_info().sms * 5;
+  const int64_t ntiles = (n + kTile - 1) / kTile;
+  int64_t g = (ntiles + 7) / 8;  // at least a tile per warp
+  // the resident blocks: 4 per SM (64 registers, 16 KiB of shared memory),
+  // every warp with a whole tile in flight
+  const int64_t cap = (int64_t)device_info().sms * 4;
   const int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
 #define QAT_PP(T, A, P) k_pct_pass<T, A, P><<<grid, 256, 0, s>>>(x, n, w.st, w.hist, w.part)
 #define QAT_PPS(T, A) QAT_PP(T, A, 0); QAT_PP(T, A, 1); QAT_PP(T, A, 2)

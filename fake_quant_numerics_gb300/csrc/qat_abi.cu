@@ -55,6 +55,10 @@ constexpr uintptr_t kAlignBuf = 16;
 
 bool valid_dtype(qat_dtype d) { return d == QAT_F32 || d == QAT_BF16; }
 
+// x, y, grad, grad_in must hold whole elements; off the 32-byte vector grid
+// they take the element-per-lane kernels (kernels_unaligned.cu)
+bool elem_aligned(const void* p, qat_dtype d) { return aligned(p, d == QAT_F32 ? 4 : 2); }
+
 // number of elements with overflow / sign checks
 bool elems(int64_t rows, int64_t cols, int64_t* n) {
   if (rows < 0 || cols < 0) return false;
@@ -148,21 +152,25 @@ size_t qat_workspace_bytes(int64_t rows, int64_t cols, qat_granularity g, int64_
 qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t cols,
                           qat_granularity g, int64_t group, float* absmax, float* minv, float* maxv,
                           int32_t* flags, void* ws, size_t ws_bytes, qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_amax_stats");
   if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
   int64_t n, L, units;
   if (!elems(rows, cols, &n)) return QAT_ERR_INVALID_ARGUMENT;
   if (!unit_shape(rows, cols, g, group, &L, &units)) return QAT_ERR_INVALID_ARGUMENT;
   if (n == 0) return QAT_OK;
   if (!x) return QAT_ERR_INVALID_ARGUMENT;
-  if (!aligned(x, kAlignVec) || (absmax && !aligned(absmax, 4)) || (minv && !aligned(minv, 4)) ||
+  if (!elem_aligned(x, dtype) || (absmax && !aligned(absmax, 4)) || (minv && !aligned(minv, 4)) ||
       (maxv && !aligned(maxv, 4)))
     return QAT_ERR_MISALIGNED;
+  const bool ua = !aligned(x, kAlignVec);
+  if (ua && g == QAT_PER_COLUMN) return QAT_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (g == QAT_PER_TENSOR) {
     if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
     if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
     int grid = stats_grid(n);
-    qat_status st = launch_stats_tensor(dtype, x, n, kMMKeys, ws, grid, s);
+    qat_status st = ua ? launch_ua_stats(dtype, kMMKeys, x, n, ws, grid, s)
+                       : launch_stats_tensor(dtype, x, n, kMMKeys, ws, grid, s);
     if (st) return st;
     return launch_stats_finalize(ws, grid, absmax, minv, maxv, flags, s);
   }
@@ -175,7 +183,7 @@ qat_status qat_amax_stats(const void* x, qat_dtype dtype, int64_t rows, int64_t 
     return launch_col_finalize(0, 8, false, ws, cols, absmax, minv, maxv, nullptr, kCalPlain, flags,
                                s);
   }
-  if (fused_units_supported(dtype, L))
+  if (!ua && fused_units_supported(dtype, L))
     return launch_int_fused(dtype, 8, false, true, x, units, L, nullptr, nullptr, absmax, minv, maxv,
                             SrCtx{}, kCalPlain, nullptr, nullptr, nullptr, flags, s);
   return launch_unit_generic(dtype, 0, 8, false, x, units, L, absmax, minv, maxv, nullptr, nullptr,
@@ -201,12 +209,36 @@ static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t ro
   if (g == QAT_PER_COLUMN && cols > kMaxColumns) return QAT_ERR_UNSUPPORTED;
   if (!x || !scale) return QAT_ERR_INVALID_ARGUMENT;
   if (params_given && affine && !zp) return QAT_ERR_INVALID_ARGUMENT;
-  if (!aligned(x, kAlignVec) || (y && !aligned(y, kAlignVec)) ||
+  if (!elem_aligned(x, dtype) || (y && !elem_aligned(y, dtype)) ||
       (codes && !aligned(codes, kAlignBuf)) || (mask && !aligned(mask, kAlignBuf)) ||
       !aligned(scale, 4) || (zp && !aligned(zp, 4)))
     return QAT_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const SrCtx c = sr ? *sr : SrCtx{};
+  if (!aligned(x, kAlignVec) || (y && !aligned(y, kAlignVec))) {
+    // element-aligned tensors off the vector grid: per tensor, rows, groups
+    if (g == QAT_PER_COLUMN) return QAT_ERR_MISALIGNED;
+    if (params_given)
+      return launch_ua_int_map(dtype, bits, affine, g == QAT_PER_TENSOR ? 1 : 3, sr != nullptr, x,
+                               n, L, nullptr, 0, scale, zp, nullptr, c, co, y, codes, mask, flags,
+                               s);
+    if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
+    if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+    if (g == QAT_PER_TENSOR) {
+      const int grid = stats_grid(n);
+      qat_status st = launch_ua_stats(dtype, affine ? kMMFloat : kMMNone, x, n, ws, grid, s);
+      if (st) return st;
+      return launch_ua_int_map(dtype, bits, affine, 0, sr != nullptr, x, n, n, ws, grid, scale,
+                               zp, nullptr, c, co, y, codes, mask, flags, s);
+    }
+    uint8_t* dead = ws_dead(ws, cols, g);
+    int32_t* zpu = (affine && !zp) ? ws_zp(ws, cols, g, units) : zp;
+    qat_status st = launch_unit_generic(dtype, 1, bits, affine, x, units, L, nullptr, nullptr,
+                                        nullptr, scale, zpu, dead, co, flags, s);
+    if (st) return st;
+    return launch_ua_int_map(dtype, bits, affine, 2, sr != nullptr, x, n, L, nullptr, 0, scale,
+                             zpu, dead, c, co, y, codes, mask, flags, s);
+  }
   auto map_tensor = sr ? launch_int_tensor_sr : launch_int_tensor;
   auto map_units = sr ? launch_int_units_sr : launch_int_units;
   auto map_fused = sr ? launch_int_fused_sr : launch_int_fused;
@@ -269,6 +301,7 @@ qat_status qat_fake_quant_int(const void* x, qat_dtype dtype, int64_t rows, int6
                               qat_scheme scheme, qat_granularity g, int64_t group, int params_given,
                               float* scale, int32_t* zp, void* y, void* codes, uint32_t* mask,
                               int32_t* flags, void* ws, size_t ws_bytes, qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_fake_quant_int");
   return fake_quant_int_impl(x, dtype, rows, cols, bits, scheme, g, group, params_given, scale, zp,
                              nullptr, kCalPlain, y, codes, mask, flags, ws, ws_bytes, stream);
 }
@@ -278,6 +311,7 @@ static SrCtx sr_ctx(uint64_t seed, uint64_t offset) {
   c.k0 = (uint32_t)seed;
   c.k1 = (uint32_t)(seed >> 32);
   c.offset = offset;
+  sr_set_round_keys(c);
   return c;
 }
 
@@ -286,6 +320,7 @@ qat_status qat_fake_quant_int_sr(const void* x, qat_dtype dtype, int64_t rows, i
                                  int params_given, float* scale, int32_t* zp, uint64_t seed,
                                  uint64_t offset, void* y, void* codes, uint32_t* mask,
                                  int32_t* flags, void* ws, size_t ws_bytes, qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_fake_quant_int_sr");
   const SrCtx c = sr_ctx(seed, offset);
   return fake_quant_int_impl(x, dtype, rows, cols, bits, scheme, g, group, params_given, scale, zp,
                              &c, kCalPlain, y, codes, mask, flags, ws, ws_bytes, stream);
@@ -297,6 +332,7 @@ qat_status qat_fake_quant_int_opts(const void* x, qat_dtype dtype, int64_t rows,
                                    uint64_t offset, float* scale, int32_t* zp, void* y, void* codes,
                                    uint32_t* mask, int32_t* flags, void* ws, size_t ws_bytes,
                                    qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_fake_quant_int_opts");
   CalOpts co = kCalPlain;
   if (options) {
     if (!(options->clip > 0.0f && options->clip <= 1.0f)) return QAT_ERR_INVALID_ARGUMENT;
@@ -316,6 +352,7 @@ qat_status qat_fake_quant_int_percentile(const void* x, qat_dtype dtype, int64_t
                                          uint64_t seed, uint64_t offset, float* scale, int32_t* zp,
                                          void* y, void* codes, uint32_t* mask, int32_t* flags,
                                          void* ws, size_t ws_bytes, qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_fake_quant_int_percentile");
   if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
   if (bits != 8 && bits != 4) return QAT_ERR_UNSUPPORTED;
   if (scheme != QAT_SYMMETRIC && scheme != QAT_AFFINE) return QAT_ERR_UNSUPPORTED;
@@ -352,6 +389,7 @@ qat_status qat_fake_quant_block(const void* x, qat_dtype dtype, int64_t n, qat_e
                                 int64_t block, qat_block_scale kind, float* tensor_scale, void* y,
                                 uint8_t* codes, void* bscales, uint32_t* mask, int32_t* flags,
                                 void* ws, size_t ws_bytes, qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_fake_quant_block");
   if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
   if (elem < QAT_ELEM_E4M3 || elem > QAT_ELEM_E2M1) return QAT_ERR_UNSUPPORTED;
   if (kind < QAT_BLOCK_SCALE_E8M0 || kind > QAT_BLOCK_SCALE_FP32) return QAT_ERR_UNSUPPORTED;
@@ -386,11 +424,25 @@ static qat_status fake_quant_fp8_impl(const void* x, qat_dtype dtype, int64_t n,
   if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;
   if (n == 0) return QAT_OK;
   if (!x || !y || !scale) return QAT_ERR_INVALID_ARGUMENT;
-  if (!aligned(x, kAlignVec) || !aligned(y, kAlignVec) || (codes && !aligned(codes, kAlignBuf)) ||
-      (mask && !aligned(mask, kAlignBuf)) || !aligned(scale, 4))
+  if (!elem_aligned(x, dtype) || !elem_aligned(y, dtype) ||
+      (codes && !aligned(codes, kAlignBuf)) || (mask && !aligned(mask, kAlignBuf)) ||
+      !aligned(scale, 4))
     return QAT_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const SrCtx c = sr ? *sr : SrCtx{};
+  if (!aligned(x, kAlignVec) || !aligned(y, kAlignVec)) {
+    // element-aligned tensors off the vector grid
+    if (scale_given)
+      return launch_ua_fp8_map(dtype, fmt, true, sr != nullptr, x, n, nullptr, 0, scale, c, y,
+                               codes, mask, flags, s);
+    if (!ws || ws_bytes < ws_bytes_for(1, n, QAT_PER_TENSOR, 0)) return QAT_ERR_WORKSPACE;
+    if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
+    const int grid = stats_grid(n);
+    qat_status st = launch_ua_stats(dtype, kMMNone, x, n, ws, grid, s);
+    if (st) return st;
+    return launch_ua_fp8_map(dtype, fmt, false, sr != nullptr, x, n, ws, grid, scale, c, y, codes,
+                             mask, flags, s);
+  }
   auto map = sr ? launch_fp8_tensor_sr : launch_fp8_tensor;
   if (scale_given)
     return map(dtype, fmt, true, x, n, nullptr, 0, scale, c, y, codes, mask, flags, s);
@@ -406,6 +458,7 @@ qat_status qat_fake_quant_fp8(const void* x, qat_dtype dtype, int64_t n, qat_fp8
                               int scale_given, float* scale, void* y, uint8_t* codes,
                               uint32_t* mask, int32_t* flags, void* ws, size_t ws_bytes,
                               qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_fake_quant_fp8");
   return fake_quant_fp8_impl(x, dtype, n, fmt, scale_given, scale, nullptr, y, codes, mask, flags,
                              ws, ws_bytes, stream);
 }
@@ -414,6 +467,7 @@ qat_status qat_fake_quant_fp8_sr(const void* x, qat_dtype dtype, int64_t n, qat_
                                  int scale_given, float* scale, uint64_t seed, uint64_t offset,
                                  void* y, uint8_t* codes, uint32_t* mask, int32_t* flags,
                                  void* ws, size_t ws_bytes, qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_fake_quant_fp8_sr");
   const SrCtx c = sr_ctx(seed, offset);
   return fake_quant_fp8_impl(x, dtype, n, fmt, scale_given, scale, &c, y, codes, mask, flags, ws,
                              ws_bytes, stream);
@@ -425,6 +479,7 @@ qat_status qat_optimizer_step(float* master, const float* grad, float* exp_avg, 
                               uint64_t offset, float* view, void* codes, uint32_t* mask,
                               float* scale, int32_t* zp, int32_t* flags, void* ws,
                               size_t ws_bytes, qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_optimizer_step");
   if (!hp) return QAT_ERR_INVALID_ARGUMENT;
   if (bits != 0 && bits != 4 && bits != 8) return QAT_ERR_UNSUPPORTED;
   if (bits == 0 && format != QAT_E4M3 && format != QAT_E5M2) return QAT_ERR_UNSUPPORTED;
@@ -476,17 +531,21 @@ qat_status qat_optimizer_step(float* master, const float* grad, float* exp_avg, 
 
 qat_status qat_ste_backward(const void* grad, qat_dtype dtype, int64_t n, const uint32_t* mask,
                             void* grad_in, qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_ste_backward");
   if (!valid_dtype(dtype)) return QAT_ERR_UNSUPPORTED;
   if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;
   if (n == 0) return QAT_OK;
   if (!grad || !mask || !grad_in) return QAT_ERR_INVALID_ARGUMENT;
-  if (!aligned(grad, kAlignVec) || !aligned(grad_in, kAlignVec) || !aligned(mask, kAlignBuf))
+  if (!elem_aligned(grad, dtype) || !elem_aligned(grad_in, dtype) || !aligned(mask, kAlignBuf))
     return QAT_ERR_MISALIGNED;
+  if (!aligned(grad, kAlignVec) || !aligned(grad_in, kAlignVec))
+    return launch_ua_ste(dtype, grad, n, mask, grad_in, reinterpret_cast<cudaStream_t>(stream));
   return launch_ste(dtype, grad, n, mask, grad_in, reinterpret_cast<cudaStream_t>(stream));
 }
 
 qat_status qat_quant4_double(const float* x, int64_t n, uint8_t* data, uint8_t* qscales,
                              float* super_scales, float* y, qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_quant4_double");
   if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;
   if (n == 0) return QAT_OK;
   if (!x || !data || !qscales || !super_scales) return QAT_ERR_INVALID_ARGUMENT;
@@ -499,6 +558,7 @@ qat_status qat_quant4_double(const float* x, int64_t n, uint8_t* data, uint8_t* 
 
 qat_status qat_dequant4_double(const uint8_t* data, const uint8_t* qscales, const float* super_scales,
                                int64_t n, float* y, qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_dequant4_double");
   if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;
   if (n == 0) return QAT_OK;
   if (!data || !qscales || !super_scales || !y) return QAT_ERR_INVALID_ARGUMENT;

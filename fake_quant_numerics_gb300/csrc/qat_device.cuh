@@ -819,10 +819,11 @@ __device__ __forceinline__ void int_vec_cal(const V32& v, const IntParams& p, in
 // of offset + i / 4, 0, 0); u = (w >> 9) * 2^-23.  r - floor(r) and u are
 // exact in binary32, so the decision is exact.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint4 philox4x32_10(uint64_t ctr, uint32_t k0, uint32_t k1) {
+__device__ __forceinline__ uint4 philox4x32_10(uint64_t ctr, const uint32_t (&rk)[2 * kPhiloxRounds]) {
   uint32_t x0 = (uint32_t)ctr, x1 = (uint32_t)(ctr >> 32), x2 = 0u, x3 = 0u;
 #pragma unroll
-  for (int round = 0; round < 10; ++round) {
+  for (int round = 0; round < kPhiloxRounds; ++round) {
+    const uint32_t k0 = rk[2 * round], k1 = rk[2 * round + 1];  // the round's key (Weyl schedule)
     // the Philox S-box: 32 x 32 -> 64-bit products by the two round
     // multipliers, high halves mixed with the other words and the round key
     const uint64_t p0 = (uint64_t)0xD2511F53u * x0;  // one 32 x 32 -> 64-bit multiply each
@@ -834,15 +835,13 @@ __device__ __forceinline__ uint4 philox4x32_10(uint64_t ctr, uint32_t k0, uint32
     x1 = lo1;
     x2 = n2;
     x3 = lo0;
-    k0 += 0x9E3779B9u;  // Weyl key schedule
-    k1 += 0xBB67AE85u;
   }
   return make_uint4(x0, x1, x2, x3);
 }
 
 // draws of the four elements 4 g .. 4 g + 3 (g = element index / 4)
 __device__ __forceinline__ void sr_draws4(const SrCtx& sr, int64_t g, float (&u)[4]) {
-  const uint4 w = philox4x32_10(sr.offset + (uint64_t)g, sr.k0, sr.k1);
+  const uint4 w = philox4x32_10(sr.offset + (uint64_t)g, sr.rk);
   // (w >> 9) * 2^-23 exactly: 1 + (w >> 9) 2^-23 has those bits, minus 1
   u[0] = __uint_as_float(0x3f800000u | (w.x >> 9)) - 1.0f;
   u[1] = __uint_as_float(0x3f800000u | (w.y >> 9)) - 1.0f;

@@ -4,11 +4,22 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "qat.h"
 #include "qat_sr.h"
 
 namespace qat {
+
+// An NVTX range around one C-ABI call, so a profiler's timeline shows which
+// entry point issued which kernels (header-only NVTX: without a tool attached
+// a push / pop is a check of a function pointer).
+struct NvtxScope {
+  explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+  ~NvtxScope() { nvtxRangePop(); }
+  NvtxScope(const NvtxScope&) = delete;
+  NvtxScope& operator=(const NvtxScope&) = delete;
+};
 
 struct Dev {
   int sms;  // streaming multiprocessors of the current device
@@ -23,6 +34,26 @@ int stats_grid(int64_t n);
 // Polls a bounded device wait makes before it gives up (QAT_FLAG_DEVICE_TIMEOUT);
 // the default, or the value set by qat_debug_set_wait_limit.
 uint32_t device_wait_limit();
+
+// Element-per-lane kernels for tensors aligned to their element but not to
+// 32-byte vectors (kernels_unaligned.cu).  ua_stats: per-tensor partials
+// (grid blocks) in ws.  ua_int_map mode 0: per tensor calibrated from the
+// nparts partials in ws; 1: per tensor given (scale[0], zp[0]); 2: per unit
+// (unit = i / L) with arrays calibrated by launch_unit_generic (dead); 3: per
+// unit given.  ua_fp8_map: per tensor, calibrated from the partials or given.
+qat_status launch_ua_stats(qat_dtype dt, int mm, const void* x, int64_t n, void* ws, int grid,
+                           cudaStream_t s);
+qat_status launch_ua_int_map(qat_dtype dt, int bits, bool affine, int mode, bool stoch,
+                             const void* x, int64_t n, int64_t L, const void* ws, int nparts,
+                             float* scale, int32_t* zp, const uint8_t* dead, const SrCtx& sr,
+                             const CalOpts& co, void* y, void* codes, uint32_t* mask,
+                             int32_t* flags, cudaStream_t s);
+qat_status launch_ua_fp8_map(qat_dtype dt, int fmt, bool given, bool stoch, const void* x,
+                             int64_t n, const void* ws, int nparts, float* scale, const SrCtx& sr,
+                             void* y, uint8_t* codes, uint32_t* mask, int32_t* flags,
+                             cudaStream_t s);
+qat_status launch_ua_ste(qat_dtype dt, const void* g, int64_t n, const uint32_t* mask, void* dx,
+                         cudaStream_t s);
 
 // Calibrated per-tensor integer fake quant (nearest rounding, plain
 // calibration) of a tensor that fits in the registers of the resident blocks,

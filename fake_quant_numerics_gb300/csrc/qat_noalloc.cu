@@ -57,6 +57,7 @@ extern "C" qat_status qat_fake_quant_fp8_noalloc(const void* x, qat_dtype dtype,
                                                  qat_fp8_format fmt, int scale_given, float* scale,
                                                  void* y, uint8_t* codes, uint32_t* mask,
                                                  int32_t* flags, qat_stream_t stream) {
+  qat::NvtxScope nvtx("qat_fake_quant_fp8_noalloc");
   if (dtype != QAT_F32 && dtype != QAT_BF16) return QAT_ERR_UNSUPPORTED;
   if (fmt != QAT_E4M3 && fmt != QAT_E5M2) return QAT_ERR_UNSUPPORTED;
   if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;

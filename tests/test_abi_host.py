@@ -12,7 +12,8 @@ import pytest
 from fake_quant_numerics_gb300 import _lib as L
 
 A = ctypes.c_void_p(0x10000)        # 32-byte aligned fake address, never dereferenced
-MIS = ctypes.c_void_p(0x10000 + 8)  # misaligned fake address
+MIS = ctypes.c_void_p(0x10000 + 8)  # off the 32-byte grid (whole fp32 / bf16 elements)
+ODD = ctypes.c_void_p(0x10000 + 1)  # inside an element of every dtype
 
 
 @pytest.fixture(scope="module")
@@ -72,8 +73,14 @@ def test_int_argument_errors(lib):
     assert _int(lib, x=None) == L.QAT_ERR_INVALID_ARGUMENT
     assert _int(lib, scale=None) == L.QAT_ERR_INVALID_ARGUMENT
     assert _int(lib, given=1, scheme=L.AFFINE, zp=None) == L.QAT_ERR_INVALID_ARGUMENT
-    assert _int(lib, x=MIS) == L.QAT_ERR_MISALIGNED
-    assert _int(lib, y=MIS) == L.QAT_ERR_MISALIGNED
+    assert _int(lib, x=ODD) == L.QAT_ERR_MISALIGNED
+    assert _int(lib, y=ODD) == L.QAT_ERR_MISALIGNED
+    # whole elements off the vector grid are accepted (the element-per-lane
+    # path); the missing workspace is then the error
+    assert _int(lib, x=MIS, ws=None) == L.QAT_ERR_WORKSPACE
+    assert _int(lib, y=MIS, ws=None) == L.QAT_ERR_WORKSPACE
+    # per column they are not
+    assert _int(lib, x=MIS, gran=L.PER_COLUMN, ws=A, wsb=1 << 20) == L.QAT_ERR_MISALIGNED
     assert _int(lib, mask=ctypes.c_void_p(0x10004)) == L.QAT_ERR_MISALIGNED
     # per-tensor calibration needs the workspace
     assert _int(lib, ws=None) == L.QAT_ERR_WORKSPACE
@@ -95,14 +102,16 @@ def test_fp8_argument_errors(lib):
     assert f(A, L.F32, -1, 0, 0, A, A, None, None, None, None, 0, None) == L.QAT_ERR_INVALID_ARGUMENT
     assert f(A, L.F32, 0, 0, 0, None, None, None, None, None, None, 0, None) == L.QAT_OK
     assert f(A, L.F32, 100, 0, 0, A, None, None, None, None, None, 0, None) == L.QAT_ERR_INVALID_ARGUMENT
-    assert f(MIS, L.F32, 100, 0, 0, A, A, None, None, None, None, 0, None) == L.QAT_ERR_MISALIGNED
+    assert f(ODD, L.F32, 100, 0, 0, A, A, None, None, None, None, 0, None) == L.QAT_ERR_MISALIGNED
+    assert f(MIS, L.F32, 100, 0, 0, A, A, None, None, None, None, 0, None) == L.QAT_ERR_WORKSPACE
     assert f(A, L.F32, 100, 0, 0, A, A, None, None, None, None, 0, None) == L.QAT_ERR_WORKSPACE
 
 
 def test_ste_and_q4_argument_errors(lib):
     assert lib.qat_ste_backward(A, L.F32, 10, None, A, None) == L.QAT_ERR_INVALID_ARGUMENT
     assert lib.qat_ste_backward(A, 3, 10, A, A, None) == L.QAT_ERR_UNSUPPORTED
-    assert lib.qat_ste_backward(MIS, L.F32, 10, A, A, None) == L.QAT_ERR_MISALIGNED
+    assert lib.qat_ste_backward(ODD, L.F32, 10, A, A, None) == L.QAT_ERR_MISALIGNED
+    assert lib.qat_ste_backward(A, L.BF16, 10, A, ODD, None) == L.QAT_ERR_MISALIGNED
     assert lib.qat_ste_backward(None, L.F32, 0, None, None, None) == L.QAT_OK
     assert lib.qat_quant4_double(A, -5, A, A, A, None, None) == L.QAT_ERR_INVALID_ARGUMENT
     assert lib.qat_quant4_double(A, 64, None, A, A, None, None) == L.QAT_ERR_INVALID_ARGUMENT
@@ -118,7 +127,9 @@ def test_stats_argument_errors(lib):
     assert f(A, L.F32, 4, 4, L.PER_TENSOR, 0, None, None, None, None, None, 0, None) == L.QAT_ERR_WORKSPACE
     assert f(None, L.F32, 4, 4, L.PER_ROW, 0, None, None, None, None, None, 0, None) == L.QAT_ERR_INVALID_ARGUMENT
     assert f(A, L.F32, 4, 6, L.PER_GROUP, 4, None, None, None, None, None, 0, None) == L.QAT_ERR_INVALID_ARGUMENT
-    assert f(MIS, L.F32, 4, 4, L.PER_ROW, 0, None, None, None, None, None, 0, None) == L.QAT_ERR_MISALIGNED
+    assert f(ODD, L.F32, 4, 4, L.PER_ROW, 0, None, None, None, None, None, 0, None) == L.QAT_ERR_MISALIGNED
+    assert f(MIS, L.F32, 4, 4, L.PER_COLUMN, 0, None, None, None, None, A, 1 << 20, None) == \
+        L.QAT_ERR_MISALIGNED
     assert f(A, L.F32, 4, 4, L.PER_COLUMN, 0, None, None, None, None, None, 0, None) == L.QAT_ERR_WORKSPACE
 
 
@@ -139,7 +150,7 @@ def test_calibration_options_argument_errors(lib):
     ok = L.CalibOptions(0.7, 1)
     # valid options, then the integer path's own checks
     assert _opts(lib, ctypes.addressof(ok), bits=3) == L.QAT_ERR_UNSUPPORTED
-    assert _opts(lib, ctypes.addressof(ok), x=MIS) == L.QAT_ERR_MISALIGNED
+    assert _opts(lib, ctypes.addressof(ok), x=ODD) == L.QAT_ERR_MISALIGNED
     assert _opts(lib, ctypes.addressof(ok)) == L.QAT_ERR_WORKSPACE        # per tensor, no workspace
     assert _opts(lib, None, sr=1) == L.QAT_ERR_WORKSPACE                  # NULL options: plain
     assert _opts(lib, ctypes.addressof(ok), rows=0, x=None, scale=None) == L.QAT_OK

@@ -445,15 +445,25 @@ def test_q4_double_exact_ties(qat, orc):
 # ---------------------------------------------------------------------------
 # binding behaviour
 # ---------------------------------------------------------------------------
-def test_misaligned_pointer_is_rejected(qat):
-    from fake_quant_numerics_gb300 import QatError
+def test_pointer_inside_an_element_is_rejected(qat):
+    """A pointer that does not hold whole elements is refused before any
+    launch (views at element offsets are accepted; tests/test_gpu_unaligned.py)."""
+    import ctypes
 
+    from fake_quant_numerics_gb300 import _lib
+
+    lib = _lib.load()
     x = torch.randn(1000, device="cuda")
     y = torch.empty_like(x)
     s = torch.empty(1, device="cuda")
-    with pytest.raises(QatError, match="misaligned"):
-        qat.qat_fake_quant_int(x[1:], 1, 999, 8, 0, 0, 0, False, s, None, y[1:], None, None, None,
-                               torch.empty(1 << 14, dtype=torch.uint8, device="cuda"))
+    ws = torch.empty(1 << 14, dtype=torch.uint8, device="cuda")
+    c0 = lib.qat_kernel_launch_count()
+    st = lib.qat_fake_quant_int(ctypes.c_void_p(x.data_ptr() + 2), _lib.F32, 1, 999, 8, 0, 0, 0,
+                                0, ctypes.c_void_p(s.data_ptr()), None,
+                                ctypes.c_void_p(y.data_ptr()), None, None, None,
+                                ctypes.c_void_p(ws.data_ptr()), ws.numel(), None)
+    assert st == _lib.QAT_ERR_MISALIGNED
+    assert lib.qat_kernel_launch_count() == c0
 
 
 def test_named_ops_and_launch_count(qat, orc):
