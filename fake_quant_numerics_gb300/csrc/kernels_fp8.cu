@@ -314,6 +314,14 @@ __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, 
       if (blockIdx.x == 0) flag_or(flags, sp.mode == 2 ? QAT_FLAG_BAD_PARAMS : 0);
     }
   } else {
+    // launched early (after the statistics pass): request the warp's first
+    // tile into L2, then wait for the partials
+    {
+      const int64_t ntiles = (n + kTile - 1) / kTile;
+      const int64_t t0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+      if (t0 < ntiles) prefetch_tile_l2<T>(x, n, ntiles - 1 - t0, threadIdx.x & 31);
+    }
+    pdl_wait();
     Stats st = reduce_partials<kMMNone>(part, nparts, red);
     if (threadIdx.x == 0) {
       float s = __fdiv_rn(st.absmax_f(), kMax);
@@ -355,15 +363,15 @@ __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, 
 template <typename T, int FMT>
 static void fp8_t(bool given, const void* x, int64_t n, const void* ws, int nparts, float* scale,
                   const SrCtx& sr, void* y, uint8_t* codes, uint32_t* mask, int32_t* flags,
-                  cudaStream_t s) {
+                  cudaStream_t s, bool pdl) {
   const int64_t ntiles = (n + kTile - 1) / kTile;
   int64_t g = (ntiles + 7) / 8;
   int64_t cap = (int64_t)device_info().sms * 8;
   int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
   const uint4* part = static_cast<const uint4*>(ws);
-#define QAT_K(G, C)                                                                              \
-  k_fp8_tensor<T, FMT, G, C, QAT_SR><<<grid, 256, 0, s>>>(x, n, part, nparts, scale, sr, y, codes, \
-                                                          mask, flags)
+#define QAT_K(G, C)                                                                             \
+  launch_kernel(k_fp8_tensor<T, FMT, G, C, QAT_SR>, dim3(grid), dim3(256), 0, s, pdl, x, n, part, \
+                nparts, scale, sr, y, codes, mask, flags)
   if (given) {
     if (codes) QAT_K(true, true); else QAT_K(true, false);
   } else {
@@ -373,7 +381,7 @@ static void fp8_t(bool given, const void* x, int64_t n, const void* ws, int npar
 }
 
 QAT_DECL_FP8_TENSOR(QAT_SR_NAME(launch_fp8_tensor)) {
-#define QAT_F8(T, F) fp8_t<T, F>(given, x, n, ws, nparts, scale, sr, y, codes, mask, flags, s)
+#define QAT_F8(T, F) fp8_t<T, F>(given, x, n, ws, nparts, scale, sr, y, codes, mask, flags, s, pdl)
   if (dt == QAT_F32) {
     if (fmt == QAT_E4M3) QAT_F8(F32, QAT_E4M3);
     else QAT_F8(F32, QAT_E5M2);

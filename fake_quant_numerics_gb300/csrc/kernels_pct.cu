@@ -50,6 +50,7 @@ static PctWs pct_ws(void* ws) {
 
 __global__ void k_pct_init(PctState* st, unsigned long long* hist, unsigned long long rank_lo,
                            unsigned long long rank_hi) {
+  pdl_trigger();
   for (int i = threadIdx.x; i < 2 * kPctBins; i += blockDim.x) hist[i] = 0ull;
   if (threadIdx.x == 0) {
     st->prefix[0] = st->prefix[1] = 0u;
@@ -174,9 +175,17 @@ __global__ void __launch_bounds__(256, 4) k_pct_pass(const void* __restrict__ x,
   __shared__ uint32_t pick_bin[2];
   __shared__ unsigned long long pick_below[2];
   __shared__ int last;
+  // launched early (after the previous kernel of the call): clear the block
+  // histograms and request the warp's first tile into L2 while that kernel
+  // finishes, then wait for its state
   for (int i = threadIdx.x; i < 2 * kPctBins; i += blockDim.x) (&h[0][0])[i] = 0u;
-  __syncthreads();
   const int lane = threadIdx.x & 31;
+  {
+    const int64_t t0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t0 * kTile < n) prefetch_tile_l2<T>(x, n, t0, lane);
+  }
+  pdl_wait();
+  __syncthreads();
   const int shift = pct_shift(pass);
   const uint32_t dmask = (1u << pct_bits(pass)) - 1u;
   const uint32_t km0 = st->known[0], km1 = st->known[1];
@@ -189,6 +198,7 @@ __global__ void __launch_bounds__(256, 4) k_pct_pass(const void* __restrict__ x,
   else
     pct_walk<T, PASS, false>(x, n, rp0, km0, rp1, km1, h[0], h[1], bad);
   if (pass == 0 && __reduce_or_sync(kFull, bad) && lane == 0) atomicOr(&st->nonfinite, 1u);
+  pdl_trigger();  // the next kernel may be scheduled as the blocks finish
   __syncthreads();
   for (int i = threadIdx.x; i < 2 * kPctBins; i += blockDim.x) {
     const uint32_t c = (&h[0][0])[i];
@@ -262,7 +272,8 @@ qat_status launch_percentile(qat_dtype dt, const void* x, int64_t n, bool affine
   // every warp with a whole tile in flight
   const int64_t cap = (int64_t)device_info().sms * 4;
   const int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
-#define QAT_PP(T, A, P) k_pct_pass<T, A, P><<<grid, 256, 0, s>>>(x, n, w.st, w.hist, w.part)
+#define QAT_PP(T, A, P)                                                                       \
+  launch_kernel(k_pct_pass<T, A, P>, dim3(grid), dim3(256), 0, s, true, x, n, w.st, w.hist, w.part)
 #define QAT_PPS(T, A) QAT_PP(T, A, 0); QAT_PP(T, A, 1); QAT_PP(T, A, 2)
   static_assert(kPctPasses == 3, "three radix-select passes");
   if (dt == QAT_F32) {

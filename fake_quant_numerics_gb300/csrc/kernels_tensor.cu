@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(512) k_stats_tensor(const void* __restrict__ x
     else stats_tile<T, MM, false>(x, n, t, v, have, next, st, lane);
     have = next >= 0;
   }
+  pdl_trigger();  // the map may be scheduled as the blocks finish
   Stats b = block_reduce_stats<MM>(st, red);
   if (threadIdx.x == 0) part[blockIdx.x] = b.pack();
 }
@@ -170,6 +171,14 @@ __global__ void __maxnreg__(SR ? 128 : 80) k_int_tensor(const void* __restrict__
     }
   } else {
     constexpr int MM = AFFINE ? kMMFloat : kMMNone;
+    // launched early (after the statistics pass): request the warp's first
+    // tile into L2, then wait for the partials
+    {
+      const int64_t ntiles = (n + kTile - 1) / kTile;
+      const int64_t t0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+      if (t0 < ntiles) prefetch_tile_l2<T>(x, n, ntiles - 1 - t0, threadIdx.x & 31);
+    }
+    pdl_wait();
     Stats st = reduce_partials<MM>(part, nparts, red);
     if (threadIdx.x == 0) {
       int f = calibrate<BITS, AFFINE, MM>(st, sp, OPT ? co : CalOpts{1.0f, 0, 0});
@@ -394,7 +403,7 @@ qat_status launch_stats_finalize(const void* ws, int nparts, float* absmax, floa
 template <typename T, int BITS, bool AFFINE>
 static void int_tensor_t(bool given, const void* x, int64_t n, const void* ws, int nparts,
                          float* scale, int32_t* zp, const SrCtx& sr, const CalOpts& co, void* y,
-                         void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s) {
+                         void* codes, uint32_t* mask, int32_t* flags, cudaStream_t s, bool pdl) {
   const int grid = map_grid(n, 8);
   const uint4* part = static_cast<const uint4*>(ws);
   // calibration options as a compile-time switch (the plain build keeps its registers)
@@ -403,19 +412,19 @@ static void int_tensor_t(bool given, const void* x, int64_t n, const void* ws, i
     k_int_tensor<T, BITS, AFFINE, true, QAT_SR, false>
         <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, co, y, codes, mask, flags);
   else if (opt)
-    k_int_tensor<T, BITS, AFFINE, false, QAT_SR, true>
-        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, co, y, codes, mask, flags);
+    launch_kernel(k_int_tensor<T, BITS, AFFINE, false, QAT_SR, true>, dim3(grid), dim3(256), 0, s,
+                  pdl, x, n, part, nparts, scale, zp, sr, co, y, codes, mask, flags);
   else
-    k_int_tensor<T, BITS, AFFINE, false, QAT_SR, false>
-        <<<grid, 256, 0, s>>>(x, n, part, nparts, scale, zp, sr, co, y, codes, mask, flags);
+    launch_kernel(k_int_tensor<T, BITS, AFFINE, false, QAT_SR, false>, dim3(grid), dim3(256), 0, s,
+                  pdl, x, n, part, nparts, scale, zp, sr, co, y, codes, mask, flags);
 }
 
 qat_status QAT_SR_NAME(launch_int_tensor)(qat_dtype dt, int bits, bool affine, bool given,
                                           const void* x, int64_t n, const void* ws, int nparts,
                                           float* scale, int32_t* zp, const SrCtx& sr,
                                           const CalOpts& co, void* y, void* codes, uint32_t* mask,
-                                          int32_t* flags, cudaStream_t s) {
-#define QAT_IT(T, B, A) int_tensor_t<T, B, A>(given, x, n, ws, nparts, scale, zp, sr, co, y, codes, mask, flags, s)
+                                          int32_t* flags, cudaStream_t s, bool pdl) {
+#define QAT_IT(T, B, A) int_tensor_t<T, B, A>(given, x, n, ws, nparts, scale, zp, sr, co, y, codes, mask, flags, s, pdl)
   if (dt == QAT_F32) {
     if (bits == 8) { if (affine) QAT_IT(F32, 8, true); else QAT_IT(F32, 8, false); }
     else { if (affine) QAT_IT(F32, 4, true); else QAT_IT(F32, 4, false); }

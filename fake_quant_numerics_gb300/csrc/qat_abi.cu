@@ -245,7 +245,7 @@ static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t ro
   if (g == QAT_PER_TENSOR) {
     if (params_given)
       return map_tensor(dtype, bits, affine, true, x, n, nullptr, 0, scale, zp, c, co, y, codes, mask,
-                        flags, s);
+                        flags, s, false);
     if (!ws || ws_bytes < ws_bytes_for(rows, cols, g, group)) return QAT_ERR_WORKSPACE;
     if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
     const bool plain = co.clip == 1.0f && !co.fp16 && !co.clamp;
@@ -260,7 +260,7 @@ static qat_status fake_quant_int_impl(const void* x, qat_dtype dtype, int64_t ro
     qat_status st = launch_stats_tensor(dtype, x, n, affine ? kMMFloat : kMMNone, ws, grid, s);
     if (st) return st;
     return map_tensor(dtype, bits, affine, false, x, n, ws, grid, scale, zp, c, co, y, codes, mask,
-                      flags, s);
+                      flags, s, true);
   }
   const bool col = g == QAT_PER_COLUMN;
   const int64_t ucols = col ? cols : 0;
@@ -382,7 +382,8 @@ qat_status qat_fake_quant_int_percentile(const void* x, qat_dtype dtype, int64_t
   const CalOpts co{1.0f, 0, 1};
   const SrCtx c = sr_ctx(seed, offset);
   auto map = stochastic ? launch_int_tensor_sr : launch_int_tensor;
-  return map(dtype, bits, affine, false, x, n, ws, 1, scale, zp, c, co, y, codes, mask, flags, s);
+  return map(dtype, bits, affine, false, x, n, ws, 1, scale, zp, c, co, y, codes, mask, flags, s,
+             true);
 }
 
 qat_status qat_fake_quant_block(const void* x, qat_dtype dtype, int64_t n, qat_elem_format elem,
@@ -445,13 +446,13 @@ static qat_status fake_quant_fp8_impl(const void* x, qat_dtype dtype, int64_t n,
   }
   auto map = sr ? launch_fp8_tensor_sr : launch_fp8_tensor;
   if (scale_given)
-    return map(dtype, fmt, true, x, n, nullptr, 0, scale, c, y, codes, mask, flags, s);
+    return map(dtype, fmt, true, x, n, nullptr, 0, scale, c, y, codes, mask, flags, s, false);
   if (!ws || ws_bytes < ws_bytes_for(1, n, QAT_PER_TENSOR, 0)) return QAT_ERR_WORKSPACE;
   if (!aligned(ws, kAlignBuf)) return QAT_ERR_MISALIGNED;
   int grid = stats_grid(n);
   qat_status st = launch_stats_tensor(dtype, x, n, kMMNone, ws, grid, s);
   if (st) return st;
-  return map(dtype, fmt, false, x, n, ws, grid, scale, c, y, codes, mask, flags, s);
+  return map(dtype, fmt, false, x, n, ws, grid, scale, c, y, codes, mask, flags, s, true);
 }
 
 qat_status qat_fake_quant_fp8(const void* x, qat_dtype dtype, int64_t n, qat_fp8_format fmt,
@@ -522,11 +523,11 @@ qat_status qat_optimizer_step(float* master, const float* grad, float* exp_avg, 
   if (int_view) {
     auto map = stochastic ? launch_int_tensor_sr : launch_int_tensor;
     return map(QAT_F32, bits, affine, false, master, n, ws, grid, scale, zp, c, kCalPlain, view,
-               codes, mask, flags, s);
+               codes, mask, flags, s, false);
   }
   auto map = stochastic ? launch_fp8_tensor_sr : launch_fp8_tensor;
   return map(QAT_F32, format, true, master, n, nullptr, 0, scale, c, view,
-             static_cast<uint8_t*>(codes), mask, flags, s);
+             static_cast<uint8_t*>(codes), mask, flags, s, false);
 }
 
 qat_status qat_ste_backward(const void* grad, qat_dtype dtype, int64_t n, const uint32_t* mask,

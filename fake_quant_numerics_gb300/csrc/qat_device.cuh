@@ -983,6 +983,25 @@ __device__ __forceinline__ void int_map_vec(const V32& v, const IntParams& p, Ou
   }
 }
 
+// Programmatic dependent launch: pdl_wait() returns once the previous kernel
+// of the stream has completed and its writes are visible (at once for an
+// ordinary launch); pdl_trigger() lets the next kernel, if it was launched with
+// the attribute, be scheduled while this one finishes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// the 128-byte line at p into L2 (no registers held)
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+// each lane of the warp prefetches one 128-byte line of a 1024-element tile
+template <typename T>
+__device__ __forceinline__ void prefetch_tile_l2(const void* x, int64_t n, int64_t tile, int lane) {
+  const int64_t e = tile * kTile + (int64_t)lane * (128 / T::BYTES);
+  if (e < n) prefetch_l2(static_cast<const char*>(x) + e * T::BYTES);
+}
+
 __device__ __forceinline__ void flag_or(int32_t* flags, int bits) {
   if (flags && bits) atomicOr(flags, bits);
 }

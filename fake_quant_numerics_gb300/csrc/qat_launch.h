@@ -21,6 +21,27 @@ struct NvtxScope {
   NvtxScope& operator=(const NvtxScope&) = delete;
 };
 
+// Launch a kernel, with programmatic dependent launch when pdl is set: the
+// kernel may then be scheduled while the previous kernel of the stream (the
+// call's own previous kernel) finishes, and must call pdl_wait() before it
+// reads anything that kernel wrote.  Only a call's second and later kernels
+// are launched so.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+
 struct Dev {
   int sms;  // streaming multiprocessors of the current device
 };
@@ -80,7 +101,7 @@ qat_status launch_stats_finalize(const void* ws, int nparts, float* absmax, floa
   qat_status name(qat_dtype dt, int bits, bool affine, bool given, const void* x, int64_t n,    \
                   const void* ws, int nparts, float* scale, int32_t* zp, const SrCtx& sr,       \
                   const CalOpts& co, void* y, void* codes, uint32_t* mask, int32_t* flags,      \
-                  cudaStream_t s)
+                  cudaStream_t s, bool pdl)
 QAT_DECL_INT_TENSOR(launch_int_tensor);
 QAT_DECL_INT_TENSOR(launch_int_tensor_sr);
 
@@ -177,7 +198,7 @@ qat_status launch_block_fq(qat_dtype dt, int fmt, int kind, int64_t block, const
 #define QAT_DECL_FP8_TENSOR(name)                                                               \
   qat_status name(qat_dtype dt, qat_fp8_format fmt, bool given, const void* x, int64_t n,       \
                   const void* ws, int nparts, float* scale, const SrCtx& sr, void* y,           \
-                  uint8_t* codes, uint32_t* mask, int32_t* flags, cudaStream_t s)
+                  uint8_t* codes, uint32_t* mask, int32_t* flags, cudaStream_t s, bool pdl)
 QAT_DECL_FP8_TENSOR(launch_fp8_tensor);
 QAT_DECL_FP8_TENSOR(launch_fp8_tensor_sr);
 

@@ -69,7 +69,7 @@ extern "C" qat_status qat_fake_quant_fp8_noalloc(const void* x, qat_dtype dtype,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (scale_given)
     return qat::launch_fp8_tensor(dtype, fmt, true, x, n, nullptr, 0, scale, qat::SrCtx{}, y, codes,
-                                  mask, flags, s);
+                                  mask, flags, s, false);
   const int grid = qat::stats_grid(n);  // at most kMaxPartials = kNoAllocSlots
   void* ws = nullptr;
   qat_status st = scratch_of_current_context(&ws);
@@ -77,5 +77,5 @@ extern "C" qat_status qat_fake_quant_fp8_noalloc(const void* x, qat_dtype dtype,
   st = qat::launch_stats_tensor(dtype, x, n, qat::kMMNone, ws, grid, s);
   if (st) return st;
   return qat::launch_fp8_tensor(dtype, fmt, false, x, n, ws, grid, scale, qat::SrCtx{}, y, codes,
-                                mask, flags, s);
+                                mask, flags, s, false);
 }
