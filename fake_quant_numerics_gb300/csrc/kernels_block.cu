@@ -142,6 +142,13 @@ __global__ void __launch_bounds__(256) k_block_fq(const void* __restrict__ x, in
   // E4M3 scales: the tensor's finite absmax from the statistics pass (g and
   // the non-finite flag); the other kinds see their non-finite values here
   if (KIND == QAT_BLOCK_SCALE_E4M3) {
+    // launched early (after the statistics pass): request the warp's first
+    // tile into L2, then wait for the partials
+    {
+      const int64_t t0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+      if (t0 * kTile < n) prefetch_tile_l2<T>(x, n, t0, threadIdx.x & 31);
+    }
+    pdl_wait();
     const Stats st = reduce_partials<kMMNone>(part, nparts, red);
     if (threadIdx.x == 0) {
       const float g = __fdiv_rn(st.absmax_f(), kMax * 448.0f);
@@ -282,12 +289,14 @@ static void block_t(int64_t block, const void* x, int64_t n, const void* ws, int
   const int64_t cap = (int64_t)device_info().sms * 8;
   const int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
   const uint4* part = static_cast<const uint4*>(ws);
+  // E4M3 scales follow the call's statistics pass: launched early
+  const bool pdl = KIND == QAT_BLOCK_SCALE_E4M3;
   if (block == 16)
-    k_block_fq<T, FMT, KIND, 16><<<grid, 256, 0, s>>>(x, n, part, nparts, tensor_scale, y, codes,
-                                                      bscales, mask, flags);
+    launch_kernel(k_block_fq<T, FMT, KIND, 16>, dim3(grid), dim3(256), 0, s, pdl, x, n, part,
+                  nparts, tensor_scale, y, codes, bscales, mask, flags);
   else
-    k_block_fq<T, FMT, KIND, 32><<<grid, 256, 0, s>>>(x, n, part, nparts, tensor_scale, y, codes,
-                                                      bscales, mask, flags);
+    launch_kernel(k_block_fq<T, FMT, KIND, 32>, dim3(grid), dim3(256), 0, s, pdl, x, n, part,
+                  nparts, tensor_scale, y, codes, bscales, mask, flags);
 }
 
 template <typename T, int FMT>

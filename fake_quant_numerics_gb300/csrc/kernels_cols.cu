@@ -256,6 +256,7 @@ __device__ __forceinline__ void col_add(Stats& st, uint32_t u) {
 }
 
 __global__ void k_col_init(uint4* __restrict__ acc, int64_t cols) {
+  pdl_trigger();
   const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (c < cols) acc[c] = make_uint4(0u, 0u, kKeyPosInf, kKeyNegInf);
 }
@@ -328,6 +329,7 @@ __global__ void k_col_finalize(const uint4* __restrict__ acc, int64_t cols, floa
                                float* out1, float* out2, int32_t* zp, uint8_t* dead, CalOpts co,
                                int32_t* flags) {
   constexpr int MM = (MODE == 0 || AFFINE) ? kMMKeys : kMMNone;
+  pdl_wait();  // launched early: the accumulators come from the statistics kernel
   const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   int f = 0;
   if (c < cols) {
@@ -394,6 +396,8 @@ __global__ void __launch_bounds__(256, 3)
       }
     }
   }
+  pdl_trigger();
+  pdl_wait();  // launched early: the accumulators are set by k_col_init
   col_stats_combine<T, MM>(st, red, wc, cols, acc);
 }
 
@@ -516,6 +520,8 @@ __global__ void __launch_bounds__(256, 2)
       }
     }
   }
+  pdl_trigger();
+  pdl_wait();  // launched early: the accumulators are set by k_col_init
   col_stats_combine<T, MM>(st, reinterpret_cast<uint4*>(col_stage), wc, cols, acc);
 }
 #endif  // !QAT_SR
@@ -728,6 +734,7 @@ __global__ void __launch_bounds__(256, 2)
   uint32_t slowm = 0u, deadm = 0u;
   bool slow = false;
   const auto calibrate_columns = [&] {
+    pdl_wait();  // launched early: the accumulators come from the statistics kernel
     int f = 0;
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
@@ -810,10 +817,11 @@ static void col_stats_t(bool keys, const void* x, int64_t rows, int64_t cols, ui
   do {                                                                                          \
     if (staged) {                                                                               \
       col_staged_smem<k_col_stats_staged<T, M>>();                                              \
-      k_col_stats_staged<T, M><<<grid, 256, kColStagedBytes, s>>>(x, rows, cols, g.wc, g.rchunk, \
-                                                                  tr, limit, acc, flags);       \
+      launch_kernel(k_col_stats_staged<T, M>, grid, dim3(256), kColStagedBytes, s, true, x, rows, \
+                    cols, g.wc, g.rchunk, tr, limit, acc, flags);                               \
     } else {                                                                                    \
-      k_col_stats<T, M><<<grid, 256, 0, s>>>(x, rows, cols, g.wc, g.rchunk, acc);                \
+      launch_kernel(k_col_stats<T, M>, grid, dim3(256), 0, s, true, x, rows, cols, g.wc,        \
+                    g.rchunk, acc);                                                             \
     }                                                                                           \
   } while (0)
   if (keys) QAT_CS(kMMKeys);
@@ -837,8 +845,9 @@ qat_status launch_col_finalize(int mode, int bits, bool affine, void* ws, int64_
                                int32_t* flags, cudaStream_t s) {
   const ColWs w = col_ws(ws, cols);
   const unsigned g = (unsigned)((cols + 255) / 256);
-#define QAT_CF(M, B, A) \
-  k_col_finalize<M, B, A><<<g, 256, 0, s>>>(w.acc, cols, out0, out1, out2, zp, w.dead, co, flags)
+#define QAT_CF(M, B, A)                                                                        \
+  launch_kernel(k_col_finalize<M, B, A>, dim3(g), dim3(256), 0, s, true, w.acc, cols, out0, out1, \
+                out2, zp, w.dead, co, flags)
   if (mode == 0) QAT_CF(0, 8, false);
   else if (bits == 8) { if (affine) QAT_CF(1, 8, true); else QAT_CF(1, 8, false); }
   else { if (affine) QAT_CF(1, 4, true); else QAT_CF(1, 4, false); }
@@ -857,9 +866,9 @@ static void int_cols_t(const void* x, int64_t rows, int64_t cols, const uint4* a
   const int tr = col_tile_rows((int64_t)kColStrip<T> * g.wc, T::BYTES);
   const dim3 grid((unsigned)g.strips, (unsigned)g.chunks);
   col_staged_smem<k_int_cols<T, BITS, AFFINE, QAT_SR>>();
-  k_int_cols<T, BITS, AFFINE, QAT_SR><<<grid, 256, kColStagedBytes, s>>>(
-      x, rows, cols, g.wc, g.rchunk, tr, device_wait_limit(), acc, scale, zp, sr, co, y, codes,
-      mask, flags);
+  launch_kernel(k_int_cols<T, BITS, AFFINE, QAT_SR>, grid, dim3(256), kColStagedBytes, s, true, x,
+                rows, cols, g.wc, g.rchunk, tr, device_wait_limit(), acc, scale, zp, sr, co, y,
+                codes, mask, flags);
 }
 
 qat_status QAT_SR_NAME(launch_int_cols)(qat_dtype dt, int bits, bool affine, const void* x,

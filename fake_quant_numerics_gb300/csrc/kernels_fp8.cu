@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(256) k_fp8_tensor(const void* __restrict__ x, 
   __shared__ __align__(16) uint32_t red[4 * 8];
   __shared__ Fp8Params sp;
   if (GIVEN) {
+    pdl_wait();  // after the optimizer's update, x and the scale are its outputs
     if (threadIdx.x == 0) {
       float s = scale[0];
       sp.s = s;

@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(512) k_adam(float* __restrict__ w, const float
       }
     }
   }
+  pdl_trigger();  // the view may be scheduled as the blocks finish
   if (STATS) {
     const Stats b = block_reduce_stats<MM>(st, red);
     if (threadIdx.x == 0) part[blockIdx.x] = b.pack();

@@ -523,11 +523,11 @@ qat_status qat_optimizer_step(float* master, const float* grad, float* exp_avg, 
   if (int_view) {
     auto map = stochastic ? launch_int_tensor_sr : launch_int_tensor;
     return map(QAT_F32, bits, affine, false, master, n, ws, grid, scale, zp, c, kCalPlain, view,
-               codes, mask, flags, s, false);
+               codes, mask, flags, s, true);
   }
   auto map = stochastic ? launch_fp8_tensor_sr : launch_fp8_tensor;
   return map(QAT_F32, format, true, master, n, nullptr, 0, scale, c, view,
-             static_cast<uint8_t*>(codes), mask, flags, s, false);
+             static_cast<uint8_t*>(codes), mask, flags, s, true);
 }
 
 qat_status qat_ste_backward(const void* grad, qat_dtype dtype, int64_t n, const uint32_t* mask,
