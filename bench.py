@@ -807,35 +807,79 @@ def compact_per_call(per_wl):
     return out
 
 
-def run_e2e(args, suite, calls, step_bytes):
+def run_e2e(args, suite, calls, step_bytes, keep=None):
     """The same step with host inputs: pinned H2D copies of every input, the
-    calls, and D2H copies of every output, all inside the timed region."""
+    calls, and D2H copies of every output, all inside the timed region.
+
+    Two device buffer sets and three streams (copies in, calls, copies out)
+    pipeline the steps: step k's inputs come in while step k - 1 computes and
+    step k - 2's outputs go out, so the two directions of the host link run
+    at once.  Step k's copies into a set wait for the calls of step k - 2 on
+    that set, its calls wait for its inputs and for the copy-out of step
+    k - 2 from the set's outputs; every step still moves all its inputs in
+    and all its outputs out.  `keep` receives the host outputs of the last
+    step (a test compares them with the direct calls)."""
+    dev = suite.x1.device
+    if not args.only:
+        calls = suite.calls()
+    sets = [(suite, calls)]
+    other = Suite(dev, suite.fq, [t.cpu() for t in suite.inputs])
+    sets.append((other, other.calls() if not args.only else [other.calls()[i] for i in
+                                                              _subset(args, suite)]))
     host_in = [t.cpu().pin_memory() for t in suite.inputs]
-    outs = suite.outputs_for_host()
-    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in suite.outputs_for_host()]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     k = max(2, min(args.steps, args.e2e_steps))
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    cmp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        for d, h in zip(suite.inputs, host_in):
-            d.copy_(h, non_blocking=True)
-        for c in calls:
-            c()
-        for h, d in zip(host_out, outs):
-            h.copy_(d, non_blocking=True)
+    def step(i):
+        b = i % 2
+        S, cs = sets[b]
+        if i >= 2:
+            s_in.wait_event(cmp_done[b])  # the calls of step i - 2 have read this set
+        with torch.cuda.stream(s_in):
+            for d, h in zip(S.inputs, host_in):
+                d.copy_(h, non_blocking=True)
+            in_done[b].record(s_in)
+        s_cmp.wait_event(in_done[b])
+        if i >= 2:
+            s_cmp.wait_event(out_done[b])  # step i - 2's outputs have left this set
+        with torch.cuda.stream(s_cmp):
+            for c in cs:
+                c()
+            cmp_done[b].record(s_cmp)
+        s_out.wait_event(cmp_done[b])
+        with torch.cuda.stream(s_out):
+            for h, d in zip(host_out, S.outputs_for_host()):
+                h.copy_(d, non_blocking=True)
+            out_done[b].record(s_out)
 
-    step()
+    step(0)
+    step(1)
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
-    for _ in range(k):
-        step()
+    for i in range(k):
+        step(i)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
     secs, tot = reduce_max_sum(t1 - t0, step_bytes * k)
+    if keep is not None:
+        keep["host_out"] = host_out
+    del other
     return {"value": round(tot / secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": k}
+            "d2h_bytes_per_step": d2h, "steps": k,
+            "pipeline": "2 device buffer sets; copies in, calls, copies out on 3 streams"}
+
+
+def _subset(args, suite):
+    n1, n2, n3, n4, n5 = suite.n
+    wb = workload_bytes(n1, suite.r2, suite.c2, n3, suite.r4, suite.c4, n5)
+    return [i for i, w in enumerate(wb) if any(w[0].startswith(p) for p in args.only.split(","))]
 
 
 # ---------------------------------------------------------------------------
@@ -1087,7 +1131,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-passes", type=int, default=3,
                     help="oracle passes over the full workloads for cpu_baseline")
     ap.add_argument("--ref-fraction", type=float, default=0.0,
