@@ -197,7 +197,9 @@ __device__ __forceinline__ void q4_codes16(const V32 (&v)[2], float s, bool has_
   }
 }
 
-template <bool ROUNDTRIP>
+// UA: x and y hold whole elements but may be off the 32-byte grid (element
+// loads and stores, no prefetch of the next super-block)
+template <bool ROUNDTRIP, bool UA>
 __global__ void __launch_bounds__(kQ4Threads, 2) k_q4_quant(const float* __restrict__ x, int64_t n,
                                                          uint8_t* __restrict__ data,
                                                          uint8_t* __restrict__ qscales,
@@ -226,13 +228,13 @@ __global__ void __launch_bounds__(kQ4Threads, 2) k_q4_quant(const float* __restr
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int64_t base = e0 + (int64_t)j * (kQ4Threads * 16) + tid * 16 + h * 8;
-        if (full) {
+        if (full && !UA) {
           cnt[j][h] = 8;
           if (!have) v[j][h] = ld_v32(x + base);
         } else {
           const int64_t c = n - base;
           cnt[j][h] = c >= 8 ? 8 : (c > 0 ? (int)c : 0);
-          v[j][h] = load_vec<F32>(x, cnt[j][h] > 0 ? base : 0, cnt[j][h]);
+          v[j][h] = load_vec<F32, UA>(x, cnt[j][h] > 0 ? base : 0, cnt[j][h]);
         }
       }
     }
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kQ4Threads, 2) k_q4_quant(const float* __restr
     }
     {
       const int64_t nsb = sb + gridDim.x;
-      have = nsb < nsuper && nsb * kQ4SuperElems + kQ4SuperElems <= n;
+      have = !UA && nsb < nsuper && nsb * kQ4SuperElems + kQ4SuperElems <= n;
       if (have) {
 #pragma unroll
         for (int j = 0; j < kQ4Pairs; ++j)
@@ -315,7 +317,7 @@ __global__ void __launch_bounds__(kQ4Threads, 2) k_q4_quant(const float* __restr
         for (int h = 0; h < 2; ++h) {
           const V32 o = dequant8(packed[j][h], rs);
           const int64_t base = e0 + (int64_t)j * (kQ4Threads * 16) + tid * 16 + h * 8;
-          if (cnt[j][h] > 0) store_vec<F32>(y, base, o, cnt[j][h]);
+          if (cnt[j][h] > 0) store_vec<F32, UA>(y, base, o, cnt[j][h]);
         }
       }
     }
@@ -324,12 +326,17 @@ __global__ void __launch_bounds__(kQ4Threads, 2) k_q4_quant(const float* __restr
 }
 
 qat_status launch_q4_quant(const float* x, int64_t n, uint8_t* data, uint8_t* qscales, float* sup,
-                           float* y, cudaStream_t s) {
+                           float* y, bool ua, cudaStream_t s) {
   const int64_t nsuper = (n + kQ4SuperElems - 1) / kQ4SuperElems;
   int64_t cap = (int64_t)device_info().sms * 4;
   int grid = (int)(nsuper > cap ? cap : (nsuper < 1 ? 1 : nsuper));
-  if (y) k_q4_quant<true><<<grid, kQ4Threads, 0, s>>>(x, n, data, qscales, sup, y);
-  else k_q4_quant<false><<<grid, kQ4Threads, 0, s>>>(x, n, data, qscales, sup, y);
+  if (ua) {
+    if (y) k_q4_quant<true, true><<<grid, kQ4Threads, 0, s>>>(x, n, data, qscales, sup, y);
+    else k_q4_quant<false, true><<<grid, kQ4Threads, 0, s>>>(x, n, data, qscales, sup, y);
+  } else {
+    if (y) k_q4_quant<true, false><<<grid, kQ4Threads, 0, s>>>(x, n, data, qscales, sup, y);
+    else k_q4_quant<false, false><<<grid, kQ4Threads, 0, s>>>(x, n, data, qscales, sup, y);
+  }
   count_launch(1);
   return launch_status();
 }
@@ -361,6 +368,8 @@ __device__ __forceinline__ void q4_step_full(const uint8_t* __restrict__ data,
   d.sup = __ldg(sup + (st >> 4));
 }
 
+// UA: y holds whole elements but may be off the 32-byte grid (element stores)
+template <bool UA>
 __global__ void __launch_bounds__(256) k_q4_dequant(const uint8_t* __restrict__ data,
                                                     const uint8_t* __restrict__ qscales,
                                                     const float* __restrict__ sup, int64_t n,
@@ -389,7 +398,7 @@ __global__ void __launch_bounds__(256) k_q4_dequant(const uint8_t* __restrict__ 
           if (e0 / 2 + b < nbytes) pk |= (uint32_t)data[e0 / 2 + b] << (8 * b);
         const float rs = __fmul_rn(s_inv255[qscales[e0 / kQ4Block]], sup[e0 / kQ4SuperElems]);
         const int64_t c = n - e0;
-        store_vec<F32>(y, e0, dequant8(pk, rs), c >= 8 ? 8 : (int)c);
+        store_vec<F32, UA>(y, e0, dequant8(pk, rs), c >= 8 ? 8 : (int)c);
       }
       continue;
     }
@@ -405,18 +414,24 @@ __global__ void __launch_bounds__(256) k_q4_dequant(const uint8_t* __restrict__ 
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float rs = __fmul_rn(s_inv255[(qw[k] >> qb) & 0xffu], cur.sup);
-      st_v32(y + (st * 128 + k * 32 + lane) * 8, dequant8(cur.pk[k], rs));
+      if (UA)
+        store_vec<F32, true>(y, (st * 128 + k * 32 + lane) * 8, dequant8(cur.pk[k], rs), 8);
+      else
+        st_v32(y + (st * 128 + k * 32 + lane) * 8, dequant8(cur.pk[k], rs));
     }
   }
 }
 
 qat_status launch_q4_dequant(const uint8_t* data, const uint8_t* qscales, const float* sup,
-                             int64_t n, float* y, cudaStream_t s) {
+                             int64_t n, float* y, bool ua, cudaStream_t s) {
   const int64_t nsteps = (n + 1023) / 1024;
   int64_t g = (nsteps + 7) / 8;
   int64_t cap = (int64_t)device_info().sms * 8;
   int grid = (int)(g > cap ? cap : (g < 1 ? 1 : g));
-  k_q4_dequant<<<grid, 256, 0, s>>>(data, qscales, sup, n, y);
+  if (ua)
+    k_q4_dequant<true><<<grid, 256, 0, s>>>(data, qscales, sup, n, y);
+  else
+    k_q4_dequant<false><<<grid, 256, 0, s>>>(data, qscales, sup, n, y);
   count_launch(1);
   return launch_status();
 }

@@ -550,10 +550,11 @@ qat_status qat_quant4_double(const float* x, int64_t n, uint8_t* data, uint8_t* 
   if (n < 0 || n > (INT64_C(1) << 50)) return QAT_ERR_INVALID_ARGUMENT;
   if (n == 0) return QAT_OK;
   if (!x || !data || !qscales || !super_scales) return QAT_ERR_INVALID_ARGUMENT;
-  if (!aligned(x, kAlignVec) || !aligned(data, kAlignBuf) || !aligned(qscales, kAlignBuf) ||
-      !aligned(super_scales, 4) || (y && !aligned(y, kAlignVec)))
+  if (!aligned(x, 4) || !aligned(data, kAlignBuf) || !aligned(qscales, kAlignBuf) ||
+      !aligned(super_scales, 4) || (y && !aligned(y, 4)))
     return QAT_ERR_MISALIGNED;
-  return launch_q4_quant(x, n, data, qscales, super_scales, y,
+  const bool ua = !aligned(x, kAlignVec) || (y && !aligned(y, kAlignVec));
+  return launch_q4_quant(x, n, data, qscales, super_scales, y, ua,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -564,9 +565,9 @@ qat_status qat_dequant4_double(const uint8_t* data, const uint8_t* qscales, cons
   if (n == 0) return QAT_OK;
   if (!data || !qscales || !super_scales || !y) return QAT_ERR_INVALID_ARGUMENT;
   if (!aligned(data, kAlignBuf) || !aligned(qscales, kAlignBuf) || !aligned(super_scales, 4) ||
-      !aligned(y, kAlignVec))
+      !aligned(y, 4))
     return QAT_ERR_MISALIGNED;
-  return launch_q4_dequant(data, qscales, super_scales, n, y,
+  return launch_q4_dequant(data, qscales, super_scales, n, y, !aligned(y, kAlignVec),
                            reinterpret_cast<cudaStream_t>(stream));
 }
 

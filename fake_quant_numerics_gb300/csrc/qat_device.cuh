@@ -91,10 +91,12 @@ __device__ __forceinline__ uint32_t load_elem_bits<BF16>(const void* x, int64_t 
 
 // Load the VEC elements starting at element `base`; `cnt` of them exist
 // (cnt == VEC is the fast path; missing elements read as +0).  The tail loop
-// is fully unrolled with predicates so the vector stays in registers.
-template <typename T>
+// is fully unrolled with predicates so the vector stays in registers.  UA: x
+// holds whole elements but may be off the 32-byte grid, so every element is
+// loaded on its own.
+template <typename T, bool UA = false>
 __device__ __forceinline__ V32 load_vec(const void* x, int64_t base, int cnt) {
-  if (cnt >= T::VEC) return ld_v32(static_cast<const char*>(x) + base * T::BYTES);
+  if (!UA && cnt >= T::VEC) return ld_v32(static_cast<const char*>(x) + base * T::BYTES);
   V32 v;
 #pragma unroll
   for (int j = 0; j < 8; ++j) v.w[j] = 0u;
@@ -179,10 +181,11 @@ struct OutVec<BF16> {
   __device__ __forceinline__ void set2(int e, float ya, float yb) { v.w[e >> 1] = pack_bf16x2(ya, yb); }
 };
 
-// Store the first `cnt` elements of an output vector at element `base`.
-template <typename T>
+// Store the first `cnt` elements of an output vector at element `base` (UA:
+// element by element, y being possibly off the 32-byte grid).
+template <typename T, bool UA = false>
 __device__ __forceinline__ void store_vec(void* y, int64_t base, const V32& v, int cnt) {
-  if (cnt >= T::VEC) {
+  if (!UA && cnt >= T::VEC) {
     st_v32(static_cast<char*>(y) + base * T::BYTES, v);
     return;
   }

@@ -220,8 +220,8 @@ qat_status launch_ste(qat_dtype dt, const void* g, int64_t n, const uint32_t* ma
 
 // two-level 4-bit
 qat_status launch_q4_quant(const float* x, int64_t n, uint8_t* data, uint8_t* qscales, float* sup,
-                           float* y, cudaStream_t s);
+                           float* y, bool ua, cudaStream_t s);
 qat_status launch_q4_dequant(const uint8_t* data, const uint8_t* qscales, const float* sup,
-                             int64_t n, float* y, cudaStream_t s);
+                             int64_t n, float* y, bool ua, cudaStream_t s);
 
 }  // namespace qat

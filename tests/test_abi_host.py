@@ -115,8 +115,10 @@ def test_ste_and_q4_argument_errors(lib):
     assert lib.qat_ste_backward(None, L.F32, 0, None, None, None) == L.QAT_OK
     assert lib.qat_quant4_double(A, -5, A, A, A, None, None) == L.QAT_ERR_INVALID_ARGUMENT
     assert lib.qat_quant4_double(A, 64, None, A, A, None, None) == L.QAT_ERR_INVALID_ARGUMENT
-    assert lib.qat_quant4_double(MIS, 64, A, A, A, None, None) == L.QAT_ERR_MISALIGNED
-    assert lib.qat_quant4_double(A, 64, A, A, A, MIS, None) == L.QAT_ERR_MISALIGNED
+    assert lib.qat_quant4_double(ODD, 64, A, A, A, None, None) == L.QAT_ERR_MISALIGNED
+    assert lib.qat_quant4_double(A, 64, A, A, A, ODD, None) == L.QAT_ERR_MISALIGNED
+    assert lib.qat_quant4_double(A, 64, MIS, A, A, None, None) == L.QAT_ERR_MISALIGNED  # data: 16 B
+    assert lib.qat_dequant4_double(A, A, A, 64, ODD, None) == L.QAT_ERR_MISALIGNED
     assert lib.qat_dequant4_double(A, A, A, 64, None, None) == L.QAT_ERR_INVALID_ARGUMENT
     assert lib.qat_dequant4_double(A, A, A, 0, None, None) == L.QAT_OK
 

@@ -4,7 +4,8 @@ kernels.  x, y, grad and grad_in at offsets 1-7 (fp32) and 1-15 (bf16),
 against the oracle bit for bit: integer fake quant per tensor, per row and per
 group (calibrated or given parameters, nearest or stochastic rounding,
 calibration options), FP8 (amax-scaled or given scale, nearest or
-stochastic), the STE backward and the statistics."""
+stochastic), the STE backward, the statistics, and the two-level 4-bit
+quantize (x, the fused round trip's y) and dequantize (y)."""
 import numpy as np
 import pytest
 import torch
@@ -201,3 +202,32 @@ def test_per_column_off_the_grid_is_refused(qat):
     r = qat.fake_quant_int(x.view(64, 64), 8, "symmetric", "column")  # copied, then quantized
     torch.cuda.synchronize()
     assert r.y.shape == (64, 64)
+
+
+def test_q4_double_at_element_offsets(qat, orc):
+    """x and the fused round trip's y of quantize_4bit_double, and y of
+    dequantize_4bit_double, at fp32 offsets 1-7; a ragged tail and a full
+    super-block or more."""
+    rng = np.random.default_rng(7400)
+    for k, off in enumerate(range(1, 8)):
+        n = 16384 * (1 + k % 3) + 37 * k + 5
+        a = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        a[rng.integers(0, n, size=3)] = 0.0
+        xd = at_offset(torch.from_numpy(a), off)
+        nd, nb, ns = orc.q4_sizes(n)
+        data = Poisoned(nd, torch.uint8)
+        qs = Poisoned(nb, torch.uint8)
+        sup = Poisoned(ns, torch.float32)
+        yr = empty_at(n, torch.float32, (off * 3) % 8)
+        qat.qat_quant4_double(xd, n, data.t, qs.t, sup.t, yr)
+        y = empty_at(n, torch.float32, (off + 4) % 8)
+        qat.qat_dequant4_double(data.t, qs.t, sup.t, n, y)
+        torch.cuda.synchronize()
+        o = orc.quant4_double(a, roundtrip=True)
+        tag = f"n={n} off={off}"
+        assert data.canary_ok() and qs.canary_ok() and sup.canary_ok(), tag
+        assert_same(bits(data.t), o["data"], "data " + tag)
+        assert_same(bits(qs.t), o["qscales"], "qscales " + tag)
+        assert_same(bits(sup.t), o["super_scales"].view(np.uint32), "supers " + tag)
+        assert_same(bits(yr), o["y"].view(np.uint32), "round trip " + tag)
+        assert_same(bits(y), o["y"].view(np.uint32), "dequant " + tag)
