@@ -138,6 +138,96 @@ __device__ __forceinline__ float fp8_sr_value(float t, float u) {
   return copysignf(mag, t);
 }
 
+// fp8_sr_value for the quotient t of x, in fewer integer operations: 2^max(e,
+// emin) is max(exponent field of |t|, that of 2^emin) (a zero or binary32
+// subnormal t has field 0), ulp = 2^max(e, emin) 2^-mbits and 1 / ulp, whose
+// exponent field is 254 + mbits - that field, are exact; the sign is that of
+// x, which t = RN(x/s) (s > 0) shares, so a quotient whose sign or value the
+// residual steps lost needs no repair: t = +0 for x = -0 gives -0 again, and
+// a NaN quotient of x = +-inf (or of an x whose quotient overflows) gives
+// fminf(NaN, max) = max, the rule's value for an infinite t (an element
+// with x NaN is replaced by the caller).  u = (w >> 9) 2^-23 as (1 + u) - 1,
+// 1 + u having the bits hi(w 2^23) + 0x3f800000 (one multiply-add).
+template <int FMT>
+__device__ __forceinline__ float fp8_sr_value_x(float t, float x, uint32_t w) {
+  constexpr uint32_t MB = FMT == QAT_E4M3 ? 3u : 2u;
+  constexpr uint32_t kEminField = (uint32_t)((FMT == QAT_E4M3 ? -6 : -14) + 127) << 23;
+  constexpr float kMaxF = FMT == QAT_E4M3 ? 448.0f : 57344.0f;
+  constexpr float kStepOfExp = FMT == QAT_E4M3 ? 0x1p-3f : 0x1p-2f;  // 2^-mbits
+  uint32_t ub;
+  asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(ub) : "r"(w), "r"(0x00800000u), "r"(0x3f800000u));
+  const float u = __fsub_rn(__uint_as_float(ub), 1.0f);
+  const float a = fabsf(t);
+  const uint32_t eb = max(__float_as_uint(a) & 0x7f800000u, kEminField);
+  const float inv = __uint_as_float(((254u + MB) << 23) - eb);
+  const float step = __fmul_rn(__uint_as_float(eb), kStepOfExp);
+  const float k = sr_round(__fmul_rn(a, inv), u);
+  return copysignf(fminf(__fmul_rn(k, step), kMaxF), x);
+}
+
+// One vector with stochastic rounding for a usable scale (mode 0): the
+// quotient t = RN(x/s) (exact residual-step quotient for a safe scale, the
+// division otherwise), fp8_sr_value_x, y = g s and the code of the grid value
+// g; NaN elements get the canonical NaN and code 0x7F.  For bf16 the window
+// and the NaN test run on the packed magnitudes a = w & 0x7fff7fff as in
+// fp8_vec_bf16_fast (a half above 0x7f80 is a NaN: adding 0x7f carries into
+// its top bit).
+template <typename T, int FMT, bool CODES, bool FULL>
+__device__ __forceinline__ void fp8_vec_sr_mode0(const V32& v, const Fp8Params& p, const SrCtx& sr,
+                                                 int64_t base, int cnt, V32& out,
+                                                 CodeVec<8, T::VEC>& cv, uint32_t& mb) {
+  constexpr int VEC = T::VEC;
+  cv.clear();
+  uint32_t macc = 0u;
+  mb = 0u;
+#pragma unroll
+  for (int g = VEC / 4 - 1; g >= 0; --g) {
+    const uint4 wd = philox4x32_10(sr.offset + (uint64_t)(base / 4 + g), sr.rk);
+    const uint32_t w4[4] = {wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+    for (int h = 1; h >= 0; --h) {
+      const int e = 4 * g + 2 * h;
+      const float x0 = elem<T>(v, e), x1 = elem<T>(v, e + 1);
+      float t0, t1;
+      if (p.fast) {
+        quotient_rn2(x0, x1, p.rcp, p.ns, t0, t1);
+      } else {
+        t0 = __fdiv_rn(x0, p.s);
+        t1 = __fdiv_rn(x1, p.s);
+      }
+      const float g0 = fp8_sr_value_x<FMT>(t0, x0, w4[2 * h]);
+      const float g1 = fp8_sr_value_x<FMT>(t1, x1, w4[2 * h + 1]);
+      float y0, y1;
+      mul2(g0, g1, p.s, p.s, y0, y1);
+      bool n0, n1;
+      if constexpr (T::BYTES == 4) {
+        n0 = isnan(x0);
+        n1 = isnan(x1);
+        mb |= (uint32_t)(fabsf(x0) <= p.lim) << e;
+        mb |= (uint32_t)(fabsf(x1) <= p.lim) << (e + 1);
+        out.w[e] = n0 ? kNaN32 : __float_as_uint(y0);
+        out.w[e + 1] = n1 ? kNaN32 : __float_as_uint(y1);
+      } else {
+        const uint32_t am = v.w[e >> 1] & 0x7fff7fffu;
+        // window bits of elements e and e + 1 land on bits e and 16 + e
+        macc |= ((p.limh2 - am) & 0x80008000u) >> (15 - e);
+        const uint32_t nan = (am + 0x007f007fu) & 0x80008000u;
+        const uint32_t keep = (nan >> 15) * 0xffffu;  // 0xffff in each NaN half
+        out.w[e >> 1] = (pack_bf16x2(y0, y1) & ~keep) | (((kNaN16 << 16) | kNaN16) & keep);
+        n0 = (nan & 0x8000u) != 0u;
+        n1 = (nan >> 31) != 0u;
+      }
+      if (CODES) {
+        const uint32_t c2 = fp8x2_encode<FMT>(g0, g1);
+        const uint32_t c0 = n0 ? 0x7fu : (c2 & 0xffu), c1 = n1 ? 0x7fu : ((c2 >> 8) & 0xffu);
+        cv.set2(e, (FULL || e < cnt) ? (int)(int8_t)c0 : 0,
+                (FULL || e + 1 < cnt) ? (int)(int8_t)c1 : 0);
+      }
+    }
+  }
+  if constexpr (T::BYTES == 2) mb = (macc & 0x5555u) | ((macc >> 15) & 0xaaaau);
+}
+
 // One vector with stochastic rounding: the IEEE quotient t = RN(x/s) (exact
 // residual-step quotient for a safe scale, the division otherwise; its sign
 // is that of x), the grid value of fp8_sr_value, its code by the saturating
@@ -148,6 +238,10 @@ __device__ __forceinline__ void fp8_vec_sr(const V32& v, const Fp8Params& p, con
                                            int64_t base, int cnt, V32& out,
                                            CodeVec<8, T::VEC>& cv, uint32_t& mb) {
   constexpr int VEC = T::VEC;
+  if (p.mode == 0) {
+    fp8_vec_sr_mode0<T, FMT, CODES, FULL>(v, p, sr, base, cnt, out, cv, mb);
+    return;
+  }
   cv.clear();
   mb = 0u;
 #pragma unroll

@@ -155,3 +155,25 @@ def test_fp8_sr(qat, orc, fmt, dt):
             run_fp8_sr(qat, orc, x, fmt, seed, off, scale=1.0)        # the unscaled cast
             run_fp8_sr(qat, orc, x, fmt, seed, off, scale=1e-30)      # outside the safe range
         run_fp8_sr(qat, orc, x, fmt, 3, 4, scale=0.0)                 # zero scale
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_fp8_sr_at_the_normal_boundary(qat, orc, fmt, dt):
+    """Whole vectors of quotients just above, at and just below 2^emin (the
+    smallest normal of the format), where the kernel switches between the
+    bit rule for normal targets and the general rule; given scales that are
+    not powers of two, and the amax scale."""
+    emin = -6 if fmt == 0 else -14
+    rng = np.random.default_rng(740 + fmt)
+    n = 4096 + 5
+    for s in (0.3, 1.7e-3, 3.0e4):
+        edge = np.float64(s) * 2.0 ** emin
+        rel = rng.choice(np.array([-2.0 ** -8, -2.0 ** -20, 0.0, 2.0 ** -20, 2.0 ** -8, 1.0, 7.5]),
+                         size=n)
+        a = (edge * (1.0 + rel) * rng.choice(np.array([-1.0, 1.0]), size=n)).astype(np.float32)
+        t = torch.from_numpy(a)
+        x = t.to(DT[dt]) if dt != "f32" else t
+        for seed, off in SEEDS[:2]:
+            run_fp8_sr(qat, orc, x, fmt, seed, off, scale=s)
+        run_fp8_sr(qat, orc, x, fmt, 5, 0)
