@@ -161,7 +161,13 @@ __device__ __forceinline__ float fp8_sr_value_x(float t, float x, uint32_t w) {
   const uint32_t eb = max(__float_as_uint(a) & 0x7f800000u, kEminField);
   const float inv = __uint_as_float(((254u + MB) << 23) - eb);
   const float step = __fmul_rn(__uint_as_float(eb), kStepOfExp);
-  const float k = sr_round(__fmul_rn(a, inv), u);
+  // sr_round(r, u) as floor(r) + ceil(frac - u): frac - u is exact in sign
+  // (u a multiple of 2^-23 in [0, 1), frac in [0, 1)) and in (-1, 1), so its
+  // ceiling is 1 when u < frac and +-0 otherwise.  An infinite or NaN r gives
+  // a NaN k here (r itself in sr_round), and fminf turns either into max.
+  const float r = __fmul_rn(a, inv);
+  const float lower = floorf(r);
+  const float k = __fadd_rn(lower, ceilf(__fsub_rn(__fsub_rn(r, lower), u)));
   return copysignf(fminf(__fmul_rn(k, step), kMaxF), x);
 }
 
@@ -178,7 +184,7 @@ __device__ __forceinline__ void fp8_vec_sr_mode0(const V32& v, const Fp8Params& 
                                                  CodeVec<8, T::VEC>& cv, uint32_t& mb) {
   constexpr int VEC = T::VEC;
   cv.clear();
-  uint32_t macc = 0u;
+  uint32_t macc = 0u, amax2 = 0u;
   mb = 0u;
 #pragma unroll
   for (int g = VEC / 4 - 1; g >= 0; --g) {
@@ -199,7 +205,7 @@ __device__ __forceinline__ void fp8_vec_sr_mode0(const V32& v, const Fp8Params& 
       const float g1 = fp8_sr_value_x<FMT>(t1, x1, w4[2 * h + 1]);
       float y0, y1;
       mul2(g0, g1, p.s, p.s, y0, y1);
-      bool n0, n1;
+      bool n0 = false, n1 = false;
       if constexpr (T::BYTES == 4) {
         n0 = isnan(x0);
         n1 = isnan(x1);
@@ -211,11 +217,16 @@ __device__ __forceinline__ void fp8_vec_sr_mode0(const V32& v, const Fp8Params& 
         const uint32_t am = v.w[e >> 1] & 0x7fff7fffu;
         // window bits of elements e and e + 1 land on bits e and 16 + e
         macc |= ((p.limh2 - am) & 0x80008000u) >> (15 - e);
-        const uint32_t nan = (am + 0x007f007fu) & 0x80008000u;
-        const uint32_t keep = (nan >> 15) * 0xffffu;  // 0xffff in each NaN half
-        out.w[e >> 1] = (pack_bf16x2(y0, y1) & ~keep) | (((kNaN16 << 16) | kNaN16) & keep);
-        n0 = (nan & 0x8000u) != 0u;
-        n1 = (nan >> 31) != 0u;
+        out.w[e >> 1] = pack_bf16x2(y0, y1);
+        if (CODES) {
+          const uint32_t nan = (am + 0x007f007fu) & 0x80008000u;
+          const uint32_t keep = (nan >> 15) * 0xffffu;  // 0xffff in each NaN half
+          out.w[e >> 1] = (out.w[e >> 1] & ~keep) | (((kNaN16 << 16) | kNaN16) & keep);
+          n0 = (nan & 0x8000u) != 0u;
+          n1 = (nan >> 31) != 0u;
+        } else {
+          amax2 = __vmaxu2(amax2, am);
+        }
       }
       if (CODES) {
         const uint32_t c2 = fp8x2_encode<FMT>(g0, g1);
@@ -225,7 +236,19 @@ __device__ __forceinline__ void fp8_vec_sr_mode0(const V32& v, const Fp8Params& 
       }
     }
   }
-  if constexpr (T::BYTES == 2) mb = (macc & 0x5555u) | ((macc >> 15) & 0xaaaau);
+  if constexpr (T::BYTES == 2) {
+    mb = (macc & 0x5555u) | ((macc >> 15) & 0xaaaau);
+    // without codes, the NaN elements (magnitude bits above 0x7f80) are
+    // patched only in a vector that holds one
+    if (!CODES && max(amax2 & 0xffffu, amax2 >> 16) > 0x7f80u) {
+#pragma unroll
+      for (int i = 0; i < VEC / 2; ++i) {
+        const uint32_t nan = ((v.w[i] & 0x7fff7fffu) + 0x007f007fu) & 0x80008000u;
+        const uint32_t keep = (nan >> 15) * 0xffffu;
+        out.w[i] = (out.w[i] & ~keep) | (((kNaN16 << 16) | kNaN16) & keep);
+      }
+    }
+  }
 }
 
 // One vector with stochastic rounding: the IEEE quotient t = RN(x/s) (exact
