@@ -64,6 +64,28 @@ def test_percentile_sizes_and_fractions(qat, orc, dt, scheme):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_percentile_large_equal_bins(qat, orc, dt):
+    """The low quantile inside a run of 65536 (then 65537) equal values, the
+    high one among spread values; then both quantiles in runs of about
+    175,000 equal values."""
+    rng = np.random.default_rng(3150)
+    n = 200000
+    for k in (65536, 65537):
+        a = np.concatenate([np.full(k, -5.0, np.float32),
+                            rng.uniform(1.0, 1000.0, size=n - k).astype(np.float32)])
+        rng.shuffle(a)
+        t = torch.from_numpy(a)
+        x = t.to(DT[dt]) if dt != "f32" else t
+        for scheme in (0, 1):
+            run_pct(qat, orc, x, 8, scheme, 0.001)
+    a = rng.choice(np.array([-2.0, -0.5, -0.0, 0.0, 0.25, 3.0], np.float32), size=1 << 20)
+    t = torch.from_numpy(a)
+    x = t.to(DT[dt]) if dt != "f32" else t
+    for c in (0.1, 0.3):
+        run_pct(qat, orc, x, 8, 1, c)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_percentile_duplicates_and_signed_zeros(qat, orc, dt):
     rng = np.random.default_rng(3100)
     # few distinct values (long runs of equal keys), zeros of both signs
