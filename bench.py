@@ -282,12 +282,12 @@ def isolated_call_ms(calls, stream, iters=30, warm=3):
     return out
 
 
-def run_next_rows(args, suite, wb, peak):
+def run_next_rows(args, suite, wb, peak, only=None):
     """Rows past the headline path, timed like it (CUDA events per call on the
     launching stream, after warm-up) but reported outside `value`:
     - stochastic rounding (the *_sr entry points) of the w2, w3 and w4 maps,
       same inputs, outputs and algorithmic bytes as their nearest-rounding
-      calls;
+      calls (only: name prefixes, profiling runs of these rows alone);
     - config 1 (w1 int8 per-tensor fwd + STE) replayed as one CUDA graph
       against the same two calls issued directly, with an L2 flush (L2Flush)
       before every timed iteration."""
@@ -310,6 +310,8 @@ def run_next_rows(args, suite, wb, peak):
          lambda: fq.qat_fake_quant_int_sr(suite.w4, r4, c4, 4, 0, 2, 128, False, o["s4"], None,
                                           seed, 0, o["y4"], o["c4"], o["m4"], fl, ws)),
     ]
+    if only:
+        sr = [r for r in sr if any(r[0].startswith(p) for p in only)]
     stream = torch.cuda.current_stream()
     steps = max(3, min(args.steps, 200))
     for _ in range(3):
@@ -330,6 +332,8 @@ def run_next_rows(args, suite, wb, peak):
         out[name] = {"us": round(ms * 1e3, 2), "GB_s": round(b / (ms * 1e-3) / 1e9, 1),
                      "frac_of_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peak, 4),
                      "bytes": b, "launches": 2 if base.startswith("w3") else 1}
+    if only:
+        return {"stochastic_rounding": out}
 
     # config 1: direct calls and one CUDA graph of the same calls
     calls = suite.calls()[:2]
@@ -683,6 +687,7 @@ def run_ours(args, rank, world, local):
     calls = suite.calls()
     n1, n2, n3, n4, n5 = suite.n
     wb = workload_bytes(n1, suite.r2, suite.c2, n3, suite.r4, suite.c4, n5)
+    wb_all = list(wb)
     if args.only:
         keep = [i for i, w in enumerate(wb) if any(w[0].startswith(p) for p in args.only.split(","))]
         calls = [calls[i] for i in keep]
@@ -732,8 +737,11 @@ def run_ours(args, rank, world, local):
 
     peak, peak_kind = measured_peak()
     next_rows = None
+    sr_only = [p for p in args.only.split(",") if p.endswith("_sr")] if args.only else []
     if not args.only and args.fraction >= 1.0 and not args.no_next:
         next_rows = run_next_rows(args, suite, wb, peak)
+    elif sr_only and args.fraction >= 1.0:
+        next_rows = run_next_rows(args, suite, wb_all, peak, only=sr_only)
     iso_ms = isolated_call_ms(calls, stream) if not args.no_isolated else None
     per_wl = {}
     for i, ((name, elems, b, nl), ms) in enumerate(zip(wb, mean_ms)):
@@ -1142,7 +1150,9 @@ def main(argv=None):
     ap.add_argument("--no-next", action="store_true",
                     help="skip the stochastic-rounding and CUDA-graph timings (next_rows)")
     ap.add_argument("--only", default="",
-                    help="profiling: comma-separated call-name prefixes to run (e.g. w5,w4_int4)")
+                    help="profiling: comma-separated call-name prefixes to run (e.g. w5,w4_int4); "
+                         "names ending in _sr select stochastic-rounding rows (e.g. "
+                         "w1,w3_fp8_e4m3_tensor_sr)")
     ap.add_argument("--fraction", type=float, default=1.0,
                     help="profiling: fraction of every workload's rows to generate")
     args = ap.parse_args(argv)
