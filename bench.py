@@ -740,7 +740,7 @@ def run_ours(args, rank, world, local):
     sr_only = [p for p in args.only.split(",") if p.endswith("_sr")] if args.only else []
     if not args.only and args.fraction >= 1.0 and not args.no_next:
         next_rows = run_next_rows(args, suite, wb, peak)
-    elif sr_only and args.fraction >= 1.0:
+    elif sr_only:
         next_rows = run_next_rows(args, suite, wb_all, peak, only=sr_only)
     iso_ms = isolated_call_ms(calls, stream) if not args.no_isolated else None
     per_wl = {}
