@@ -815,6 +815,41 @@ def compact_per_call(per_wl):
     return out
 
 
+def host_link_gbs(dev, nbytes=256 << 20, reps=3):
+    """Pinned host <-> device copy bandwidth of this machine (GB/s), timed with
+    CUDA events after one warm-up copy: host to device alone, device to host
+    alone, and both at once on two streams (their bytes summed)."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    out = {}
+    for name in ("h2d", "d2h", "both"):
+        best = None
+        for _ in range(reps + 1):
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            s1.wait_event(e0)
+            s2.wait_event(e0)
+            if name in ("h2d", "both"):
+                with torch.cuda.stream(s1):
+                    d_in.copy_(h_in, non_blocking=True)
+            if name in ("d2h", "both"):
+                with torch.cuda.stream(s2):
+                    h_out.copy_(d_out, non_blocking=True)
+            torch.cuda.current_stream().wait_stream(s1)
+            torch.cuda.current_stream().wait_stream(s2)
+            e1.record()
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) / 1e3
+            best = t if best is None else min(best, t)
+        out[name] = round((2 if name == "both" else 1) * nbytes / best / 1e9, 1)
+    return out
+
+
 def run_e2e(args, suite, calls, step_bytes, keep=None):
     """The same step with host inputs: pinned H2D copies of every input, the
     calls, and D2H copies of every output, all inside the timed region.
@@ -879,9 +914,18 @@ def run_e2e(args, suite, calls, step_bytes, keep=None):
     if keep is not None:
         keep["host_out"] = host_out
     del other
-    return {"value": round(tot / secs / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    # the host link bounds this figure: a step's copies take at least the
+    # longer of its two directions alone and its total at the rate of both
+    link = host_link_gbs(dev)
+    t_copy = max(h2d / (link["h2d"] * 1e9), d2h / (link["d2h"] * 1e9),
+                 (h2d + d2h) / (link["both"] * 1e9))
+    value = tot / secs / 1e9
+    bound = step_bytes / t_copy / 1e9
+    return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": k,
-            "pipeline": "2 device buffer sets; copies in, calls, copies out on 3 streams"}
+            "pipeline": "2 device buffer sets; copies in, calls, copies out on 3 streams",
+            "host_link_gbs": link, "link_bound": round(bound, 1),
+            "frac_of_link_bound": round(value / bound, 3)}
 
 
 def _subset(args, suite):
