@@ -852,7 +852,8 @@ def host_link_gbs(dev, nbytes=256 << 20, reps=3):
 
 def run_e2e(args, suite, calls, step_bytes, keep=None):
     """The same step with host inputs: pinned H2D copies of every input, the
-    calls, and D2H copies of every output, all inside the timed region.
+    calls, and D2H copies of every output, all inside the timed region; three
+    windows of k steps, the median window's rate reported.
 
     Two device buffer sets and three streams (copies in, calls, copies out)
     pipeline the steps: step k's inputs come in while step k - 1 computes and
@@ -904,13 +905,19 @@ def run_e2e(args, suite, calls, step_bytes, keep=None):
     step(0)
     step(1)
     torch.cuda.synchronize()
-    barrier()
-    t0 = time.perf_counter()
-    for i in range(k):
-        step(i)
-    torch.cuda.synchronize()
-    t1 = time.perf_counter()
-    secs, tot = reduce_max_sum(t1 - t0, step_bytes * k)
+    # three timed windows of k steps each, the median reported: the host link
+    # is shared with the machine's other jobs, and a window now and then runs
+    # at about 60% of the others
+    runs = []
+    for _ in range(3):
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(k):
+            step(i)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        secs, tot = reduce_max_sum(t1 - t0, step_bytes * k)
+        runs.append(tot / secs / 1e9)
     if keep is not None:
         keep["host_out"] = host_out
     del other
@@ -919,10 +926,10 @@ def run_e2e(args, suite, calls, step_bytes, keep=None):
     link = host_link_gbs(dev)
     t_copy = max(h2d / (link["h2d"] * 1e9), d2h / (link["d2h"] * 1e9),
                  (h2d + d2h) / (link["both"] * 1e9))
-    value = tot / secs / 1e9
+    value = sorted(runs)[1]
     bound = step_bytes / t_copy / 1e9
     return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": k,
+            "d2h_bytes_per_step": d2h, "steps": k, "windows": [round(r, 1) for r in runs],
             "pipeline": "2 device buffer sets; copies in, calls, copies out on 3 streams",
             "host_link_gbs": link, "link_bound": round(bound, 1),
             "frac_of_link_bound": round(value / bound, 3)}
