@@ -333,7 +333,11 @@ def run_next_rows(args, suite, wb, peak, only=None):
                      "frac_of_measured_hbm": round(b / (ms * 1e-3) / 1e9 / peak, 4),
                      "bytes": b, "launches": 2 if base.startswith("w3") else 1}
     if only:
-        return {"stochastic_rounding": out}
+        res = {"stochastic_rounding": out} if out else {}
+        cols = run_column_rows(args, suite, peak, only)
+        if cols:
+            res["per_column"] = cols
+        return res
 
     # config 1: direct calls and one CUDA graph of the same calls
     calls = suite.calls()[:2]
@@ -496,7 +500,7 @@ def run_calib_option_rows(args, suite, wb, peak):
     return out
 
 
-def run_column_rows(args, suite, peak):
+def run_column_rows(args, suite, peak, only=None):
     """Per-column (channel axis 1) calibrated fake quant: affine int8 and
     symmetric int4 of the w2 weights fp32[4096, 4096] (the per-row calls'
     shape, one scale per column instead of per row), the int8 affine call
@@ -506,7 +510,8 @@ def run_column_rows(args, suite, peak):
     column statistics must see every row before the first element is mapped,
     so x is read twice (statistics, then the map), as for per-tensor
     calibration; algorithmic bytes count both reads.  An L2 flush (L2Flush)
-    precedes every timed call (CUDA events on the launching stream)."""
+    precedes every timed call (CUDA events on the launching stream).  only:
+    name prefixes (profiling runs of some rows alone)."""
     fq, o, fl = suite.fq, suite.o, suite.flags
     r2, c2 = suite.r2, suite.c2
     dev = suite.x1.device
@@ -542,6 +547,10 @@ def run_column_rows(args, suite, peak):
             ("w3_sym_int8_col_bf16", n3 * (2 + 2 + 2 + 1) + m(n3) + side3 * 4,
              lambda: fq.qat_fake_quant_int(a3c, side3, side3, 8, 0, 3, 0, False, s3, None,
                                            o["y3a"], c3, o["m3a"], fl, ws)))
+    if only:
+        rows = [r for r in rows if any(r[0].startswith(p) for p in only)]
+        if not rows:
+            return {}
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     steps = max(3, min(args.steps, 100))
@@ -737,11 +746,13 @@ def run_ours(args, rank, world, local):
 
     peak, peak_kind = measured_peak()
     next_rows = None
-    sr_only = [p for p in args.only.split(",") if p.endswith("_sr")] if args.only else []
+    # profiling runs: --only names of stochastic-rounding or per-column rows
+    row_only = ([p for p in args.only.split(",") if p.endswith("_sr") or "_col" in p]
+                if args.only else [])
     if not args.only and args.fraction >= 1.0 and not args.no_next:
         next_rows = run_next_rows(args, suite, wb, peak)
-    elif sr_only:
-        next_rows = run_next_rows(args, suite, wb_all, peak, only=sr_only)
+    elif row_only:
+        next_rows = run_next_rows(args, suite, wb_all, peak, only=row_only)
     iso_ms = isolated_call_ms(calls, stream) if not args.no_isolated else None
     per_wl = {}
     for i, ((name, elems, b, nl), ms) in enumerate(zip(wb, mean_ms)):
@@ -1202,8 +1213,8 @@ def main(argv=None):
                     help="skip the stochastic-rounding and CUDA-graph timings (next_rows)")
     ap.add_argument("--only", default="",
                     help="profiling: comma-separated call-name prefixes to run (e.g. w5,w4_int4); "
-                         "names ending in _sr select stochastic-rounding rows (e.g. "
-                         "w1,w3_fp8_e4m3_tensor_sr)")
+                         "names ending in _sr or holding _col select stochastic-rounding and "
+                         "per-column rows (e.g. w1,w3_fp8_e4m3_tensor_sr,w2_affine_int8_col)")
     ap.add_argument("--fraction", type=float, default=1.0,
                     help="profiling: fraction of every workload's rows to generate")
     args = ap.parse_args(argv)
