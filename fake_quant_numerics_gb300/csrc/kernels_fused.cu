@@ -151,10 +151,10 @@ __device__ __forceinline__ void group_tile(const void* __restrict__ x, int64_t n
   }
 }
 
-template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY, bool SR, bool OPT>
 // registers: bf16 nearest rounding 64 (four blocks of 256 per SM; 53.3 ->
 // 49.4 us on the w4 weights against 80), stochastic rounding 80 (three),
 // fp32 nearest rounding 96
+template <typename T, int BITS, bool AFFINE, int LPG, bool STATS_ONLY, bool SR, bool OPT>
 __global__ void __maxnreg__((T::BYTES == 4 && !SR) ? 96 : (SR ? 80 : 64))
     k_int_groups(const void* __restrict__ x, int64_t n, float* scale, int32_t* zp, float* absmax,
                  float* minv, float* maxv, SrCtx sr, CalOpts co, void* y, void* codes,
