@@ -934,11 +934,13 @@ def run_e2e(args, suite, calls, step_bytes, keep=None):
     del other
     # the host link bounds this figure: a step's copies take at least the
     # longer of its two directions alone and its total at the rate of both
+    # (each rank measures its own link; the bounds are summed over the ranks,
+    # as the value is)
     link = host_link_gbs(dev)
     t_copy = max(h2d / (link["h2d"] * 1e9), d2h / (link["d2h"] * 1e9),
                  (h2d + d2h) / (link["both"] * 1e9))
     value = sorted(runs)[len(runs) // 2]
-    bound = step_bytes / t_copy / 1e9
+    _, bound = reduce_max_sum(0.0, step_bytes / t_copy / 1e9)
     return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": k, "windows": [round(r, 1) for r in runs],
             "pipeline": "2 device buffer sets; copies in, calls, copies out on 3 streams",
