@@ -118,36 +118,20 @@ __device__ __forceinline__ bool fp8_vec_bf16_fast(const V32& v, const Fp8Params&
   return bad == 0u;
 }
 
-// fp8_quantize_magnitude with stochastic rounding (RoundingMode::Stochastic):
-// e = floor(log2 a) from the exponent field (a binary32 subnormal reads
-// e = -127, below emin), ulp = 2^(max(e, emin) - mbits), a / ulp (an exact
-// power-of-two scaling) rounded by sr_round with draw u, times ulp,
-// saturated at the format maximum; the sign of t.  A NaN t is handled by the
-// caller (canonical NaN, code 0x7F).
-template <int FMT>
-__device__ __forceinline__ float fp8_sr_value(float t, float u) {
-  constexpr int MB = FMT == QAT_E4M3 ? 3 : 2, EMIN = FMT == QAT_E4M3 ? -6 : -14;
-  constexpr float kMaxF = FMT == QAT_E4M3 ? 448.0f : 57344.0f;
-  const float a = fabsf(t);
-  const int e = (int)(__float_as_uint(a) >> 23) - 127;
-  const int se = (e > EMIN ? e : EMIN) - MB;                  // in [EMIN - MB, 128 - MB]
-  const float inv = __uint_as_float((uint32_t)(127 - se) << 23);  // 2^-se, normal
-  const float step = __uint_as_float((uint32_t)(127 + se) << 23); // 2^se, normal
-  const float k = sr_round(__fmul_rn(a, inv), u);
-  const float mag = fminf(__fmul_rn(k, step), kMaxF);
-  return copysignf(mag, t);
-}
-
-// fp8_sr_value for the quotient t of x, in fewer integer operations: 2^max(e,
-// emin) is max(exponent field of |t|, that of 2^emin) (a zero or binary32
-// subnormal t has field 0), ulp = 2^max(e, emin) 2^-mbits and 1 / ulp, whose
-// exponent field is 254 + mbits - that field, are exact; the sign is that of
-// x, which t = RN(x/s) (s > 0) shares, so a quotient whose sign or value the
-// residual steps lost needs no repair: t = +0 for x = -0 gives -0 again, and
-// a NaN quotient of x = +-inf (or of an x whose quotient overflows) gives
-// fminf(NaN, max) = max, the rule's value for an infinite t (an element
-// with x NaN is replaced by the caller).  u = (w >> 9) 2^-23 as (1 + u) - 1,
-// 1 + u having the bits hi(w 2^23) + 0x3f800000 (one multiply-add).
+// fp8_quantize_magnitude with stochastic rounding (RoundingMode::Stochastic)
+// for the quotient t = RN(x/s) of an element x (s > 0): with e = floor(log2
+// |t|), ulp = 2^(max(e, emin) - mbits); |t| / ulp (an exact power-of-two
+// scaling) is rounded by the draw u (up when u < its fraction), times ulp,
+// saturated at the format maximum, with the sign of t.  Here 2^max(e, emin)
+// is the larger of the exponent fields of |t| and of 2^emin (a zero or
+// binary32 subnormal t has field 0), ulp and 1 / ulp (exponent field 254 +
+// mbits - that field) are exact, and the sign is taken from x, which t
+// shares, so a quotient whose sign or value the residual steps lost needs no
+// repair: t = +0 for x = -0 gives -0 again, and a NaN quotient of x = +-inf
+// (or of an x whose quotient overflows) gives fminf(NaN, max) = max, the
+// rule's value for an infinite t (an element with x NaN is replaced by the
+// caller).  u = (w >> 9) 2^-23 as (1 + u) - 1, 1 + u having the bits
+// hi(w 2^23) + 0x3f800000 (one multiply-add).
 template <int FMT>
 __device__ __forceinline__ float fp8_sr_value_x(float t, float x, uint32_t w) {
   constexpr uint32_t MB = FMT == QAT_E4M3 ? 3u : 2u;
@@ -251,11 +235,9 @@ __device__ __forceinline__ void fp8_vec_sr_mode0(const V32& v, const Fp8Params& 
   }
 }
 
-// One vector with stochastic rounding: the IEEE quotient t = RN(x/s) (exact
-// residual-step quotient for a safe scale, the division otherwise; its sign
-// is that of x), the grid value of fp8_sr_value, its code by the saturating
-// cast (exact for a grid value), y = c * s; NaN, zero-scale and invalid-scale
-// handling and the window as in the nearest-rounding path.
+// One vector with stochastic rounding: fp8_vec_sr_mode0 for a usable scale;
+// for a zero or invalid scale the outputs of the nearest-rounding path (no
+// draw changes them).
 template <typename T, int FMT, bool CODES, bool FULL>
 __device__ __forceinline__ void fp8_vec_sr(const V32& v, const Fp8Params& p, const SrCtx& sr,
                                            int64_t base, int cnt, V32& out,
@@ -265,57 +247,27 @@ __device__ __forceinline__ void fp8_vec_sr(const V32& v, const Fp8Params& p, con
     fp8_vec_sr_mode0<T, FMT, CODES, FULL>(v, p, sr, base, cnt, out, cv, mb);
     return;
   }
+  // a zero scale (mode 1: codes 0, y +0, NaN kept with code 0x7F, the
+  // window |x| <= 0) or an invalid given scale (mode 2: codes 0, y +0,
+  // mask 0): no quotients and no draws
   cv.clear();
   mb = 0u;
 #pragma unroll
-  for (int g = VEC / 4 - 1; g >= 0; --g) {
-    float u[4];
-    sr_draws4(sr, base / 4 + g, u);
-#pragma unroll
-    for (int h = 1; h >= 0; --h) {
-      const int e = 4 * g + 2 * h;
-      const float x0 = elem<T>(v, e), x1 = elem<T>(v, e + 1);
-      const bool n0 = isnan(x0), n1 = isnan(x1);
-      uint32_t c0 = 0u, c1 = 0u;
-      float y0 = 0.0f, y1 = 0.0f;
-      if (p.mode == 0) {
-        float t0, t1;
-        if (p.fast) {
-          quotient_rn2(x0, x1, p.rcp, p.ns, t0, t1);
-          t0 = isfinite(x0) ? copysignf(t0, x0) : x0;  // +-inf / s = +-inf, NaN stays NaN
-          t1 = isfinite(x1) ? copysignf(t1, x1) : x1;
-        } else {
-          t0 = __fdiv_rn(x0, p.s);
-          t1 = __fdiv_rn(x1, p.s);
-        }
-        const float g0 = fp8_sr_value<FMT>(t0, u[2 * h]);
-        const float g1 = fp8_sr_value<FMT>(t1, u[2 * h + 1]);
-        const uint32_t c2 = fp8x2_encode<FMT>(g0, g1);
-        c0 = c2 & 0xffu;
-        c1 = (c2 >> 8) & 0xffu;
-        mul2(g0, g1, p.s, p.s, y0, y1);
-      }
-      if (p.mode != 2) {
-        if (n0) c0 = 0x7fu;
-        if (n1) c1 = 0x7fu;
-        mb |= (uint32_t)(fabsf(x0) <= p.lim) << e;
-        mb |= (uint32_t)(fabsf(x1) <= p.lim) << (e + 1);
-      }
-      if (CODES) {
-        cv.set2(e, (FULL || e < cnt) ? (int)(int8_t)c0 : 0,
-                (FULL || e + 1 < cnt) ? (int)(int8_t)c1 : 0);
-      }
-      if (T::BYTES == 4) {
-        out.w[e] = (p.mode != 2 && n0) ? kNaN32 : __float_as_uint(y0);
-        out.w[e + 1] = (p.mode != 2 && n1) ? kNaN32 : __float_as_uint(y1);
-      } else {
-        uint32_t w = pack_bf16x2(y0, y1);
-        if (p.mode != 2) {
-          if (n0) w = (w & 0xffff0000u) | kNaN16;
-          if (n1) w = (w & 0x0000ffffu) | (kNaN16 << 16);
-        }
-        out.w[e >> 1] = w;
-      }
+  for (int e = VEC - 2; e >= 0; e -= 2) {
+    const float x0 = elem<T>(v, e), x1 = elem<T>(v, e + 1);
+    const bool n0 = p.mode != 2 && isnan(x0), n1 = p.mode != 2 && isnan(x1);
+    if (p.mode != 2) {
+      mb |= (uint32_t)(fabsf(x0) <= p.lim) << e;
+      mb |= (uint32_t)(fabsf(x1) <= p.lim) << (e + 1);
+    }
+    if (CODES) {
+      cv.set2(e, (FULL || e < cnt) && n0 ? 0x7f : 0, (FULL || e + 1 < cnt) && n1 ? 0x7f : 0);
+    }
+    if (T::BYTES == 4) {
+      out.w[e] = n0 ? kNaN32 : 0u;
+      out.w[e + 1] = n1 ? kNaN32 : 0u;
+    } else {
+      out.w[e >> 1] = (n0 ? kNaN16 : 0u) | (n1 ? (kNaN16 << 16) : 0u);
     }
   }
 }

@@ -157,6 +157,8 @@ def test_fp8_sr(qat, orc, fmt, dt):
             run_fp8_sr(qat, orc, x, fmt, seed, off, scale=1e-30)      # outside the safe range
             run_fp8_sr(qat, orc, x, fmt, seed, off, with_codes=False)  # y and mask only
         run_fp8_sr(qat, orc, x, fmt, 3, 4, scale=0.0)                 # zero scale
+        run_fp8_sr(qat, orc, x, fmt, 3, 4, scale=-1.0)                # invalid given scales
+        run_fp8_sr(qat, orc, x, fmt, 3, 4, scale=float("inf"), with_codes=False)
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
